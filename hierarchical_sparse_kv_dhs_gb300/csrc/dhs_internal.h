@@ -1,0 +1,127 @@
+// Internal launch interface between the host pool manager (pool.cpp) and
+// the sm_103a kernels (resolve.cu, hostcopy.cu, gather.cu, append.cu).
+// Not part of the C ABI.
+//
+// Item tables travel by value in the kernel parameter space
+// (__grid_constant__), so a decode step needs no host-to-device copy of its
+// descriptors and stays capturable as plain kernel launches.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dhs {
+
+constexpr uint32_t kTierTail = 0u, kTierOpt = 1u, kTierHot = 2u;
+constexpr uint32_t kNoLoc = 0xFFFFFFFFu;
+constexpr uint32_t kStatusErange = 1u, kStatusEbudget = 2u, kStatusEloc = 4u;
+constexpr int32_t kErrRange = -5, kErrBudget = -4;  // DHS_ERANGE, DHS_EBUDGET
+constexpr int kMaxHotRows = 16384;
+
+// ------------------------------------------------------------ resolve (a-c)
+constexpr int kResolveThreads = 1024;
+constexpr int kResolveItemsLarge = 256, kResolveItemsSmall = 32;
+
+struct ResolveItem {
+  const int32_t* sel;   // [n] selected rows (Q*k, verify queries back to back)
+  uint32_t* loc;        // [n] locations out
+  uint32_t* counters;   // [8] or null
+  int64_t L;            // current length
+  int64_t N;            // imported rows
+  int32_t pair;         // req * S + src
+  int32_t n;            // Q * k
+  int32_t pad[2];
+};
+
+struct ResolveCommon {
+  int32_t* tags;         // [pairs][B]
+  uint32_t* stamps;      // [pairs][B]
+  const int32_t* map;    // [pairs][Pmax]
+  int32_t* miss_rows;    // [pairs][Mcap]
+  int32_t* miss_slots;   // [pairs][Mcap]
+  uint32_t* miss_count;  // [pairs]
+  int32_t* pair_status;  // [pairs]
+  uint32_t* status;      // sticky flags
+  int32_t T, B, Pmax, Mcap;
+  int32_t page_shift;    // log2(page_rows)
+  int32_t w64cap;        // bitmap words reserved in shared memory
+  int32_t qkcap;         // candidate slots reserved in shared memory
+  uint32_t step;
+  int32_t n_items;
+  int32_t pad;
+};
+
+size_t resolve_smem_bytes(int w64cap, int qkcap, int B);
+cudaError_t resolve_set_smem_limit(size_t bytes);
+cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,
+                           int n_items, size_t smem, cudaStream_t stream);
+
+// ------------------------------------------------------------ host copy (d)
+constexpr int kCopyThreads = 512;
+constexpr int kCopyItemsMax = 256;
+
+struct CopyItem {
+  const uint8_t* host;  // device-visible pointer of the pair's pinned host rows
+  int32_t pair;
+  int32_t pad;
+};
+
+struct CopyCommon {
+  uint8_t* hot;
+  const int32_t* miss_rows;
+  const int32_t* miss_slots;
+  const uint32_t* miss_count;
+  int32_t B, Mcap, row_bytes, n_items;
+};
+
+cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,
+                            int n_items, int ctas, cudaStream_t stream);
+
+// ------------------------------------------------------------ gather (e)
+constexpr int kGatherThreads = 256;
+constexpr int kGatherTileRows = 32;
+constexpr int kGatherItemsLarge = 512, kGatherItemsSmall = 64;
+
+struct GatherItem {
+  const uint32_t* loc;
+  uint8_t* staging;
+  int32_t n;      // entries
+  int32_t tile0;  // first tile of this item in the launch
+};
+
+struct GatherCommon {
+  const uint8_t* tail;
+  const uint8_t* opt;
+  const uint8_t* hot;
+  uint32_t tail_rows, opt_rows, hot_rows;  // arena sizes in rows
+  int32_t row_bytes;
+  uint32_t* status;
+  int32_t n_items;
+  int32_t n_tiles;
+};
+
+cudaError_t launch_gather(const GatherCommon& c, const GatherItem* items,
+                          int n_items, int impl, cudaStream_t stream);
+
+// ------------------------------------------------------------ append (A0)
+constexpr int kAppendThreads = 256;
+constexpr int kAppendItemsMax = 256;
+
+struct AppendItem {
+  const uint8_t* rows;  // [count][row_bytes] device
+  uint8_t* host;        // device-visible pointer of the pair's host rows
+  int64_t L0;           // length before the append
+  int32_t pair;
+  int32_t count;
+};
+
+struct AppendCommon {
+  uint8_t* tail;
+  int32_t T, row_bytes, n_items, pad;
+};
+
+cudaError_t launch_append(const AppendCommon& c, const AppendItem* items,
+                          int n_items, cudaStream_t stream);
+
+}  // namespace dhs

@@ -1,0 +1,144 @@
+// Host-copy kernel: step 3 of resolution ("a copy from pinned host memory
+// into the hot cache"; "Adaptive DHiSparse", How it works / Resolution).
+//
+// Reads the missing rows straight out of mapped pinned host memory over
+// NVLink-C2C into their victim hot-cache slots.  The pages note that the
+// copy kernel scales from 4 to 32 thread blocks with batch size; the grid
+// here is chosen by the host the same way (clamp(requests / 4, 4, 32)) and
+// can be overridden for sweeps.  Each warp keeps up to four 1152-byte rows
+// in flight (12 x 16-byte loads per lane) so the link sees enough
+// outstanding requests to cover its latency.
+#include "dhs_internal.h"
+
+namespace dhs {
+namespace {
+
+template <int MAXI>
+struct CopyParams {
+  CopyCommon c;
+  CopyItem items[MAXI];
+};
+
+__device__ __forceinline__ uint4 ld_sys(const uint8_t* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+constexpr int kRowsPerWarp = 4;
+constexpr int kChunksPerLane = 3;  // rows up to 96 x 16 = 1536 bytes
+
+template <int MAXI, bool kSmallRow>
+__global__ void __launch_bounds__(kCopyThreads)
+    hostcopy_kernel(const __grid_constant__ CopyParams<MAXI> P) {
+  __shared__ uint32_t s_pre[MAXI + 1];
+  __shared__ uint32_t s_scr[33];
+  const CopyCommon& c = P.c;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n_items = c.n_items;
+
+  // prefix of the per-item miss counts (n_items <= blockDim.x)
+  const uint32_t mine = tid < n_items ? c.miss_count[P.items[tid].pair] : 0u;
+  {
+    const int warp = tid >> 5, nw = blockDim.x >> 5;
+    uint32_t v = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (lane == 31) s_scr[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t w = lane < nw ? s_scr[lane] : 0u;
+      uint32_t wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+        if (lane >= o) wi += t;
+      }
+      if (lane < nw) s_scr[lane] = wi - w;
+    }
+    __syncthreads();
+    if (tid < n_items) s_pre[tid + 1] = s_scr[warp] + v;
+    if (tid == 0) s_pre[0] = 0u;
+    __syncthreads();
+  }
+  const uint32_t total = s_pre[n_items];
+  if (total == 0) return;
+
+  const int rb = c.row_bytes;
+  const int cpr = rb >> 4;
+  const uint32_t gwarp = (blockIdx.x * blockDim.x + tid) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t base = gwarp * kRowsPerWarp; base < total; base += nwarps * kRowsPerWarp) {
+    const uint8_t* src[kRowsPerWarp];
+    uint8_t* dst[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const uint32_t i = base + r;
+      src[r] = nullptr;
+      dst[r] = nullptr;
+      if (i < total) {
+        int lo = 0, hi = n_items - 1;  // last item with s_pre[item] <= i
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_pre[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        const CopyItem& it = P.items[lo];
+        const uint32_t mi = i - s_pre[lo];
+        const size_t off = (size_t)it.pair * c.Mcap + mi;
+        const int32_t row = c.miss_rows[off];
+        const int32_t slot = c.miss_slots[off];
+        src[r] = it.host + (size_t)row * rb;
+        dst[r] = c.hot + ((size_t)it.pair * c.B + slot) * rb;
+      }
+    }
+    if (kSmallRow) {
+      uint4 v[kRowsPerWarp][kChunksPerLane];
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+        for (int q = 0; q < kChunksPerLane; ++q) {
+          const int ch = lane + 32 * q;
+          if (src[r] && ch < cpr) v[r][q] = ld_sys(src[r] + ch * 16);
+        }
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+        for (int q = 0; q < kChunksPerLane; ++q) {
+          const int ch = lane + 32 * q;
+          if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
+        }
+    } else {
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        if (!src[r]) continue;
+        for (int ch = lane; ch < cpr; ch += 32)
+          *reinterpret_cast<uint4*>(dst[r] + ch * 16) = ld_sys(src[r] + ch * 16);
+      }
+    }
+  }
+}
+
+template <int MAXI>
+cudaError_t launch_t(const CopyCommon& c, const CopyItem* items, int n, int ctas,
+                     cudaStream_t stream) {
+  CopyParams<MAXI> P;
+  P.c = c;
+  P.c.n_items = n;
+  for (int i = 0; i < n; ++i) P.items[i] = items[i];
+  if ((c.row_bytes >> 4) <= 32 * kChunksPerLane)
+    hostcopy_kernel<MAXI, true><<<ctas, kCopyThreads, 0, stream>>>(P);
+  else
+    hostcopy_kernel<MAXI, false><<<ctas, kCopyThreads, 0, stream>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items, int n_items,
+                            int ctas, cudaStream_t stream) {
+  if (n_items <= 0) return cudaSuccess;
+  if (n_items > kCopyItemsMax || n_items > kCopyThreads) return cudaErrorInvalidValue;
+  return launch_t<kCopyItemsMax>(c, items, n_items, ctas, stream);
+}
+
+}  // namespace dhs

@@ -1,0 +1,704 @@
+// Host-side pool manager and C ABI of libdhs (see include/dhs.h).
+//
+// "Adaptive DHiSparse: Speculative Decoding over a Load-Adaptive KV
+// Hierarchy", How it works:
+//   Memory split -- per (request, KV source) a fixed hot cache of B rows,
+//     a mutable tail and metadata (never lent); complete imported pages in
+//     reclaimable optional capacity under required + optional + admission
+//     reserve <= pool capacity.  Required memory is laid out per request
+//     slot up front, so the rule is checked on the optional arena.
+//   Resident-first admission -- resident pages take optional slots at
+//     admission (lowest free slot first, pages ascending).
+//   Reclamation and refill -- whole requests' pages are taken in reclaim
+//     order until the deficit is covered, otherwise the admission waits.
+//     Every device read of a page is ordered on the pool's stream, so a page
+//     freed here is reused only by work enqueued after every earlier reader.
+//
+// Host metadata only: the caller owns every device buffer and every pinned
+// host buffer.  Page bytes of an admission are copied lazily, just before
+// the next device call that could observe them, so pages reclaimed before
+// any step (e.g. an admission storm under memory pressure) are never moved.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "dhs.h"
+#include "dhs_internal.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+struct MetaLayout {
+  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status, status;
+  size_t total;
+};
+
+inline int64_t pages_max_of(const dhs_pool_config& c) {
+  return (c.max_rows_per_request + c.page_rows - 1) / c.page_rows;
+}
+
+inline int64_t mcap_of(const dhs_pool_config& c) {
+  int64_t qk = (int64_t)c.max_queries * c.max_topk;
+  return std::max<int64_t>(1, std::min<int64_t>(c.hot_rows, qk));
+}
+
+MetaLayout meta_layout(const dhs_pool_config& c) {
+  MetaLayout m{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  const size_t pairs = (size_t)c.max_requests * c.sources;
+  m.tags = take(pairs * c.hot_rows * 4);
+  m.stamps = take(pairs * c.hot_rows * 4);
+  m.map = take(pairs * (size_t)pages_max_of(c) * 4);
+  m.miss_rows = take(pairs * (size_t)mcap_of(c) * 4);
+  m.miss_slots = take(pairs * (size_t)mcap_of(c) * 4);
+  m.miss_count = take(pairs * 4);
+  m.pair_status = take(pairs * 4);
+  m.status = take(64);
+  m.total = off;
+  return m;
+}
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int log2i(int64_t x) {
+  int r = 0;
+  while ((int64_t(1) << r) < x) ++r;
+  return r;
+}
+
+// Shared-memory plan of the resolve kernel at the pool's largest sizes.
+size_t max_resolve_smem(const dhs_pool_config& c) {
+  const int64_t w64 = (c.max_rows_per_request + 63) / 64;
+  const int64_t qk = std::min<int64_t>((int64_t)c.max_queries * c.max_topk,
+                                       c.max_rows_per_request);
+  return dhs::resolve_smem_bytes((int)w64, (int)qk, c.hot_rows);
+}
+
+int validate_geometry(const dhs_pool_config* c) {
+  if (!c) return DHS_EINVAL;
+  if (c->max_requests <= 0 || c->sources <= 0 || c->tail_rows <= 0) return DHS_EINVAL;
+  if (c->hot_rows <= 0 || c->hot_rows > dhs::kMaxHotRows) return DHS_EINVAL;
+  if (c->row_bytes < 16 || c->row_bytes % 16 != 0 || c->row_bytes > 65536) return DHS_EINVAL;
+  if (!is_pow2(c->page_rows) || c->page_rows > 65536) return DHS_EINVAL;
+  if (c->max_queries < 0 || c->max_topk < 0) return DHS_EINVAL;
+  if ((int64_t)c->max_queries * c->max_topk > (int64_t)1 << 20) return DHS_EINVAL;
+  if (c->max_rows_per_request <= 0 || c->max_rows_per_request > INT32_MAX) return DHS_EINVAL;
+  if (c->optional_pages < 0 || c->admission_reserve_pages < 0 ||
+      c->admission_reserve_pages > c->optional_pages)
+    return DHS_EINVAL;
+  const int64_t pairs = (int64_t)c->max_requests * c->sources;
+  const int64_t lim = (int64_t)1 << 30;  // location index bits
+  if (pairs * c->tail_rows >= lim || pairs * c->hot_rows >= lim ||
+      c->optional_pages * c->page_rows >= lim || pairs >= (1 << 24))
+    return DHS_EINVAL;
+  return DHS_OK;
+}
+
+struct PairState {
+  bool admitted = false;
+  int64_t N = 0, L = 0;
+  uint8_t* host = nullptr;      // caller's pinned host rows
+  uint8_t* host_dev = nullptr;  // device-visible address of the same rows
+  std::vector<int32_t> pending;  // resident pages whose bytes are not yet copied
+};
+
+}  // namespace
+
+struct dhs_pool {
+  dhs_pool_config cfg{};
+  cudaStream_t stream = nullptr;
+  int device = 0;
+  int64_t pairs = 0, pmax = 0, mcap = 0;
+  int page_shift = 0;
+  MetaLayout layout{};
+  int32_t* tags = nullptr;
+  uint32_t* stamps = nullptr;
+  int32_t* map = nullptr;
+  int32_t* miss_rows = nullptr;
+  int32_t* miss_slots = nullptr;
+  uint32_t* miss_count = nullptr;
+  int32_t* pair_status = nullptr;
+  uint32_t* status = nullptr;
+  std::vector<PairState> ps;
+  std::vector<int32_t> map_host;  // [pairs][pmax] mirror of the device map
+  std::vector<int32_t> slot_pair, slot_page;
+  int64_t first_free = 0, used = 0;
+  int64_t dirty_lo = INT64_MAX, dirty_hi = -1;  // pairs whose map changed
+  bool any_pending = false;
+  int copy_ctas = 0;
+  int gather_impl = 0;
+  // reusable launch tables
+  std::vector<dhs::ResolveItem> ritems;
+  std::vector<dhs::CopyItem> citems;
+  std::vector<dhs::GatherItem> gitems;
+  std::vector<dhs::AppendItem> aitems;
+  std::vector<uint8_t> seen;
+};
+
+namespace {
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? DHS_OK : DHS_ECUDA; }
+
+int enter(dhs_pool* p) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return DHS_ECUDA;
+  if (cur != p->device && cudaSetDevice(p->device) != cudaSuccess) return DHS_ECUDA;
+  return DHS_OK;
+}
+
+void mark_dirty(dhs_pool* p, int64_t pair) {
+  p->dirty_lo = std::min(p->dirty_lo, pair);
+  p->dirty_hi = std::max(p->dirty_hi, pair);
+}
+
+// Copy pending resident pages (coalescing runs of consecutive pages in
+// consecutive slots) and upload changed page maps, in stream order.
+int flush(dhs_pool* p) {
+  const dhs_pool_config& c = p->cfg;
+  const size_t page_bytes = (size_t)c.page_rows * c.row_bytes;
+  if (p->any_pending) {
+    for (int64_t pair = 0; pair < p->pairs; ++pair) {
+      PairState& s = p->ps[pair];
+      if (s.pending.empty()) continue;
+      std::sort(s.pending.begin(), s.pending.end());
+      const int32_t* pm = p->map_host.data() + pair * p->pmax;
+      size_t i = 0;
+      while (i < s.pending.size()) {
+        const int32_t page = s.pending[i];
+        const int32_t slot = pm[page];
+        size_t run = 1;
+        while (i + run < s.pending.size() && s.pending[i + run] == page + (int32_t)run &&
+               pm[page + run] == slot + (int32_t)run)
+          ++run;
+        cudaError_t e = cudaMemcpyAsync((uint8_t*)c.opt_dev + (size_t)slot * page_bytes,
+                                        s.host + (size_t)page * page_bytes, run * page_bytes,
+                                        cudaMemcpyHostToDevice, p->stream);
+        if (e != cudaSuccess) return DHS_ECUDA;
+        i += run;
+      }
+      s.pending.clear();
+    }
+    p->any_pending = false;
+  }
+  if (p->dirty_hi >= 0) {
+    const size_t off = (size_t)p->dirty_lo * p->pmax;
+    const size_t cnt = (size_t)(p->dirty_hi - p->dirty_lo + 1) * p->pmax;
+    cudaError_t e = cudaMemcpyAsync(p->map + off, p->map_host.data() + off, cnt * 4,
+                                    cudaMemcpyHostToDevice, p->stream);
+    if (e != cudaSuccess) return DHS_ECUDA;
+    p->dirty_lo = INT64_MAX;
+    p->dirty_hi = -1;
+  }
+  return DHS_OK;
+}
+
+void free_slot(dhs_pool* p, int64_t slot) {
+  p->slot_pair[slot] = -1;
+  p->slot_page[slot] = -1;
+  p->used -= 1;
+  if (slot < p->first_free) p->first_free = slot;
+}
+
+int64_t lowest_free_slot(dhs_pool* p) {
+  for (int64_t i = p->first_free; i < p->cfg.optional_pages; ++i)
+    if (p->slot_pair[i] < 0) {
+      p->first_free = i;
+      return i;
+    }
+  return -1;
+}
+
+// Free every optional page of pair; returns pages freed.
+int64_t drop_pages(dhs_pool* p, int64_t pair) {
+  int32_t* pm = p->map_host.data() + pair * p->pmax;
+  int64_t n = 0;
+  for (int64_t q = 0; q < p->pmax; ++q) {
+    if (pm[q] < 0) continue;
+    free_slot(p, pm[q]);
+    pm[q] = -1;
+    ++n;
+  }
+  if (n) mark_dirty(p, pair);
+  p->ps[pair].pending.clear();
+  return n;
+}
+
+int64_t request_pages(const dhs_pool* p, int32_t r) {
+  int64_t n = 0;
+  for (int32_t s = 0; s < p->cfg.sources; ++s) {
+    const int32_t* pm = p->map_host.data() + ((int64_t)r * p->cfg.sources + s) * p->pmax;
+    for (int64_t q = 0; q < p->pmax; ++q) n += pm[q] >= 0;
+  }
+  return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dhs_strerror(int code) {
+  switch (code) {
+    case DHS_OK: return "ok";
+    case DHS_EINVAL: return "invalid argument";
+    case DHS_ENOMEM: return "out of host memory";
+    case DHS_EWOULDWAIT: return "capacity deficit: admission waits";
+    case DHS_EBUDGET: return "more missing rows than unprotected hot slots";
+    case DHS_ERANGE: return "row or location out of range";
+    case DHS_ETIMEDOUT: return "bounded device wait gave up";
+    case DHS_ECUDA: return "CUDA runtime error";
+    case DHS_ESTATE: return "request/source not admitted or already admitted";
+    default: return "unknown error";
+  }
+}
+
+int dhs_pool_bytes(const dhs_pool_config* cfg, size_t out[DHS_NUM_BUFS]) {
+  int rc = validate_geometry(cfg);
+  if (rc) return rc;
+  if (!out) return DHS_EINVAL;
+  const size_t pairs = (size_t)cfg->max_requests * cfg->sources;
+  out[DHS_BUF_HOT] = pairs * cfg->hot_rows * (size_t)cfg->row_bytes;
+  out[DHS_BUF_TAIL] = pairs * cfg->tail_rows * (size_t)cfg->row_bytes;
+  out[DHS_BUF_OPT] = (size_t)cfg->optional_pages * cfg->page_rows * (size_t)cfg->row_bytes;
+  out[DHS_BUF_META] = meta_layout(*cfg).total;
+  return DHS_OK;
+}
+
+int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
+  if (!out) return DHS_EINVAL;
+  *out = nullptr;
+  int rc = validate_geometry(cfg);
+  if (rc) return rc;
+  auto aligned = [](const void* q) { return q && ((uintptr_t)q % kAlign) == 0; };
+  if (!aligned(cfg->hot_dev) || !aligned(cfg->tail_dev) || !aligned(cfg->meta_dev))
+    return DHS_EINVAL;
+  if (cfg->optional_pages > 0 && !aligned(cfg->opt_dev)) return DHS_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DHS_ECUDA;
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+      cudaSuccess)
+    return DHS_ECUDA;
+  const size_t smem = max_resolve_smem(*cfg);
+  if (smem + 1024 > (size_t)optin) return DHS_EINVAL;
+  if (dhs::resolve_set_smem_limit(smem) != cudaSuccess) return DHS_ECUDA;
+
+  dhs_pool* p = new (std::nothrow) dhs_pool();
+  if (!p) return DHS_ENOMEM;
+  try {
+    p->cfg = *cfg;
+    p->stream = (cudaStream_t)cfg->stream;
+    p->device = dev;
+    p->pairs = (int64_t)cfg->max_requests * cfg->sources;
+    p->pmax = pages_max_of(*cfg);
+    p->mcap = mcap_of(*cfg);
+    p->page_shift = log2i(cfg->page_rows);
+    p->layout = meta_layout(*cfg);
+    uint8_t* m = (uint8_t*)cfg->meta_dev;
+    p->tags = (int32_t*)(m + p->layout.tags);
+    p->stamps = (uint32_t*)(m + p->layout.stamps);
+    p->map = (int32_t*)(m + p->layout.map);
+    p->miss_rows = (int32_t*)(m + p->layout.miss_rows);
+    p->miss_slots = (int32_t*)(m + p->layout.miss_slots);
+    p->miss_count = (uint32_t*)(m + p->layout.miss_count);
+    p->pair_status = (int32_t*)(m + p->layout.pair_status);
+    p->status = (uint32_t*)(m + p->layout.status);
+    p->ps.resize(p->pairs);
+    p->map_host.assign((size_t)(p->pairs * p->pmax), -1);
+    p->slot_pair.assign((size_t)cfg->optional_pages + 1, -1);
+    p->slot_page.assign((size_t)cfg->optional_pages + 1, -1);
+    p->seen.assign((size_t)p->pairs, 0);
+  } catch (...) {
+    delete p;
+    return DHS_ENOMEM;
+  }
+  // empty hot caches (tag -1, stamp 0), no ready pages, zero counts/status
+  cudaError_t e = cudaMemsetAsync(p->tags, 0xFF, p->pairs * cfg->hot_rows * 4, p->stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(p->stamps, 0, p->pairs * cfg->hot_rows * 4, p->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p->map, 0xFF, p->pairs * p->pmax * 4, p->stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync((uint8_t*)cfg->meta_dev + p->layout.miss_count, 0,
+                        p->layout.total - p->layout.miss_count, p->stream);
+  if (e != cudaSuccess) {
+    delete p;
+    return DHS_ECUDA;
+  }
+  *out = p;
+  return DHS_OK;
+}
+
+void dhs_pool_destroy(dhs_pool* pool) { delete pool; }
+
+int64_t dhs_pool_used(const dhs_pool* pool) { return pool ? pool->used : -1; }
+
+int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
+  if (!pool) return DHS_EINVAL;
+  if (key == DHS_OPT_COPY_CTAS) {
+    if (value < 0 || value > 4096) return DHS_EINVAL;
+    pool->copy_ctas = (int)value;
+    return DHS_OK;
+  }
+  if (key == DHS_OPT_GATHER_IMPL) {
+    if (value < 0 || value > 1) return DHS_EINVAL;
+    pool->gather_impl = (int)value;
+    return DHS_OK;
+  }
+  return DHS_EINVAL;
+}
+
+int dhs_admit(dhs_pool* p, int32_t req, int32_t src, void* host_rows, int64_t n_rows,
+              const uint8_t* mask, int64_t* deficit) {
+  if (deficit) *deficit = 0;
+  if (!p || req < 0 || req >= p->cfg.max_requests || src < 0 || src >= p->cfg.sources)
+    return DHS_EINVAL;
+  const dhs_pool_config& c = p->cfg;
+  if (n_rows < 0 || n_rows > c.max_rows_per_request || !host_rows) return DHS_EINVAL;
+  const int64_t pair = (int64_t)req * c.sources + src;
+  PairState& s = p->ps[pair];
+  if (s.admitted) return DHS_ESTATE;
+  int rc = enter(p);
+  if (rc) return rc;
+  void* hdev = nullptr;
+  if (cudaHostGetDevicePointer(&hdev, host_rows, 0) != cudaSuccess || !hdev) {
+    cudaGetLastError();  // clear the sticky-free error state
+    return DHS_EINVAL;
+  }
+  const int64_t complete = n_rows / c.page_rows;
+  int64_t want = 0;
+  for (int64_t q = 0; q < complete; ++q) want += (!mask || mask[q]) ? 1 : 0;
+  const int64_t usable = c.optional_pages - c.admission_reserve_pages;
+  if (p->used + want > usable) {
+    if (deficit) *deficit = p->used + want - usable;
+    return DHS_EWOULDWAIT;
+  }
+  // tail ring <- rows [max(0, N-T), N)
+  const int64_t T = c.tail_rows, rb = c.row_bytes;
+  const int64_t lo = std::max<int64_t>(0, n_rows - T);
+  int64_t row = lo;
+  while (row < n_rows) {
+    const int64_t slot = row % T;
+    const int64_t run = std::min(n_rows - row, T - slot);
+    cudaError_t e = cudaMemcpyAsync((uint8_t*)c.tail_dev + ((size_t)pair * T + slot) * rb,
+                                    (uint8_t*)host_rows + (size_t)row * rb, run * rb,
+                                    cudaMemcpyHostToDevice, p->stream);
+    if (e != cudaSuccess) return DHS_ECUDA;
+    row += run;
+  }
+  int32_t* pm = p->map_host.data() + pair * p->pmax;
+  for (int64_t q = 0; q < complete; ++q) {
+    if (mask && !mask[q]) continue;
+    const int64_t slot = lowest_free_slot(p);
+    p->slot_pair[slot] = (int32_t)pair;
+    p->slot_page[slot] = (int32_t)q;
+    p->used += 1;
+    pm[q] = (int32_t)slot;
+    s.pending.push_back((int32_t)q);
+  }
+  if (want) {
+    p->any_pending = true;
+    mark_dirty(p, pair);
+  }
+  s.admitted = true;
+  s.N = n_rows;
+  s.L = n_rows;
+  s.host = (uint8_t*)host_rows;
+  s.host_dev = (uint8_t*)hdev;
+  return DHS_OK;
+}
+
+int dhs_reclaim(dhs_pool* p, const int32_t* order, int32_t n, int64_t deficit,
+                int64_t* freed) {
+  if (freed) *freed = 0;
+  if (!p || n < 0 || deficit < 0 || (n > 0 && !order)) return DHS_EINVAL;
+  for (int32_t i = 0; i < n; ++i)
+    if (order[i] < 0 || order[i] >= p->cfg.max_requests) return DHS_EINVAL;
+  int64_t avail = 0;
+  std::vector<uint8_t> counted((size_t)p->cfg.max_requests, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    if (counted[order[i]]) continue;
+    counted[order[i]] = 1;
+    avail += request_pages(p, order[i]);
+  }
+  if (avail < deficit) return DHS_EWOULDWAIT;
+  int64_t got = 0;
+  for (int32_t i = 0; i < n && got < deficit; ++i)
+    for (int32_t s = 0; s < p->cfg.sources; ++s)
+      got += drop_pages(p, (int64_t)order[i] * p->cfg.sources + s);
+  if (freed) *freed = got;
+  return DHS_OK;
+}
+
+int dhs_release(dhs_pool* p, int32_t req) {
+  if (!p || req < 0 || req >= p->cfg.max_requests) return DHS_EINVAL;
+  int rc = enter(p);
+  if (rc) return rc;
+  const int64_t B = p->cfg.hot_rows;
+  for (int32_t s = 0; s < p->cfg.sources; ++s) {
+    const int64_t pair = (int64_t)req * p->cfg.sources + s;
+    drop_pages(p, pair);
+    p->ps[pair] = PairState();
+  }
+  const int64_t pair0 = (int64_t)req * p->cfg.sources;
+  cudaError_t e = cudaMemsetAsync(p->tags + pair0 * B, 0xFF, p->cfg.sources * B * 4, p->stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(p->stamps + pair0 * B, 0, p->cfg.sources * B * 4, p->stream);
+  return cuda_rc(e);
+}
+
+int dhs_append(dhs_pool* p, const dhs_append_item* items, int32_t n_items) {
+  if (!p || n_items < 0 || (n_items > 0 && !items)) return DHS_EINVAL;
+  const dhs_pool_config& c = p->cfg;
+  std::fill(p->seen.begin(), p->seen.end(), 0);
+  for (int32_t i = 0; i < n_items; ++i) {
+    const dhs_append_item& it = items[i];
+    if (it.req < 0 || it.req >= c.max_requests || it.src < 0 || it.src >= c.sources)
+      return DHS_EINVAL;
+    if (it.count < 0 || it.count > c.tail_rows) return DHS_EINVAL;
+    if (it.count > 0 && !it.rows_dev) return DHS_EINVAL;
+    const int64_t pair = (int64_t)it.req * c.sources + it.src;
+    if (p->seen[pair]) return DHS_EINVAL;
+    p->seen[pair] = 1;
+    const PairState& s = p->ps[pair];
+    if (!s.admitted) return DHS_ESTATE;
+    if (s.L + it.count > c.max_rows_per_request) return DHS_EINVAL;
+  }
+  int rc = enter(p);
+  if (rc) return rc;
+  p->aitems.clear();
+  for (int32_t i = 0; i < n_items; ++i) {
+    const dhs_append_item& it = items[i];
+    if (it.count == 0) continue;
+    const int64_t pair = (int64_t)it.req * c.sources + it.src;
+    PairState& s = p->ps[pair];
+    dhs::AppendItem a;
+    a.rows = (const uint8_t*)it.rows_dev;
+    a.host = s.host_dev;
+    a.L0 = s.L;
+    a.pair = (int32_t)pair;
+    a.count = it.count;
+    p->aitems.push_back(a);
+    s.L += it.count;
+  }
+  dhs::AppendCommon ac{};
+  ac.tail = (uint8_t*)c.tail_dev;
+  ac.T = c.tail_rows;
+  ac.row_bytes = c.row_bytes;
+  for (size_t b = 0; b < p->aitems.size(); b += dhs::kAppendItemsMax) {
+    const int n = (int)std::min<size_t>(dhs::kAppendItemsMax, p->aitems.size() - b);
+    if (dhs::launch_append(ac, p->aitems.data() + b, n, p->stream) != cudaSuccess)
+      return DHS_ECUDA;
+  }
+  return DHS_OK;
+}
+
+static int validate_step(dhs_pool* p, const dhs_step* st, bool resolving) {
+  if (!p || !st || st->n_items < 0 || (st->n_items > 0 && !st->items)) return DHS_EINVAL;
+  if (resolving && st->step == 0) return DHS_EINVAL;
+  const dhs_pool_config& c = p->cfg;
+  if (resolving) std::fill(p->seen.begin(), p->seen.end(), 0);
+  for (int32_t i = 0; i < st->n_items; ++i) {
+    const dhs_item& it = st->items[i];
+    if (it.queries < 0 || it.topk < 0) return DHS_EINVAL;
+    const int64_t n = (int64_t)it.queries * it.topk;
+    if (n > INT32_MAX) return DHS_EINVAL;
+    if (n > 0 && !it.loc_dev) return DHS_EINVAL;
+    if (!resolving) {
+      if (n > 0 && !it.staging_dev) return DHS_EINVAL;
+      continue;
+    }
+    if (it.flags & DHS_ITEM_GATHER_ONLY) continue;
+    if (it.queries > c.max_queries || it.topk > c.max_topk) return DHS_EINVAL;
+    if (it.req < 0 || it.req >= c.max_requests || it.src < 0 || it.src >= c.sources)
+      return DHS_EINVAL;
+    if (n > 0 && !it.sel_dev) return DHS_EINVAL;
+    const int64_t pair = (int64_t)it.req * c.sources + it.src;
+    if (p->seen[pair]) return DHS_EINVAL;
+    p->seen[pair] = 1;
+    if (!p->ps[pair].admitted) return DHS_ESTATE;
+  }
+  return DHS_OK;
+}
+
+int dhs_resolve(dhs_pool* p, const dhs_step* st) {
+  int rc = validate_step(p, st, true);
+  if (rc) return rc;
+  if ((rc = enter(p))) return rc;
+  if ((rc = flush(p))) return rc;
+  const dhs_pool_config& c = p->cfg;
+  p->ritems.clear();
+  p->citems.clear();
+  for (int32_t i = 0; i < st->n_items; ++i) {
+    const dhs_item& it = st->items[i];
+    if (it.flags & DHS_ITEM_GATHER_ONLY) continue;
+    const int64_t pair = (int64_t)it.req * c.sources + it.src;
+    const PairState& s = p->ps[pair];
+    dhs::ResolveItem r{};
+    r.sel = it.sel_dev;
+    r.loc = it.loc_dev;
+    r.counters = it.counters_dev;
+    r.L = s.L;
+    r.N = s.N;
+    r.pair = (int32_t)pair;
+    r.n = it.queries * it.topk;
+    p->ritems.push_back(r);
+    dhs::CopyItem ci{};
+    ci.host = s.host_dev;
+    ci.pair = (int32_t)pair;
+    p->citems.push_back(ci);
+  }
+  dhs::ResolveCommon rcm{};
+  rcm.tags = p->tags;
+  rcm.stamps = p->stamps;
+  rcm.map = p->map;
+  rcm.miss_rows = p->miss_rows;
+  rcm.miss_slots = p->miss_slots;
+  rcm.miss_count = p->miss_count;
+  rcm.pair_status = p->pair_status;
+  rcm.status = p->status;
+  rcm.T = c.tail_rows;
+  rcm.B = c.hot_rows;
+  rcm.Pmax = (int32_t)p->pmax;
+  rcm.Mcap = (int32_t)p->mcap;
+  rcm.page_shift = p->page_shift;
+  rcm.step = st->step;
+  dhs::CopyCommon ccm{};
+  ccm.hot = (uint8_t*)c.hot_dev;
+  ccm.miss_rows = p->miss_rows;
+  ccm.miss_slots = p->miss_slots;
+  ccm.miss_count = p->miss_count;
+  ccm.B = c.hot_rows;
+  ccm.Mcap = (int32_t)p->mcap;
+  ccm.row_bytes = c.row_bytes;
+  const size_t nr = p->ritems.size();
+  for (size_t b = 0; b < nr; b += dhs::kResolveItemsLarge) {
+    const int n = (int)std::min<size_t>(dhs::kResolveItemsLarge, nr - b);
+    int64_t wmax = 0, qmax = 0, requests = 0, last_req = -1;
+    for (int i = 0; i < n; ++i) {
+      const dhs::ResolveItem& r = p->ritems[b + i];
+      wmax = std::max<int64_t>(wmax, (r.L + 63) / 64);
+      qmax = std::max<int64_t>(qmax, std::min<int64_t>(r.n, r.L));
+      const int64_t req = r.pair / c.sources;
+      if (req != last_req) ++requests;
+      last_req = req;
+    }
+    rcm.w64cap = (int32_t)wmax;
+    rcm.qkcap = (int32_t)qmax;
+    const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows);
+    if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, smem, p->stream) != cudaSuccess)
+      return DHS_ECUDA;
+    int ctas = p->copy_ctas;
+    if (ctas <= 0) ctas = (int)std::min<int64_t>(32, std::max<int64_t>(4, requests / 4));
+    if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, ctas, p->stream) != cudaSuccess)
+      return DHS_ECUDA;
+  }
+  return DHS_OK;
+}
+
+int dhs_gather(dhs_pool* p, const dhs_step* st) {
+  int rc = validate_step(p, st, false);
+  if (rc) return rc;
+  if ((rc = enter(p))) return rc;
+  if ((rc = flush(p))) return rc;
+  const dhs_pool_config& c = p->cfg;
+  dhs::GatherCommon g{};
+  g.tail = (const uint8_t*)c.tail_dev;
+  g.opt = (const uint8_t*)c.opt_dev;
+  g.hot = (const uint8_t*)c.hot_dev;
+  g.tail_rows = (uint32_t)(p->pairs * c.tail_rows);
+  g.opt_rows = (uint32_t)(c.optional_pages * c.page_rows);
+  g.hot_rows = (uint32_t)(p->pairs * c.hot_rows);
+  g.row_bytes = c.row_bytes;
+  g.status = p->status;
+  p->gitems.clear();
+  for (int32_t i = 0; i < st->n_items; ++i) {
+    const dhs_item& it = st->items[i];
+    const int32_t n = it.queries * it.topk;
+    if (n == 0) continue;
+    dhs::GatherItem gi{};
+    gi.loc = it.loc_dev;
+    gi.staging = (uint8_t*)it.staging_dev;
+    gi.n = n;
+    p->gitems.push_back(gi);
+  }
+  const size_t ng = p->gitems.size();
+  for (size_t b = 0; b < ng; b += dhs::kGatherItemsLarge) {
+    const int n = (int)std::min<size_t>(dhs::kGatherItemsLarge, ng - b);
+    int64_t tiles = 0;
+    for (int i = 0; i < n; ++i) {
+      dhs::GatherItem& gi = p->gitems[b + i];
+      gi.tile0 = (int32_t)tiles;
+      tiles += (gi.n + dhs::kGatherTileRows - 1) / dhs::kGatherTileRows;
+    }
+    if (tiles > INT32_MAX) return DHS_EINVAL;
+    g.n_tiles = (int32_t)tiles;
+    if (dhs::launch_gather(g, p->gitems.data() + b, n, p->gather_impl, p->stream) !=
+        cudaSuccess)
+      return DHS_ECUDA;
+  }
+  return DHS_OK;
+}
+
+int dhs_resolve_gather(dhs_pool* p, const dhs_step* st) {
+  int rc = dhs_resolve(p, st);
+  if (rc) return rc;
+  return dhs_gather(p, st);
+}
+
+int dhs_status(dhs_pool* p, uint32_t* flags) {
+  if (flags) *flags = 0;
+  if (!p) return DHS_EINVAL;
+  int rc = enter(p);
+  if (rc) return rc;
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, p->status, 4, cudaMemcpyDeviceToHost, p->stream) != cudaSuccess)
+    return DHS_ECUDA;
+  if (cudaStreamSynchronize(p->stream) != cudaSuccess) return DHS_ECUDA;
+  if (v && cudaMemsetAsync(p->status, 0, 4, p->stream) != cudaSuccess) return DHS_ECUDA;
+  if (flags) *flags = v;
+  if (v & (DHS_STATUS_ERANGE | DHS_STATUS_ELOC)) return DHS_ERANGE;
+  if (v & DHS_STATUS_EBUDGET) return DHS_EBUDGET;
+  return DHS_OK;
+}
+
+int dhs_read_state(dhs_pool* p, int32_t req, int32_t src, int32_t* tags, uint32_t* stamps,
+                   int32_t* page_slot, int64_t* info) {
+  if (!p || req < 0 || req >= p->cfg.max_requests || src < 0 || src >= p->cfg.sources)
+    return DHS_EINVAL;
+  int rc = enter(p);
+  if (rc) return rc;
+  const int64_t pair = (int64_t)req * p->cfg.sources + src;
+  const size_t B = (size_t)p->cfg.hot_rows;
+  int32_t st = 0;
+  cudaError_t e = cudaSuccess;
+  if (tags)
+    e = cudaMemcpyAsync(tags, p->tags + pair * B, B * 4, cudaMemcpyDeviceToHost, p->stream);
+  if (e == cudaSuccess && stamps)
+    e = cudaMemcpyAsync(stamps, p->stamps + pair * B, B * 4, cudaMemcpyDeviceToHost, p->stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&st, p->pair_status + pair, 4, cudaMemcpyDeviceToHost, p->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+  if (e != cudaSuccess) return DHS_ECUDA;
+  if (page_slot)
+    std::memcpy(page_slot, p->map_host.data() + pair * p->pmax, (size_t)p->pmax * 4);
+  if (info) {
+    const PairState& s = p->ps[pair];
+    info[0] = s.N;
+    info[1] = s.L;
+    info[2] = s.admitted ? 1 : 0;
+    info[3] = st;
+  }
+  return DHS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,505 @@
+// Resolve kernel: one CTA per (request, KV source) item of a decode step.
+//
+// "Adaptive DHiSparse: Speculative Decoding over a Load-Adaptive KV
+// Hierarchy", How it works / Resolution: the resolver checks, in order,
+// (1) the tail and the ready optional-history map, (2) a scan of the hot
+// cache bounded by B with LRU replacement, (3) a copy from pinned host memory
+// into the hot cache, stopping once every selected row is found.
+// Speculative state: verification queries share missing-row retrieval.
+//
+// GB300 design.  Everything for one item lives in shared memory:
+//   * the union of the Q verify queries is a bitmap over [0, L) (64 rows per
+//     word, one optional page per word at 64-row pages), so dedup and
+//     ascending order come from the bit positions -- no sort of Q*k ids;
+//   * step 1 masks whole words: tail rows by comparison with L-T, optional
+//     rows by one page-map read per non-empty word;
+//   * step 2 inverts the tag scan: each of the B hot slots tests its tag
+//     against the bitmap once (O(B), never more than B probes; tags are
+//     unique so the matching slot is the one a linear scan would find);
+//   * ranks of unresolved rows come from a block prefix scan of per-word
+//     popcounts; misses keep ascending row order by construction;
+//   * LRU victims: unprotected slots compacted in slot order, then a stable
+//     LSD radix sort on (stamp - min stamp) over only the bits that vary --
+//     the first m entries are the m smallest (stamp, slot) keys, which is
+//     exactly what evicting one least-recently-used slot at a time for each
+//     miss in ascending row order picks;
+//   * the misses' (row, slot) pairs go to a global miss list read by the
+//     host-copy kernel; locations and counters are written last.
+// State (tags, stamps) is written only after the budget check passes, so a
+// failing item changes nothing.
+#include "dhs_internal.h"
+
+namespace dhs {
+namespace {
+
+struct Smem {
+  uint64_t* bm;       // [w64cap] selection bitmap, then unresolved-row bitmap
+  uint32_t* wpre;     // [w64cap] popcount, then exclusive prefix
+  uint32_t* st;       // [B] working stamps
+  int32_t* cand_row;  // [qkcap] unresolved rows by rank (ascending)
+  uint16_t* slot_of;  // [qkcap] hot slot of each unresolved rank, 0xFFFF = miss
+  uint16_t* sort_a;   // [B]
+  uint16_t* sort_b;   // [B]
+};
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+__host__ __device__ inline size_t carve(int w64cap, int qkcap, int B, Smem* s,
+                                        unsigned char* base) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align16(off + bytes);
+    return base + o;
+  };
+  unsigned char* p0 = take(sizeof(uint64_t) * (size_t)w64cap);
+  unsigned char* p1 = take(sizeof(uint32_t) * (size_t)w64cap);
+  unsigned char* p2 = take(sizeof(uint32_t) * (size_t)B);
+  unsigned char* p3 = take(sizeof(int32_t) * (size_t)qkcap);
+  unsigned char* p4 = take(sizeof(uint16_t) * (size_t)qkcap);
+  unsigned char* p5 = take(sizeof(uint16_t) * (size_t)B);
+  unsigned char* p6 = take(sizeof(uint16_t) * (size_t)B);
+  if (s) {
+    s->bm = (uint64_t*)p0;
+    s->wpre = (uint32_t*)p1;
+    s->st = (uint32_t*)p2;
+    s->cand_row = (int32_t*)p3;
+    s->slot_of = (uint16_t*)p4;
+    s->sort_a = (uint16_t*)p5;
+    s->sort_b = (uint16_t*)p6;
+  }
+  return off;
+}
+
+// ---------------------------------------------------------------- block ops
+// scratch: 33 uint32 words per independent reduction lane.
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Exclusive prefix of v over the block; *total = block sum.
+__device__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  uint32_t inc = warp_incl_scan(v);
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < nw ? scratch[lane] : 0u;
+    uint32_t wi = warp_incl_scan(w);
+    if (lane < nw) scratch[lane] = wi - w;
+    if (lane == 31) scratch[32] = wi;
+  }
+  __syncthreads();
+  uint32_t r = scratch[warp] + inc - v;
+  *total = scratch[32];
+  __syncthreads();
+  return r;
+}
+
+// Sums of four values over the block in one pass.
+__device__ void block_sum4(uint32_t v[4], uint32_t* scratch /*[4*33]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[i] += __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
+    if (lane == 0) scratch[i * 33 + warp] = v[i];
+  }
+  __syncthreads();
+  if (warp < 4) {
+    uint32_t x = lane < nw ? scratch[warp * 33 + lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    if (lane == 0) scratch[warp * 33 + 32] = x;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = scratch[i * 33 + 32];
+  __syncthreads();
+}
+
+// {sum a, max b, min c, max d} over the block.
+__device__ void block_smmm(uint32_t v[4], uint32_t* scratch /*[4*33]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
+    v[1] = max(v[1], __shfl_xor_sync(0xFFFFFFFFu, v[1], o));
+    v[2] = min(v[2], __shfl_xor_sync(0xFFFFFFFFu, v[2], o));
+    v[3] = max(v[3], __shfl_xor_sync(0xFFFFFFFFu, v[3], o));
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) scratch[i * 33 + warp] = v[i];
+  }
+  __syncthreads();
+  if (warp < 4) {
+    const uint32_t ident = warp == 2 ? 0xFFFFFFFFu : 0u;
+    uint32_t x = lane < nw ? scratch[warp * 33 + lane] : ident;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, o);
+      x = warp == 0 ? x + y : (warp == 2 ? min(x, y) : max(x, y));
+    }
+    if (lane == 0) scratch[warp * 33 + 32] = x;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = scratch[i * 33 + 32];
+  __syncthreads();
+}
+
+// In-place exclusive scan of a[0, n); returns the total.
+__device__ uint32_t block_scan_array(uint32_t* a, int n, uint32_t* scratch) {
+  const int per = (n + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int b = (int)threadIdx.x * per;
+  const int e = min(n, b + per);
+  uint32_t s = 0;
+  for (int i = b; i < e; ++i) s += a[i];
+  uint32_t total;
+  uint32_t pre = block_excl_scan(s, scratch, &total);
+  for (int i = b; i < e; ++i) {
+    uint32_t t = a[i];
+    a[i] = pre;
+    pre += t;
+  }
+  __syncthreads();
+  return total;
+}
+
+// ---------------------------------------------------------------- masks
+
+// Rows of word w (rows 64w .. 64w+63) that lie in the tail [t0, ...).
+__device__ __forceinline__ uint64_t tail_mask(int w, int64_t t0) {
+  const int64_t lo = (int64_t)w << 6;
+  if (lo >= t0) return ~0ull;
+  if (lo + 63 < t0) return 0ull;
+  return ~0ull << (int)(t0 - lo);
+}
+
+// Rows of word w in complete imported pages whose optional slot is ready.
+__device__ __forceinline__ uint64_t opt_mask(int w, int64_t N, const int32_t* map,
+                                             int ps) {
+  const int64_t lo = (int64_t)w << 6;
+  if (ps >= 6) {
+    const int64_t page = lo >> ps;
+    return (((page + 1) << ps) <= N && map[page] >= 0) ? ~0ull : 0ull;
+  }
+  const int rows = 1 << ps;
+  const uint64_t one = (rows == 64) ? ~0ull : ((1ull << rows) - 1ull);
+  uint64_t m = 0;
+  for (int i = 0; i < (64 >> ps); ++i) {
+    const int64_t page = (lo >> ps) + i;
+    if (((page + 1) << ps) <= N && map[page] >= 0) m |= one << (i * rows);
+  }
+  return m;
+}
+
+// Write the failure result of one item: no state change.
+__device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t code,
+                          uint32_t flag) {
+  for (int e = threadIdx.x; e < it.n; e += blockDim.x) it.loc[e] = kNoLoc;
+  if (threadIdx.x < 8 && it.counters) it.counters[threadIdx.x] = 0u;
+  if (threadIdx.x == 0) {
+    c.miss_count[it.pair] = 0u;
+    c.pair_status[it.pair] = code;
+    atomicOr(c.status, flag);
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int MAXI>
+struct ResolveParams {
+  ResolveCommon c;
+  ResolveItem items[MAXI];
+};
+
+template <int MAXI>
+__global__ void __launch_bounds__(kResolveThreads, 1)
+    resolve_kernel(const __grid_constant__ ResolveParams<MAXI> P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ uint32_t scratch[4 * 33];
+  __shared__ int s_bad;
+
+  const ResolveCommon& c = P.c;
+  const ResolveItem& it = P.items[blockIdx.x];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int B = c.B;
+  const int64_t T = c.T;
+  const int64_t L = it.L, N = it.N;
+  const int64_t t0 = L - T;
+  const int n = it.n;
+  const int W = (int)((L + 63) >> 6);
+  const uint32_t step = c.step;
+  const int pair = it.pair;
+  int32_t* tags = c.tags + (size_t)pair * B;
+  uint32_t* stamps = c.stamps + (size_t)pair * B;
+  const int32_t* map = c.map + (size_t)pair * c.Pmax;
+
+  Smem s;
+  carve(c.w64cap, c.qkcap, B, &s, smem_raw);
+
+  // ---- union of the verify block as a bitmap; range check
+  for (int w = tid; w < W; w += nt) s.bm[w] = 0ull;
+  for (int j = tid; j < B; j += nt) s.st[j] = stamps[j];
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  for (int e = tid; e < n; e += nt) {
+    const int32_t row = it.sel[e];
+    if (row < 0 || (int64_t)row >= L) {
+      s_bad = 1;
+    } else {
+      atomicOr((unsigned long long*)&s.bm[row >> 6], 1ull << (row & 63));
+    }
+  }
+  __syncthreads();
+  if (s_bad) {
+    fail_item(c, it, kErrRange, kStatusErange);
+    return;
+  }
+
+  // ---- step 1: tail and ready optional map, word by word
+  uint32_t cnt[4] = {0u, 0u, 0u, 0u};  // unique, tail, opt, -
+  for (int w = tid; w < W; w += nt) {
+    const uint64_t bits = s.bm[w];
+    uint64_t cand = 0ull;
+    if (bits) {
+      const uint64_t tm = bits & tail_mask(w, t0);
+      const uint64_t rest = bits & ~tm;
+      const uint64_t om = rest ? (rest & opt_mask(w, N, map, c.page_shift)) : 0ull;
+      cand = rest & ~om;
+      cnt[0] += __popcll(bits);
+      cnt[1] += __popcll(tm);
+      cnt[2] += __popcll(om);
+    }
+    s.bm[w] = cand;
+    s.wpre[w] = (uint32_t)__popcll(cand);
+  }
+  block_sum4(cnt, scratch);
+  const uint32_t n_unique = cnt[0], n_tail = cnt[1], n_opt = cnt[2];
+  const uint32_t C = block_scan_array(s.wpre, W, scratch);  // unresolved rows
+
+  // rank -> row for the unresolved rows (ascending)
+  for (int w = tid; w < W; w += nt) {
+    uint64_t m = s.bm[w];
+    uint32_t r = s.wpre[w];
+    while (m) {
+      const int b = __ffsll((long long)m) - 1;
+      m &= m - 1;
+      s.cand_row[r] = (w << 6) + b;
+      s.slot_of[r] = 0xFFFFu;
+      ++r;
+    }
+  }
+  __syncthreads();
+
+  // ---- step 2: every hot slot tests its tag once (B probes in total)
+  uint32_t hv[4] = {0u, 0u, 0xFFFFFFFFu, 0u};  // hits, max probes, -, -
+  if (C) {
+    for (int j = tid; j < B; j += nt) {
+      const int32_t t = tags[j];
+      if (t >= 0 && (int64_t)t < L) {
+        const uint64_t m = s.bm[t >> 6];
+        const uint64_t bit = 1ull << (t & 63);
+        if (m & bit) {
+          const uint32_t r = s.wpre[t >> 6] + (uint32_t)__popcll(m & (bit - 1ull));
+          s.slot_of[r] = (uint16_t)j;
+          s.st[j] = step;
+          hv[0] += 1u;
+          hv[1] = max(hv[1], (uint32_t)(j + 1));
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // unprotected slots and their stamp range
+  uint32_t uv[4] = {0u, 0u, 0xFFFFFFFFu, 0u};  // count, -, min stamp, max stamp
+  for (int j = tid; j < B; j += nt) {
+    const uint32_t x = s.st[j];
+    if (x != step) {
+      uv[0] += 1u;
+      uv[2] = min(uv[2], x);
+      uv[3] = max(uv[3], x);
+    }
+  }
+  uint32_t red[4] = {hv[0], hv[1], uv[2], uv[3]};
+  // hits and max probes, min/max stamps
+  block_smmm(red, scratch);
+  uint32_t cnt2[4] = {uv[0], 0u, 0u, 0u};
+  block_sum4(cnt2, scratch);
+  const uint32_t hits = red[0];
+  const uint32_t m_miss = C - hits;
+  const uint32_t unprot = cnt2[0];
+  uint32_t scan_max = red[1];
+  if (m_miss) scan_max = (uint32_t)B;
+
+  if (m_miss > unprot) {  // more missing rows than victims: change nothing
+    fail_item(c, it, kErrBudget, kStatusEbudget);
+    return;
+  }
+
+  // ---- step 3 victims: the m smallest (stamp, slot) among unprotected slots
+  uint32_t evicted = 0u;
+  if (m_miss) {
+    // stable compaction of unprotected slots, ascending slot order
+    {
+      const int per = (B + nt - 1) / nt;
+      const int b = tid * per, e = min(B, b + per);
+      uint32_t u = 0;
+      for (int j = b; j < e; ++j) u += s.st[j] != step;
+      uint32_t tot;
+      uint32_t pos = block_excl_scan(u, scratch, &tot);
+      for (int j = b; j < e; ++j)
+        if (s.st[j] != step) s.sort_a[pos++] = (uint16_t)j;
+      __syncthreads();
+    }
+    const uint32_t kmin = red[2];
+    const uint32_t span = red[3] - kmin;
+    const int nbits = span ? 32 - __clz(span) : 0;
+    uint16_t* src = s.sort_a;
+    uint16_t* dst = s.sort_b;
+    const int U = (int)unprot;
+    const int per = (U + nt - 1) / nt;
+    const int b = tid * per, e = min(U, b + per);
+    for (int bit = 0; bit < nbits; ++bit) {  // stable LSD split per bit
+      uint32_t z = 0;
+      for (int i = b; i < e; ++i) z += !(((s.st[src[i]] - kmin) >> bit) & 1u);
+      uint32_t ztot;
+      uint32_t zpos = block_excl_scan(z, scratch, &ztot);
+      uint32_t opos = ztot + (uint32_t)max(b, 0) - zpos;
+      for (int i = b; i < e; ++i) {
+        const uint16_t v = src[i];
+        if (((s.st[v] - kmin) >> bit) & 1u) dst[opos++] = v;
+        else dst[zpos++] = v;
+      }
+      __syncthreads();
+      uint16_t* t = src;
+      src = dst;
+      dst = t;
+    }
+    // i-th missing row (ascending) -> i-th victim
+    {
+      const int perc = ((int)C + nt - 1) / nt;
+      const int cb = tid * perc, ce = min((int)C, cb + perc);
+      uint32_t mm = 0;
+      for (int i = cb; i < ce; ++i) mm += s.slot_of[i] == 0xFFFFu;
+      uint32_t mtot;
+      uint32_t mr = block_excl_scan(mm, scratch, &mtot);
+      int32_t* mrows = c.miss_rows + (size_t)pair * c.Mcap;
+      int32_t* mslots = c.miss_slots + (size_t)pair * c.Mcap;
+      for (int i = cb; i < ce; ++i) {
+        if (s.slot_of[i] != 0xFFFFu) continue;
+        const int v = src[mr];
+        const int32_t row = s.cand_row[i];
+        evicted += tags[v] != -1;
+        tags[v] = row;
+        s.st[v] = step;
+        s.slot_of[i] = (uint16_t)v;
+        mrows[mr] = row;
+        mslots[mr] = v;
+        ++mr;
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- commit stamps of every slot hit or filled in this step
+  for (int j = tid; j < B; j += nt)
+    if (s.st[j] == step) stamps[j] = step;
+
+  // ---- location vector
+  const int ps = c.page_shift;
+  const int64_t pmask = ((int64_t)1 << ps) - 1;
+  for (int e = tid; e < n; e += nt) {
+    const int32_t row = it.sel[e];
+    uint32_t loc;
+    if ((int64_t)row >= t0) {
+      loc = (kTierTail << 30) | (uint32_t)((int64_t)pair * T + (int64_t)row % T);
+    } else {
+      const uint64_t m = s.bm[row >> 6];
+      const uint64_t bit = 1ull << (row & 63);
+      if (m & bit) {
+        const uint32_t r = s.wpre[row >> 6] + (uint32_t)__popcll(m & (bit - 1ull));
+        loc = (kTierHot << 30) | (uint32_t)((int64_t)pair * B + s.slot_of[r]);
+      } else {
+        const int32_t slot = map[row >> ps];
+        loc = (kTierOpt << 30) | (uint32_t)(((int64_t)slot << ps) + (row & pmask));
+      }
+    }
+    it.loc[e] = loc;
+  }
+
+  uint32_t ev[4] = {evicted, 0u, 0u, 0u};
+  block_sum4(ev, scratch);
+  if (tid == 0) {
+    if (it.counters) {
+      it.counters[0] = (uint32_t)n;
+      it.counters[1] = n_unique;
+      it.counters[2] = n_tail;
+      it.counters[3] = n_opt;
+      it.counters[4] = hits;
+      it.counters[5] = m_miss;
+      it.counters[6] = scan_max;
+      it.counters[7] = ev[0];
+    }
+    c.miss_count[pair] = m_miss;
+    c.pair_status[pair] = 0;
+  }
+}
+
+template <int MAXI>
+cudaError_t launch_t(const ResolveCommon& c, const ResolveItem* items, int n,
+                     size_t smem, cudaStream_t stream) {
+  ResolveParams<MAXI> P;
+  P.c = c;
+  P.c.n_items = n;
+  for (int i = 0; i < n; ++i) P.items[i] = items[i];
+  resolve_kernel<MAXI><<<n, kResolveThreads, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t resolve_smem_bytes(int w64cap, int qkcap, int B) {
+  return carve(w64cap, qkcap, B, nullptr, nullptr);
+}
+
+cudaError_t resolve_set_smem_limit(size_t bytes) {
+  // The attribute is per function and device; only ever raise it, so a
+  // smaller pool created later never breaks a larger one.
+  static int device_limit[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    if ((int)bytes <= device_limit[dev]) return cudaSuccess;
+    device_limit[dev] = (int)bytes;
+  }
+  e = cudaFuncSetAttribute(resolve_kernel<kResolveItemsSmall>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(resolve_kernel<kResolveItemsLarge>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,
+                           int n_items, size_t smem, cudaStream_t stream) {
+  if (n_items <= 0) return cudaSuccess;
+  if (n_items <= kResolveItemsSmall)
+    return launch_t<kResolveItemsSmall>(c, items, n_items, smem, stream);
+  return launch_t<kResolveItemsLarge>(c, items, n_items, smem, stream);
+}
+
+}  // namespace dhs

@@ -1,0 +1,153 @@
+"""Drive a synthetic workload through libdhs on one GPU.
+
+Layout in HBM (all caller-owned, allocated once through torch):
+  * the pool's four arenas (hot cache, tail ring, optional pages, metadata);
+  * every step's selections, resident: int32 [steps][R][S_sel][Q][k];
+  * every step's appended decode rows: [steps][R*S][a_max][row_bytes];
+  * one location vector set uint32 [R][S][Q][k], one counter set
+    uint32 [R][S][8] and one staging buffer [R][layers][Q][k][row_bytes],
+    rewritten every step.
+Pinned host memory: one registered buffer [R*S][max_rows][row_bytes] holding
+every (request, source)'s imported rows, with room for the decode rows the
+library writes through.
+
+A decode step (``step``) is one ``dhs_append`` (every source's new rows)
+and one ``dhs_resolve_gather`` over R x layers items: each source's own
+resolution, then the gathers of all layers, Reuse layers gathering source
+0's location vector as DHS_ITEM_GATHER_ONLY items.  The ctypes descriptors
+of every step are built before the first step, so a step costs two C calls.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from dhs_workload.configs import Config, Workload, drive_admission
+
+from . import dhs
+
+
+class _Admit:
+    def __init__(self, run):
+        self.run = run
+
+    def admit(self, r, s, mask):
+        rc, d = self.run.pool.admit(r, s, self.run.host_ptr(r, s), self.run.cfg.history, mask)
+        return dhs.RC_NAMES[rc], d
+
+    def reclaim(self, order, deficit):
+        rc, f = self.run.pool.reclaim(order, deficit)
+        return dhs.RC_NAMES[rc], f
+
+
+class GpuRun:
+    def __init__(self, cfg: Config, wl: Workload | None = None, device="cuda",
+                 host_threads=None):
+        self.cfg = c = cfg
+        self.wl = wl or Workload(cfg)
+        self.device = torch.device(device)
+        torch.cuda.set_device(self.device)
+        self.layers = [("resolve", s) for s in range(c.sources)] + \
+            [("reuse", 0)] * c.reuse_layers
+        self.pool = dhs.Pool(
+            max_requests=c.requests, sources=c.sources, row_bytes=c.row_bytes,
+            page_rows=c.page_rows, tail_rows=c.tail, hot_rows=c.hot,
+            max_queries=c.queries, max_topk=c.topk, max_rows_per_request=c.max_rows,
+            optional_pages=c.pool_pages(), device=self.device)
+        rb = c.row_bytes
+        self.host = dhs.HostRows(c.pairs * c.max_rows * rb)
+        self.wl.fill_host_rows(self.host.ptr, c.max_rows, nthreads=host_threads)
+        drive_admission(_Admit(self), c, self.wl)
+
+        dev = self.device
+        Q, k = c.queries, c.topk
+        sel = self.wl.selections()
+        self.sel = torch.from_numpy(sel).to(dev)
+        self.loc = torch.empty((c.requests, c.sources, Q, k), dtype=torch.int32, device=dev)
+        self.counters = torch.zeros((c.requests, c.sources, 8), dtype=torch.int32, device=dev)
+        self.staging = torch.empty((c.requests, len(self.layers), Q, k, c.row_elems),
+                                   dtype=torch.bfloat16, device=dev)
+        # appended rows of every step
+        a_hi = c.append_hi
+        self.app_rows = torch.zeros((c.total_steps, c.pairs, a_hi, c.row_elems),
+                                    dtype=torch.int16, device=dev)
+        pairs = [(r, s) for r in range(c.requests) for s in range(c.sources)]
+        for step in range(1, c.total_steps + 1):
+            _, rows = self.wl.appended_rows(step, pairs)
+            self.app_rows[step - 1].copy_(torch.from_numpy(rows.view(np.int16)))
+        self._build_descriptors()
+        torch.cuda.synchronize(dev)
+
+    def host_ptr(self, r, s):
+        c = self.cfg
+        return self.host.ptr + (r * c.sources + s) * c.max_rows * c.row_bytes
+
+    def host_rows(self, r, s, row0, n):
+        c = self.cfg
+        base = (r * c.sources + s) * c.max_rows + row0
+        a = self.host.array[base * c.row_bytes:(base + n) * c.row_bytes]
+        return a.view(np.uint16).reshape(n, c.row_elems)
+
+    # ---------------------------------------------------------- descriptors
+    def _build_descriptors(self):
+        c = self.cfg
+        Q, k, rb = c.queries, c.topk, c.row_bytes
+        self._steps, self._appends = [], []
+        loc0 = self.loc.data_ptr()
+        cnt0 = self.counters.data_ptr()
+        stg0 = self.staging.data_ptr()
+        nsel = 1 if c.shared_selection else c.sources
+        for step in range(1, c.total_steps + 1):
+            items = []
+            for r in range(c.requests):
+                for layer, (kind, s) in enumerate(self.layers):
+                    it = dhs.dhs_item()
+                    it.req, it.src, it.queries, it.topk = r, s, Q, k
+                    it.flags = dhs.DHS_ITEM_GATHER_ONLY if kind == "reuse" else 0
+                    ss = 0 if c.shared_selection else s
+                    it.sel_dev = self.sel[step - 1, r, ss].data_ptr()
+                    it.loc_dev = loc0 + ((r * c.sources + s) * Q * k) * 4
+                    it.counters_dev = cnt0 + (r * c.sources + s) * 32
+                    it.staging_dev = stg0 + ((r * len(self.layers) + layer) * Q * k) * rb
+                    items.append(it)
+            self._steps.append(dhs.make_step(step, items))
+            apps = []
+            for i, (r, s) in enumerate((r, s) for r in range(c.requests)
+                                       for s in range(c.sources)):
+                a = dhs.dhs_append_item()
+                a.req, a.src = r, s
+                a.count = int(self.wl.append[r, step - 1])
+                a.rows_dev = self.app_rows[step - 1, i].data_ptr()
+                apps.append(a)
+            arr = (dhs.dhs_append_item * len(apps))(*apps)
+            self._appends.append((arr, len(apps)))
+        del nsel
+
+    # ---------------------------------------------------------- stepping
+    def append(self, step):
+        arr, n = self._appends[step - 1]
+        dhs.check(dhs.lib.dhs_append(self.pool.h, arr, n), "dhs_append")
+
+    def resolve(self, step):
+        st, _ = self._steps[step - 1]
+        dhs.check(dhs.lib.dhs_resolve(self.pool.h, ctypes.byref(st)), "dhs_resolve")
+
+    def gather(self, step):
+        st, _ = self._steps[step - 1]
+        dhs.check(dhs.lib.dhs_gather(self.pool.h, ctypes.byref(st)), "dhs_gather")
+
+    def step(self, step):
+        """One decode step: append, then resolve + gather every layer."""
+        self.append(step)
+        st, _ = self._steps[step - 1]
+        dhs.check(dhs.lib.dhs_resolve_gather(self.pool.h, ctypes.byref(st)),
+                  "dhs_resolve_gather")
+
+    def status(self):
+        return self.pool.status()
+
+    def close(self):
+        self.pool.close()
+        self.host.close()

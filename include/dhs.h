@@ -1,0 +1,293 @@
+/*
+ * dhs.h -- C ABI of the GB300 (sm_103a) hierarchical sparse KV resolve +
+ * gather library (libdhs.so).
+ *
+ * The operation is the per-decode-step path of "Adaptive DHiSparse:
+ * Speculative Decoding over a Load-Adaptive KV Hierarchy" (How it works):
+ * each request's top-k selected KV rows are resolved through three ordered
+ * places -- (1) the mutable tail and the ready optional-history page map,
+ * (2) a hot-cache tag scan bounded by B with LRU replacement, (3) a copy from
+ * pinned host memory into the victim hot-cache slot -- and the selected rows
+ * are gathered into a contiguous staging buffer for sparse attention.
+ *
+ * Conventions for every call:
+ *   - Return value: DHS_OK (0) or a negative DHS_E* code.  No call throws,
+ *     aborts or prints.  A call that fails validation changes nothing.
+ *   - Device work is asynchronous and ordered on the pool's stream; no call
+ *     on the hot path (dhs_append, dhs_resolve, dhs_gather,
+ *     dhs_resolve_gather) synchronises the host.
+ *   - Errors found on the device (a selected row outside [0, L), more missing
+ *     rows than unprotected hot slots, a gather location outside its arena)
+ *     cannot be returned by the launching call: they leave the affected
+ *     (request, source) unchanged for that step, write DHS_NO_LOC to all its
+ *     locations and zero to its counters, and set a sticky flag read by
+ *     dhs_status().
+ *   - A pool is not thread-safe: calls on one pool must not overlap.
+ *   - Ownership: the caller owns every device buffer (the four arenas,
+ *     selections, location vectors, staging, counters, appended rows) and
+ *     every pinned host buffer; the library owns only host-side metadata.
+ *
+ * Location encoding: DHS_LOC(tier, index) = (tier << 30) | index, where
+ *   tier DHS_TIER_TAIL: index = pair * tail_rows + row % tail_rows
+ *   tier DHS_TIER_OPT : index = slot * page_rows + row % page_rows
+ *   tier DHS_TIER_HOT : index = pair * hot_rows + hot slot
+ * and pair = req * sources + src.  Row `index` of the tier's arena starts at
+ * byte index * row_bytes.
+ */
+#ifndef DHS_H_
+#define DHS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ error codes */
+#define DHS_OK 0
+#define DHS_EINVAL (-1)     /* bad argument, size, alignment or configuration */
+#define DHS_ENOMEM (-2)     /* host metadata allocation failed */
+#define DHS_EWOULDWAIT (-3) /* capacity cannot be covered: the admission waits */
+#define DHS_EBUDGET (-4)    /* device: more missing rows than unprotected slots */
+#define DHS_ERANGE (-5)     /* device: selected row or location out of range */
+#define DHS_ETIMEDOUT (-6)  /* reserved: a bounded device wait gave up */
+#define DHS_ECUDA (-7)      /* a CUDA runtime call or launch failed */
+#define DHS_ESTATE (-8)     /* request/source not admitted, or already admitted */
+
+/* ------------------------------------------------------------ locations */
+#define DHS_TIER_TAIL 0u
+#define DHS_TIER_OPT 1u
+#define DHS_TIER_HOT 2u
+#define DHS_NO_LOC 0xFFFFFFFFu
+#define DHS_LOC(tier, index) ((((uint32_t)(tier)) << 30) | ((uint32_t)(index)))
+
+/* Per-resolve counters (uint32 each), one block of DHS_NUM_COUNTERS per item:
+ * entries = Q*k; unique = distinct selected rows over the verify block;
+ * tail / opt = distinct rows found in step 1 (tail, optional map);
+ * hot = distinct rows found by the hot-cache scan (step 2);
+ * host = distinct rows copied from pinned host memory (step 3);
+ * scan_max = probes of the longest hot-cache scan (slot + 1 on a hit, B on
+ * a miss; never above B); evicted = victims that held a row. */
+enum {
+  DHS_CNT_ENTRIES = 0,
+  DHS_CNT_UNIQUE,
+  DHS_CNT_TAIL,
+  DHS_CNT_OPT,
+  DHS_CNT_HOT,
+  DHS_CNT_HOST,
+  DHS_CNT_SCAN_MAX,
+  DHS_CNT_EVICTED,
+  DHS_NUM_COUNTERS
+};
+
+/* Sticky device status flags (dhs_status). */
+#define DHS_STATUS_ERANGE 1u  /* a selection held a row outside [0, L) */
+#define DHS_STATUS_EBUDGET 2u /* a resolve needed more victims than slots */
+#define DHS_STATUS_ELOC 4u    /* a gather location pointed outside its arena */
+
+/* ------------------------------------------------------------ pool */
+typedef struct dhs_pool dhs_pool;
+
+/*
+ * Pool geometry ("Memory split": every request and KV source has a fixed hot
+ * cache of B rows, a mutable tail and metadata that are never lent; complete
+ * pages of imported history may sit in reclaimable optional capacity).
+ */
+typedef struct {
+  int32_t max_requests;          /* R: request slots 0..R-1 */
+  int32_t sources;               /* S: KV sources per request (own state + payload) */
+  int32_t row_bytes;             /* bytes per KV row: multiple of 16 (576 bf16 = 1152) */
+  int32_t page_rows;             /* rows per optional page: power of two (64) */
+  int32_t tail_rows;             /* T >= 1: the tail holds rows [L-T, L) */
+  int32_t hot_rows;              /* B in [1, 16384]: hot-cache rows per (req, src) */
+  int32_t max_queries;           /* Q: verify queries per resolve item */
+  int32_t max_topk;              /* k: selected rows per query */
+  int64_t max_rows_per_request;  /* bound on L = imported + appended rows */
+  int64_t optional_pages;        /* optional capacity in pages */
+  int64_t admission_reserve_pages; /* pages an admission must leave free */
+  void *hot_dev;   /* [R][S][B] rows            (DHS_BUF_HOT bytes)  */
+  void *tail_dev;  /* [R][S][T] rows            (DHS_BUF_TAIL bytes) */
+  void *opt_dev;   /* [optional_pages][page_rows] rows (DHS_BUF_OPT bytes) */
+  void *meta_dev;  /* tags, stamps, page maps, miss lists, status (DHS_BUF_META) */
+  void *stream;    /* cudaStream_t for all device work (NULL = legacy default) */
+} dhs_pool_config;
+
+enum { DHS_BUF_HOT = 0, DHS_BUF_TAIL, DHS_BUF_OPT, DHS_BUF_META, DHS_NUM_BUFS };
+
+/*
+ * Bytes of the four device buffers the caller must allocate for `cfg`
+ * (pointer and stream fields are ignored), written to out[DHS_NUM_BUFS].
+ * Every buffer must be 256-byte aligned.  Pure host arithmetic.
+ * Errors: DHS_EINVAL for an invalid geometry.
+ */
+int dhs_pool_bytes(const dhs_pool_config *cfg, size_t out[DHS_NUM_BUFS]);
+
+/*
+ * Create a pool on the calling thread's current CUDA device.  The library
+ * keeps the pointers (it copies no payload) and enqueues on cfg->stream the
+ * initialisation of meta_dev (empty hot caches: tag -1, stamp 0; no ready
+ * pages).  Errors: DHS_EINVAL (geometry, null or misaligned buffer, or a
+ * geometry whose resolve kernel would not fit in shared memory), DHS_ENOMEM,
+ * DHS_ECUDA.
+ */
+int dhs_pool_create(const dhs_pool_config *cfg, dhs_pool **out);
+
+/* Free the host metadata (device buffers stay the caller's).  NULL is a no-op.
+ * Work already enqueued still runs; synchronise the stream before freeing
+ * the buffers. */
+void dhs_pool_destroy(dhs_pool *pool);
+
+/*
+ * Admit (req, src) with n_rows imported rows ("Resident-first admission").
+ * host_rows: caller-owned pinned + mapped host memory (cudaHostAlloc or
+ * cudaHostRegister with the mapped flag) holding rows [0, n_rows) and room
+ * for max_rows_per_request rows (appended rows are written through to it);
+ * it must outlive the admission.  resident_page_mask: one byte per complete
+ * page (n_rows / page_rows of them), nonzero = keep on device; NULL = all
+ * complete pages.  Resident pages take the lowest free optional slots, pages
+ * ascending; their bytes are copied from host_rows before the next device
+ * call observes them (pages reclaimed before then are never copied).  The
+ * tail ring is filled with rows [max(0, n_rows-T), n_rows).
+ * Capacity rule (Memory split): used + resident pages <= optional_pages -
+ * admission_reserve_pages, else DHS_EWOULDWAIT with *deficit_pages set and
+ * nothing changed; the caller may dhs_reclaim() and retry.
+ * Errors: DHS_EINVAL, DHS_ESTATE (already admitted), DHS_EWOULDWAIT,
+ * DHS_ECUDA.
+ */
+int dhs_admit(dhs_pool *pool, int32_t req, int32_t src, void *host_rows,
+              int64_t n_rows, const uint8_t *resident_page_mask,
+              int64_t *deficit_pages);
+
+/*
+ * "Reclamation and refill": walk `order` (n request ids) and take whole
+ * requests' optional pages -- every source of the request -- until
+ * deficit_pages are freed; other requests keep theirs.  If the listed
+ * requests cannot cover the deficit nothing is taken and DHS_EWOULDWAIT is
+ * returned.  Pages are freed in stream order, after every earlier reader on
+ * the pool's stream; hot-cache rows stay valid (they are copies).
+ * *freed_pages receives the pages taken.  Errors: DHS_EINVAL,
+ * DHS_EWOULDWAIT.
+ */
+int dhs_reclaim(dhs_pool *pool, const int32_t *order, int32_t n,
+                int64_t deficit_pages, int64_t *freed_pages);
+
+/* Release every source of request `req`: free its pages, empty its hot
+ * caches, forget its host rows.  Errors: DHS_EINVAL, DHS_ECUDA. */
+int dhs_release(dhs_pool *pool, int32_t req);
+
+/* Optional pages in use (host metadata). */
+int64_t dhs_pool_used(const dhs_pool *pool);
+
+/* --------------------------------------------------------- decode step */
+
+/* One append: `count` (<= tail_rows) decode rows for (req, src), row j at
+ * rows_dev + j * row_bytes (device memory, caller-owned). */
+typedef struct {
+  int32_t req;
+  int32_t src;
+  int32_t count;
+  int32_t reserved;
+  const void *rows_dev;
+} dhs_append_item;
+
+/*
+ * Append decode rows (Limits: rows generated during decoding always follow
+ * hot-cache rules).  Row L+j of (req, src) goes to tail slot (L+j) mod T and
+ * is written through to the pinned host copy, so every row that leaves the
+ * tail keeps a host copy ("every row is either ready on the GPU or has a
+ * host copy").  L grows by count.  (req, src) pairs must be distinct.
+ * Errors: DHS_EINVAL (count > T, L + count > max_rows_per_request, null
+ * rows), DHS_ESTATE, DHS_ECUDA.
+ */
+int dhs_append(dhs_pool *pool, const dhs_append_item *items, int32_t n_items);
+
+#define DHS_ITEM_GATHER_ONLY 1u /* skip resolution: gather loc_dev as given */
+
+/*
+ * One item of a decode step: the Q x k selection of one layer of one
+ * request.
+ *   sel_dev      int32 [Q][k] device, selected row ids (duplicates allowed)
+ *   loc_dev      uint32 [Q][k] device: written by resolution, read by gather
+ *   staging_dev  [Q][k][row_bytes] device gather target (gather only)
+ *   counters_dev uint32 [DHS_NUM_COUNTERS] device or NULL
+ * A DHS_ITEM_GATHER_ONLY item is a Reuse layer ("Model-specific reuse":
+ * Reuse layers inherit the prior location vector): it is not resolved and
+ * gathers loc_dev as given (req/src unused).
+ */
+typedef struct {
+  int32_t req;
+  int32_t src;
+  int32_t queries;
+  int32_t topk;
+  uint32_t flags;
+  int32_t reserved;
+  const int32_t *sel_dev;
+  uint32_t *loc_dev;
+  void *staging_dev;
+  uint32_t *counters_dev;
+} dhs_item;
+
+typedef struct {
+  uint32_t step; /* >= 1; stamps record it; one verify block = one step */
+  int32_t n_items;
+  const dhs_item *items;
+} dhs_step;
+
+/*
+ * "Resolution" for every item without DHS_ITEM_GATHER_ONLY.  Per item, over
+ * the union of its Q verify queries ("Speculative state": verification
+ * queries share missing-row retrieval): each distinct row resolves in the
+ * first place that holds it -- tail (rows >= L-T, checked first), the ready
+ * optional map (complete imported pages), the hot cache (B tags; a hit
+ * refreshes the slot's stamp to `step`) -- and the remaining rows, in
+ * ascending row order, take the least recently used unprotected slots
+ * (smallest (stamp, slot); slots hit or filled in this step are protected),
+ * get their bytes copied from pinned host memory, and become hot.  Writes
+ * loc_dev and counters_dev.  Items must name distinct (req, src) pairs.
+ * Errors (synchronous): DHS_EINVAL, DHS_ESTATE, DHS_ECUDA; device-side
+ * DHS_ERANGE / DHS_EBUDGET go to dhs_status().
+ */
+int dhs_resolve(dhs_pool *pool, const dhs_step *step);
+
+/*
+ * Gather: staging_dev[q][i] = the row at loc_dev[q][i] for every item
+ * (resolved or gather-only); DHS_NO_LOC rows become zeros.  Stream-ordered
+ * after any earlier dhs_resolve.  Errors: DHS_EINVAL, DHS_ECUDA;
+ * out-of-arena locations -> zeros + DHS_STATUS_ELOC.
+ */
+int dhs_gather(dhs_pool *pool, const dhs_step *step);
+
+/* dhs_resolve followed by dhs_gather on the same step. */
+int dhs_resolve_gather(dhs_pool *pool, const dhs_step *step);
+
+/*
+ * Synchronise the pool's stream, read and clear the sticky device status.
+ * *flags (may be NULL) receives DHS_STATUS_* bits.  Returns DHS_OK when no
+ * flag was set, else DHS_ERANGE (ERANGE or ELOC) or DHS_EBUDGET, or
+ * DHS_ECUDA if the stream reported an error.
+ */
+int dhs_status(dhs_pool *pool, uint32_t *flags);
+
+/*
+ * Read one source's hot-cache state and page map (synchronises the stream;
+ * for tests and diagnostics).  tags int32[B], stamps uint32[B],
+ * page_slot int32[ceil(max_rows_per_request / page_rows)] (host view, -1 =
+ * not ready), info int64[4] = {imported rows N, length L, admitted, last
+ * resolve status (0, DHS_ERANGE or DHS_EBUDGET)}.  Any pointer may be NULL.
+ */
+int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
+                   uint32_t *stamps, int32_t *page_slot, int64_t *info);
+
+/* Tunables (performance only; results do not depend on them). */
+#define DHS_OPT_COPY_CTAS 1 /* host-copy CTAs; 0 = clamp(requests/4, 4, 32) */
+#define DHS_OPT_GATHER_IMPL 2 /* 0 = 16-byte vector copy, 1 = TMA bulk copy */
+int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
+
+/* Static string for a DHS_* code. */
+const char *dhs_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DHS_H_ */

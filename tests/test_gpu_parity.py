@@ -1,0 +1,139 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+Small configurations (every request, every step, every output): locations,
+counters, hot-cache tags and stamps, page maps, gathered bytes, and the
+written-through host rows must be identical -- the path is integer and byte
+work, so the bar is bit-exact.  The hand-worked golden traces run through
+the library too.  Full-size workloads run every request on the GPU in the
+launch configuration the benchmark times, and compare a sample of requests
+against the oracle (requests are independent once admitted, so the sampled
+ones are exact), plus properties of every request.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+from dhs_workload.configs import C8, C64, C128, LONG, TINY, Config, Workload  # noqa: E402
+from fixture_runner import run_trace  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from hierarchical_sparse_kv_dhs_gb300.build import build
+    import oracle
+    import dhs_workload
+    build()
+    oracle.build()
+    dhs_workload.build()
+
+
+def _as_u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def compare_run(cfg: Config, sampled=None, check_all_bytes=True):
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    from oracle.run import OracleRun
+    wl = Workload(cfg)
+    gpu = GpuRun(cfg, wl)
+    sampled = list(range(cfg.requests)) if sampled is None else sampled
+    orc = OracleRun(cfg, wl, requests=sampled)
+    try:
+        for r in sampled:
+            for s in range(cfg.sources):
+                g_pages = gpu.pool.read_state(r, s)[2]
+                o_pages = orc.pool.state(r, s)[2]
+                assert np.array_equal(g_pages, o_pages), (r, s)
+        assert gpu.pool.used() == orc.pool.used()
+        for step in range(1, cfg.total_steps + 1):
+            gpu.step(step)
+            res = orc.step(step)
+            rc, flags = gpu.status()
+            want_flags = 0
+            for r in sampled:
+                for s in range(cfg.sources):
+                    if res[r]["rc"][s] == "ebudget":
+                        want_flags |= 2
+            assert rc == 0 or want_flags, (step, rc, flags)
+            loc_all = _as_u32(gpu.loc)
+            cnt_all = _as_u32(gpu.counters)
+            for r in sampled:
+                o = res[r]
+                assert np.array_equal(loc_all[r], o["loc"]), (cfg.name, step, r)
+                assert np.array_equal(cnt_all[r], o["counters"]), \
+                    (cfg.name, step, r, cnt_all[r], o["counters"])
+                stg = gpu.staging[r].cpu().view(torch.int16).numpy().view(np.uint16)
+                if check_all_bytes:
+                    assert np.array_equal(stg, o["staging"]), (cfg.name, step, r)
+                else:
+                    idx = np.linspace(0, cfg.topk - 1, 67).astype(int)
+                    assert np.array_equal(stg[:, :, idx], o["staging"][:, :, idx])
+                for s in range(cfg.sources):
+                    gt, gs, _, info = gpu.pool.read_state(r, s)
+                    ot, os_, _, ln = orc.pool.state(r, s)
+                    assert np.array_equal(gt, ot) and np.array_equal(gs, os_), (step, r, s)
+                    assert int(info[1]) == ln[1]
+            # every request: counters add up, scan bounded by B
+            c = cnt_all.reshape(-1, 8)
+            assert (c[:, 2] + c[:, 3] + c[:, 4] + c[:, 5] == c[:, 1]).all()
+            assert (c[:, 6] <= cfg.hot).all()
+        # written-through host rows of the sampled pairs
+        for r in sampled:
+            for s in range(cfg.sources):
+                L = wl.length(r, cfg.total_steps)
+                got = gpu.host_rows(r, s, 0, L)
+                want = orc.pool.rows(r, s, 0, 0, L)
+                assert np.array_equal(got, want), (r, s)
+    finally:
+        gpu.close()
+        orc.pool.close()
+
+
+# ------------------------------------------------------------ golden traces
+
+@pytest.mark.parametrize("trace", ["resolve_micro_b2.txt", "resolve_micro_b3_pairs.txt",
+                                   "admission_micro.txt"])
+def test_golden_trace_gpu(trace):
+    from gpu_adapter import GpuAdapter
+    run_trace(trace, GpuAdapter(), elems=8)  # 16-byte rows
+
+
+# ------------------------------------------------------------ small, every output
+
+SMALL = [
+    TINY,
+    # verify block of 3 queries, speculative appends, ragged k (not a tile multiple)
+    TINY.scaled(name="v3", tag=41, queries=3, topk=77, verify_core=50, hot=300,
+                steps=10, append_lo=1, append_hi=4, requests=3, sources=2),
+    # Reuse layers with a shared selection over 3 sources, low residency
+    TINY.scaled(name="reuse", tag=42, requests=3, sources=3, reuse_layers=3,
+                shared_selection=True, residency=0.2, steps=8, hot=700),
+    # admission-driven residency under capacity pressure, temporal locality
+    TINY.scaled(name="pressure", tag=43, requests=6, sources=2, residency=None,
+                capacity_frac=0.3, rho=0.9, steps=12, warmup_steps=4, hot=256),
+    # tiny hot cache: heavy eviction every step
+    TINY.scaled(name="evict", tag=44, requests=2, sources=1, hot=200, topk=150,
+                residency=0.0, steps=12),
+    # non-1152-byte rows (generic gather/copy paths), short tail, 2 sources
+    TINY.scaled(name="rows", tag=45, row_elems=200, tail=5, requests=2, sources=2,
+                steps=6, topk=100),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=[c.name for c in SMALL])
+def test_small_configs_bit_exact(cfg):
+    compare_run(cfg)
+
+
+# ------------------------------------------------------------ full size
+
+def test_c8_full_size_sampled():
+    compare_run(C8, sampled=[0, 5])
+
+
+def test_c64_full_size_sampled():
+    compare_run(C64, sampled=[0, 63], check_all_bytes=False)
