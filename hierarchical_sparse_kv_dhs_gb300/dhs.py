@@ -250,6 +250,8 @@ class Pool:
                  stream=None):
         import torch
         self.device = torch.device(device or "cuda")
+        if self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
         self.stream = stream or torch.cuda.current_stream(self.device)
         cfg = dhs_pool_config()
         cfg.max_requests, cfg.sources, cfg.row_bytes = max_requests, sources, row_bytes

@@ -48,6 +48,8 @@ class GpuRun:
         self.cfg = c = cfg
         self.wl = wl or Workload(cfg)
         self.device = torch.device(device)
+        if self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
         torch.cuda.set_device(self.device)
         self.layers = [("resolve", s) for s in range(c.sources)] + \
             [("reuse", 0)] * c.reuse_layers
