@@ -10,4 +10,3 @@ synthetic workloads through it.
 Build with ``hierarchical_sparse_kv_dhs_gb300.build.build()``.  Importing
 ``hierarchical_sparse_kv_dhs_gb300.dhs`` without the built library raises.
 """
-from .build import build  # noqa: F401

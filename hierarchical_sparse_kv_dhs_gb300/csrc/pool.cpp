@@ -456,6 +456,13 @@ int dhs_release(dhs_pool* p, int32_t req) {
   return cuda_rc(e);
 }
 
+int dhs_flush(dhs_pool* p) {
+  if (!p) return DHS_EINVAL;
+  int rc = enter(p);
+  if (rc) return rc;
+  return flush(p);
+}
+
 int dhs_append(dhs_pool* p, const dhs_append_item* items, int32_t n_items) {
   if (!p || n_items < 0 || (n_items > 0 && !items)) return DHS_EINVAL;
   const dhs_pool_config& c = p->cfg;

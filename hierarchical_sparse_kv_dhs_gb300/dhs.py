@@ -83,6 +83,7 @@ def _load():
         "dhs_reclaim": (ctypes.c_int, [_vp, _vp, _i32, _i64, P(_i64)]),
         "dhs_release": (ctypes.c_int, [_vp, _i32]),
         "dhs_pool_used": (_i64, [_vp]),
+        "dhs_flush": (ctypes.c_int, [_vp]),
         "dhs_append": (ctypes.c_int, [_vp, P(dhs_append_item), _i32]),
         "dhs_resolve": (ctypes.c_int, [_vp, P(dhs_step)]),
         "dhs_gather": (ctypes.c_int, [_vp, P(dhs_step)]),
@@ -156,6 +157,10 @@ def dhs_release(h, req):
 
 def dhs_pool_used(h):
     return lib.dhs_pool_used(h)
+
+
+def dhs_flush(h):
+    return lib.dhs_flush(h)
 
 
 def dhs_append(h, items):
@@ -306,6 +311,9 @@ class Pool:
 
     def used(self):
         return dhs_pool_used(self.h)
+
+    def flush(self):
+        return dhs_flush(self.h)
 
     def append(self, items):
         return dhs_append(self.h, items)

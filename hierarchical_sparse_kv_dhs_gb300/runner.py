@@ -62,6 +62,7 @@ class GpuRun:
         self.host = dhs.HostRows(c.pairs * c.max_rows * rb)
         self.wl.fill_host_rows(self.host.ptr, c.max_rows, nthreads=host_threads)
         drive_admission(_Admit(self), c, self.wl)
+        dhs.check(self.pool.flush(), "dhs_flush")
 
         dev = self.device
         Q, k = c.queries, c.topk
@@ -146,6 +147,14 @@ class GpuRun:
         st, _ = self._steps[step - 1]
         dhs.check(dhs.lib.dhs_resolve_gather(self.pool.h, ctypes.byref(st)),
                   "dhs_resolve_gather")
+
+    def reset(self):
+        """Release every request and admit it again: the pool returns to its
+        state before step 1 (stream-ordered; no synchronisation)."""
+        for r in range(self.cfg.requests):
+            dhs.check(self.pool.release(r), "dhs_release")
+        drive_admission(_Admit(self), self.cfg, self.wl)
+        dhs.check(self.pool.flush(), "dhs_flush")
 
     def status(self):
         return self.pool.status()

@@ -179,6 +179,15 @@ int dhs_release(dhs_pool *pool, int32_t req);
 /* Optional pages in use (host metadata). */
 int64_t dhs_pool_used(const dhs_pool *pool);
 
+/*
+ * Make every admitted page ready now ("Reclamation and refill": a page is
+ * read only once its copy is complete): enqueue on the pool's stream the
+ * page copies and page-map updates that admissions, reclaims and releases
+ * left pending (dhs_append, dhs_resolve and dhs_gather otherwise do this
+ * first).  Asynchronous.  Errors: DHS_EINVAL, DHS_ECUDA.
+ */
+int dhs_flush(dhs_pool *pool);
+
 /* --------------------------------------------------------- decode step */
 
 /* One append: `count` (<= tail_rows) decode rows for (req, src), row j at

@@ -42,17 +42,29 @@ class OracleRun:
         self.wl = wl or Workload(cfg)
         self.requests = list(range(cfg.requests)) if requests is None else list(requests)
         self.payload = payload
-        cap = cfg.pool_pages() if capacity is None else capacity
-        self.pool = OraclePool(cfg.requests, cfg.sources, cfg.tail, cfg.hot,
-                               cfg.row_elems, cfg.page_rows, cfg.max_rows, cap)
+        self._cap = cfg.pool_pages() if capacity is None else capacity
         self._sim = set(self.requests)
+        self._host = {}
+        self.reset()
+
+    def reset(self):
+        """A fresh pool with every request admitted again (row bytes of the
+        simulated requests are generated once and kept)."""
+        cfg = self.cfg
+        if getattr(self, "pool", None) is not None:
+            self.pool.close()
+        self.pool = OraclePool(cfg.requests, cfg.sources, cfg.tail, cfg.hot,
+                               cfg.row_elems, cfg.page_rows, cfg.max_rows, self._cap)
         drive_admission(_AdmitAdapter(self), cfg, self.wl)
 
     def admit(self, r, s, mask):
         host = None
         if self.payload and r in self._sim:
-            host = np.empty((self.cfg.history, self.cfg.row_elems), np.uint16)
-            self.wl.fill_host_rows(host.ctypes.data, self.cfg.history, [(r, s)])
+            host = self._host.get((r, s))
+            if host is None:
+                host = np.empty((self.cfg.history, self.cfg.row_elems), np.uint16)
+                self.wl.fill_host_rows(host.ctypes.data, self.cfg.history, [(r, s)])
+                self._host[(r, s)] = host
         return self.pool.admit(r, s, self.cfg.history, mask, host)
 
     def layers(self):

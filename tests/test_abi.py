@@ -1,0 +1,80 @@
+"""The C ABI without a GPU: libdhs.so builds for sm_103a, loads, exports every
+function include/dhs.h declares, and its host-only calls (sizes, validation,
+error strings) behave as documented.  No device work is issued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def dhs():
+    from hierarchical_sparse_kv_dhs_gb300.build import build
+    build()
+    from hierarchical_sparse_kv_dhs_gb300 import dhs as mod
+    return mod
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "dhs.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dhs_[a-z_]+)\s*\(", text)) - {"dhs_pool_config"})
+
+
+def test_every_declared_symbol_is_exported(dhs):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(dhs.lib, n), f"{n} declared in dhs.h but not exported"
+
+
+def test_strerror(dhs):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -99):
+        s = dhs.lib.dhs_strerror(code)
+        assert isinstance(s, bytes) and s
+
+
+def _cfg(dhs, **kw):
+    c = dhs.dhs_pool_config()
+    c.max_requests, c.sources, c.row_bytes, c.page_rows = 8, 4, 1152, 64
+    c.tail_rows, c.hot_rows, c.max_queries, c.max_topk = 256, 4096, 1, 2048
+    c.max_rows_per_request, c.optional_pages = 32832, 16384
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_pool_bytes(dhs):
+    sizes = dhs.dhs_pool_bytes(_cfg(dhs))
+    assert sizes[dhs.DHS_BUF_HOT] == 8 * 4 * 4096 * 1152
+    assert sizes[dhs.DHS_BUF_TAIL] == 8 * 4 * 256 * 1152
+    assert sizes[dhs.DHS_BUF_OPT] == 16384 * 64 * 1152
+    # tags + stamps + page maps + miss lists dominate the metadata
+    pairs, pmax = 32, -(-32832 // 64)
+    assert sizes[dhs.DHS_BUF_META] >= pairs * (4096 * 8 + pmax * 4 + 2048 * 8)
+
+
+@pytest.mark.parametrize("field,value", [
+    ("row_bytes", 1000), ("page_rows", 48), ("hot_rows", 0), ("hot_rows", 20000),
+    ("tail_rows", 0), ("max_requests", 0), ("admission_reserve_pages", 99999),
+    ("max_rows_per_request", 0)])
+def test_invalid_geometry_rejected_on_host(dhs, field, value):
+    out = (ctypes.c_size_t * 4)()
+    assert dhs.lib.dhs_pool_bytes(ctypes.byref(_cfg(dhs, **{field: value})), out) == dhs.DHS_EINVAL
+    h = ctypes.c_void_p()
+    assert dhs.lib.dhs_pool_create(ctypes.byref(_cfg(dhs, **{field: value})),
+                                   ctypes.byref(h)) == dhs.DHS_EINVAL
+
+
+def test_null_arguments(dhs):
+    assert dhs.lib.dhs_pool_create(None, None) == dhs.DHS_EINVAL
+    h = ctypes.c_void_p()
+    # valid geometry but null device buffers
+    assert dhs.lib.dhs_pool_create(ctypes.byref(_cfg(dhs)), ctypes.byref(h)) == dhs.DHS_EINVAL
+    assert dhs.lib.dhs_status(None, None) == dhs.DHS_EINVAL
+    assert dhs.lib.dhs_flush(None) == dhs.DHS_EINVAL
+    assert dhs.lib.dhs_pool_used(None) == -1
+    dhs.lib.dhs_pool_destroy(None)
