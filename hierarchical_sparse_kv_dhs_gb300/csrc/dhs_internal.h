@@ -125,3 +125,25 @@ cudaError_t launch_append(const AppendCommon& c, const AppendItem* items,
                           int n_items, cudaStream_t stream);
 
 }  // namespace dhs
+
+namespace dhs {
+
+// ------------------------------------------------------------ no-alloc scratch
+// Fixed miss-list storage for dhs_resolve_noalloc (noalloc_scratch.cu):
+// up to kNoallocMissCap (row, slot) entries, i.e. pairs * min(B, Q*k) of the
+// pool, and kNoallocPairs per-pair counts.
+constexpr int kNoallocMissCap = 65536;
+constexpr int kNoallocPairs = 4096;
+constexpr int kNoallocMaxDevices = 64;
+
+struct NoallocScratch {
+  int32_t* miss_rows;
+  int32_t* miss_slots;
+  uint32_t* miss_count;
+};
+
+// Device address of the scratch on the current device (looked up once per
+// device with cudaGetSymbolAddress).
+cudaError_t noalloc_scratch(NoallocScratch* out);
+
+}  // namespace dhs

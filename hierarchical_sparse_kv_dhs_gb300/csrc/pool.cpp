@@ -709,3 +709,85 @@ int dhs_read_state(dhs_pool* p, int32_t req, int32_t src, int32_t* tags, uint32_
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dhs_resolve_noalloc: dhs_resolve with the miss lists in the library's fixed
+// device array instead of the pool's metadata buffer (see include/dhs.h).
+extern "C" int dhs_resolve_noalloc(dhs_pool* p, const dhs_step* st) {
+  int rc = validate_step(p, st, true);
+  if (rc) return rc;
+  if (p->pairs > dhs::kNoallocPairs || p->pairs * p->mcap > dhs::kNoallocMissCap)
+    return DHS_EINVAL;  // the pool's miss lists do not fit the fixed scratch
+  if ((rc = enter(p))) return rc;
+  dhs::NoallocScratch scr{};
+  if (dhs::noalloc_scratch(&scr) != cudaSuccess) return DHS_ECUDA;
+  if ((rc = flush(p))) return rc;
+  const dhs_pool_config& c = p->cfg;
+  std::vector<dhs::ResolveItem> ritems;
+  std::vector<dhs::CopyItem> citems;
+  for (int32_t i = 0; i < st->n_items; ++i) {
+    const dhs_item& it = st->items[i];
+    if (it.flags & DHS_ITEM_GATHER_ONLY) continue;
+    const int64_t pair = (int64_t)it.req * c.sources + it.src;
+    const PairState& s = p->ps[pair];
+    dhs::ResolveItem r{};
+    r.sel = it.sel_dev;
+    r.loc = it.loc_dev;
+    r.counters = it.counters_dev;
+    r.L = s.L;
+    r.N = s.N;
+    r.pair = (int32_t)pair;
+    r.n = it.queries * it.topk;
+    ritems.push_back(r);
+    dhs::CopyItem ci{};
+    ci.host = s.host_dev;
+    ci.pair = (int32_t)pair;
+    citems.push_back(ci);
+  }
+  dhs::ResolveCommon rcm{};
+  rcm.tags = p->tags;
+  rcm.stamps = p->stamps;
+  rcm.map = p->map;
+  rcm.miss_rows = scr.miss_rows;
+  rcm.miss_slots = scr.miss_slots;
+  rcm.miss_count = scr.miss_count;
+  rcm.pair_status = p->pair_status;
+  rcm.status = p->status;
+  rcm.T = c.tail_rows;
+  rcm.B = c.hot_rows;
+  rcm.Pmax = (int32_t)p->pmax;
+  rcm.Mcap = (int32_t)p->mcap;
+  rcm.page_shift = p->page_shift;
+  rcm.step = st->step;
+  dhs::CopyCommon ccm{};
+  ccm.hot = (uint8_t*)c.hot_dev;
+  ccm.miss_rows = scr.miss_rows;
+  ccm.miss_slots = scr.miss_slots;
+  ccm.miss_count = scr.miss_count;
+  ccm.B = c.hot_rows;
+  ccm.Mcap = (int32_t)p->mcap;
+  ccm.row_bytes = c.row_bytes;
+  const size_t nr = ritems.size();
+  for (size_t b = 0; b < nr; b += dhs::kResolveItemsLarge) {
+    const int n = (int)std::min<size_t>(dhs::kResolveItemsLarge, nr - b);
+    int64_t wmax = 0, qmax = 0, requests = 0, last_req = -1;
+    for (int i = 0; i < n; ++i) {
+      const dhs::ResolveItem& r = ritems[b + i];
+      wmax = std::max<int64_t>(wmax, (r.L + 63) / 64);
+      qmax = std::max<int64_t>(qmax, std::min<int64_t>(r.n, r.L));
+      const int64_t req = r.pair / c.sources;
+      if (req != last_req) ++requests;
+      last_req = req;
+    }
+    rcm.w64cap = (int32_t)wmax;
+    rcm.qkcap = (int32_t)qmax;
+    const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows);
+    if (dhs::launch_resolve(rcm, ritems.data() + b, n, smem, p->stream) != cudaSuccess)
+      return DHS_ECUDA;
+    int ctas = p->copy_ctas;
+    if (ctas <= 0) ctas = (int)std::min<int64_t>(32, std::max<int64_t>(4, requests / 4));
+    if (dhs::launch_hostcopy(ccm, citems.data() + b, n, ctas, p->stream) != cudaSuccess)
+      return DHS_ECUDA;
+  }
+  return DHS_OK;
+}

@@ -267,6 +267,31 @@ int dhs_resolve(dhs_pool *pool, const dhs_step *step);
  */
 int dhs_gather(dhs_pool *pool, const dhs_step *step);
 
+/*
+ * dhs_resolve for callers that cannot allocate device memory where they
+ * resolve (an embedding runtime that hands the library only the buffers it
+ * owns, or code running where allocation calls are not permitted).  The
+ * results are the same as dhs_resolve's; the only difference is where the
+ * per-item miss lists (rows to fetch from host memory and their hot slots)
+ * live: in one fixed 540,672-byte device array inside libdhs.so instead of the
+ * pool's metadata buffer.  The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).  The pages describe no such
+ * entry point; it has no counterpart there.
+ *   - Limit: the pool's R*S*min(B, max_queries*max_topk) must be at most
+ *     65536 and R*S at most 4096; larger pools get DHS_EINVAL and nothing
+ *     is launched.
+ *   - The array is shared by every call in the process and keeps the last
+ *     call's contents; every entry a call reads is written earlier in the
+ *     same call, so nothing needs clearing.  Calls that overlap on the GPU
+ *     (other streams, other pools) race on it: issue them in one stream
+ *     order.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first
+ *     call before any stream capture.
+ * Errors: as dhs_resolve, plus DHS_EINVAL for pools beyond the limit.
+ */
+int dhs_resolve_noalloc(dhs_pool *pool, const dhs_step *step);
+
 /* dhs_resolve followed by dhs_gather on the same step. */
 int dhs_resolve_gather(dhs_pool *pool, const dhs_step *step);
 
