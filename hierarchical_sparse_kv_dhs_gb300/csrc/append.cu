@@ -37,6 +37,10 @@ __global__ void __launch_bounds__(kAppendThreads)
 
 }  // namespace
 
+cudaError_t append_set_carveout() {
+  return cudaFuncSetAttribute(append_kernel<kAppendItemsMax>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t launch_append(const AppendCommon& c, const AppendItem* items, int n_items,
                           cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;

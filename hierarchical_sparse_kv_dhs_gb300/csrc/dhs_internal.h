@@ -16,8 +16,29 @@ namespace dhs {
 constexpr uint32_t kTierTail = 0u, kTierOpt = 1u, kTierHot = 2u;
 constexpr uint32_t kNoLoc = 0xFFFFFFFFu;
 constexpr uint32_t kStatusErange = 1u, kStatusEbudget = 2u, kStatusEloc = 4u;
+constexpr uint32_t kStatusEtimeout = 8u;
 constexpr int32_t kErrRange = -5, kErrBudget = -4;  // DHS_ERANGE, DHS_EBUDGET
 constexpr int kMaxHotRows = 16384;
+
+// Optional timeline (DHS_OPT_TRACE): per kernel kind, the earliest CTA start
+// and the latest CTA end in %globaltimer nanoseconds.
+enum TraceSlot { kTraceResolve = 0, kTraceCopy = 1, kTraceGather = 2, kTraceKinds = 4 };
+
+#ifdef __CUDACC__
+__device__ __forceinline__ unsigned long long trace_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Called by thread 0 of every CTA at start (end = false) and at end.
+__device__ __forceinline__ void trace_mark(unsigned long long* trace, int kind, bool end) {
+  if (!trace) return;
+  const unsigned long long t = trace_now();
+  if (end) atomicMax(&trace[2 * kind + 1], t);
+  else atomicMin(&trace[2 * kind], t);
+}
+#endif
 
 // ------------------------------------------------------------ resolve (a-c)
 constexpr int kResolveThreads = 1024;
@@ -27,11 +48,16 @@ struct ResolveItem {
   const int32_t* sel;   // [n] selected rows (Q*k, verify queries back to back)
   uint32_t* loc;        // [n] locations out
   uint32_t* counters;   // [8] or null
-  int64_t L;            // current length
+  int64_t L;            // current length (after this step's append)
   int64_t N;            // imported rows
   int32_t pair;         // req * S + src
   int32_t n;            // Q * k
-  int32_t pad[2];
+  // decode rows appended by this launch (dhs_decode_step), else count 0
+  const uint8_t* app_rows;  // [app_count][row_bytes] device
+  uint8_t* app_host;        // device-visible pointer of the pair's host rows
+  int64_t app_L0;           // length before the append
+  int32_t app_count;
+  int32_t pad;
 };
 
 struct ResolveCommon {
@@ -49,7 +75,9 @@ struct ResolveCommon {
   int32_t qkcap;         // candidate slots reserved in shared memory
   uint32_t step;
   int32_t n_items;
-  int32_t pad;
+  int32_t row_bytes;
+  uint8_t* tail;         // tail arena (appends folded into the launch)
+  unsigned long long* trace;  // null = off
 };
 
 size_t resolve_smem_bytes(int w64cap, int qkcap, int B);
@@ -73,36 +101,62 @@ struct CopyCommon {
   const int32_t* miss_slots;
   const uint32_t* miss_count;
   int32_t B, Mcap, row_bytes, n_items;
+  unsigned long long* trace;  // null = off
 };
 
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,
-                            int n_items, int ctas, cudaStream_t stream);
+                            int n_items, int ctas, bool pdl, cudaStream_t stream);
 
 // ------------------------------------------------------------ gather (e)
 constexpr int kGatherThreads = 256;
 constexpr int kGatherTileRows = 32;
-constexpr int kGatherItemsLarge = 512, kGatherItemsSmall = 64;
+constexpr int kGatherItemsLarge = 384, kGatherItemsSmall = 64;
 
 struct GatherItem {
   const uint32_t* loc;
   uint8_t* staging;
-  int32_t n;      // entries
-  int32_t tile0;  // first tile of this item in the launch
+  const int32_t* sel;  // non-null: a resolved item whose step-1 rows may be copied early
+  int64_t L, N;        // length and imported rows of the item's source
+  int64_t L0;          // rows >= L0 were appended by this launch: never early
+  int32_t n;           // entries
+  int32_t tile0;       // first tile of this item in the launch
+  int32_t pair;        // req * S + src (resolved items)
+  int32_t ent0;        // first entry of this item in the launch (items back to back)
 };
 
 struct GatherCommon {
   const uint8_t* tail;
   const uint8_t* opt;
   const uint8_t* hot;
+  const int32_t* map;          // [pairs][Pmax] page map (early phase)
+  const int32_t* pair_status;  // resolve status per pair (early phase)
   uint32_t tail_rows, opt_rows, hot_rows;  // arena sizes in rows
   int32_t row_bytes;
   uint32_t* status;
   int32_t n_items;
   int32_t n_tiles;
+  int64_t n_entries;  // entries of all items of the launch
+  int32_t T, Pmax, page_shift;
+  int32_t early;    // copy step-1 rows before waiting for the resolve grid
+  int32_t tma_grid; // co-resident warps of the TMA gather (persistent grid)
+  uint32_t* done;   // finished-CTA ticket of the running launch (reset by its last CTA)
+  unsigned long long* trace;  // null = off
 };
 
+// Each kernel file sets its kernels' shared-memory carveout to the maximum,
+// so consecutive kernels of a step never make an SM reconfigure its L1 /
+// shared split.
+cudaError_t resolve_set_carveout();
+cudaError_t hostcopy_set_carveout();
+cudaError_t gather_set_carveout();
+cudaError_t append_set_carveout();
+
 cudaError_t launch_gather(const GatherCommon& c, const GatherItem* items,
-                          int n_items, int impl, cudaStream_t stream);
+                          int n_items, bool pdl, int impl, cudaStream_t stream);
+
+// Co-resident warps of the TMA gather on the current device (0 on error);
+// also raises its shared-memory limit.
+int gather_tma_grid(int row_bytes);
 
 // ------------------------------------------------------------ append (A0)
 constexpr int kAppendThreads = 256;

@@ -35,6 +35,12 @@ __global__ void __launch_bounds__(kCopyThreads)
   const int tid = threadIdx.x, lane = tid & 31;
   const int n_items = c.n_items;
 
+  // The gather may be launched now; the miss lists are read only after the
+  // resolve grid has finished writing them.
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (tid == 0) trace_mark(c.trace, kTraceCopy, false);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   // prefix of the per-item miss counts (n_items <= blockDim.x)
   const uint32_t mine = tid < n_items ? c.miss_count[P.items[tid].pair] : 0u;
   {
@@ -63,7 +69,10 @@ __global__ void __launch_bounds__(kCopyThreads)
     __syncthreads();
   }
   const uint32_t total = s_pre[n_items];
-  if (total == 0) return;
+  if (total == 0) {
+    if (tid == 0) trace_mark(c.trace, kTraceCopy, true);
+    return;
+  }
 
   const int rb = c.row_bytes;
   const int cpr = rb >> 4;
@@ -116,29 +125,46 @@ __global__ void __launch_bounds__(kCopyThreads)
       }
     }
   }
+  __syncthreads();
+  if (tid == 0) trace_mark(c.trace, kTraceCopy, true);
 }
 
 template <int MAXI>
 cudaError_t launch_t(const CopyCommon& c, const CopyItem* items, int n, int ctas,
-                     cudaStream_t stream) {
+                     bool pdl, cudaStream_t stream) {
   CopyParams<MAXI> P;
   P.c = c;
   P.c.n_items = n;
   for (int i = 0; i < n; ++i) P.items[i] = items[i];
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kCopyThreads);
+  cfg.stream = stream;
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   if ((c.row_bytes >> 4) <= 32 * kChunksPerLane)
-    hostcopy_kernel<MAXI, true><<<ctas, kCopyThreads, 0, stream>>>(P);
-  else
-    hostcopy_kernel<MAXI, false><<<ctas, kCopyThreads, 0, stream>>>(P);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, hostcopy_kernel<MAXI, true>, P);
+  return cudaLaunchKernelEx(&cfg, hostcopy_kernel<MAXI, false>, P);
 }
 
 }  // namespace
 
+cudaError_t hostcopy_set_carveout() {
+  cudaError_t e = cudaFuncSetAttribute(hostcopy_kernel<kCopyItemsMax, true>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(hostcopy_kernel<kCopyItemsMax, false>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items, int n_items,
-                            int ctas, cudaStream_t stream) {
+                            int ctas, bool pdl, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
   if (n_items > kCopyItemsMax || n_items > kCopyThreads) return cudaErrorInvalidValue;
-  return launch_t<kCopyItemsMax>(c, items, n_items, ctas, stream);
+  return launch_t<kCopyItemsMax>(c, items, n_items, ctas, pdl, stream);
 }
 
 }  // namespace dhs

@@ -35,7 +35,7 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct MetaLayout {
-  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status, status;
+  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status, status, done;
   size_t total;
 };
 
@@ -65,6 +65,7 @@ MetaLayout meta_layout(const dhs_pool_config& c) {
   m.miss_count = take(pairs * 4);
   m.pair_status = take(pairs * 4);
   m.status = take(64);
+  m.done = take(64);
   m.total = off;
   return m;
 }
@@ -137,13 +138,19 @@ struct dhs_pool {
   int64_t dirty_lo = INT64_MAX, dirty_hi = -1;  // pairs whose map changed
   bool any_pending = false;
   int copy_ctas = 0;
-  int gather_impl = 0;
+  int gather_impl = 1;  // TMA bulk copy
+  int early = 1;        // fused gathers copy step-1 rows before the resolve ends
+  uint32_t* done = nullptr;  // gather grid ticket
+  int tma_grid = 0;          // co-resident warps of the TMA gather
+  unsigned long long* trace = nullptr;  // DHS_OPT_TRACE buffer, null = off
   // reusable launch tables
   std::vector<dhs::ResolveItem> ritems;
   std::vector<dhs::CopyItem> citems;
   std::vector<dhs::GatherItem> gitems;
   std::vector<dhs::AppendItem> aitems;
   std::vector<uint8_t> seen;
+  std::vector<int32_t> app_of_pair;  // decode step: append item of each pair, -1 = none
+  std::vector<int64_t> l0_of_pair;   // length of each resolved pair before this step's append
 };
 
 namespace {
@@ -313,14 +320,27 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->miss_count = (uint32_t*)(m + p->layout.miss_count);
     p->pair_status = (int32_t*)(m + p->layout.pair_status);
     p->status = (uint32_t*)(m + p->layout.status);
+    p->done = (uint32_t*)(m + p->layout.done);
     p->ps.resize(p->pairs);
     p->map_host.assign((size_t)(p->pairs * p->pmax), -1);
     p->slot_pair.assign((size_t)cfg->optional_pages + 1, -1);
     p->slot_page.assign((size_t)cfg->optional_pages + 1, -1);
     p->seen.assign((size_t)p->pairs, 0);
+    p->app_of_pair.assign((size_t)p->pairs, -1);
+    p->l0_of_pair.assign((size_t)p->pairs, 0);
   } catch (...) {
     delete p;
     return DHS_ENOMEM;
+  }
+  if (dhs::resolve_set_carveout() != cudaSuccess || dhs::hostcopy_set_carveout() != cudaSuccess ||
+      dhs::gather_set_carveout() != cudaSuccess || dhs::append_set_carveout() != cudaSuccess) {
+    delete p;
+    return DHS_ECUDA;
+  }
+  p->tma_grid = dhs::gather_tma_grid(cfg->row_bytes);
+  if (p->tma_grid <= 0) {
+    delete p;
+    return DHS_ECUDA;
   }
   // empty hot caches (tag -1, stamp 0), no ready pages, zero counts/status
   cudaError_t e = cudaMemsetAsync(p->tags, 0xFF, p->pairs * cfg->hot_rows * 4, p->stream);
@@ -347,6 +367,16 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
   if (key == DHS_OPT_COPY_CTAS) {
     if (value < 0 || value > 4096) return DHS_EINVAL;
     pool->copy_ctas = (int)value;
+    return DHS_OK;
+  }
+  if (key == DHS_OPT_TRACE) {
+    if (value < 0 || (value & 7)) return DHS_EINVAL;
+    pool->trace = (unsigned long long*)(uintptr_t)value;
+    return DHS_OK;
+  }
+  if (key == DHS_OPT_EARLY) {
+    if (value < 0 || value > 1) return DHS_EINVAL;
+    pool->early = (int)value;
     return DHS_OK;
   }
   if (key == DHS_OPT_GATHER_IMPL) {
@@ -537,11 +567,10 @@ static int validate_step(dhs_pool* p, const dhs_step* st, bool resolving) {
   return DHS_OK;
 }
 
-int dhs_resolve(dhs_pool* p, const dhs_step* st) {
-  int rc = validate_step(p, st, true);
-  if (rc) return rc;
-  if ((rc = enter(p))) return rc;
-  if ((rc = flush(p))) return rc;
+// Launch resolve + host copy for every resolving item of a validated,
+// flushed step.  `apps` (may be null): appends folded into the resolve
+// kernel, one per pair listed in p->app_of_pair.
+static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* apps) {
   const dhs_pool_config& c = p->cfg;
   p->ritems.clear();
   p->citems.clear();
@@ -549,8 +578,17 @@ int dhs_resolve(dhs_pool* p, const dhs_step* st) {
     const dhs_item& it = st->items[i];
     if (it.flags & DHS_ITEM_GATHER_ONLY) continue;
     const int64_t pair = (int64_t)it.req * c.sources + it.src;
-    const PairState& s = p->ps[pair];
+    PairState& s = p->ps[pair];
     dhs::ResolveItem r{};
+    p->l0_of_pair[pair] = s.L;
+    if (apps && p->app_of_pair[pair] >= 0) {
+      const dhs_append_item& a = apps[p->app_of_pair[pair]];
+      r.app_rows = (const uint8_t*)a.rows_dev;
+      r.app_host = s.host_dev;
+      r.app_L0 = s.L;
+      r.app_count = a.count;
+      s.L += a.count;
+    }
     r.sel = it.sel_dev;
     r.loc = it.loc_dev;
     r.counters = it.counters_dev;
@@ -579,6 +617,9 @@ int dhs_resolve(dhs_pool* p, const dhs_step* st) {
   rcm.Mcap = (int32_t)p->mcap;
   rcm.page_shift = p->page_shift;
   rcm.step = st->step;
+  rcm.row_bytes = c.row_bytes;
+  rcm.tail = (uint8_t*)c.tail_dev;
+  rcm.trace = p->trace;
   dhs::CopyCommon ccm{};
   ccm.hot = (uint8_t*)c.hot_dev;
   ccm.miss_rows = p->miss_rows;
@@ -587,6 +628,7 @@ int dhs_resolve(dhs_pool* p, const dhs_step* st) {
   ccm.B = c.hot_rows;
   ccm.Mcap = (int32_t)p->mcap;
   ccm.row_bytes = c.row_bytes;
+  ccm.trace = p->trace;
   const size_t nr = p->ritems.size();
   for (size_t b = 0; b < nr; b += dhs::kResolveItemsLarge) {
     const int n = (int)std::min<size_t>(dhs::kResolveItemsLarge, nr - b);
@@ -606,7 +648,82 @@ int dhs_resolve(dhs_pool* p, const dhs_step* st) {
       return DHS_ECUDA;
     int ctas = p->copy_ctas;
     if (ctas <= 0) ctas = (int)std::min<int64_t>(32, std::max<int64_t>(4, requests / 4));
-    if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, ctas, p->stream) != cudaSuccess)
+    if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, ctas, true, p->stream) !=
+        cudaSuccess)
+      return DHS_ECUDA;
+  }
+  return DHS_OK;
+}
+
+int dhs_resolve(dhs_pool* p, const dhs_step* st) {
+  int rc = validate_step(p, st, true);
+  if (rc) return rc;
+  if ((rc = enter(p))) return rc;
+  if ((rc = flush(p))) return rc;
+  return resolve_impl(p, st, nullptr);
+}
+
+// Launch the gather for every item of a validated, flushed step.  `fused`:
+// the step was resolved by the immediately preceding launches, so step-1 rows
+// may be copied before the resolve grid finishes (programmatic dependent
+// launch; see gather.cu).
+static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
+  const dhs_pool_config& c = p->cfg;
+  dhs::GatherCommon g{};
+  g.tail = (const uint8_t*)c.tail_dev;
+  g.opt = (const uint8_t*)c.opt_dev;
+  g.hot = (const uint8_t*)c.hot_dev;
+  g.map = p->map;
+  g.pair_status = p->pair_status;
+  g.tail_rows = (uint32_t)(p->pairs * c.tail_rows);
+  g.opt_rows = (uint32_t)(c.optional_pages * c.page_rows);
+  g.hot_rows = (uint32_t)(p->pairs * c.hot_rows);
+  g.row_bytes = c.row_bytes;
+  g.status = p->status;
+  g.T = c.tail_rows;
+  g.Pmax = (int32_t)p->pmax;
+  g.page_shift = p->page_shift;
+  g.early = fused && p->early ? 1 : 0;
+  g.done = p->done;
+  g.tma_grid = p->tma_grid;
+  g.trace = p->trace;
+  p->gitems.clear();
+  for (int32_t i = 0; i < st->n_items; ++i) {
+    const dhs_item& it = st->items[i];
+    const int32_t n = it.queries * it.topk;
+    if (n == 0) continue;
+    dhs::GatherItem gi{};
+    gi.loc = it.loc_dev;
+    gi.staging = (uint8_t*)it.staging_dev;
+    gi.n = n;
+    if (fused && !(it.flags & DHS_ITEM_GATHER_ONLY)) {
+      const int64_t pair = (int64_t)it.req * c.sources + it.src;
+      gi.sel = it.sel_dev;
+      gi.pair = (int32_t)pair;
+      gi.L = p->ps[pair].L;
+      gi.N = p->ps[pair].N;
+      gi.L0 = p->l0_of_pair[pair];
+    }
+    p->gitems.push_back(gi);
+  }
+  const size_t ng = p->gitems.size();
+  for (size_t b = 0; b < ng; b += dhs::kGatherItemsLarge) {
+    const int n = (int)std::min<size_t>(dhs::kGatherItemsLarge, ng - b);
+    int64_t tiles = 0, entries = 0;
+    for (int i = 0; i < n; ++i) {
+      dhs::GatherItem& gi = p->gitems[b + i];
+      gi.tile0 = (int32_t)tiles;
+      gi.ent0 = (int32_t)entries;
+      tiles += (gi.n + dhs::kGatherTileRows - 1) / dhs::kGatherTileRows;
+      entries += gi.n;
+    }
+    if (tiles > INT32_MAX || entries > INT32_MAX) return DHS_EINVAL;
+    g.n_tiles = (int32_t)tiles;
+    g.n_entries = entries;
+    // only the first gather launch directly follows the resolve launches
+    if (dhs::launch_gather(g, p->gitems.data() + b, n, fused && b == 0, p->gather_impl,
+                          p->stream) !=
+        cudaSuccess)
       return DHS_ECUDA;
   }
   return DHS_OK;
@@ -617,49 +734,66 @@ int dhs_gather(dhs_pool* p, const dhs_step* st) {
   if (rc) return rc;
   if ((rc = enter(p))) return rc;
   if ((rc = flush(p))) return rc;
+  return launch_gathers(p, st, false);
+}
+
+int dhs_resolve_gather(dhs_pool* p, const dhs_step* st) {
+  int rc = validate_step(p, st, false);
+  if (rc) return rc;
+  if ((rc = dhs_resolve(p, st))) return rc;
+  return launch_gathers(p, st, true);
+}
+
+// Validate appends as dhs_append does (distinct admitted pairs, count <= T,
+// room left) without launching anything.
+static int validate_appends(dhs_pool* p, const dhs_append_item* items, int32_t n_items) {
+  if (n_items < 0 || (n_items > 0 && !items)) return DHS_EINVAL;
   const dhs_pool_config& c = p->cfg;
-  dhs::GatherCommon g{};
-  g.tail = (const uint8_t*)c.tail_dev;
-  g.opt = (const uint8_t*)c.opt_dev;
-  g.hot = (const uint8_t*)c.hot_dev;
-  g.tail_rows = (uint32_t)(p->pairs * c.tail_rows);
-  g.opt_rows = (uint32_t)(c.optional_pages * c.page_rows);
-  g.hot_rows = (uint32_t)(p->pairs * c.hot_rows);
-  g.row_bytes = c.row_bytes;
-  g.status = p->status;
-  p->gitems.clear();
-  for (int32_t i = 0; i < st->n_items; ++i) {
-    const dhs_item& it = st->items[i];
-    const int32_t n = it.queries * it.topk;
-    if (n == 0) continue;
-    dhs::GatherItem gi{};
-    gi.loc = it.loc_dev;
-    gi.staging = (uint8_t*)it.staging_dev;
-    gi.n = n;
-    p->gitems.push_back(gi);
-  }
-  const size_t ng = p->gitems.size();
-  for (size_t b = 0; b < ng; b += dhs::kGatherItemsLarge) {
-    const int n = (int)std::min<size_t>(dhs::kGatherItemsLarge, ng - b);
-    int64_t tiles = 0;
-    for (int i = 0; i < n; ++i) {
-      dhs::GatherItem& gi = p->gitems[b + i];
-      gi.tile0 = (int32_t)tiles;
-      tiles += (gi.n + dhs::kGatherTileRows - 1) / dhs::kGatherTileRows;
-    }
-    if (tiles > INT32_MAX) return DHS_EINVAL;
-    g.n_tiles = (int32_t)tiles;
-    if (dhs::launch_gather(g, p->gitems.data() + b, n, p->gather_impl, p->stream) !=
-        cudaSuccess)
-      return DHS_ECUDA;
+  std::fill(p->seen.begin(), p->seen.end(), 0);
+  for (int32_t i = 0; i < n_items; ++i) {
+    const dhs_append_item& it = items[i];
+    if (it.req < 0 || it.req >= c.max_requests || it.src < 0 || it.src >= c.sources)
+      return DHS_EINVAL;
+    if (it.count < 0 || it.count > c.tail_rows) return DHS_EINVAL;
+    if (it.count > 0 && !it.rows_dev) return DHS_EINVAL;
+    const int64_t pair = (int64_t)it.req * c.sources + it.src;
+    if (p->seen[pair]) return DHS_EINVAL;
+    p->seen[pair] = 1;
+    const PairState& s = p->ps[pair];
+    if (!s.admitted) return DHS_ESTATE;
+    if (s.L + it.count > c.max_rows_per_request) return DHS_EINVAL;
   }
   return DHS_OK;
 }
 
-int dhs_resolve_gather(dhs_pool* p, const dhs_step* st) {
-  int rc = dhs_resolve(p, st);
+int dhs_decode_step(dhs_pool* p, const dhs_append_item* apps, int32_t n_apps,
+                    const dhs_step* st) {
+  if (!p) return DHS_EINVAL;
+  int rc = validate_appends(p, apps, n_apps);
   if (rc) return rc;
-  return dhs_gather(p, st);
+  if ((rc = validate_step(p, st, true))) return rc;
+  // fold an append into the resolve kernel only when its pair is resolved
+  // in this step; otherwise fall back to a separate append launch
+  const dhs_pool_config& c = p->cfg;
+  bool foldable = true;
+  for (int32_t i = 0; i < n_apps && foldable; ++i) {
+    const int64_t pair = (int64_t)apps[i].req * c.sources + apps[i].src;
+    foldable = p->seen[pair] != 0 || apps[i].count == 0;  // seen: resolving pairs
+  }
+  if (!foldable) {
+    if ((rc = dhs_append(p, apps, n_apps))) return rc;
+    return dhs_resolve_gather(p, st);
+  }
+  if ((rc = enter(p))) return rc;
+  if ((rc = flush(p))) return rc;
+  for (int32_t i = 0; i < n_apps; ++i)
+    if (apps[i].count > 0)
+      p->app_of_pair[(int64_t)apps[i].req * c.sources + apps[i].src] = i;
+  rc = resolve_impl(p, st, apps);
+  for (int32_t i = 0; i < n_apps; ++i)
+    p->app_of_pair[(int64_t)apps[i].req * c.sources + apps[i].src] = -1;
+  if (rc) return rc;
+  return launch_gathers(p, st, true);
 }
 
 int dhs_status(dhs_pool* p, uint32_t* flags) {
@@ -675,6 +809,7 @@ int dhs_status(dhs_pool* p, uint32_t* flags) {
   if (flags) *flags = v;
   if (v & (DHS_STATUS_ERANGE | DHS_STATUS_ELOC)) return DHS_ERANGE;
   if (v & DHS_STATUS_EBUDGET) return DHS_EBUDGET;
+  if (v & DHS_STATUS_ETIMEDOUT) return DHS_ETIMEDOUT;
   return DHS_OK;
 }
 
@@ -786,7 +921,7 @@ extern "C" int dhs_resolve_noalloc(dhs_pool* p, const dhs_step* st) {
       return DHS_ECUDA;
     int ctas = p->copy_ctas;
     if (ctas <= 0) ctas = (int)std::min<int64_t>(32, std::max<int64_t>(4, requests / 4));
-    if (dhs::launch_hostcopy(ccm, citems.data() + b, n, ctas, p->stream) != cudaSuccess)
+    if (dhs::launch_hostcopy(ccm, citems.data() + b, n, ctas, true, p->stream) != cudaSuccess)
       return DHS_ECUDA;
   }
   return DHS_OK;

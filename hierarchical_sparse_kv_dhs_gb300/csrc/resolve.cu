@@ -214,6 +214,7 @@ __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t
     c.miss_count[it.pair] = 0u;
     c.pair_status[it.pair] = code;
     atomicOr(c.status, flag);
+    trace_mark(c.trace, kTraceResolve, true);
   }
 }
 
@@ -232,7 +233,12 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   __shared__ uint32_t scratch[4 * 33];
   __shared__ int s_bad;
 
+  // Dependent launches (the host copy, then the gather) may start now: they
+  // wait for this grid's completion before reading anything it writes.
+  asm volatile("griddepcontrol.launch_dependents;");
+
   const ResolveCommon& c = P.c;
+  if (threadIdx.x == 0) trace_mark(c.trace, kTraceResolve, false);
   const ResolveItem& it = P.items[blockIdx.x];
   const int tid = threadIdx.x, nt = blockDim.x;
   const int B = c.B;
@@ -250,9 +256,24 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   Smem s;
   carve(c.w64cap, c.qkcap, B, &s, smem_raw);
 
+  // ---- decode rows appended by this launch (dhs_decode_step): row L0+j to
+  // tail slot (L0+j) mod T and through to the pinned host copy.  Nothing
+  // below reads them; the gather reads them only after this grid completes.
+  if (it.app_count) {
+    const int rb = c.row_bytes, cpr = rb >> 4;
+    const int total = it.app_count * cpr;
+    for (int ch = tid; ch < total; ch += nt) {
+      const int j = ch / cpr, p = ch - j * cpr;
+      const int64_t row = it.app_L0 + j;
+      const uint4 v = *reinterpret_cast<const uint4*>(it.app_rows + (size_t)j * rb + p * 16);
+      *reinterpret_cast<uint4*>(c.tail + ((size_t)pair * T + (size_t)(row % T)) * rb +
+                                p * 16) = v;
+      *reinterpret_cast<uint4*>(it.app_host + (size_t)row * rb + p * 16) = v;
+    }
+  }
+
   // ---- union of the verify block as a bitmap; range check
   for (int w = tid; w < W; w += nt) s.bm[w] = 0ull;
-  for (int j = tid; j < B; j += nt) s.st[j] = stamps[j];
   if (tid == 0) s_bad = 0;
   __syncthreads();
   for (int e = tid; e < n; e += nt) {
@@ -270,7 +291,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   }
 
   // ---- step 1: tail and ready optional map, word by word
-  uint32_t cnt[4] = {0u, 0u, 0u, 0u};  // unique, tail, opt, -
+  uint32_t cnt[4] = {0u, 0u, 0u, 0u};  // unique, tail, opt, unresolved
   for (int w = tid; w < W; w += nt) {
     const uint64_t bits = s.bm[w];
     uint64_t cand = 0ull;
@@ -282,31 +303,35 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
       cnt[0] += __popcll(bits);
       cnt[1] += __popcll(tm);
       cnt[2] += __popcll(om);
+      cnt[3] += __popcll(cand);
     }
     s.bm[w] = cand;
     s.wpre[w] = (uint32_t)__popcll(cand);
   }
   block_sum4(cnt, scratch);
   const uint32_t n_unique = cnt[0], n_tail = cnt[1], n_opt = cnt[2];
-  const uint32_t C = block_scan_array(s.wpre, W, scratch);  // unresolved rows
+  const uint32_t C = cnt[3];  // rows left for the hot cache (block-uniform)
 
-  // rank -> row for the unresolved rows (ascending)
-  for (int w = tid; w < W; w += nt) {
-    uint64_t m = s.bm[w];
-    uint32_t r = s.wpre[w];
-    while (m) {
-      const int b = __ffsll((long long)m) - 1;
-      m &= m - 1;
-      s.cand_row[r] = (w << 6) + b;
-      s.slot_of[r] = 0xFFFFu;
-      ++r;
-    }
-  }
-  __syncthreads();
-
-  // ---- step 2: every hot slot tests its tag once (B probes in total)
-  uint32_t hv[4] = {0u, 0u, 0xFFFFFFFFu, 0u};  // hits, max probes, -, -
+  uint32_t hits = 0u, m_miss = 0u, scan_max = 0u, evicted = 0u;
   if (C) {
+    block_scan_array(s.wpre, W, scratch);  // candidate ranks
+    for (int j = tid; j < B; j += nt) s.st[j] = stamps[j];
+    // rank -> row for the unresolved rows (ascending)
+    for (int w = tid; w < W; w += nt) {
+      uint64_t m = s.bm[w];
+      uint32_t r = s.wpre[w];
+      while (m) {
+        const int b = __ffsll((long long)m) - 1;
+        m &= m - 1;
+        s.cand_row[r] = (w << 6) + b;
+        s.slot_of[r] = 0xFFFFu;
+        ++r;
+      }
+    }
+    __syncthreads();
+
+    // ---- step 2: every hot slot tests its tag once (B probes in total)
+    uint32_t hv0 = 0u, hv1 = 0u;  // hits, max probes
     for (int j = tid; j < B; j += nt) {
       const int32_t t = tags[j];
       if (t >= 0 && (int64_t)t < L) {
@@ -316,107 +341,103 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
           const uint32_t r = s.wpre[t >> 6] + (uint32_t)__popcll(m & (bit - 1ull));
           s.slot_of[r] = (uint16_t)j;
           s.st[j] = step;
-          hv[0] += 1u;
-          hv[1] = max(hv[1], (uint32_t)(j + 1));
+          hv0 += 1u;
+          hv1 = max(hv1, (uint32_t)(j + 1));
         }
       }
     }
-  }
-  __syncthreads();
-  // unprotected slots and their stamp range
-  uint32_t uv[4] = {0u, 0u, 0xFFFFFFFFu, 0u};  // count, -, min stamp, max stamp
-  for (int j = tid; j < B; j += nt) {
-    const uint32_t x = s.st[j];
-    if (x != step) {
-      uv[0] += 1u;
-      uv[2] = min(uv[2], x);
-      uv[3] = max(uv[3], x);
-    }
-  }
-  uint32_t red[4] = {hv[0], hv[1], uv[2], uv[3]};
-  // hits and max probes, min/max stamps
-  block_smmm(red, scratch);
-  uint32_t cnt2[4] = {uv[0], 0u, 0u, 0u};
-  block_sum4(cnt2, scratch);
-  const uint32_t hits = red[0];
-  const uint32_t m_miss = C - hits;
-  const uint32_t unprot = cnt2[0];
-  uint32_t scan_max = red[1];
-  if (m_miss) scan_max = (uint32_t)B;
-
-  if (m_miss > unprot) {  // more missing rows than victims: change nothing
-    fail_item(c, it, kErrBudget, kStatusEbudget);
-    return;
-  }
-
-  // ---- step 3 victims: the m smallest (stamp, slot) among unprotected slots
-  uint32_t evicted = 0u;
-  if (m_miss) {
-    // stable compaction of unprotected slots, ascending slot order
-    {
-      const int per = (B + nt - 1) / nt;
-      const int b = tid * per, e = min(B, b + per);
-      uint32_t u = 0;
-      for (int j = b; j < e; ++j) u += s.st[j] != step;
-      uint32_t tot;
-      uint32_t pos = block_excl_scan(u, scratch, &tot);
-      for (int j = b; j < e; ++j)
-        if (s.st[j] != step) s.sort_a[pos++] = (uint16_t)j;
-      __syncthreads();
-    }
-    const uint32_t kmin = red[2];
-    const uint32_t span = red[3] - kmin;
-    const int nbits = span ? 32 - __clz(span) : 0;
-    uint16_t* src = s.sort_a;
-    uint16_t* dst = s.sort_b;
-    const int U = (int)unprot;
-    const int per = (U + nt - 1) / nt;
-    const int b = tid * per, e = min(U, b + per);
-    for (int bit = 0; bit < nbits; ++bit) {  // stable LSD split per bit
-      uint32_t z = 0;
-      for (int i = b; i < e; ++i) z += !(((s.st[src[i]] - kmin) >> bit) & 1u);
-      uint32_t ztot;
-      uint32_t zpos = block_excl_scan(z, scratch, &ztot);
-      uint32_t opos = ztot + (uint32_t)max(b, 0) - zpos;
-      for (int i = b; i < e; ++i) {
-        const uint16_t v = src[i];
-        if (((s.st[v] - kmin) >> bit) & 1u) dst[opos++] = v;
-        else dst[zpos++] = v;
-      }
-      __syncthreads();
-      uint16_t* t = src;
-      src = dst;
-      dst = t;
-    }
-    // i-th missing row (ascending) -> i-th victim
-    {
-      const int perc = ((int)C + nt - 1) / nt;
-      const int cb = tid * perc, ce = min((int)C, cb + perc);
-      uint32_t mm = 0;
-      for (int i = cb; i < ce; ++i) mm += s.slot_of[i] == 0xFFFFu;
-      uint32_t mtot;
-      uint32_t mr = block_excl_scan(mm, scratch, &mtot);
-      int32_t* mrows = c.miss_rows + (size_t)pair * c.Mcap;
-      int32_t* mslots = c.miss_slots + (size_t)pair * c.Mcap;
-      for (int i = cb; i < ce; ++i) {
-        if (s.slot_of[i] != 0xFFFFu) continue;
-        const int v = src[mr];
-        const int32_t row = s.cand_row[i];
-        evicted += tags[v] != -1;
-        tags[v] = row;
-        s.st[v] = step;
-        s.slot_of[i] = (uint16_t)v;
-        mrows[mr] = row;
-        mslots[mr] = v;
-        ++mr;
-      }
-    }
     __syncthreads();
-  }
+    // unprotected slots and their stamp range
+    uint32_t un = 0u, umin = 0xFFFFFFFFu, umax = 0u;
+    for (int j = tid; j < B; j += nt) {
+      const uint32_t x = s.st[j];
+      if (x != step) {
+        un += 1u;
+        umin = min(umin, x);
+        umax = max(umax, x);
+      }
+    }
+    uint32_t red[4] = {hv0, hv1, umin, umax};  // {sum, max, min, max}
+    block_smmm(red, scratch);
+    uint32_t cnt2[4] = {un, 0u, 0u, 0u};
+    block_sum4(cnt2, scratch);
+    hits = red[0];
+    m_miss = C - hits;
+    const uint32_t unprot = cnt2[0];
+    scan_max = m_miss ? (uint32_t)B : red[1];
 
-  // ---- commit stamps of every slot hit or filled in this step
-  for (int j = tid; j < B; j += nt)
-    if (s.st[j] == step) stamps[j] = step;
+    if (m_miss > unprot) {  // more missing rows than victims: change nothing
+      fail_item(c, it, kErrBudget, kStatusEbudget);
+      return;
+    }
+
+    // ---- step 3 victims: the m smallest (stamp, slot) among unprotected slots
+    if (m_miss) {
+      {  // stable compaction of unprotected slots, ascending slot order
+        const int per = (B + nt - 1) / nt;
+        const int b = tid * per, e = min(B, b + per);
+        uint32_t u = 0;
+        for (int j = b; j < e; ++j) u += s.st[j] != step;
+        uint32_t tot;
+        uint32_t pos = block_excl_scan(u, scratch, &tot);
+        for (int j = b; j < e; ++j)
+          if (s.st[j] != step) s.sort_a[pos++] = (uint16_t)j;
+        __syncthreads();
+      }
+      const uint32_t kmin = red[2];
+      const uint32_t span = red[3] - kmin;
+      const int nbits = span ? 32 - __clz(span) : 0;
+      uint16_t* src = s.sort_a;
+      uint16_t* dst = s.sort_b;
+      const int U = (int)unprot;
+      const int per = (U + nt - 1) / nt;
+      const int b = tid * per, e = min(U, b + per);
+      for (int bit = 0; bit < nbits; ++bit) {  // stable LSD split per bit
+        uint32_t z = 0;
+        for (int i = b; i < e; ++i) z += !(((s.st[src[i]] - kmin) >> bit) & 1u);
+        uint32_t ztot;
+        uint32_t zpos = block_excl_scan(z, scratch, &ztot);
+        uint32_t opos = ztot + (uint32_t)b - zpos;
+        for (int i = b; i < e; ++i) {
+          const uint16_t v = src[i];
+          if (((s.st[v] - kmin) >> bit) & 1u) dst[opos++] = v;
+          else dst[zpos++] = v;
+        }
+        __syncthreads();
+        uint16_t* t = src;
+        src = dst;
+        dst = t;
+      }
+      // i-th missing row (ascending) -> i-th victim
+      {
+        const int perc = ((int)C + nt - 1) / nt;
+        const int cb = tid * perc, ce = min((int)C, cb + perc);
+        uint32_t mm = 0;
+        for (int i = cb; i < ce; ++i) mm += s.slot_of[i] == 0xFFFFu;
+        uint32_t mtot;
+        uint32_t mr = block_excl_scan(mm, scratch, &mtot);
+        int32_t* mrows = c.miss_rows + (size_t)pair * c.Mcap;
+        int32_t* mslots = c.miss_slots + (size_t)pair * c.Mcap;
+        for (int i = cb; i < ce; ++i) {
+          if (s.slot_of[i] != 0xFFFFu) continue;
+          const int v = src[mr];
+          const int32_t row = s.cand_row[i];
+          evicted += tags[v] != -1;
+          tags[v] = row;
+          s.st[v] = step;
+          s.slot_of[i] = (uint16_t)v;
+          mrows[mr] = row;
+          mslots[mr] = v;
+          ++mr;
+        }
+      }
+      __syncthreads();
+    }
+
+    // ---- commit stamps of every slot hit or filled in this step
+    for (int j = tid; j < B; j += nt)
+      if (s.st[j] == step) stamps[j] = step;
+  }
 
   // ---- location vector
   const int ps = c.page_shift;
@@ -440,8 +461,11 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
     it.loc[e] = loc;
   }
 
-  uint32_t ev[4] = {evicted, 0u, 0u, 0u};
-  block_sum4(ev, scratch);
+  if (m_miss) {
+    uint32_t ev[4] = {evicted, 0u, 0u, 0u};
+    block_sum4(ev, scratch);
+    evicted = ev[0];
+  }
   if (tid == 0) {
     if (it.counters) {
       it.counters[0] = (uint32_t)n;
@@ -451,10 +475,11 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
       it.counters[4] = hits;
       it.counters[5] = m_miss;
       it.counters[6] = scan_max;
-      it.counters[7] = ev[0];
+      it.counters[7] = evicted;
     }
     c.miss_count[pair] = m_miss;
     c.pair_status[pair] = 0;
+    trace_mark(c.trace, kTraceResolve, true);
   }
 }
 
@@ -492,6 +517,12 @@ cudaError_t resolve_set_smem_limit(size_t bytes) {
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(resolve_kernel<kResolveItemsLarge>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+cudaError_t resolve_set_carveout() {
+  cudaError_t e = cudaFuncSetAttribute(resolve_kernel<kResolveItemsSmall>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(resolve_kernel<kResolveItemsLarge>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
 }
 
 cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,

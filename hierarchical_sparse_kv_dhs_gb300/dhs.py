@@ -34,10 +34,12 @@ RC_NAMES = {0: 0, -1: "einval", -2: "enomem", -3: "wouldwait", -4: "ebudget",
 DHS_TIER_TAIL, DHS_TIER_OPT, DHS_TIER_HOT = 0, 1, 2
 DHS_NO_LOC = 0xFFFFFFFF
 DHS_NUM_COUNTERS = 8
-DHS_STATUS_ERANGE, DHS_STATUS_EBUDGET, DHS_STATUS_ELOC = 1, 2, 4
+DHS_STATUS_ERANGE, DHS_STATUS_EBUDGET, DHS_STATUS_ELOC, DHS_STATUS_ETIMEDOUT = 1, 2, 4, 8
 DHS_ITEM_GATHER_ONLY = 1
 DHS_OPT_COPY_CTAS = 1
 DHS_OPT_GATHER_IMPL = 2
+DHS_OPT_TRACE = 3
+DHS_OPT_EARLY = 4
 DHS_BUF_HOT, DHS_BUF_TAIL, DHS_BUF_OPT, DHS_BUF_META = range(4)
 
 _i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
@@ -88,6 +90,7 @@ def _load():
         "dhs_resolve": (ctypes.c_int, [_vp, P(dhs_step)]),
         "dhs_gather": (ctypes.c_int, [_vp, P(dhs_step)]),
         "dhs_resolve_gather": (ctypes.c_int, [_vp, P(dhs_step)]),
+        "dhs_decode_step": (ctypes.c_int, [_vp, P(dhs_append_item), _i32, P(dhs_step)]),
         "dhs_status": (ctypes.c_int, [_vp, P(_u32)]),
         "dhs_read_state": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp]),
         "dhs_set_option": (ctypes.c_int, [_vp, _i32, _i64]),
@@ -184,6 +187,11 @@ def dhs_gather(h, st: dhs_step):
 
 def dhs_resolve_gather(h, st: dhs_step):
     return lib.dhs_resolve_gather(h, ctypes.byref(st))
+
+
+def dhs_decode_step(h, appends, st: dhs_step):
+    arr = (dhs_append_item * max(1, len(appends)))(*appends)
+    return lib.dhs_decode_step(h, arr, len(appends), ctypes.byref(st))
 
 
 def dhs_status(h):

@@ -11,11 +11,12 @@ Pinned host memory: one registered buffer [R*S][max_rows][row_bytes] holding
 every (request, source)'s imported rows, with room for the decode rows the
 library writes through.
 
-A decode step (``step``) is one ``dhs_append`` (every source's new rows)
-and one ``dhs_resolve_gather`` over R x layers items: each source's own
-resolution, then the gathers of all layers, Reuse layers gathering source
-0's location vector as DHS_ITEM_GATHER_ONLY items.  The ctypes descriptors
-of every step are built before the first step, so a step costs two C calls.
+A decode step (``step``) is one ``dhs_decode_step``: every source's new
+rows are appended, then R x layers items are resolved and gathered -- each
+source's own resolution, then the gathers of all layers, Reuse layers
+gathering source 0's location vector as DHS_ITEM_GATHER_ONLY items.  The
+ctypes descriptors of every step are built before the first step, so a step
+costs one C call.
 """
 from __future__ import annotations
 
@@ -44,7 +45,7 @@ class _Admit:
 
 class GpuRun:
     def __init__(self, cfg: Config, wl: Workload | None = None, device="cuda",
-                 host_threads=None):
+                 host_threads=None, gather_impl=None):
         self.cfg = c = cfg
         self.wl = wl or Workload(cfg)
         self.device = torch.device(device)
@@ -58,6 +59,8 @@ class GpuRun:
             page_rows=c.page_rows, tail_rows=c.tail, hot_rows=c.hot,
             max_queries=c.queries, max_topk=c.topk, max_rows_per_request=c.max_rows,
             optional_pages=c.pool_pages(), device=self.device)
+        if gather_impl is not None:
+            self.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, gather_impl)
         rb = c.row_bytes
         self.host = dhs.HostRows(c.pairs * c.max_rows * rb)
         self.wl.fill_host_rows(self.host.ptr, c.max_rows, nthreads=host_threads)
@@ -141,12 +144,18 @@ class GpuRun:
         st, _ = self._steps[step - 1]
         dhs.check(dhs.lib.dhs_gather(self.pool.h, ctypes.byref(st)), "dhs_gather")
 
-    def step(self, step):
-        """One decode step: append, then resolve + gather every layer."""
-        self.append(step)
+    def step(self, step, fused=True):
+        """One decode step: append, then resolve + gather every layer -- one
+        dhs_decode_step call, or dhs_append, dhs_resolve, dhs_gather."""
+        if not fused:
+            self.append(step)
+            self.resolve(step)
+            self.gather(step)
+            return
+        arr, n = self._appends[step - 1]
         st, _ = self._steps[step - 1]
-        dhs.check(dhs.lib.dhs_resolve_gather(self.pool.h, ctypes.byref(st)),
-                  "dhs_resolve_gather")
+        dhs.check(dhs.lib.dhs_decode_step(self.pool.h, arr, n, ctypes.byref(st)),
+                  "dhs_decode_step")
 
     def reset(self):
         """Release every request and admit it again: the pool returns to its

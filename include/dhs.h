@@ -51,7 +51,7 @@ extern "C" {
 #define DHS_EWOULDWAIT (-3) /* capacity cannot be covered: the admission waits */
 #define DHS_EBUDGET (-4)    /* device: more missing rows than unprotected slots */
 #define DHS_ERANGE (-5)     /* device: selected row or location out of range */
-#define DHS_ETIMEDOUT (-6)  /* reserved: a bounded device wait gave up */
+#define DHS_ETIMEDOUT (-6)  /* device: a bounded wait gave up (sticky flag) */
 #define DHS_ECUDA (-7)      /* a CUDA runtime call or launch failed */
 #define DHS_ESTATE (-8)     /* request/source not admitted, or already admitted */
 
@@ -85,6 +85,7 @@ enum {
 #define DHS_STATUS_ERANGE 1u  /* a selection held a row outside [0, L) */
 #define DHS_STATUS_EBUDGET 2u /* a resolve needed more victims than slots */
 #define DHS_STATUS_ELOC 4u    /* a gather location pointed outside its arena */
+#define DHS_STATUS_ETIMEDOUT 8u /* a bounded device wait gave up; its tile was skipped */
 
 /* ------------------------------------------------------------ pool */
 typedef struct dhs_pool dhs_pool;
@@ -261,9 +262,10 @@ int dhs_resolve(dhs_pool *pool, const dhs_step *step);
 
 /*
  * Gather: staging_dev[q][i] = the row at loc_dev[q][i] for every item
- * (resolved or gather-only); DHS_NO_LOC rows become zeros.  Stream-ordered
- * after any earlier dhs_resolve.  Errors: DHS_EINVAL, DHS_ECUDA;
- * out-of-arena locations -> zeros + DHS_STATUS_ELOC.
+ * (resolved or gather-only); DHS_NO_LOC rows become zeros.  staging_dev must
+ * be 16-byte aligned.  Stream-ordered after any earlier dhs_resolve.
+ * Errors: DHS_EINVAL, DHS_ECUDA; out-of-arena locations -> zeros +
+ * DHS_STATUS_ELOC.
  */
 int dhs_gather(dhs_pool *pool, const dhs_step *step);
 
@@ -292,14 +294,31 @@ int dhs_gather(dhs_pool *pool, const dhs_step *step);
  */
 int dhs_resolve_noalloc(dhs_pool *pool, const dhs_step *step);
 
-/* dhs_resolve followed by dhs_gather on the same step. */
+/*
+ * dhs_resolve followed by dhs_gather on the same step, with the same results.
+ * The kernels overlap (programmatic dependent launch): rows that resolve in
+ * step 1 (tail, ready optional page) are copied into staging while the
+ * resolve kernel still runs; rows that need the hot cache wait for it.
+ */
 int dhs_resolve_gather(dhs_pool *pool, const dhs_step *step);
+
+/*
+ * One whole decode step: dhs_append(appends) then dhs_resolve_gather(step),
+ * with the same results.  When every appending pair is also resolved in
+ * `step`, the appends are carried out by the resolve kernel itself (one
+ * launch fewer), and the gather copies those new rows only after the resolve
+ * kernel has finished.  Otherwise it runs the three calls in order.
+ * Errors: as dhs_append and dhs_resolve_gather; on a validation error
+ * nothing is appended or launched.
+ */
+int dhs_decode_step(dhs_pool *pool, const dhs_append_item *appends, int32_t n_appends,
+                    const dhs_step *step);
 
 /*
  * Synchronise the pool's stream, read and clear the sticky device status.
  * *flags (may be NULL) receives DHS_STATUS_* bits.  Returns DHS_OK when no
- * flag was set, else DHS_ERANGE (ERANGE or ELOC) or DHS_EBUDGET, or
- * DHS_ECUDA if the stream reported an error.
+ * flag was set, else DHS_ERANGE (ERANGE or ELOC), DHS_EBUDGET or
+ * DHS_ETIMEDOUT, or DHS_ECUDA if the stream reported an error.
  */
 int dhs_status(dhs_pool *pool, uint32_t *flags);
 
@@ -315,7 +334,18 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
 
 /* Tunables (performance only; results do not depend on them). */
 #define DHS_OPT_COPY_CTAS 1 /* host-copy CTAs; 0 = clamp(requests/4, 4, 32) */
-#define DHS_OPT_GATHER_IMPL 2 /* 0 = 16-byte vector copy, 1 = TMA bulk copy */
+#define DHS_OPT_GATHER_IMPL 2 /* 1 = TMA bulk copy, persistent (default);
+                                 0 = 16-byte vector copy, one CTA per tile */
+/* Timeline: value = address of a device buffer of 8 uint64 (0 = off).  Each
+ * kernel kind k (0 resolve, 1 host copy, 2 gather) atomically lowers
+ * buf[2k] to its earliest CTA start and raises buf[2k+1] to its latest CTA
+ * end (%globaltimer, ns); the caller initialises buf[2k] to UINT64_MAX and
+ * buf[2k+1] to 0.  buf[6] / buf[7]: sum / count of the TMA gather's warp
+ * start times after buf[0] (initialise both to 0). */
+#define DHS_OPT_TRACE 3
+/* 1 (default): fused gathers copy step-1 rows while the resolve kernel runs;
+ * 0: they wait for it first. */
+#define DHS_OPT_EARLY 4
 int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
 
 /* Static string for a DHS_* code. */

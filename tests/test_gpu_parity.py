@@ -35,11 +35,17 @@ def _as_u32(t):
     return t.cpu().numpy().view(np.uint32)
 
 
-def compare_run(cfg: Config, sampled=None, check_all_bytes=True):
+def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
+                gather_impl=0, patch=None, early=1):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
-    gpu = GpuRun(cfg, wl)
+    if patch:
+        patch(wl)
+    gpu = GpuRun(cfg, wl, gather_impl=gather_impl)
+    if not early:
+        from hierarchical_sparse_kv_dhs_gb300 import dhs
+        gpu.pool.set_option(dhs.DHS_OPT_EARLY, 0)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
     orc = OracleRun(cfg, wl, requests=sampled)
     try:
@@ -50,15 +56,17 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True):
                 assert np.array_equal(g_pages, o_pages), (r, s)
         assert gpu.pool.used() == orc.pool.used()
         for step in range(1, cfg.total_steps + 1):
-            gpu.step(step)
+            gpu.step(step, fused=fused)
             res = orc.step(step)
             rc, flags = gpu.status()
             want_flags = 0
             for r in sampled:
                 for s in range(cfg.sources):
-                    if res[r]["rc"][s] == "ebudget":
-                        want_flags |= 2
-            assert rc == 0 or want_flags, (step, rc, flags)
+                    want_flags |= {0: 0, "erange": 1, "ebudget": 2}[res[r]["rc"][s]]
+            if len(sampled) == cfg.requests:
+                assert flags == want_flags, (step, rc, flags, want_flags)
+            else:
+                assert (flags & ~3) == 0 and (flags & want_flags) == want_flags
             loc_all = _as_u32(gpu.loc)
             cnt_all = _as_u32(gpu.counters)
             for r in sampled:
@@ -125,15 +133,79 @@ SMALL = [
 
 
 @pytest.mark.parametrize("cfg", SMALL, ids=[c.name for c in SMALL])
-def test_small_configs_bit_exact(cfg):
-    compare_run(cfg)
+@pytest.mark.parametrize("mode", ["fused-lsu", "fused-tma", "split-tma", "fused-tma-late",
+                                  "fused-lsu-late"])
+def test_small_configs_bit_exact(cfg, mode):
+    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=1 if "tma" in mode else 0,
+                early=0 if mode.endswith("late") else 1)
+
+
+def _bad_row(wl):
+    """Step 3 of request 1 source 0 selects row L (one past the end)."""
+    sel = wl.selections()
+    sel[2, 1, 0, 0, 5] = wl.length(1, 3)
+
+
+@pytest.mark.parametrize("mode", ["fused-lsu", "fused-tma", "split-lsu"])
+def test_out_of_range_row_zeroes_the_item(mode):
+    cfg = TINY.scaled(name="range", tag=46, requests=2, sources=2, steps=4, residency=0.6)
+    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=1 if "tma" in mode else 0,
+                patch=_bad_row)
+
+
+@pytest.mark.parametrize("mode", ["fused-lsu", "fused-tma"])
+def test_budget_overflow_zeroes_the_item(mode):
+    # 16 hot slots, no residency: most steps need more victims than slots
+    cfg = TINY.scaled(name="budget", tag=47, requests=2, sources=1, hot=16, topk=64,
+                      residency=0.0, steps=4)
+    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=1 if "tma" in mode else 0)
 
 
 # ------------------------------------------------------------ full size
 
-def test_c8_full_size_sampled():
-    compare_run(C8, sampled=[0, 5])
+@pytest.mark.parametrize("impl,early", [(0, 1), (1, 1), (1, 0)])
+def test_c8_full_size_sampled(impl, early):
+    compare_run(C8, sampled=[0, 5], gather_impl=impl, early=early)
 
 
 def test_c64_full_size_sampled():
     compare_run(C64, sampled=[0, 63], check_all_bytes=False)
+
+
+def test_decode_step_fallback_matches_split_calls():
+    """dhs_decode_step where some appending pairs are not resolved in the
+    step (it must append separately) gives what dhs_append + dhs_resolve +
+    dhs_gather give."""
+    import ctypes
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    cfg = TINY.scaled(name="fallback", tag=48, requests=3, sources=2, steps=3,
+                      residency=0.3, hot=300)
+    wl = Workload(cfg)
+    a, b = GpuRun(cfg, wl), GpuRun(cfg, wl)
+    try:
+        for step in range(1, cfg.total_steps + 1):
+            apps, n = a._appends[step - 1]
+            st, items = a._steps[step - 1]
+            sub = [items[i] for i in range(len(items)) if items[i].req == 1]
+            st_a, keep_a = dhs.make_step(step, sub)
+            assert dhs.lib.dhs_append(a.pool.h, apps, n) == 0
+            assert dhs.lib.dhs_resolve(a.pool.h, ctypes.byref(st_a)) == 0
+            assert dhs.lib.dhs_gather(a.pool.h, ctypes.byref(st_a)) == 0
+            apps_b, nb = b._appends[step - 1]
+            st_b0, items_b = b._steps[step - 1]
+            sub_b = [items_b[i] for i in range(len(items_b)) if items_b[i].req == 1]
+            st_b, keep_b = dhs.make_step(step, sub_b)
+            assert dhs.lib.dhs_decode_step(b.pool.h, apps_b, nb, ctypes.byref(st_b)) == 0
+            torch.cuda.synchronize()
+            assert a.status() == (0, 0) and b.status() == (0, 0)
+            assert torch.equal(a.loc[1], b.loc[1]) and torch.equal(a.counters[1], b.counters[1])
+            assert torch.equal(a.staging[1].view(torch.int16), b.staging[1].view(torch.int16))
+        for r in range(cfg.requests):
+            for s in range(cfg.sources):
+                L = wl.length(r, cfg.total_steps)
+                assert np.array_equal(a.host_rows(r, s, 0, L), b.host_rows(r, s, 0, L))
+                assert a.pool.read_state(r, s)[3][1] == b.pool.read_state(r, s)[3][1] == L
+    finally:
+        a.close()
+        b.close()
