@@ -432,7 +432,7 @@ def main():
     n_gather = -(-cfg.requests * cfg.layers // 384)
     launches = K * (2 * n_resolve + n_gather)  # append folded into resolve
     step_bytes = alg_bytes + cfg.resolved_per_step * 4
-    impl = ["lsu", "tma"][args.gather_impl]
+    impl = ["vector", "tma"][args.gather_impl]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": sum(step_ms) / K,

@@ -20,6 +20,12 @@ constexpr uint32_t kStatusEtimeout = 8u;
 constexpr int32_t kErrRange = -5, kErrBudget = -4;  // DHS_ERANGE, DHS_EBUDGET
 constexpr int kMaxHotRows = 16384;
 
+// Per-item verdicts the resolve kernel publishes as soon as they are decided
+// (read by the fused gather): ((launch sequence & kSeqMask) << kVerdictShift)
+// | code.
+constexpr uint32_t kVerdictOk = 1u, kVerdictRange = 2u, kVerdictBudget = 3u;
+constexpr uint32_t kVerdictShift = 3u, kVerdictCodeMask = 7u, kSeqMask = 0x1FFFFFFFu;
+
 // Optional timeline (DHS_OPT_TRACE): per kernel kind, the earliest CTA start
 // and the latest CTA end in %globaltimer nanoseconds.
 enum TraceSlot { kTraceResolve = 0, kTraceCopy = 1, kTraceGather = 2, kTraceKinds = 4 };
@@ -78,6 +84,9 @@ struct ResolveCommon {
   int32_t row_bytes;
   uint8_t* tail;         // tail arena (appends folded into the launch)
   unsigned long long* trace;  // null = off
+  uint32_t* verdict;     // [pairs] published verdicts, null = none
+  uint32_t seq;          // sequence number of this launch
+  int32_t pad2;
 };
 
 size_t resolve_smem_bytes(int w64cap, int qkcap, int B);
@@ -109,6 +118,7 @@ cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,
 
 // ------------------------------------------------------------ gather (e)
 constexpr int kGatherThreads = 256;
+constexpr int kGatherVector = 0, kGatherTma = 1;  // DHS_OPT_GATHER_IMPL values
 constexpr int kGatherTileRows = 32;
 constexpr int kGatherItemsLarge = 384, kGatherItemsSmall = 64;
 
@@ -121,7 +131,7 @@ struct GatherItem {
   int32_t n;           // entries
   int32_t tile0;       // first tile of this item in the launch
   int32_t pair;        // req * S + src (resolved items)
-  int32_t ent0;        // first entry of this item in the launch (items back to back)
+  uint32_t seq;        // sequence number of the resolve launch that resolved it
 };
 
 struct GatherCommon {
@@ -135,11 +145,9 @@ struct GatherCommon {
   uint32_t* status;
   int32_t n_items;
   int32_t n_tiles;
-  int64_t n_entries;  // entries of all items of the launch
   int32_t T, Pmax, page_shift;
-  int32_t early;    // copy step-1 rows before waiting for the resolve grid
-  int32_t tma_grid; // co-resident warps of the TMA gather (persistent grid)
-  uint32_t* done;   // finished-CTA ticket of the running launch (reset by its last CTA)
+  int32_t early;             // copy step-1 rows before waiting for the resolve grid
+  const uint32_t* verdict;   // [pairs] verdicts published by the resolve kernel
   unsigned long long* trace;  // null = off
 };
 
@@ -154,9 +162,8 @@ cudaError_t append_set_carveout();
 cudaError_t launch_gather(const GatherCommon& c, const GatherItem* items,
                           int n_items, bool pdl, int impl, cudaStream_t stream);
 
-// Co-resident warps of the TMA gather on the current device (0 on error);
-// also raises its shared-memory limit.
-int gather_tma_grid(int row_bytes);
+// Raise the TMA gather's dynamic shared-memory limit for a row size.
+cudaError_t gather_set_smem_limit(int row_bytes);
 
 // ------------------------------------------------------------ append (A0)
 constexpr int kAppendThreads = 256;

@@ -1,30 +1,29 @@
-// Gather kernel: staging[item][q][i] = the KV row at loc[item][q][i].
+// Gather kernels: staging[item][q][i] = the KV row at loc[item][q][i].
 //
 // "Adaptive DHiSparse", How it works: selected rows are consumed by sparse
 // attention from verification staging; Reuse layers gather an inherited
-// location vector.  This is the byte-dominant step of the decode path (2 x
-// 1152 bytes per entry against 4 bytes of location), a pure HBM copy, so it
-// is built for coalescing, not arithmetic:
-//   * one CTA per tile of 32 entries of one item; the 32 row addresses are
-//     resolved once into shared memory (tier -> arena, bounds-checked);
-//   * the tile is 32 x 72 chunks of 16 bytes = 2304 chunks = 9 per thread;
-//     consecutive threads read consecutive 16-byte chunks of a row (each
-//     1152-byte row is nine whole 128-byte lines) and write consecutive
-//     chunks of the contiguous staging tile, so every load and store is a
-//     full-line coalesced access;
-//   * all nine loads are issued before the first store (36 KB in flight per
-//     CTA) to cover HBM latency; loads use the non-coherent no-allocate path.
+// location vector.  This is the byte-dominant step of the decode path
+// (1152 bytes read + 1152 written per entry against 4 bytes of location), a
+// pure HBM copy, so it is built for memory-level parallelism, not arithmetic.
+// One CTA per tile of 32 entries of one item; two implementations:
+//   * TMA (default): one warp per tile; lane e moves entry e with one bulk
+//     copy (cp.async.bulk) global -> shared, completion counted on an
+//     mbarrier, then one bulk copy shared -> staging.  No row byte passes
+//     through registers; six 36 KB tiles stay in flight per SM.
+//   * vector: 256 threads per tile, 9 x 16-byte loads in flight per thread,
+//     consecutive threads on consecutive 16-byte chunks (full-line coalesced).
 //
-// Early phase (fused resolve + gather only).  Where a row resolves in step 1
-// of "Resolution" -- the tail (row >= L - T) or a ready optional page -- its
-// location is a pure function of the row, L, T and the page map, none of
+// Early phase (fused resolve + gather).  A row that resolves in step 1 of
+// "Resolution" -- the tail (row >= L - T) or a ready optional page -- has a
+// location that is a pure function of the row, L, T and the page map, none of
 // which the resolve kernel of the same step changes.  The fused launch
-// therefore copies those rows at once, while the resolve and host-copy
-// kernels still run (programmatic dependent launch), and waits for them
-// (griddepcontrol.wait) only before rows that need the hot cache.  After the
-// wait a tile re-checks its item's resolve status: a failed item (row out of
-// range, budget overflow) gets zeros everywhere, exactly as without the
-// early phase.
+// (programmatic dependent launch) therefore copies those rows while the
+// resolve kernel still runs, and only tiles with rows that need the hot cache
+// wait (griddepcontrol.wait) for the resolve / host-copy grids.  The resolve
+// kernel publishes each item's verdict (resolved / row out of range / budget
+// overflow) as soon as it is decided; after its early copies a tile reads its
+// item's verdict -- or waits for the resolve grid if it is not out yet -- and
+// a failed item's rows become zeros, exactly as its locations say.
 #include "dhs_internal.h"
 
 namespace dhs {
@@ -41,6 +40,15 @@ __device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
+  return v;
+}
+
+// A verdict guards no other data (it only decides whether a tile's rows
+// become zeros), so a relaxed load suffices and does not hold back the
+// address loads issued after it.
+__device__ __forceinline__ uint32_t ld_verdict(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
@@ -71,10 +79,11 @@ __device__ __forceinline__ const uint8_t* row_ptr(const GatherCommon& c, uint32_
 }
 
 // Step-1 row address of `row` of an item, or nullptr if the row needs the
-// hot cache (or is out of range, which the resolve kernel reports).
+// hot cache, was appended by this launch, or is out of range (which the
+// resolve kernel reports).
 __device__ __forceinline__ const uint8_t* step1_ptr(const GatherCommon& c,
                                                     const GatherItem& it, int32_t row) {
-  if (row < 0 || (int64_t)row >= it.L0) return nullptr;  // incl. rows appended now
+  if (row < 0 || (int64_t)row >= it.L0) return nullptr;
   const int64_t T = c.T;
   if ((int64_t)row >= it.L - T)
     return c.tail + ((size_t)it.pair * T + (size_t)((int64_t)row % T)) * c.row_bytes;
@@ -86,6 +95,34 @@ __device__ __forceinline__ const uint8_t* step1_ptr(const GatherCommon& c,
   const int64_t idx = ((int64_t)slot << ps) + (row & (((int64_t)1 << ps) - 1));
   return c.opt + (size_t)idx * c.row_bytes;
 }
+
+// Verdict of an early item's resolution (kVerdictOk / kVerdictRange /
+// kVerdictBudget).  `v` was read when the CTA started (in parallel with its
+// address loads); if it was not published then, read it again, and if it is
+// still not out, wait for the resolve grid (*waited = true) and read it.
+// Every thread of the CTA calls it and gets the same result.
+__device__ __forceinline__ uint32_t item_verdict(const GatherCommon& c, const GatherItem& it,
+                                                 uint32_t v, bool* waited) {
+  const uint32_t want = it.seq & kSeqMask;
+  if ((v >> kVerdictShift) != want) v = ld_verdict(&c.verdict[it.pair]);
+  if ((v >> kVerdictShift) != want) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    *waited = true;
+    v = ld_verdict(&c.verdict[it.pair]);
+  }
+  return v & kVerdictCodeMask;
+}
+
+// End of a gather CTA.  The gather grid must not complete before the resolve
+// / host-copy grids it overlaps (stream order for whatever follows), so its
+// last block waits for them; every other CTA leaves as soon as its rows are
+// written.
+__device__ __forceinline__ void end_grid(const GatherCommon& c) {
+  if (blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) trace_mark(c.trace, kTraceGather, true);
+}
+
+// ---------------------------------------------------------------- vector variant
 
 // Copy the entries of the tile whose s_phase equals `phase`.
 template <int CPR>
@@ -128,40 +165,6 @@ __device__ __forceinline__ void copy_tile(const GatherCommon& c, uint8_t* dst,
   }
 }
 
-// After the whole grid has written its rows: the last CTA to finish (an
-// atomic ticket, no waiting on other CTAs) waits for the resolve / host-copy
-// grids -- so the gather grid never completes before them -- zeroes the
-// staging of every early item whose resolution failed (its step-1 rows may
-// already have been copied), and resets the ticket for the next launch.
-template <int MAXI>
-__device__ void finish_grid(const GatherParams<MAXI>& P) {
-  const GatherCommon& c = P.c;
-  __shared__ int s_last;
-  __threadfence();  // this CTA's staging writes are visible before its ticket
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    s_last = atomicAdd(c.done, 1u) == gridDim.x - 1;
-    trace_mark(c.trace, kTraceGather, true);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  __threadfence();
-  if (c.early) {
-    for (int i = 0; i < c.n_items; ++i) {
-      const GatherItem& it = P.items[i];
-      if (!it.sel || c.pair_status[it.pair] == 0) continue;
-      uint4* d = reinterpret_cast<uint4*>(it.staging);
-      const size_t chunks = (size_t)it.n * (c.row_bytes >> 4);
-      for (size_t j = threadIdx.x; j < chunks; j += blockDim.x) d[j] = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  if (threadIdx.x == 0) {
-    *c.done = 0u;
-    trace_mark(c.trace, kTraceGather, true);
-  }
-}
-
 // CPR = 16-byte chunks per row (0: runtime value).
 template <int MAXI, int CPR>
 __global__ void __launch_bounds__(kGatherThreads)
@@ -174,11 +177,13 @@ __global__ void __launch_bounds__(kGatherThreads)
   const int e0 = (tile - it.tile0) * kGatherTileRows;
   const int ne = min(kGatherTileRows, it.n - e0);
   const int tid = threadIdx.x;
-  if (tid == 0) trace_mark(c.trace, kTraceGather, false);
   uint8_t* dst = it.staging + (size_t)e0 * c.row_bytes;
   const bool early = c.early && it.sel != nullptr;
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (tid == 0) trace_mark(c.trace, kTraceGather, false);
 
   // phase 0: rows resolved in step 1 (fused launch only)
+  const uint32_t v0 = early ? ld_verdict(&c.verdict[it.pair]) : 0u;
   int deferred = 0;
   if (tid < ne) {
     const uint8_t* p = early ? step1_ptr(c, it, it.sel[e0 + tid]) : nullptr;
@@ -187,31 +192,35 @@ __global__ void __launch_bounds__(kGatherThreads)
     deferred = p == nullptr;
   }
   const int any_deferred = __syncthreads_or(deferred);
-#pragma unroll 1
-  for (int ph = early ? 0 : 1; ph < 2; ++ph) {
-    if (ph == 1) {
-      if (!any_deferred) break;
-      // rows that needed the hot cache: wait for the resolve / host-copy grids
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      if (tid < ne && s_phase[tid] == 1) s_src[tid] = row_ptr(c, it.loc[e0 + tid]);
+  bool waited = false;
+  if (early) {
+    copy_tile<CPR>(c, dst, s_src, s_phase, ne, 0);
+    if (item_verdict(c, it, v0, &waited) != kVerdictOk) {
+      // the item failed: every entry becomes zeros (each 16-byte chunk is
+      // rewritten by the thread that wrote it above)
       __syncthreads();
+      if (tid < ne) s_src[tid] = nullptr;
+      __syncthreads();
+      copy_tile<CPR>(c, dst, s_src, s_phase, ne, 0);
+      copy_tile<CPR>(c, dst, s_src, s_phase, ne, 1);
+      end_grid(c);
+      return;
     }
-    copy_tile<CPR>(c, dst, s_src, s_phase, ne, ph);
   }
-  finish_grid(P);
+  if (any_deferred) {
+    // rows that needed the hot cache (or no early phase): wait for the
+    // resolve / host-copy grids (a no-op without programmatic dependent launch)
+    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid < ne && s_phase[tid] == 1) s_src[tid] = row_ptr(c, it.loc[e0 + tid]);
+    __syncthreads();
+    copy_tile<CPR>(c, dst, s_src, s_phase, ne, 1);
+  }
+  end_grid(c);
 }
 
 // ---------------------------------------------------------------- TMA variant
-// One warp per 32-entry tile: lane e moves entry e with one bulk copy
-// (cp.async.bulk) global -> shared, completion counted on an mbarrier, then
-// one bulk copy shared -> staging.  No row bytes pass through registers, so
-// 6 tiles (36 KB each) stay in flight per SM with 32 threads apiece.
-constexpr int kTmaThreads = 32;
-constexpr int kTmaMaxLocal = 256;  // tiles per warp (deferred-lane masks in shared memory)
 
-__host__ __device__ inline size_t tma_smem_bytes(int row_bytes) {
-  return 2 * (size_t)kGatherTileRows * row_bytes + kTmaMaxLocal * sizeof(uint32_t);
-}
+constexpr int kTmaThreads = 32;
 constexpr uint32_t kWaitPolls = 1u << 26;  // bounded mbarrier wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -257,179 +266,87 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uin
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Persistent, double-buffered, software-pipelined.  The launch's entries
-// (all items back to back) are split evenly over the warps; warp b moves its
-// range in chunks of 32 rows (lane l: entry chunk_start + l, each lane finds
-// its own item, so a chunk may straddle items).  Four chunks are in the pipe:
-// the bulk copies of chunk i land in one buffer while chunk i+1's bulk loads
-// fill the other, chunk i+2's row addresses are computed (for step-1 rows:
-// one page-map read) and chunk i+3's selection / location entries are loaded,
-// so address latency overlaps data movement.  With the early phase on, pass 0
-// moves the step-1 rows and records, per chunk, the lanes still waiting for
-// the hot cache; after one griddepcontrol.wait, pass 1 moves only those.
-struct TmaSlot {
-  const uint8_t* src;  // row to load (nullptr: zeros)
-  uint8_t* dst;        // staging row
-  bool mine;           // this lane moves a row in this chunk
-  unsigned lmask;      // lanes with a bulk load in flight
-};
-
-template <int MAXI>
-__device__ __forceinline__ int find_item_entry(const GatherParams<MAXI>& P, int g) {
-  int lo = 0, hi = P.c.n_items - 1;  // last item whose first entry <= g
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.items[mid].ent0 <= g) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 template <int MAXI>
 __global__ void __launch_bounds__(kTmaThreads)
     gather_tma_kernel(const __grid_constant__ GatherParams<MAXI> P) {
-  extern __shared__ __align__(128) uint8_t s_dyn[];  // [2][32][rb], then chunk masks
-  __shared__ __align__(8) uint64_t s_bar[2];
+  extern __shared__ __align__(128) uint8_t s_rows[];  // [32][row_bytes]
+  __shared__ __align__(8) uint64_t s_bar;
   const GatherCommon& c = P.c;
+  const int tile = blockIdx.x;
+  const GatherItem& it = P.items[find_item(P, tile)];
+  const int e0 = (tile - it.tile0) * kGatherTileRows;
+  const int ne = min(kGatherTileRows, it.n - e0);
   const int lane = threadIdx.x;
   const uint32_t rb = (uint32_t)c.row_bytes;
-  const size_t buf_bytes = (size_t)kGatherTileRows * rb;
-  uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_dyn + 2 * buf_bytes);
+  uint8_t* my_row = s_rows + (size_t)lane * rb;
+  uint8_t* dst = it.staging + ((size_t)e0 + lane) * rb;
+  const bool early = c.early && it.sel != nullptr;
+  asm volatile("griddepcontrol.launch_dependents;");
   if (lane == 0) {
     trace_mark(c.trace, kTraceGather, false);
-    if (c.trace) {  // mean warp start, relative to the resolve kernel's start
-      const unsigned long long t0 = *(volatile unsigned long long*)&c.trace[0];
-      atomicAdd(&c.trace[6], trace_now() - t0);
-      atomicAdd(&c.trace[7], 1ull);
-    }
-    mbar_init(&s_bar[0], 1);
-    mbar_init(&s_bar[1], 1);
+    mbar_init(&s_bar, 1);
   }
   __syncwarp();
-  // this warp's entries [lo, hi)
-  const int64_t E = c.n_entries, G = gridDim.x;
-  const int lo = (int)(E * blockIdx.x / G), hi = (int)(E * (blockIdx.x + 1) / G);
-  const int n_local = (hi - lo + kGatherTileRows - 1) / kGatherTileRows;
-  uint32_t parity = 0u;  // bit b: phase parity to wait for on buffer b
+  uint32_t parity = 0;
+  bool stored = false, ok = true, waited = false;
 
-  // pass 0: step-1 rows of early items; pass 1: the rest (after the wait);
-  // pass 2: plain gather, every row from its location.
-  // Stage 1: the lane's entry (selected row or location) of local chunk li.
-  auto load_entry = [&](int li, int pass) -> uint32_t {
-    const int g = lo + li * kGatherTileRows + lane;
-    if (li >= n_local || g >= hi) return 0u;
-    const GatherItem& it = P.items[find_item_entry(P, g)];
-    const int e = g - it.ent0;
-    if (pass == 0) return (c.early && it.sel) ? (uint32_t)it.sel[e] : 0u;
-    if (pass == 1 && !((s_mask[li] >> lane) & 1u)) return 0u;
-    return it.loc[e];
-  };
-  // Stage 2: the lane's row address for local chunk li from its entry.
-  auto prep = [&](int li, int pass, uint32_t entry) -> TmaSlot {
-    TmaSlot t{nullptr, nullptr, false, 0u};
-    if (li >= n_local) return t;
-    const int g = lo + li * kGatherTileRows + lane;
-    const bool valid = g < hi;
-    const GatherItem& it = P.items[find_item_entry(P, valid ? g : hi - 1)];
-    t.dst = it.staging + (size_t)(g - it.ent0) * rb;
-    if (pass == 0) {
-      const bool early = c.early && it.sel != nullptr;
-      const uint8_t* p = (early && valid) ? step1_ptr(c, it, (int32_t)entry) : nullptr;
-      const unsigned defer = __ballot_sync(0xFFFFFFFFu, valid && p == nullptr);
-      if (lane == 0) s_mask[li] = defer;
-      t.src = p;
-      t.mine = p != nullptr;
-    } else {
-      t.mine = pass == 2 ? valid : ((s_mask[li] >> lane) & 1u) != 0u;
-      if (t.mine) t.src = row_ptr(c, entry);
-    }
-    return t;
-  };
-  auto issue = [&](TmaSlot& t, int b) {
-    uint8_t* row = s_dyn + b * buf_bytes + (size_t)lane * rb;
-    const bool load = t.mine && t.src != nullptr;
-    if (t.mine && !load) {  // zeros: plain stores, then hand over to the async proxy
+  // Move entry `lane` (src: row address, nullptr = zeros) when `mine`;
+  // false if the bounded wait gave up.
+  auto move = [&](bool mine, const uint8_t* src) -> bool {
+    const bool load = mine && src != nullptr;
+    const unsigned lmask = __ballot_sync(0xFFFFFFFFu, load);
+    if (mine && !load) {  // zeros: plain stores, then hand over to the async proxy
       for (uint32_t o = 0; o < rb; o += 16)
-        *reinterpret_cast<uint4*>(row + o) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(my_row + o) = make_uint4(0u, 0u, 0u, 0u);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    t.lmask = __ballot_sync(0xFFFFFFFFu, load);
-    if (t.lmask) {
-      if (lane == 0) mbar_arrive_expect(&s_bar[b], (uint32_t)__popc(t.lmask) * rb);
+    if (lmask) {
+      if (lane == 0) mbar_arrive_expect(&s_bar, (uint32_t)__popc(lmask) * rb);
       __syncwarp();
-      if (load) bulk_load(row, t.src, rb, &s_bar[b]);
-    }
-  };
-  auto drain = [&](const TmaSlot& t, int b) -> bool {
-    if (t.lmask) {
-      if (!mbar_wait(&s_bar[b], (parity >> b) & 1u)) {
+      if (load) bulk_load(my_row, src, rb, &s_bar);
+      if (!mbar_wait(&s_bar, parity)) {
         if (lane == 0) atomicOr(c.status, kStatusEtimeout);
         return false;
       }
-      parity ^= 1u << b;
+      parity ^= 1u;
     }
     __syncwarp();
-    if (t.mine)
-      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                   ::"l"(t.dst), "r"(smem_u32(s_dyn + b * buf_bytes + (size_t)lane * rb)),
-                     "r"(rb)
-                   : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");  // one group per chunk
-    return true;
-  };
-  auto run_pass = [&](int pass) -> bool {
-    if (n_local == 0) return true;
-    uint32_t e1 = load_entry(1, pass), e2 = load_entry(2, pass), e3 = 0u;
-    TmaSlot cur = prep(0, pass, load_entry(0, pass));
-    issue(cur, 0);
-    TmaSlot nxt = prep(1, pass, e1);
-    for (int li = 0; li < n_local; ++li) {
-      const int b = li & 1;
-      e3 = load_entry(li + 3, pass);  // in flight while chunk li drains
-      if (li + 1 < n_local) {
-        // the other buffer last held chunk li-1: its stores must have read it
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        issue(nxt, b ^ 1);
-      }
-      const TmaSlot after = prep(li + 2, pass, e2);
-      if (!drain(cur, b)) return false;
-      cur = nxt;
-      nxt = after;
-      e2 = e3;
+    if (mine) {
+      bulk_store(dst, my_row, rb);
+      stored = true;
     }
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     return true;
   };
 
-  if (c.early) {
-    if (run_pass(0)) {
-      __syncwarp();
-      unsigned any = 0u;
-      for (int li = lane; li < n_local; li += 32) any |= s_mask[li];
-      if (__any_sync(0xFFFFFFFFu, any != 0u)) {
-        // rows that needed the hot cache: wait for the resolve / host-copy grids
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        run_pass(1);
-      }
+  const uint32_t v0 = early ? ld_verdict(&c.verdict[it.pair]) : 0u;
+  const uint8_t* src = nullptr;
+  if (early && lane < ne) src = step1_ptr(c, it, it.sel[e0 + lane]);
+  bool deferred = lane < ne && src == nullptr;
+  if (early) {
+    ok = move(src != nullptr, src);  // rows resolved in step 1
+    if (ok && item_verdict(c, it, v0, &waited) != kVerdictOk) {
+      // the item failed: every entry becomes zeros; a row stored above must
+      // be fully written (and its shared-memory copy read) before it is
+      // overwritten
+      if (stored) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      ok = move(lane < ne, nullptr);
+      deferred = false;
     }
-  } else {
-    // locations come from the resolve grid when this launch overlaps it
-    // (a no-op without programmatic dependent launch)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    run_pass(2);
   }
-  // staging writes complete (not only their shared-memory reads) before the
-  // grid-level ticket
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-  finish_grid(P);
+  if (ok && __any_sync(0xFFFFFFFFu, deferred)) {
+    // rows that needed the hot cache (or no early phase): wait for the
+    // resolve / host-copy grids (a no-op without programmatic dependent launch)
+    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+    ok = move(deferred, deferred ? row_ptr(c, it.loc[e0 + lane]) : nullptr);
+  }
+  // shared memory must outlive the stores' reads
+  if (stored) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  end_grid(c);
 }
 
 template <int MAXI>
-cudaError_t launch_t(const GatherCommon& c, const GatherItem* items, int n,
-                     bool pdl, int impl, cudaStream_t stream) {
+cudaError_t launch_t(const GatherCommon& c, const GatherItem* items, int n, bool pdl,
+                     int impl, cudaStream_t stream) {
   GatherParams<MAXI> P;
   P.c = c;
   P.c.n_items = n;
@@ -445,16 +362,9 @@ cudaError_t launch_t(const GatherCommon& c, const GatherItem* items, int n,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  if (impl == 1) {
-    // persistent grid: as many warps as fit, each with at most kTmaMaxLocal
-    // chunks of 32 entries
-    int grid = c.tma_grid;
-    const int64_t per_warp = kTmaMaxLocal * (int64_t)kGatherTileRows;
-    if ((int64_t)grid * per_warp < c.n_entries) grid = (int)((c.n_entries + per_warp - 1) / per_warp);
-    if (grid > c.n_tiles) grid = c.n_tiles;
-    cfg.gridDim = dim3((unsigned)grid);
+  if (impl == kGatherTma) {
     cfg.blockDim = dim3(kTmaThreads);
-    cfg.dynamicSmemBytes = tma_smem_bytes(c.row_bytes);
+    cfg.dynamicSmemBytes = (size_t)kGatherTileRows * c.row_bytes;
     return cudaLaunchKernelEx(&cfg, gather_tma_kernel<MAXI>, P);
   }
   cfg.blockDim = dim3(kGatherThreads);
@@ -462,54 +372,41 @@ cudaError_t launch_t(const GatherCommon& c, const GatherItem* items, int n,
   return cudaLaunchKernelEx(&cfg, gather_kernel<MAXI, 0>, P);
 }
 
-cudaError_t tma_smem_limit(size_t bytes) {
-  cudaError_t e = cudaFuncSetAttribute(gather_tma_kernel<kGatherItemsSmall>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gather_tma_kernel<kGatherItemsLarge>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
 }  // namespace
 
 cudaError_t gather_set_carveout() {
-  const void* ks[] = {
-      (const void*)gather_kernel<kGatherItemsSmall, 72>, (const void*)gather_kernel<kGatherItemsSmall, 0>,
-      (const void*)gather_kernel<kGatherItemsLarge, 72>, (const void*)gather_kernel<kGatherItemsLarge, 0>,
-      (const void*)gather_tma_kernel<kGatherItemsSmall>, (const void*)gather_tma_kernel<kGatherItemsLarge>};
+  const void* ks[] = {(const void*)gather_kernel<kGatherItemsSmall, 72>,
+                      (const void*)gather_kernel<kGatherItemsSmall, 0>,
+                      (const void*)gather_kernel<kGatherItemsLarge, 72>,
+                      (const void*)gather_kernel<kGatherItemsLarge, 0>,
+                      (const void*)gather_tma_kernel<kGatherItemsSmall>,
+                      (const void*)gather_tma_kernel<kGatherItemsLarge>};
   for (const void* k : ks) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
+cudaError_t gather_set_smem_limit(int row_bytes) {
+  const int bytes = kGatherTileRows * row_bytes;
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute((const void*)gather_tma_kernel<kGatherItemsSmall>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute((const void*)gather_tma_kernel<kGatherItemsLarge>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
 cudaError_t launch_gather(const GatherCommon& c, const GatherItem* items, int n_items,
                           bool pdl, int impl, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
-
   if (n_items <= kGatherItemsSmall)
     return launch_t<kGatherItemsSmall>(c, items, n_items, pdl, impl, stream);
   if (n_items <= kGatherItemsLarge)
     return launch_t<kGatherItemsLarge>(c, items, n_items, pdl, impl, stream);
   return cudaErrorInvalidValue;
-}
-
-}  // namespace dhs
-
-
-namespace dhs {
-
-int gather_tma_grid(int row_bytes) {
-  int dev = 0, sms = 0, per_sm = 0;
-  const size_t smem = tma_smem_bytes(row_bytes);
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (tma_smem_limit(smem) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_tma_kernel<kGatherItemsLarge>,
-                                                    kTmaThreads, smem) != cudaSuccess)
-    return 0;
-  return per_sm > 0 ? sms * per_sm : 0;
 }
 
 }  // namespace dhs

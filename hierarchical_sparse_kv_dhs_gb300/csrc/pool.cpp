@@ -35,7 +35,7 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct MetaLayout {
-  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status, status, done;
+  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status, verdict, status;
   size_t total;
 };
 
@@ -64,8 +64,8 @@ MetaLayout meta_layout(const dhs_pool_config& c) {
   m.miss_slots = take(pairs * (size_t)mcap_of(c) * 4);
   m.miss_count = take(pairs * 4);
   m.pair_status = take(pairs * 4);
+  m.verdict = take(pairs * 4);
   m.status = take(64);
-  m.done = take(64);
   m.total = off;
   return m;
 }
@@ -138,10 +138,10 @@ struct dhs_pool {
   int64_t dirty_lo = INT64_MAX, dirty_hi = -1;  // pairs whose map changed
   bool any_pending = false;
   int copy_ctas = 0;
-  int gather_impl = 1;  // TMA bulk copy
+  int gather_impl = dhs::kGatherTma;
   int early = 1;        // fused gathers copy step-1 rows before the resolve ends
-  uint32_t* done = nullptr;  // gather grid ticket
-  int tma_grid = 0;          // co-resident warps of the TMA gather
+  uint32_t* verdict = nullptr;  // [pairs] resolve verdicts for the fused gather
+  uint32_t seq = 0;             // resolve launches so far
   unsigned long long* trace = nullptr;  // DHS_OPT_TRACE buffer, null = off
   // reusable launch tables
   std::vector<dhs::ResolveItem> ritems;
@@ -151,6 +151,7 @@ struct dhs_pool {
   std::vector<uint8_t> seen;
   std::vector<int32_t> app_of_pair;  // decode step: append item of each pair, -1 = none
   std::vector<int64_t> l0_of_pair;   // length of each resolved pair before this step's append
+  std::vector<uint32_t> seq_of_pair; // resolve launch that last resolved each pair
 };
 
 namespace {
@@ -319,8 +320,8 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->miss_slots = (int32_t*)(m + p->layout.miss_slots);
     p->miss_count = (uint32_t*)(m + p->layout.miss_count);
     p->pair_status = (int32_t*)(m + p->layout.pair_status);
+    p->verdict = (uint32_t*)(m + p->layout.verdict);
     p->status = (uint32_t*)(m + p->layout.status);
-    p->done = (uint32_t*)(m + p->layout.done);
     p->ps.resize(p->pairs);
     p->map_host.assign((size_t)(p->pairs * p->pmax), -1);
     p->slot_pair.assign((size_t)cfg->optional_pages + 1, -1);
@@ -328,6 +329,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->seen.assign((size_t)p->pairs, 0);
     p->app_of_pair.assign((size_t)p->pairs, -1);
     p->l0_of_pair.assign((size_t)p->pairs, 0);
+    p->seq_of_pair.assign((size_t)p->pairs, 0);
   } catch (...) {
     delete p;
     return DHS_ENOMEM;
@@ -337,8 +339,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     delete p;
     return DHS_ECUDA;
   }
-  p->tma_grid = dhs::gather_tma_grid(cfg->row_bytes);
-  if (p->tma_grid <= 0) {
+  if (dhs::gather_set_smem_limit(cfg->row_bytes) != cudaSuccess) {
     delete p;
     return DHS_ECUDA;
   }
@@ -380,7 +381,7 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     return DHS_OK;
   }
   if (key == DHS_OPT_GATHER_IMPL) {
-    if (value < 0 || value > 1) return DHS_EINVAL;
+    if (value != dhs::kGatherVector && value != dhs::kGatherTma) return DHS_EINVAL;
     pool->gather_impl = (int)value;
     return DHS_OK;
   }
@@ -620,6 +621,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   rcm.row_bytes = c.row_bytes;
   rcm.tail = (uint8_t*)c.tail_dev;
   rcm.trace = p->trace;
+  rcm.verdict = p->verdict;
   dhs::CopyCommon ccm{};
   ccm.hot = (uint8_t*)c.hot_dev;
   ccm.miss_rows = p->miss_rows;
@@ -643,6 +645,9 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     }
     rcm.w64cap = (int32_t)wmax;
     rcm.qkcap = (int32_t)qmax;
+    rcm.seq = ++p->seq & dhs::kSeqMask;
+    if (rcm.seq == 0) rcm.seq = p->seq = 1;  // 0 never matches a published verdict
+    for (int i = 0; i < n; ++i) p->seq_of_pair[p->ritems[b + i].pair] = rcm.seq;
     const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows);
     if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, smem, p->stream) != cudaSuccess)
       return DHS_ECUDA;
@@ -684,8 +689,7 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   g.Pmax = (int32_t)p->pmax;
   g.page_shift = p->page_shift;
   g.early = fused && p->early ? 1 : 0;
-  g.done = p->done;
-  g.tma_grid = p->tma_grid;
+  g.verdict = p->verdict;
   g.trace = p->trace;
   p->gitems.clear();
   for (int32_t i = 0; i < st->n_items; ++i) {
@@ -703,23 +707,21 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
       gi.L = p->ps[pair].L;
       gi.N = p->ps[pair].N;
       gi.L0 = p->l0_of_pair[pair];
+      gi.seq = p->seq_of_pair[pair];
     }
     p->gitems.push_back(gi);
   }
   const size_t ng = p->gitems.size();
   for (size_t b = 0; b < ng; b += dhs::kGatherItemsLarge) {
     const int n = (int)std::min<size_t>(dhs::kGatherItemsLarge, ng - b);
-    int64_t tiles = 0, entries = 0;
+    int64_t tiles = 0;
     for (int i = 0; i < n; ++i) {
       dhs::GatherItem& gi = p->gitems[b + i];
       gi.tile0 = (int32_t)tiles;
-      gi.ent0 = (int32_t)entries;
       tiles += (gi.n + dhs::kGatherTileRows - 1) / dhs::kGatherTileRows;
-      entries += gi.n;
     }
-    if (tiles > INT32_MAX || entries > INT32_MAX) return DHS_EINVAL;
+    if (tiles > INT32_MAX) return DHS_EINVAL;
     g.n_tiles = (int32_t)tiles;
-    g.n_entries = entries;
     // only the first gather launch directly follows the resolve launches
     if (dhs::launch_gather(g, p->gitems.data() + b, n, fused && b == 0, p->gather_impl,
                           p->stream) !=

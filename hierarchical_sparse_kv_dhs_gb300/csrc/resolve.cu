@@ -205,6 +205,14 @@ __device__ __forceinline__ uint64_t opt_mask(int w, int64_t N, const int32_t* ma
   return m;
 }
 
+// Publish an item's verdict for the fused gather (thread 0 only).
+__device__ __forceinline__ void publish(const ResolveCommon& c, int pair, uint32_t code) {
+  if (!c.verdict) return;
+  const uint32_t v = ((c.seq & kSeqMask) << kVerdictShift) | code;
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(c.verdict + pair), "r"(v)
+               : "memory");
+}
+
 // Write the failure result of one item: no state change.
 __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t code,
                           uint32_t flag) {
@@ -213,6 +221,7 @@ __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t
   if (threadIdx.x == 0) {
     c.miss_count[it.pair] = 0u;
     c.pair_status[it.pair] = code;
+    publish(c, it.pair, code == kErrRange ? kVerdictRange : kVerdictBudget);
     atomicOr(c.status, flag);
     trace_mark(c.trace, kTraceResolve, true);
   }
@@ -311,6 +320,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   block_sum4(cnt, scratch);
   const uint32_t n_unique = cnt[0], n_tail = cnt[1], n_opt = cnt[2];
   const uint32_t C = cnt[3];  // rows left for the hot cache (block-uniform)
+  if (C == 0 && tid == 0) publish(c, pair, kVerdictOk);  // nothing can fail now
 
   uint32_t hits = 0u, m_miss = 0u, scan_max = 0u, evicted = 0u;
   if (C) {
@@ -370,6 +380,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
       fail_item(c, it, kErrBudget, kStatusEbudget);
       return;
     }
+    if (tid == 0) publish(c, pair, kVerdictOk);
 
     // ---- step 3 victims: the m smallest (stamp, slot) among unprotected slots
     if (m_miss) {

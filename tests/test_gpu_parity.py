@@ -132,11 +132,14 @@ SMALL = [
 ]
 
 
+IMPLS = {"vec": 0, "tma": 1}
+
+
 @pytest.mark.parametrize("cfg", SMALL, ids=[c.name for c in SMALL])
-@pytest.mark.parametrize("mode", ["fused-lsu", "fused-tma", "split-tma", "fused-tma-late",
-                                  "fused-lsu-late"])
+@pytest.mark.parametrize("mode", ["fused-vec", "fused-tma", "split-vec", "split-tma",
+                                  "fused-tma-late", "fused-vec-late"])
 def test_small_configs_bit_exact(cfg, mode):
-    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=1 if "tma" in mode else 0,
+    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
                 early=0 if mode.endswith("late") else 1)
 
 
@@ -146,19 +149,19 @@ def _bad_row(wl):
     sel[2, 1, 0, 0, 5] = wl.length(1, 3)
 
 
-@pytest.mark.parametrize("mode", ["fused-lsu", "fused-tma", "split-lsu"])
+@pytest.mark.parametrize("mode", ["fused-vec", "fused-tma", "split-vec", "split-tma"])
 def test_out_of_range_row_zeroes_the_item(mode):
     cfg = TINY.scaled(name="range", tag=46, requests=2, sources=2, steps=4, residency=0.6)
-    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=1 if "tma" in mode else 0,
+    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
                 patch=_bad_row)
 
 
-@pytest.mark.parametrize("mode", ["fused-lsu", "fused-tma"])
+@pytest.mark.parametrize("mode", ["fused-vec", "fused-tma"])
 def test_budget_overflow_zeroes_the_item(mode):
     # 16 hot slots, no residency: most steps need more victims than slots
     cfg = TINY.scaled(name="budget", tag=47, requests=2, sources=1, hot=16, topk=64,
                       residency=0.0, steps=4)
-    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=1 if "tma" in mode else 0)
+    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]])
 
 
 # ------------------------------------------------------------ full size
