@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=5.0)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--kernel-steps", type=int, default=500)
+    ap.add_argument("--trace-steps", type=int, default=100)
+    ap.add_argument("--no-hugepages", action="store_true")
     return ap.parse_args()
 
 
@@ -259,6 +261,60 @@ def traffic_from_profile(kernel_src: str, profile: str):
         return None
 
 
+def h2d_peak_gbs(dev, nbytes=1 << 30, reps=5):
+    """Pinned host -> device copy bandwidth (cudaMemcpyAsync via torch), best
+    of `reps`: the host-link roofline for the copy kernel."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        best = max(best, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    return best
+
+
+def traced_pass(run, cycle, steps, dev, flush_l2):
+    """Kernel timeline of `steps` fused steps (DHS_OPT_TRACE, synchronised per
+    step -- not the headline): per-kernel durations, and the host-copy
+    kernel's bytes and time for the host-link roofline."""
+    import torch
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    cfg = run.cfg
+    trace = torch.zeros(8, dtype=torch.int64, device=dev)
+    run.pool.set_option(dhs.DHS_OPT_TRACE, trace.data_ptr())
+    res, cp, ga, host_b, copy_s = [], [], [], 0, 0.0
+    for _ in range(steps):
+        s = cycle.next()
+        while not cycle.timed(s):
+            run.step(s)
+            s = cycle.next()
+        flush_l2()
+        trace[0::2] = (1 << 63) - 1
+        trace[1::2] = 0
+        run.step(s)
+        torch.cuda.synchronize(dev)
+        t = trace.cpu().tolist()
+        hb = int(run.counters[..., 5].sum().item()) * cfg.row_bytes
+        res.append((t[1] - t[0]) / 1e3)
+        ga.append((t[5] - t[4]) / 1e3)
+        if t[3] > t[2] > 0:
+            cp.append((t[3] - t[2]) / 1e3)
+            if hb:
+                host_b += hb
+                copy_s += (t[3] - t[2]) / 1e9
+    run.pool.set_option(dhs.DHS_OPT_TRACE, 0)
+    med = statistics.median
+    return {"resolve_us": med(res), "gather_us": med(ga),
+            "copy_us": med(cp) if cp else None,
+            "host_bytes_per_step": host_b / steps,
+            "copy_gbs": (host_b / copy_s / 1e9) if copy_s else None}
+
+
 def measure_e2e(run, cycle, steps, dev, stream):
     """The metric through the C ABI for `steps` further decode steps: each
     step's selections and decode rows are copied in from pinned host memory,
@@ -315,7 +371,7 @@ def main():
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
 
     wl = Workload(cfg)
-    run = GpuRun(cfg, wl, device=dev)
+    run = GpuRun(cfg, wl, device=dev, hugepages=not args.no_hugepages)
     if args.copy_ctas:
         run.pool.set_option(dhs.DHS_OPT_COPY_CTAS, args.copy_ctas)
     run.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, args.gather_impl)
@@ -388,6 +444,17 @@ def main():
     gather_ms = [e[1].elapsed_time(e[2]) for e in ev2]
     resolve_ms = [e[0].elapsed_time(e[1]) for e in ev2]
 
+    trace_info = traced_pass(run, cycle, min(K, args.trace_steps), dev, flush_l2)
+    h2d = h2d_peak_gbs(dev)
+    link = None
+    if trace_info["copy_gbs"]:
+        link = {"bound": "host link (NVLink-C2C)", "kernel": "hostcopy",
+                "achieved": trace_info["copy_gbs"], "peak": h2d, "unit": "GB/s",
+                "frac": trace_info["copy_gbs"] / h2d,
+                "peak_source": "measured in this run: pinned H2D cudaMemcpyAsync, 1 GiB",
+                "bytes_per_step": trace_info["host_bytes_per_step"],
+                "copy_us": trace_info["copy_us"]}
+
     cnt = run.counters.cpu().numpy().reshape(-1, 8).astype("int64")
     tiers = {"unique": int(cnt[:, 1].sum()), "tail": int(cnt[:, 2].sum()),
              "optional": int(cnt[:, 3].sum()), "hot": int(cnt[:, 4].sum()),
@@ -444,6 +511,7 @@ def main():
                      "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
                      "timed": f"{K2} launches, CUDA events around dhs_gather "
                               "(L2 flushed before each step)"},
+        "host_link": link,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -453,6 +521,8 @@ def main():
                     f"and gather PDL-overlapped), gather {impl}",
             "step_ms_median": statistics.median(step_ms),
             "step_GBps_alg": step_bytes / (sum(step_ms) / K / 1e3) / 1e9,
+            "traced_kernel_us": trace_info,
+            "h2d_peak_gbs": h2d,
             "split_append_resolve_hostcopy_ms": sum(resolve_ms) / K2,
             "split_gather_ms": sum(gather_ms) / K2,
             "wall_s_timed_region": t_wall1 - t_wall0,

@@ -36,7 +36,7 @@ def build(force: bool = False) -> str:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared",
-                           "-o", tmp, _SRC, "-lm", "-lpthread"])
+                           "-fno-math-errno", "-o", tmp, _SRC, "-lm", "-lpthread"])
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 

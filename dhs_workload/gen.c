@@ -87,18 +87,23 @@ static inline uint64_t row_key(uint64_t seed, uint32_t cfg, uint32_t src,
                   ((uint64_t)src << 32) | (uint64_t)req, (uint64_t)row);
 }
 
+/* Single-precision Box-Muller: one 64-bit draw gives two 24-bit uniforms,
+ * u1 in (0, 1] and u2 in [0, 1); the pair of normals is
+ * sqrt(-2 ln u1) * (cos 2 pi u2, sin 2 pi u2). */
 static void payload_row(uint64_t seed, uint32_t cfg, uint32_t src,
                         uint32_t req, int64_t row, int32_t elems,
                         uint16_t *out) {
   uint64_t st = row_key(seed, cfg, src, req, row);
-  const double two_pi = 6.283185307179586476925286766559;
+  const float two_pi = 6.28318530717958647692f;
+  const float inv24 = 1.0f / 16777216.0f;
   for (int32_t e = 0; e < elems; e += 2) {
-    double u1 = u01(&st);
-    double u2 = u01(&st);
-    if (u1 <= 0.0) u1 = 1.0 / 9007199254740992.0;
-    double r = sqrt(-2.0 * log(u1));
-    out[e] = dhsw_f32_to_bf16((float)(r * cos(two_pi * u2)));
-    if (e + 1 < elems) out[e + 1] = dhsw_f32_to_bf16((float)(r * sin(two_pi * u2)));
+    uint64_t x = sm64_next(&st);
+    float u1 = (float)((x >> 40) + 1) * inv24;            /* (0, 1] */
+    float u2 = (float)((x >> 16) & 0xFFFFFFu) * inv24;    /* [0, 1) */
+    float r = sqrtf(-2.0f * logf(u1));
+    float a = two_pi * u2;
+    out[e] = dhsw_f32_to_bf16(r * cosf(a));
+    if (e + 1 < elems) out[e + 1] = dhsw_f32_to_bf16(r * sinf(a));
   }
 }
 

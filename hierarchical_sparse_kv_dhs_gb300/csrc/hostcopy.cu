@@ -38,8 +38,8 @@ __global__ void __launch_bounds__(kCopyThreads)
   // The gather may be launched now; the miss lists are read only after the
   // resolve grid has finished writing them.
   asm volatile("griddepcontrol.launch_dependents;");
-  if (tid == 0) trace_mark(c.trace, kTraceCopy, false);
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0) trace_mark(c.trace, kTraceCopy, false);  // the copy phase starts
 
   // prefix of the per-item miss counts (n_items <= blockDim.x)
   const uint32_t mine = tid < n_items ? c.miss_count[P.items[tid].pair] : 0u;

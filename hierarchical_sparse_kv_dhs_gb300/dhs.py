@@ -223,10 +223,18 @@ class HostRows:
     receives (it derives the device-visible address itself).
     """
 
-    def __init__(self, nbytes: int):
+    def __init__(self, nbytes: int, hugepages: bool = True):
         import torch
         self.nbytes = max(int(nbytes), 4096)
         self._mm = mmap.mmap(-1, self.nbytes)
+        if hugepages and hasattr(mmap, "MADV_HUGEPAGE"):
+            # 2 MB host pages: the GPU reads missing rows straight from this
+            # memory at random offsets, and large pages keep its address
+            # translations cached across tens of GB
+            try:
+                self._mm.madvise(mmap.MADV_HUGEPAGE)
+            except OSError:
+                pass
         self.array = np.frombuffer(self._mm, dtype=np.uint8)
         self.ptr = self.array.ctypes.data
         rc = torch._C._cudart.cudaHostRegister(self.ptr, self.nbytes, 3)  # portable|mapped

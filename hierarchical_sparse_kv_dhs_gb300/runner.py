@@ -45,7 +45,11 @@ class _Admit:
 
 class GpuRun:
     def __init__(self, cfg: Config, wl: Workload | None = None, device="cuda",
-                 host_threads=None, gather_impl=None):
+                 host_threads=None, gather_impl=None, payload_requests=None,
+                 hugepages=True):
+        """payload_requests: requests whose imported rows are generated
+        (default all); the others' pinned rows stay zero -- for parity runs
+        that compare sampled requests on workloads too large to fill."""
         self.cfg = c = cfg
         self.wl = wl or Workload(cfg)
         self.device = torch.device(device)
@@ -62,8 +66,16 @@ class GpuRun:
         if gather_impl is not None:
             self.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, gather_impl)
         rb = c.row_bytes
-        self.host = dhs.HostRows(c.pairs * c.max_rows * rb)
-        self.wl.fill_host_rows(self.host.ptr, c.max_rows, nthreads=host_threads)
+        self.host = dhs.HostRows(c.pairs * c.max_rows * rb, hugepages=hugepages)
+        pairs = None if payload_requests is None else [
+            (r, s) for r in range(c.requests) for s in range(c.sources)
+            if r in set(payload_requests)]
+        if pairs is None:
+            self.wl.fill_host_rows(self.host.ptr, c.max_rows, nthreads=host_threads)
+        else:
+            for (r, s) in pairs:  # pair (r, s) lives at its own offset
+                self.wl.fill_host_rows(self.host_ptr(r, s), c.max_rows, [(r, s)],
+                                       nthreads=host_threads)
         drive_admission(_Admit(self), c, self.wl)
         dhs.check(self.pool.flush(), "dhs_flush")
 

@@ -338,10 +338,11 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
                                      (default); 0 = 16-byte vector copy, 256
                                      threads per tile */
 /* Timeline: value = address of a device buffer of 8 uint64 (0 = off).  Each
- * kernel kind k (0 resolve, 1 host copy, 2 gather)
- * atomically lowers buf[2k] to its earliest CTA start and raises buf[2k+1]
- * to its latest CTA end (%globaltimer, ns); the caller initialises buf[2k]
- * to UINT64_MAX and buf[2k+1] to 0. */
+ * kernel kind k (0 resolve, 1 host copy, 2 gather) atomically lowers buf[2k]
+ * to its earliest CTA start and raises buf[2k+1] to its latest CTA end
+ * (%globaltimer, ns; the host copy's start is when its copying begins, after
+ * it has waited for the resolve kernel); the caller initialises buf[2k] to
+ * UINT64_MAX and buf[2k+1] to 0. */
 #define DHS_OPT_TRACE 3
 /* 1 (default): fused gathers copy step-1 rows while the resolve kernel runs;
  * 0: they wait for it first. */

@@ -42,7 +42,9 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
     wl = Workload(cfg)
     if patch:
         patch(wl)
-    gpu = GpuRun(cfg, wl, gather_impl=gather_impl)
+    big = cfg.pairs * cfg.max_rows * cfg.row_bytes > (8 << 30)
+    gpu = GpuRun(cfg, wl, gather_impl=gather_impl,
+                 payload_requests=sampled if (big and sampled is not None) else None)
     if not early:
         from hierarchical_sparse_kv_dhs_gb300 import dhs
         gpu.pool.set_option(dhs.DHS_OPT_EARLY, 0)
@@ -212,3 +214,12 @@ def test_decode_step_fallback_matches_split_calls():
     finally:
         a.close()
         b.close()
+
+
+def test_c128_full_size_sampled():
+    # request 0 is reclaimed (no optional pages), request 127 stays resident
+    compare_run(C128, sampled=[0, 127])
+
+
+def test_long_full_size_sampled():
+    compare_run(LONG, sampled=[0, 31], check_all_bytes=False)
