@@ -14,8 +14,8 @@ timed.  A workload's own warm-up steps (C128: 16) always run untimed.
 
 Prints one JSON line.  value = selected rows resolved + gathered per second
 with every input resident in HBM: device time from CUDA events on the
-launching stream, L2 flushed (a 256 MB write, then read) before every
-timed step.  A second pass times the same steps through dhs_resolve and
+launching stream, L2 flushed (a 256 MB write, then a 256 MB read of another
+buffer) before every timed step.  A second pass times the same steps through dhs_resolve and
 dhs_gather separately, so the gather kernel's own duration gives the roofline.
 e2e = the same metric through the C ABI with each step's selections and
 decode rows copied from pinned host memory and its locations + counters
@@ -42,7 +42,20 @@ sys.path.insert(0, ROOT)
 METRIC = ("selected KV rows resolved+gathered/sec and GB/s vs HBM & host-link "
           "roofline")
 UNIT = "rows/s"
-GATHER_BYTES_PER_ENTRY = 1152 + 1152 + 4  # row read + row write + location read
+GATHER_WRITE_BYTES_PER_ENTRY = 1152 + 4  # staging row write + location read
+
+
+def gather_alg_bytes(cfg, wl, step):
+    """Algorithmic HBM bytes of one step's gather launch: every unique
+    selected row of a resolved (request, source) read once (verify queries
+    and reuse layers read the same rows again), and every gathered entry
+    written to staging with its location read."""
+    import numpy as np
+    reads = 0
+    for r in range(cfg.requests):
+        for s in range(cfg.sources):
+            reads += int(np.unique(wl.sel(step, r, s)).size)
+    return reads * cfg.row_bytes + cfg.entries_per_step * GATHER_WRITE_BYTES_PER_ENTRY
 
 
 def parse():
@@ -75,7 +88,7 @@ def workload_desc(cfg):
         "residency": cfg.residency if cfg.residency is not None else
         f"admission-driven, pool {cfg.capacity_frac:.0%} of pages",
         "entries_per_step": cfg.entries_per_step,
-        "l2": "flushed before every timed step (256 MB write, then read)",
+        "l2": "flushed before every timed step (256 MB write, then a read of another 256 MB)",
     }
 
 
@@ -392,13 +405,14 @@ def main():
     if rc != 0:
         raise RuntimeError(f"device status {rc} flags {flags} during warm-up")
 
-    flush64 = flush.view(torch.int64)
+    clean64 = torch.zeros(32 << 20, dtype=torch.int64, device=dev)  # 256 MB
 
     def flush_l2():
-        # write 256 MB (evicts the previous step's lines), then read it back
-        # so L2 holds clean lines whose eviction costs the next step nothing
+        # write 256 MB (evicts the previous step's lines and writes back its
+        # dirty ones), then read another 256 MB so that L2 holds only clean
+        # lines whose eviction costs the timed step nothing
         flush.zero_()
-        flush64.sum()
+        clean64.sum()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     clocks = ClockSampler(local)
@@ -431,8 +445,10 @@ def main():
     # (the byte-dominant one) is timed alone for the roofline.
     K2 = min(K, args.kernel_steps)
     ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K2)]
+    k_steps = []
     for i in range(K2):
         s = next_timed()
+        k_steps.append(s)
         flush_l2()
         ev2[i][0].record(stream)
         run.append(s)
@@ -489,7 +505,8 @@ def main():
     peak_src = "of measured" if peak else "of fallback"
     peak = peak or 6800.0
     gather_avg = sum(gather_ms) / K2 / 1e3
-    alg_bytes = entries * GATHER_BYTES_PER_ENTRY
+    alg_of = {s: gather_alg_bytes(cfg, wl, s) for s in set(k_steps)}
+    alg_bytes = sum(alg_of[s] for s in k_steps) / K2  # per launch, averaged
     achieved = alg_bytes / gather_avg / 1e9
     gather_src = "gather.cu"
     traffic = traffic_from_profile(
