@@ -26,6 +26,7 @@ _lib = None
 _lock = threading.Lock()
 
 NO_LOC = 0xFFFFFFFF
+END_LOC = 0xFFFFFFFE  # past the end of a union location list
 TIER_TAIL, TIER_OPT, TIER_HOT = 0, 1, 2
 RC_NAMES = {0: 0, -1: "einval", -2: "enomem", -3: "wouldwait", -4: "ebudget",
             -5: "erange", -8: "estate"}
@@ -69,6 +70,8 @@ def lib() -> ctypes.CDLL:
             L.orc_append.argtypes = [vp, i32, i32, i32, vp]
             L.orc_resolve.restype = ctypes.c_int
             L.orc_resolve.argtypes = [vp, u32, i32, i32, i32, i32, vp, vp, vp]
+            L.orc_resolve_union.restype = ctypes.c_int
+            L.orc_resolve_union.argtypes = [vp, u32, i32, i32, i32, i32, vp, vp, vp, vp]
             L.orc_gather.restype = ctypes.c_int
             L.orc_gather.argtypes = [vp, vp, i64, vp]
             L.orc_read_state.restype = ctypes.c_int
@@ -145,6 +148,20 @@ class OraclePool:
         cnt = np.empty(8, np.uint32)
         rc = lib().orc_resolve(self._h, step, r, s, Q, k, _p(sel), _p(loc), _p(cnt))
         return RC_NAMES[rc], loc[: Q * k].reshape(Q, k), cnt
+
+    def resolve_union(self, step, r, s, sel):
+        """Union staging layout: (rc, loc [Q*k] -- U union locations then
+        END_LOC, index [Q][k] into the union, counters)."""
+        sel = np.ascontiguousarray(sel, dtype=np.int32)
+        if sel.ndim == 1:
+            sel = sel[None]
+        Q, k = sel.shape
+        loc = np.empty(max(Q * k, 1), np.uint32)
+        idx = np.empty(max(Q * k, 1), np.int32)
+        cnt = np.empty(8, np.uint32)
+        rc = lib().orc_resolve_union(self._h, step, r, s, Q, k, _p(sel), _p(loc),
+                                     _p(idx), _p(cnt))
+        return RC_NAMES[rc], loc[: Q * k], idx[: Q * k].reshape(Q, k), cnt
 
     def gather(self, loc):
         loc = np.ascontiguousarray(loc, dtype=np.uint32)

@@ -38,7 +38,8 @@
  *
  * Location encoding: (tier << 30) | index; tier 0 = tail (index
  * pair*T + row mod T), 1 = optional (index slot*page_rows + row mod
- * page_rows), 2 = hot (index pair*B + slot); 0xFFFFFFFF = no location.
+ * page_rows), 2 = hot (index pair*B + slot); 0xFFFFFFFF = no location;
+ * 0xFFFFFFFE = past the end of a union location list (union staging).
  * Counters per resolve: entries, unique, tail, optional, hot, host,
  * scan_max (probes of the longest hot-cache scan), evicted (victims that
  * held a row).
@@ -63,6 +64,7 @@
 #define ORC_TIER_OPT 1u
 #define ORC_TIER_HOT 2u
 #define ORC_NO_LOC 0xFFFFFFFFu
+#define ORC_END_LOC 0xFFFFFFFEu /* past the end of a union location list */
 
 typedef struct {
   int admitted;
@@ -416,10 +418,55 @@ int orc_resolve(orc_pool *p, uint32_t step, int32_t r, int32_t s, int32_t Q,
   return ORC_OK;
 }
 
+/*
+ * Union verification staging ("Memory split": verification staging;
+ * "Speculative state": verification queries share missing-row
+ * retrieval).  The same resolution as orc_resolve, laid out so that each
+ * distinct row of the verify block is staged once:
+ *   loc[u]     u < U: location of the u-th distinct selected row, ascending
+ *              row order; loc[u] = ORC_END_LOC for U <= u < Q*k;
+ *   index[e]   position of sel[e] among those U rows.
+ * U is counters[1].  On an error nothing changes, every loc is ORC_END_LOC
+ * and every index -1.
+ */
+int orc_resolve_union(orc_pool *p, uint32_t step, int32_t r, int32_t s,
+                      int32_t Q, int32_t k, const int32_t *sel, uint32_t *loc,
+                      int32_t *index, uint32_t *counters) {
+  if (Q < 0 || k < 0) return ORC_EINVAL;
+  int64_t n = (int64_t)Q * k;
+  uint32_t *per_entry = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(n + 1));
+  int32_t *U = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n + 1));
+  if (!per_entry || !U) {
+    free(per_entry); free(U);
+    return ORC_ENOMEM;
+  }
+  int rc = orc_resolve(p, step, r, s, Q, k, sel, per_entry, counters);
+  for (int64_t e = 0; e < n; ++e) {
+    loc[e] = ORC_END_LOC;
+    index[e] = -1;
+  }
+  if (rc == ORC_OK) {
+    memcpy(U, sel, sizeof(int32_t) * (size_t)n);
+    qsort(U, (size_t)n, sizeof(int32_t), cmp_i32);
+    int64_t nu = 0;
+    for (int64_t e = 0; e < n; ++e)
+      if (nu == 0 || U[nu - 1] != U[e]) U[nu++] = U[e];
+    /* every entry of one row has the same location: take the entry's */
+    for (int64_t e = 0; e < n; ++e) {
+      int64_t u = find_sorted(U, nu, sel[e]);
+      index[e] = (int32_t)u;
+      loc[u] = per_entry[e];
+    }
+  }
+  free(per_entry); free(U);
+  return rc;
+}
+
 /* ------------------------------------------------------------ gather */
 
 /*
- * staging[e] = the row bytes at loc[e] (zeros for ORC_NO_LOC).  Optional
+ * staging[e] = the row bytes at loc[e] (zeros for ORC_NO_LOC; ORC_END_LOC
+ * leaves staging[e] untouched).  Optional
  * slots hold copies of their owner's imported rows, which never change, so
  * they are read from the owner's host copy.  Every location must point at
  * a payload-tracked source, else ORC_EINVAL.
@@ -433,7 +480,9 @@ int orc_gather(const orc_pool *p, const uint32_t *loc, int64_t n,
     uint16_t *dst = staging + (size_t)e * E;
     uint32_t tier = loc[e] >> 30, idx = loc[e] & 0x3FFFFFFFu;
     const uint16_t *from = NULL;
-    if (loc[e] == ORC_NO_LOC) {
+    if (loc[e] == ORC_END_LOC) { /* past a union list: staging untouched */
+      continue;
+    } else if (loc[e] == ORC_NO_LOC) {
       memset(dst, 0, E * 2);
       continue;
     } else if (tier == ORC_TIER_TAIL) {

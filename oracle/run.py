@@ -10,6 +10,10 @@ Per step s of a configuration, for every simulated request r:
      vectors, then `reuse_layers` Reuse layers gather source 0's location
      vector again ("Model-specific reuse": they inherit it, no resolution).
 
+With union=True every source resolves in the union staging layout (each
+distinct row of a verify block staged once, plus per-query index lists) and
+each layer gathers the U union rows only.
+
 Admission runs for every request (page slots depend on admission order), but
 only the simulated requests hold row bytes and are stepped; requests are
 independent once admitted, so a sampled subset gives exact per-request
@@ -37,8 +41,10 @@ class _AdmitAdapter:
 
 class OracleRun:
     def __init__(self, cfg: Config, wl: Workload | None = None,
-                 requests=None, payload: bool = True, capacity=None):
+                 requests=None, payload: bool = True, capacity=None,
+                 union: bool = False):
         self.cfg = cfg
+        self.union = union
         self.wl = wl or Workload(cfg)
         self.requests = list(range(cfg.requests)) if requests is None else list(requests)
         self.payload = payload
@@ -75,7 +81,9 @@ class OracleRun:
 
     def step(self, step: int, gather: bool = True):
         """Run one step; returns {r: {"rc": [S], "loc": [S][Q][k],
-        "counters": [S][8], "staging": [layers][Q][k][E] or None}}."""
+        "counters": [S][8], "staging": [layers][Q][k][E] or None}}.
+        Union layout: "loc" is [S][Q*k] (U union locations, then END_LOC),
+        "index" [S][Q][k], and "staging" a list of [U][E] arrays per layer."""
         c = self.cfg
         out = {}
         pairs = [(r, s) for r in self.requests for s in range(c.sources)]
@@ -87,21 +95,29 @@ class OracleRun:
             if rc != 0:
                 raise RuntimeError(f"oracle append failed: {rc}")
         for r in self.requests:
-            rcs, locs, cnts = [], [], []
+            rcs, locs, cnts, idxs = [], [], [], []
             for s in range(c.sources):
-                rc, loc, cnt = self.pool.resolve(step, r, s, self.wl.sel(step, r, s))
+                sel = self.wl.sel(step, r, s)
+                if self.union:
+                    rc, loc, idx, cnt = self.pool.resolve_union(step, r, s, sel)
+                    idxs.append(idx)
+                else:
+                    rc, loc, cnt = self.pool.resolve(step, r, s, sel)
                 rcs.append(rc)
                 locs.append(loc)
                 cnts.append(cnt)
             res = {"rc": rcs, "loc": np.stack(locs), "counters": np.stack(cnts),
                    "staging": None}
+            if self.union:
+                res["index"] = np.stack(idxs)
             if gather and self.payload:
                 st = []
                 for kind, s in self.layers():
-                    rc, g = self.pool.gather(locs[s])
+                    want = locs[s][: int(cnts[s][1])] if self.union else locs[s]
+                    rc, g = self.pool.gather(want)
                     if rc != 0:
                         raise RuntimeError(f"oracle gather failed: {rc}")
                     st.append(g)
-                res["staging"] = np.stack(st)
+                res["staging"] = st if self.union else np.stack(st)
             out[r] = res
         return out
