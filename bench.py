@@ -45,17 +45,22 @@ UNIT = "rows/s"
 GATHER_WRITE_BYTES_PER_ENTRY = 1152 + 4  # staging row write + location read
 
 
-def gather_alg_bytes(cfg, wl, step):
+def gather_alg_bytes(cfg, wl, step, union=False):
     """Algorithmic HBM bytes of one step's gather launch: every unique
     selected row of a resolved (request, source) read once (verify queries
     and reuse layers read the same rows again), and every gathered entry
-    written to staging with its location read."""
+    written to staging with its location read.  Union staging writes each
+    layer's distinct rows once and still reads every entry's location."""
     import numpy as np
-    reads = 0
+    reads = writes = 0
     for r in range(cfg.requests):
-        for s in range(cfg.sources):
-            reads += int(np.unique(wl.sel(step, r, s)).size)
-    return reads * cfg.row_bytes + cfg.entries_per_step * GATHER_WRITE_BYTES_PER_ENTRY
+        u = [int(np.unique(wl.sel(step, r, s)).size) for s in range(cfg.sources)]
+        reads += sum(u)
+        if union:
+            writes += sum(u) + cfg.reuse_layers * u[0]
+    if not union:
+        return reads * cfg.row_bytes + cfg.entries_per_step * GATHER_WRITE_BYTES_PER_ENTRY
+    return (reads + writes) * cfg.row_bytes + cfg.entries_per_step * 4
 
 
 def parse():
@@ -73,11 +78,15 @@ def parse():
     ap.add_argument("--kernel-steps", type=int, default=500)
     ap.add_argument("--trace-steps", type=int, default=100)
     ap.add_argument("--no-hugepages", action="store_true")
+    ap.add_argument("--union", action="store_true",
+                    help="union verification staging (DHS_ITEM_UNION)")
     return ap.parse_args()
 
 
-def workload_desc(cfg):
+def workload_desc(cfg, union=False):
     return {
+        "staging": ("union: each distinct row of a verify block staged once, plus "
+                    "per-query index lists") if union else "per query [Q][k] rows",
         "workload": (f"{cfg.name}: {cfg.requests} requests x {cfg.layers} layers "
                      f"({cfg.sources} KV sources), {cfg.history}-row histories of "
                      f"{cfg.row_elems} bf16, top-k {cfg.topk} x {cfg.queries} queries, "
@@ -135,12 +144,12 @@ class OracleTimer:
     releases the GIL inside the oracle); threads run each step together and
     wall time is taken around the step."""
 
-    def __init__(self, cfg, wl, threads=None):
+    def __init__(self, cfg, wl, threads=None, union=False):
         from oracle.run import OracleRun
         self.cfg = cfg
         reqs = list(range(cfg.requests))
         self.threads = threads or min(len(reqs), os.cpu_count() or 1)
-        self.runs = [OracleRun(cfg, wl, requests=reqs[i::self.threads])
+        self.runs = [OracleRun(cfg, wl, requests=reqs[i::self.threads], union=union)
                      for i in range(self.threads)]
         self.cycle = Cycle(cfg, self._reset)
 
@@ -177,7 +186,7 @@ def run_reference(args, cfg):
         return
     from dhs_workload.configs import Workload
     wl = Workload(cfg)
-    ot = OracleTimer(cfg, wl)
+    ot = OracleTimer(cfg, wl, union=args.union)
     for _ in range(args.warmup):
         ot.step()
     K = args.steps
@@ -189,7 +198,7 @@ def run_reference(args, cfg):
         "n_gpus": args.gpus, "steps": K, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": workload_desc(cfg),
+        "config": workload_desc(cfg, args.union),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": ot.threads,
                          "kind": "oracle",
                          "sample": f"{K} decode steps of the workload, all requests"},
@@ -340,6 +349,8 @@ def measure_e2e(run, cycle, steps, dev, stream):
     rows_host = [run.app_rows[s].cpu().pin_memory() for s in range(T)]
     loc_host = torch.empty(run.loc.shape, dtype=run.loc.dtype).pin_memory()
     cnt_host = torch.empty(run.counters.shape, dtype=run.counters.dtype).pin_memory()
+    idx_host = (torch.empty(run.index.shape, dtype=run.index.dtype).pin_memory()
+                if run.index is not None else None)  # union staging: entry -> row
     torch.cuda.synchronize(dev)
     dt = 0.0
     for _ in range(steps):
@@ -354,10 +365,14 @@ def measure_e2e(run, cycle, steps, dev, stream):
         run.step(s)
         loc_host.copy_(run.loc, non_blocking=True)
         cnt_host.copy_(run.counters, non_blocking=True)
+        if idx_host is not None:
+            idx_host.copy_(run.index, non_blocking=True)
         stream.synchronize()
         dt += time.perf_counter() - t0
     h2d = sel_host[0].numel() * 4 + rows_host[0].numel() * 2
     d2h = loc_host.numel() * 4 + cnt_host.numel() * 4
+    if idx_host is not None:
+        d2h += idx_host.numel() * 4
     return {"value": run.cfg.entries_per_step * steps / dt, "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": steps, "seconds": dt}
@@ -384,7 +399,7 @@ def main():
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
 
     wl = Workload(cfg)
-    run = GpuRun(cfg, wl, device=dev, hugepages=not args.no_hugepages)
+    run = GpuRun(cfg, wl, device=dev, hugepages=not args.no_hugepages, union=args.union)
     if args.copy_ctas:
         run.pool.set_option(dhs.DHS_OPT_COPY_CTAS, args.copy_ctas)
     run.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, args.gather_impl)
@@ -484,7 +499,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        ot = OracleTimer(cfg, wl)
+        ot = OracleTimer(cfg, wl, union=args.union)
         dt, n = 0.0, 0
         while dt < args.cpu_seconds:
             dt += ot.step()
@@ -505,7 +520,7 @@ def main():
     peak_src = "of measured" if peak else "of fallback"
     peak = peak or 6800.0
     gather_avg = sum(gather_ms) / K2 / 1e3
-    alg_of = {s: gather_alg_bytes(cfg, wl, s) for s in set(k_steps)}
+    alg_of = {s: gather_alg_bytes(cfg, wl, s, args.union) for s in set(k_steps)}
     alg_bytes = sum(alg_of[s] for s in k_steps) / K2  # per launch, averaged
     achieved = alg_bytes / gather_avg / 1e9
     gather_src = "gather.cu"
@@ -521,7 +536,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": sum(step_ms) / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u8", "data": "synthetic", "config": workload_desc(cfg),
+        "dtype": "u8", "data": "synthetic", "config": workload_desc(cfg, args.union),
         "roofline": {"bound": "hbm", "kernel": f"gather_{impl}", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"hbm_gbs {peak_src} (copy, read+write bytes)",

@@ -15,6 +15,7 @@ namespace dhs {
 
 constexpr uint32_t kTierTail = 0u, kTierOpt = 1u, kTierHot = 2u;
 constexpr uint32_t kNoLoc = 0xFFFFFFFFu;
+constexpr uint32_t kEndLoc = 0xFFFFFFFEu;  // past the end of a union location list
 constexpr uint32_t kStatusErange = 1u, kStatusEbudget = 2u, kStatusEloc = 4u;
 constexpr uint32_t kStatusEtimeout = 8u;
 constexpr int32_t kErrRange = -5, kErrBudget = -4;  // DHS_ERANGE, DHS_EBUDGET
@@ -64,6 +65,7 @@ struct ResolveItem {
   int64_t app_L0;           // length before the append
   int32_t app_count;
   int32_t pad;
+  int32_t* index;  // union staging: [n] union rank of each entry; null = per-query
 };
 
 struct ResolveCommon {
@@ -86,10 +88,10 @@ struct ResolveCommon {
   unsigned long long* trace;  // null = off
   uint32_t* verdict;     // [pairs] published verdicts, null = none
   uint32_t seq;          // sequence number of this launch
-  int32_t pad2;
+  int32_t uni;           // shared-memory plan includes the union bitmap
 };
 
-size_t resolve_smem_bytes(int w64cap, int qkcap, int B);
+size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni);
 cudaError_t resolve_set_smem_limit(size_t bytes);
 cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,
                            int n_items, size_t smem, cudaStream_t stream);

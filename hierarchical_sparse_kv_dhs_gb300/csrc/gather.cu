@@ -211,7 +211,11 @@ __global__ void __launch_bounds__(kGatherThreads)
     // rows that needed the hot cache (or no early phase): wait for the
     // resolve / host-copy grids (a no-op without programmatic dependent launch)
     if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (tid < ne && s_phase[tid] == 1) s_src[tid] = row_ptr(c, it.loc[e0 + tid]);
+    if (tid < ne && s_phase[tid] == 1) {
+      const uint32_t l = it.loc[e0 + tid];
+      if (l == kEndLoc) s_phase[tid] = 2;  // past a union list: nothing to write
+      else s_src[tid] = row_ptr(c, l);
+    }
     __syncthreads();
     copy_tile<CPR>(c, dst, s_src, s_phase, ne, 1);
   }
@@ -337,7 +341,9 @@ __global__ void __launch_bounds__(kTmaThreads)
     // rows that needed the hot cache (or no early phase): wait for the
     // resolve / host-copy grids (a no-op without programmatic dependent launch)
     if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
-    ok = move(deferred, deferred ? row_ptr(c, it.loc[e0 + lane]) : nullptr);
+    const uint32_t l = deferred ? it.loc[e0 + lane] : kEndLoc;
+    const bool live = l != kEndLoc;  // past a union list: nothing to write
+    ok = move(live, live ? row_ptr(c, l) : nullptr);
   }
   // shared memory must outlive the stores' reads
   if (stored) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");

@@ -79,11 +79,11 @@ int log2i(int64_t x) {
 }
 
 // Shared-memory plan of the resolve kernel at the pool's largest sizes.
-size_t max_resolve_smem(const dhs_pool_config& c) {
+size_t max_resolve_smem(const dhs_pool_config& c, bool uni) {
   const int64_t w64 = (c.max_rows_per_request + 63) / 64;
   const int64_t qk = std::min<int64_t>((int64_t)c.max_queries * c.max_topk,
                                        c.max_rows_per_request);
-  return dhs::resolve_smem_bytes((int)w64, (int)qk, c.hot_rows);
+  return dhs::resolve_smem_bytes((int)w64, (int)qk, c.hot_rows, uni);
 }
 
 int validate_geometry(const dhs_pool_config* c) {
@@ -138,6 +138,7 @@ struct dhs_pool {
   int64_t dirty_lo = INT64_MAX, dirty_hi = -1;  // pairs whose map changed
   bool any_pending = false;
   int copy_ctas = 0;
+  bool union_ok = false;  // the union staging plan fits in shared memory
   int gather_impl = dhs::kGatherTma;
   int early = 1;        // fused gathers copy step-1 rows before the resolve ends
   uint32_t* verdict = nullptr;  // [pairs] resolve verdicts for the fused gather
@@ -297,14 +298,17 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
       cudaSuccess)
     return DHS_ECUDA;
-  const size_t smem = max_resolve_smem(*cfg);
+  const size_t smem = max_resolve_smem(*cfg, false);
   if (smem + 1024 > (size_t)optin) return DHS_EINVAL;
-  if (dhs::resolve_set_smem_limit(smem) != cudaSuccess) return DHS_ECUDA;
+  const size_t smem_u = max_resolve_smem(*cfg, true);
+  const bool union_ok = smem_u + 1024 <= (size_t)optin;
+  if (dhs::resolve_set_smem_limit(union_ok ? smem_u : smem) != cudaSuccess) return DHS_ECUDA;
 
   dhs_pool* p = new (std::nothrow) dhs_pool();
   if (!p) return DHS_ENOMEM;
   try {
     p->cfg = *cfg;
+    p->union_ok = union_ok;
     p->stream = (cudaStream_t)cfg->stream;
     p->device = dev;
     p->pairs = (int64_t)cfg->max_requests * cfg->sources;
@@ -560,6 +564,8 @@ static int validate_step(dhs_pool* p, const dhs_step* st, bool resolving) {
     if (it.req < 0 || it.req >= c.max_requests || it.src < 0 || it.src >= c.sources)
       return DHS_EINVAL;
     if (n > 0 && !it.sel_dev) return DHS_EINVAL;
+    if ((it.flags & DHS_ITEM_UNION) && (!p->union_ok || (n > 0 && !it.index_dev)))
+      return DHS_EINVAL;
     const int64_t pair = (int64_t)it.req * c.sources + it.src;
     if (p->seen[pair]) return DHS_EINVAL;
     p->seen[pair] = 1;
@@ -593,6 +599,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     r.sel = it.sel_dev;
     r.loc = it.loc_dev;
     r.counters = it.counters_dev;
+    r.index = (it.flags & DHS_ITEM_UNION) ? it.index_dev : nullptr;
     r.L = s.L;
     r.N = s.N;
     r.pair = (int32_t)pair;
@@ -635,8 +642,10 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   for (size_t b = 0; b < nr; b += dhs::kResolveItemsLarge) {
     const int n = (int)std::min<size_t>(dhs::kResolveItemsLarge, nr - b);
     int64_t wmax = 0, qmax = 0, requests = 0, last_req = -1;
+    bool uni = false;
     for (int i = 0; i < n; ++i) {
       const dhs::ResolveItem& r = p->ritems[b + i];
+      uni |= r.index != nullptr;
       wmax = std::max<int64_t>(wmax, (r.L + 63) / 64);
       qmax = std::max<int64_t>(qmax, std::min<int64_t>(r.n, r.L));
       const int64_t req = r.pair / c.sources;
@@ -648,7 +657,8 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     rcm.seq = ++p->seq & dhs::kSeqMask;
     if (rcm.seq == 0) rcm.seq = p->seq = 1;  // 0 never matches a published verdict
     for (int i = 0; i < n; ++i) p->seq_of_pair[p->ritems[b + i].pair] = rcm.seq;
-    const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows);
+    rcm.uni = uni ? 1 : 0;
+    const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni);
     if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, smem, p->stream) != cudaSuccess)
       return DHS_ECUDA;
     int ctas = p->copy_ctas;
@@ -700,7 +710,9 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
     gi.loc = it.loc_dev;
     gi.staging = (uint8_t*)it.staging_dev;
     gi.n = n;
-    if (fused && !(it.flags & DHS_ITEM_GATHER_ONLY)) {
+    // a union item's rows are known only once the resolve kernel has ranked
+    // them, so it has no early phase
+    if (fused && !(it.flags & (DHS_ITEM_GATHER_ONLY | DHS_ITEM_UNION))) {
       const int64_t pair = (int64_t)it.req * c.sources + it.src;
       gi.sel = it.sel_dev;
       gi.pair = (int32_t)pair;
@@ -871,6 +883,7 @@ extern "C" int dhs_resolve_noalloc(dhs_pool* p, const dhs_step* st) {
     r.sel = it.sel_dev;
     r.loc = it.loc_dev;
     r.counters = it.counters_dev;
+    r.index = (it.flags & DHS_ITEM_UNION) ? it.index_dev : nullptr;
     r.L = s.L;
     r.N = s.N;
     r.pair = (int32_t)pair;
@@ -908,8 +921,10 @@ extern "C" int dhs_resolve_noalloc(dhs_pool* p, const dhs_step* st) {
   for (size_t b = 0; b < nr; b += dhs::kResolveItemsLarge) {
     const int n = (int)std::min<size_t>(dhs::kResolveItemsLarge, nr - b);
     int64_t wmax = 0, qmax = 0, requests = 0, last_req = -1;
+    bool uni = false;
     for (int i = 0; i < n; ++i) {
       const dhs::ResolveItem& r = ritems[b + i];
+      uni |= r.index != nullptr;
       wmax = std::max<int64_t>(wmax, (r.L + 63) / 64);
       qmax = std::max<int64_t>(qmax, std::min<int64_t>(r.n, r.L));
       const int64_t req = r.pair / c.sources;
@@ -918,7 +933,8 @@ extern "C" int dhs_resolve_noalloc(dhs_pool* p, const dhs_step* st) {
     }
     rcm.w64cap = (int32_t)wmax;
     rcm.qkcap = (int32_t)qmax;
-    const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows);
+    rcm.uni = uni ? 1 : 0;
+    const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni);
     if (dhs::launch_resolve(rcm, ritems.data() + b, n, smem, p->stream) != cudaSuccess)
       return DHS_ECUDA;
     int ctas = p->copy_ctas;

@@ -40,11 +40,13 @@ struct Smem {
   uint16_t* slot_of;  // [qkcap] hot slot of each unresolved rank, 0xFFFF = miss
   uint16_t* sort_a;   // [B]
   uint16_t* sort_b;   // [B]
+  uint64_t* ubm;      // [w64cap] union bitmap (union staging launches only)
+  uint32_t* upre;     // [w64cap] exclusive prefix of its popcounts
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-__host__ __device__ inline size_t carve(int w64cap, int qkcap, int B, Smem* s,
+__host__ __device__ inline size_t carve(int w64cap, int qkcap, int B, bool uni, Smem* s,
                                         unsigned char* base) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -59,6 +61,8 @@ __host__ __device__ inline size_t carve(int w64cap, int qkcap, int B, Smem* s,
   unsigned char* p4 = take(sizeof(uint16_t) * (size_t)qkcap);
   unsigned char* p5 = take(sizeof(uint16_t) * (size_t)B);
   unsigned char* p6 = take(sizeof(uint16_t) * (size_t)B);
+  unsigned char* p7 = uni ? take(sizeof(uint64_t) * (size_t)w64cap) : nullptr;
+  unsigned char* p8 = uni ? take(sizeof(uint32_t) * (size_t)w64cap) : nullptr;
   if (s) {
     s->bm = (uint64_t*)p0;
     s->wpre = (uint32_t*)p1;
@@ -67,6 +71,8 @@ __host__ __device__ inline size_t carve(int w64cap, int qkcap, int B, Smem* s,
     s->slot_of = (uint16_t*)p4;
     s->sort_a = (uint16_t*)p5;
     s->sort_b = (uint16_t*)p6;
+    s->ubm = (uint64_t*)p7;
+    s->upre = (uint32_t*)p8;
   }
   return off;
 }
@@ -216,7 +222,14 @@ __device__ __forceinline__ void publish(const ResolveCommon& c, int pair, uint32
 // Write the failure result of one item: no state change.
 __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t code,
                           uint32_t flag) {
-  for (int e = threadIdx.x; e < it.n; e += blockDim.x) it.loc[e] = kNoLoc;
+  if (it.index) {  // union staging: an empty union list
+    for (int e = threadIdx.x; e < it.n; e += blockDim.x) {
+      it.loc[e] = kEndLoc;
+      it.index[e] = -1;
+    }
+  } else {
+    for (int e = threadIdx.x; e < it.n; e += blockDim.x) it.loc[e] = kNoLoc;
+  }
   if (threadIdx.x < 8 && it.counters) it.counters[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
     c.miss_count[it.pair] = 0u;
@@ -263,7 +276,8 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   const int32_t* map = c.map + (size_t)pair * c.Pmax;
 
   Smem s;
-  carve(c.w64cap, c.qkcap, B, &s, smem_raw);
+  carve(c.w64cap, c.qkcap, B, c.uni != 0, &s, smem_raw);
+  const bool uni = it.index != nullptr;  // union staging (launch has c.uni)
 
   // ---- decode rows appended by this launch (dhs_decode_step): row L0+j to
   // tail slot (L0+j) mod T and through to the pinned host copy.  Nothing
@@ -303,6 +317,10 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   uint32_t cnt[4] = {0u, 0u, 0u, 0u};  // unique, tail, opt, unresolved
   for (int w = tid; w < W; w += nt) {
     const uint64_t bits = s.bm[w];
+    if (uni) {
+      s.ubm[w] = bits;
+      s.upre[w] = (uint32_t)__popcll(bits);
+    }
     uint64_t cand = 0ull;
     if (bits) {
       const uint64_t tm = bits & tail_mask(w, t0);
@@ -321,6 +339,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   const uint32_t n_unique = cnt[0], n_tail = cnt[1], n_opt = cnt[2];
   const uint32_t C = cnt[3];  // rows left for the hot cache (block-uniform)
   if (C == 0 && tid == 0) publish(c, pair, kVerdictOk);  // nothing can fail now
+  if (uni) block_scan_array(s.upre, W, scratch);  // union ranks
 
   uint32_t hits = 0u, m_miss = 0u, scan_max = 0u, evicted = 0u;
   if (C) {
@@ -453,23 +472,39 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   // ---- location vector
   const int ps = c.page_shift;
   const int64_t pmask = ((int64_t)1 << ps) - 1;
-  for (int e = tid; e < n; e += nt) {
-    const int32_t row = it.sel[e];
-    uint32_t loc;
-    if ((int64_t)row >= t0) {
-      loc = (kTierTail << 30) | (uint32_t)((int64_t)pair * T + (int64_t)row % T);
-    } else {
-      const uint64_t m = s.bm[row >> 6];
+  auto loc_of = [&](int32_t row) -> uint32_t {
+    if ((int64_t)row >= t0)
+      return (kTierTail << 30) | (uint32_t)((int64_t)pair * T + (int64_t)row % T);
+    const uint64_t m = s.bm[row >> 6];  // rows that went to the hot cache
+    const uint64_t bit = 1ull << (row & 63);
+    if (m & bit) {
+      const uint32_t r = s.wpre[row >> 6] + (uint32_t)__popcll(m & (bit - 1ull));
+      return (kTierHot << 30) | (uint32_t)((int64_t)pair * B + s.slot_of[r]);
+    }
+    const int32_t slot = map[row >> ps];
+    return (kTierOpt << 30) | (uint32_t)(((int64_t)slot << ps) + (row & pmask));
+  };
+  if (!uni) {
+    for (int e = tid; e < n; e += nt) it.loc[e] = loc_of(it.sel[e]);
+  } else {
+    // union staging: each entry's rank among the distinct rows, the distinct
+    // rows' locations in ascending row order, then the end marker
+    for (int e = tid; e < n; e += nt) {
+      const int32_t row = it.sel[e];
       const uint64_t bit = 1ull << (row & 63);
-      if (m & bit) {
-        const uint32_t r = s.wpre[row >> 6] + (uint32_t)__popcll(m & (bit - 1ull));
-        loc = (kTierHot << 30) | (uint32_t)((int64_t)pair * B + s.slot_of[r]);
-      } else {
-        const int32_t slot = map[row >> ps];
-        loc = (kTierOpt << 30) | (uint32_t)(((int64_t)slot << ps) + (row & pmask));
+      it.index[e] = (int32_t)(s.upre[row >> 6] +
+                              (uint32_t)__popcll(s.ubm[row >> 6] & (bit - 1ull)));
+    }
+    for (int w = tid; w < W; w += nt) {
+      uint64_t m = s.ubm[w];
+      uint32_t u = s.upre[w];
+      while (m) {
+        const int b = __ffsll((long long)m) - 1;
+        m &= m - 1;
+        it.loc[u++] = loc_of((w << 6) + b);
       }
     }
-    it.loc[e] = loc;
+    for (int u = (int)n_unique + tid; u < n; u += nt) it.loc[u] = kEndLoc;
   }
 
   if (m_miss) {
@@ -507,8 +542,8 @@ cudaError_t launch_t(const ResolveCommon& c, const ResolveItem* items, int n,
 
 }  // namespace
 
-size_t resolve_smem_bytes(int w64cap, int qkcap, int B) {
-  return carve(w64cap, qkcap, B, nullptr, nullptr);
+size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni) {
+  return carve(w64cap, qkcap, B, uni, nullptr, nullptr);
 }
 
 cudaError_t resolve_set_smem_limit(size_t bytes) {

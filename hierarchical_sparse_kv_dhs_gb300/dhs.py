@@ -33,9 +33,11 @@ RC_NAMES = {0: 0, -1: "einval", -2: "enomem", -3: "wouldwait", -4: "ebudget",
 
 DHS_TIER_TAIL, DHS_TIER_OPT, DHS_TIER_HOT = 0, 1, 2
 DHS_NO_LOC = 0xFFFFFFFF
+DHS_END_LOC = 0xFFFFFFFE
 DHS_NUM_COUNTERS = 8
 DHS_STATUS_ERANGE, DHS_STATUS_EBUDGET, DHS_STATUS_ELOC, DHS_STATUS_ETIMEDOUT = 1, 2, 4, 8
 DHS_ITEM_GATHER_ONLY = 1
+DHS_ITEM_UNION = 2
 DHS_OPT_COPY_CTAS = 1
 DHS_OPT_GATHER_IMPL = 2
 DHS_OPT_TRACE = 3
@@ -63,7 +65,8 @@ class dhs_append_item(ctypes.Structure):
 class dhs_item(ctypes.Structure):
     _fields_ = [("req", _i32), ("src", _i32), ("queries", _i32), ("topk", _i32),
                 ("flags", _u32), ("reserved", _i32), ("sel_dev", _vp),
-                ("loc_dev", _vp), ("staging_dev", _vp), ("counters_dev", _vp)]
+                ("loc_dev", _vp), ("staging_dev", _vp), ("counters_dev", _vp),
+                ("index_dev", _vp)]
 
 
 class dhs_step(ctypes.Structure):

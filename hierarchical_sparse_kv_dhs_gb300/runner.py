@@ -46,11 +46,15 @@ class _Admit:
 class GpuRun:
     def __init__(self, cfg: Config, wl: Workload | None = None, device="cuda",
                  host_threads=None, gather_impl=None, payload_requests=None,
-                 hugepages=True):
+                 hugepages=True, union=False):
         """payload_requests: requests whose imported rows are generated
         (default all); the others' pinned rows stay zero -- for parity runs
-        that compare sampled requests on workloads too large to fill."""
+        that compare sampled requests on workloads too large to fill.
+        union: resolve in the union staging layout (DHS_ITEM_UNION): `loc`
+        holds each source's union locations then DHS_END_LOC, `index` the
+        entries' union ranks, and each layer's staging its first U rows."""
         self.cfg = c = cfg
+        self.union = union
         self.wl = wl or Workload(cfg)
         self.device = torch.device(device)
         if self.device.index is None:
@@ -85,6 +89,8 @@ class GpuRun:
         self.sel = torch.from_numpy(sel).to(dev)
         self.loc = torch.empty((c.requests, c.sources, Q, k), dtype=torch.int32, device=dev)
         self.counters = torch.zeros((c.requests, c.sources, 8), dtype=torch.int32, device=dev)
+        self.index = (torch.empty((c.requests, c.sources, Q, k), dtype=torch.int32, device=dev)
+                      if union else None)
         self.staging = torch.empty((c.requests, len(self.layers), Q, k, c.row_elems),
                                    dtype=torch.bfloat16, device=dev)
         # appended rows of every step
@@ -124,6 +130,9 @@ class GpuRun:
                     it = dhs.dhs_item()
                     it.req, it.src, it.queries, it.topk = r, s, Q, k
                     it.flags = dhs.DHS_ITEM_GATHER_ONLY if kind == "reuse" else 0
+                    if self.union and kind != "reuse":
+                        it.flags |= dhs.DHS_ITEM_UNION
+                        it.index_dev = self.index[r, s].data_ptr()
                     ss = 0 if c.shared_selection else s
                     it.sel_dev = self.sel[step - 1, r, ss].data_ptr()
                     it.loc_dev = loc0 + ((r * c.sources + s) * Q * k) * 4

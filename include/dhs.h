@@ -20,8 +20,8 @@
  *     rows than unprotected hot slots, a gather location outside its arena)
  *     cannot be returned by the launching call: they leave the affected
  *     (request, source) unchanged for that step, write DHS_NO_LOC to all its
- *     locations and zero to its counters, and set a sticky flag read by
- *     dhs_status().
+ *     locations (a union item: DHS_END_LOC, index -1) and zero to its
+ *     counters, and set a sticky flag read by dhs_status().
  *   - A pool is not thread-safe: calls on one pool must not overlap.
  *   - Ownership: the caller owns every device buffer (the four arenas,
  *     selections, location vectors, staging, counters, appended rows) and
@@ -60,6 +60,8 @@ extern "C" {
 #define DHS_TIER_OPT 1u
 #define DHS_TIER_HOT 2u
 #define DHS_NO_LOC 0xFFFFFFFFu
+/* Past the end of a union location list (DHS_ITEM_UNION): gathers skip it. */
+#define DHS_END_LOC 0xFFFFFFFEu
 #define DHS_LOC(tier, index) ((((uint32_t)(tier)) << 30) | ((uint32_t)(index)))
 
 /* Per-resolve counters (uint32 each), one block of DHS_NUM_COUNTERS per item:
@@ -213,6 +215,22 @@ typedef struct {
 int dhs_append(dhs_pool *pool, const dhs_append_item *items, int32_t n_items);
 
 #define DHS_ITEM_GATHER_ONLY 1u /* skip resolution: gather loc_dev as given */
+/* Union verification staging ("Memory split": verification staging;
+ * "Speculative state": verification queries share missing-row retrieval):
+ * each distinct row of the verify block is staged once.  Resolution writes
+ *   loc_dev[u]   u < U: location of the u-th distinct selected row, in
+ *                ascending row order; DHS_END_LOC for U <= u < Q*k;
+ *   index_dev    int32 [Q][k]: position of sel[q][i] among the U rows;
+ * U = counters[1] (distinct rows).  The gather then writes staging rows
+ * [0, U) only and leaves the rest of staging_dev untouched; a Reuse item
+ * (DHS_ITEM_GATHER_ONLY) given such a location vector does the same.  On
+ * DHS_ERANGE / DHS_EBUDGET the list is empty: every loc_dev entry is
+ * DHS_END_LOC and every index_dev entry -1.  Needs index_dev; pools whose
+ * histories are too long for the union's shared-memory plan (about
+ * 12 bytes per 64 rows more than a plain resolve) refuse it with DHS_EINVAL.
+ * This layout is not the pages' own: they describe per-query staging and
+ * shared retrieval, not how staging is laid out. */
+#define DHS_ITEM_UNION 2u
 
 /*
  * One item of a decode step: the Q x k selection of one layer of one
@@ -221,6 +239,7 @@ int dhs_append(dhs_pool *pool, const dhs_append_item *items, int32_t n_items);
  *   loc_dev      uint32 [Q][k] device: written by resolution, read by gather
  *   staging_dev  [Q][k][row_bytes] device gather target (gather only)
  *   counters_dev uint32 [DHS_NUM_COUNTERS] device or NULL
+ *   index_dev    int32 [Q][k] device (DHS_ITEM_UNION only, else ignored)
  * A DHS_ITEM_GATHER_ONLY item is a Reuse layer ("Model-specific reuse":
  * Reuse layers inherit the prior location vector): it is not resolved and
  * gathers loc_dev as given (req/src unused).
@@ -236,6 +255,7 @@ typedef struct {
   uint32_t *loc_dev;
   void *staging_dev;
   uint32_t *counters_dev;
+  int32_t *index_dev;
 } dhs_item;
 
 typedef struct {
@@ -262,7 +282,8 @@ int dhs_resolve(dhs_pool *pool, const dhs_step *step);
 
 /*
  * Gather: staging_dev[q][i] = the row at loc_dev[q][i] for every item
- * (resolved or gather-only); DHS_NO_LOC rows become zeros.  staging_dev must
+ * (resolved or gather-only); DHS_NO_LOC rows become zeros and DHS_END_LOC
+ * entries are skipped (staging untouched).  staging_dev must
  * be 16-byte aligned.  Stream-ordered after any earlier dhs_resolve.
  * Errors: DHS_EINVAL, DHS_ECUDA; out-of-arena locations -> zeros +
  * DHS_STATUS_ELOC.

@@ -36,7 +36,7 @@ def _as_u32(t):
 
 
 def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
-                gather_impl=0, patch=None, early=1):
+                gather_impl=0, patch=None, early=1, union=False):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
@@ -44,12 +44,13 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
         patch(wl)
     big = cfg.pairs * cfg.max_rows * cfg.row_bytes > (8 << 30)
     gpu = GpuRun(cfg, wl, gather_impl=gather_impl,
-                 payload_requests=sampled if (big and sampled is not None) else None)
+                 payload_requests=sampled if (big and sampled is not None) else None,
+                 union=union)
     if not early:
         from hierarchical_sparse_kv_dhs_gb300 import dhs
         gpu.pool.set_option(dhs.DHS_OPT_EARLY, 0)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
-    orc = OracleRun(cfg, wl, requests=sampled)
+    orc = OracleRun(cfg, wl, requests=sampled, union=union)
     try:
         for r in sampled:
             for s in range(cfg.sources):
@@ -71,13 +72,23 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
                 assert (flags & ~3) == 0 and (flags & want_flags) == want_flags
             loc_all = _as_u32(gpu.loc)
             cnt_all = _as_u32(gpu.counters)
+            idx_all = gpu.index.cpu().numpy() if union else None
             for r in sampled:
                 o = res[r]
-                assert np.array_equal(loc_all[r], o["loc"]), (cfg.name, step, r)
+                assert np.array_equal(loc_all[r].reshape(cfg.sources, -1),
+                                      o["loc"].reshape(cfg.sources, -1)), (cfg.name, step, r)
                 assert np.array_equal(cnt_all[r], o["counters"]), \
                     (cfg.name, step, r, cnt_all[r], o["counters"])
                 stg = gpu.staging[r].cpu().view(torch.int16).numpy().view(np.uint16)
-                if check_all_bytes:
+                if union:
+                    assert np.array_equal(idx_all[r], o["index"]), (cfg.name, step, r)
+                    for layer, want in enumerate(o["staging"]):
+                        got = stg[layer].reshape(-1, cfg.row_elems)[: len(want)]
+                        if not check_all_bytes and len(want):
+                            pick = np.linspace(0, len(want) - 1, 67).astype(int)
+                            got, want = got[pick], want[pick]
+                        assert np.array_equal(got, want), (cfg.name, step, r, layer)
+                elif check_all_bytes:
                     assert np.array_equal(stg, o["staging"]), (cfg.name, step, r)
                 else:
                     idx = np.linspace(0, cfg.topk - 1, 67).astype(int)
@@ -145,6 +156,28 @@ def test_small_configs_bit_exact(cfg, mode):
                 early=0 if mode.endswith("late") else 1)
 
 
+UNION = [SMALL[1], SMALL[2], SMALL[4],
+         TINY.scaled(name="v8", tag=49, queries=8, verify_core=40, topk=64, hot=400,
+                     steps=8, append_lo=1, append_hi=8, requests=2, sources=2,
+                     residency=0.3)]
+
+
+@pytest.mark.parametrize("cfg", UNION, ids=[c.name for c in UNION])
+@pytest.mark.parametrize("mode", ["fused-tma", "fused-vec", "split-tma"])
+def test_union_staging_bit_exact(cfg, mode):
+    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
+                union=True)
+
+
+def test_union_staging_failures():
+    # an out-of-range row and budget overflows: empty union lists
+    cfg = TINY.scaled(name="ubudget", tag=50, requests=2, sources=1, hot=16, topk=64,
+                      queries=2, verify_core=32, residency=0.0, steps=4)
+    compare_run(cfg, union=True, gather_impl=1)
+    cfg = TINY.scaled(name="urange", tag=46, requests=2, sources=2, steps=4, residency=0.6)
+    compare_run(cfg, union=True, gather_impl=1, patch=_bad_row)
+
+
 def _bad_row(wl):
     """Step 3 of request 1 source 0 selects row L (one past the end)."""
     sel = wl.selections()
@@ -175,6 +208,10 @@ def test_c8_full_size_sampled(impl, early):
 
 def test_c64_full_size_sampled():
     compare_run(C64, sampled=[0, 63], check_all_bytes=False)
+
+
+def test_c64_union_full_size_sampled():
+    compare_run(C64, sampled=[0, 63], check_all_bytes=False, union=True)
 
 
 def test_decode_step_fallback_matches_split_calls():
