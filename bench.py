@@ -309,7 +309,7 @@ def traced_pass(run, cycle, steps, dev, flush_l2):
     cfg = run.cfg
     trace = torch.zeros(8, dtype=torch.int64, device=dev)
     run.pool.set_option(dhs.DHS_OPT_TRACE, trace.data_ptr())
-    res, cp, ga, host_b, copy_s = [], [], [], 0, 0.0
+    res, cp, ga, lt, span, host_b, copy_s = [], [], [], [], [], 0, 0.0
     for _ in range(steps):
         s = cycle.next()
         while not cycle.timed(s):
@@ -324,6 +324,11 @@ def traced_pass(run, cycle, steps, dev, flush_l2):
         hb = int(run.counters[..., 5].sum().item()) * cfg.row_bytes
         res.append((t[1] - t[0]) / 1e3)
         ga.append((t[5] - t[4]) / 1e3)
+        end = max(t[1], t[3], t[5])
+        if t[7] > t[6] > 0:  # fresh-row list copy
+            lt.append((t[7] - t[6]) / 1e3)
+            end = max(end, t[7])
+        span.append((end - t[0]) / 1e3)
         if t[3] > t[2] > 0:
             cp.append((t[3] - t[2]) / 1e3)
             if hb:
@@ -333,6 +338,8 @@ def traced_pass(run, cycle, steps, dev, flush_l2):
     med = statistics.median
     return {"resolve_us": med(res), "gather_us": med(ga),
             "copy_us": med(cp) if cp else None,
+            "fresh_list_us": med(lt) if lt else None,
+            "step_span_us": med(span),
             "host_bytes_per_step": host_b / steps,
             "copy_gbs": (host_b / copy_s / 1e9) if copy_s else None}
 
@@ -529,7 +536,10 @@ def main():
         os.path.join(ROOT, "profiles", f"gather_{cfg.name}_traffic.json"))
     n_resolve = -(-cfg.requests * cfg.sources // 256)
     n_gather = -(-cfg.requests * cfg.layers // 384)
-    launches = K * (2 * n_resolve + n_gather)  # append folded into resolve
+    fresh = run.pool.get_option(dhs.DHS_OPT_FRESH_LIST)
+    # append folded into resolve; resolve + host copy per chunk, the gathers,
+    # and the fresh-row list copy when it is on
+    launches = K * (2 * n_resolve + n_gather + fresh)
     step_bytes = alg_bytes + cfg.resolved_per_step * 4
     impl = ["vector", "tma"][args.gather_impl]
     line = {
@@ -550,7 +560,8 @@ def main():
         "clocks": clock_info,
         "breakdown": {
             "path": f"dhs_decode_step (append folded into resolve; resolve, host copy "
-                    f"and gather PDL-overlapped), gather {impl}",
+                    f"and gather PDL-overlapped{', fresh-row list copy' if fresh else ''}), "
+                    f"gather {impl}",
             "step_ms_median": statistics.median(step_ms),
             "step_GBps_alg": step_bytes / (sum(step_ms) / K / 1e3) / 1e9,
             "traced_kernel_us": trace_info,

@@ -29,7 +29,18 @@ constexpr uint32_t kVerdictShift = 3u, kVerdictCodeMask = 7u, kSeqMask = 0x1FFFF
 
 // Optional timeline (DHS_OPT_TRACE): per kernel kind, the earliest CTA start
 // and the latest CTA end in %globaltimer nanoseconds.
-enum TraceSlot { kTraceResolve = 0, kTraceCopy = 1, kTraceGather = 2, kTraceKinds = 4 };
+enum TraceSlot { kTraceResolve = 0, kTraceCopy = 1, kTraceGather = 2, kTraceLater = 3,
+                 kTraceKinds = 4 };
+
+// Fused steps: rows in hot slots that this step's host copy fills ("fresh"
+// rows) are the only ones a gather must leave until the copy grid is done.
+// Gather tiles append them to a device list of LaterEntry, copied by a
+// second launch once the copy grid has completed.
+struct LaterEntry {
+  uint8_t* dst;   // staging row (null: unused slot)
+  uint32_t loc;   // hot location of the row
+  uint32_t pad;
+};
 
 #ifdef __CUDACC__
 __device__ __forceinline__ unsigned long long trace_now() {
@@ -89,6 +100,11 @@ struct ResolveCommon {
   uint32_t* verdict;     // [pairs] published verdicts, null = none
   uint32_t seq;          // sequence number of this launch
   int32_t uni;           // shared-memory plan includes the union bitmap
+  uint32_t* loc_ready;   // [pairs] seq once the item's locations are written; null = off
+  uint32_t* fill;        // [pairs][fill_words] hot slots filled by this step's copy
+  uint32_t* later_count; // [2] fresh-row list lengths; the launch zeroes [gen ^ 1]
+  int32_t fill_words;
+  uint32_t gen;          // fused-step generation (parity picks the list counter)
 };
 
 size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni);
@@ -122,6 +138,7 @@ cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,
 constexpr int kGatherThreads = 256;
 constexpr int kGatherVector = 0, kGatherTma = 1;  // DHS_OPT_GATHER_IMPL values
 constexpr int kGatherTileRows = 32;
+constexpr int kLaterThreads = 512;
 constexpr int kGatherItemsLarge = 384, kGatherItemsSmall = 64;
 
 struct GatherItem {
@@ -134,7 +151,12 @@ struct GatherItem {
   int32_t tile0;       // first tile of this item in the launch
   int32_t pair;        // req * S + src (resolved items)
   uint32_t seq;        // sequence number of the resolve launch that resolved it
+  uint32_t flags;      // kGiLocReady
+  int32_t pad;
 };
+// The item's locations are those of a pair resolved by the preceding resolve
+// launch of the same fused step, published through loc_ready[pair] == seq.
+constexpr uint32_t kGiLocReady = 1u;
 
 struct GatherCommon {
   const uint8_t* tail;
@@ -151,6 +173,14 @@ struct GatherCommon {
   int32_t early;             // copy step-1 rows before waiting for the resolve grid
   const uint32_t* verdict;   // [pairs] verdicts published by the resolve kernel
   unsigned long long* trace;  // null = off
+  const uint32_t* loc_ready;  // [pairs] (kGiLocReady items)
+  const uint32_t* fill;       // [pairs][fill_words]
+  int32_t fill_words;
+  int32_t B;
+  LaterEntry* later;          // fresh-row list, null = fresh rows wait in their tile
+  uint32_t* later_count;      // [2]
+  uint32_t later_cap;
+  uint32_t gen;
 };
 
 // Each kernel file sets its kernels' shared-memory carveout to the maximum,
@@ -163,6 +193,9 @@ cudaError_t append_set_carveout();
 
 cudaError_t launch_gather(const GatherCommon& c, const GatherItem* items,
                           int n_items, bool pdl, int impl, cudaStream_t stream);
+// Copy the fresh-row list of generation c.gen once the gather (and through
+// it the copy grid) has completed; programmatic dependent of the gather.
+cudaError_t launch_gather_later(const GatherCommon& c, int ctas, cudaStream_t stream);
 
 // Raise the TMA gather's dynamic shared-memory limit for a row size.
 cudaError_t gather_set_smem_limit(int row_bytes);

@@ -52,6 +52,42 @@ __device__ __forceinline__ uint32_t ld_verdict(const uint32_t* p) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait (whole warp) until the resolve kernel has published the
+// item's locations; false if they did not come out in time -- the caller
+// then waits for the resolve / host-copy grids instead, so giving up costs
+// time, never correctness.  Every lane takes its own acquire.
+constexpr uint32_t kLocPolls = 1u << 20;
+__device__ __forceinline__ bool wait_loc_ready(const GatherCommon& c, const GatherItem& it) {
+  const uint32_t want = it.seq & kSeqMask;
+  for (uint32_t i = 0; i < kLocPolls; ++i) {
+    const bool r = ld_acquire(&c.loc_ready[it.pair]) == want;
+    if (__all_sync(0xFFFFFFFFu, r)) return true;
+    __nanosleep(200);
+  }
+  return false;
+}
+
+// True if `loc` names a hot slot that this step's host copy fills.
+__device__ __forceinline__ bool fresh_loc(const GatherCommon& c, uint32_t loc) {
+  if ((loc >> 30) != kTierHot || loc == kNoLoc || loc == kEndLoc) return false;
+  const uint32_t idx = loc & 0x3FFFFFFFu;
+  if (idx >= c.hot_rows) return false;  // invalid: the copy reports it
+  const uint32_t pair = idx / (uint32_t)c.B, slot = idx - pair * (uint32_t)c.B;
+  return (ld_relaxed(&c.fill[(size_t)pair * c.fill_words + (slot >> 5)]) >> (slot & 31)) & 1u;
+}
+
 template <int MAXI>
 __device__ __forceinline__ int find_item(const GatherParams<MAXI>& P, int tile) {
   int lo = 0, hi = P.c.n_items - 1;  // last item whose first tile <= tile
@@ -308,7 +344,9 @@ __global__ void __launch_bounds__(kTmaThreads)
       if (lane == 0) mbar_arrive_expect(&s_bar, (uint32_t)__popc(lmask) * rb);
       __syncwarp();
       if (load) bulk_load(my_row, src, rb, &s_bar);
-      if (!mbar_wait(&s_bar, parity)) {
+      // one answer for the whole warp, so every later warp collective is
+      // reached by all lanes
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s_bar, parity))) {
         if (lane == 0) atomicOr(c.status, kStatusEtimeout);
         return false;
       }
@@ -337,6 +375,33 @@ __global__ void __launch_bounds__(kTmaThreads)
       deferred = false;
     }
   }
+  const bool lr = c.early && (it.flags & kGiLocReady) && !waited;
+  if (ok && __any_sync(0xFFFFFFFFu, deferred) && lr && wait_loc_ready(c, it)) {
+    // the item's locations are out: every row but the fresh ones (hot slots
+    // the host copy is still filling) can move now
+    const uint32_t l = deferred ? ld_relaxed(&it.loc[e0 + lane]) : kEndLoc;
+    const bool fresh = deferred && fresh_loc(c, l);
+    const bool now = deferred && l != kEndLoc && !fresh;
+    ok = move(now, now ? row_ptr(c, l) : nullptr);
+    bool later = fresh;
+    if (c.later) {  // hand the fresh rows to the list copied after the copy grid
+      const unsigned fm = __ballot_sync(0xFFFFFFFFu, fresh);
+      uint32_t base = 0;
+      if (lane == 0 && fm) base = atomicAdd(&c.later_count[c.gen & 1u], (uint32_t)__popc(fm));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      const uint32_t cnt = (uint32_t)__popc(fm);
+      const bool fits = (uint64_t)base + cnt <= c.later_cap;
+      const uint32_t slot = base + (uint32_t)__popc(fm & ((1u << lane) - 1u));
+      if (fresh && fits) {
+        c.later[slot].dst = dst;
+        c.later[slot].loc = l;
+        later = false;
+      } else if (fresh && slot < c.later_cap) {
+        c.later[slot].dst = nullptr;  // the list is full: the tile copies it
+      }
+    }
+    deferred = later;
+  }
   if (ok && __any_sync(0xFFFFFFFFu, deferred)) {
     // rows that needed the hot cache (or no early phase): wait for the
     // resolve / host-copy grids (a no-op without programmatic dependent launch)
@@ -348,6 +413,37 @@ __global__ void __launch_bounds__(kTmaThreads)
   // shared memory must outlive the stores' reads
   if (stored) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   end_grid(c);
+}
+
+// ---------------------------------------------------------------- fresh rows
+
+// Copy the fresh-row list of this generation (hot slot -> staging) once the
+// gather grid -- whose last block waits for the host-copy grid -- is done.
+// Each warp keeps four rows in flight, as the host copy does.
+__global__ void __launch_bounds__(kLaterThreads) gather_later_kernel(const GatherCommon c) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) trace_mark(c.trace, kTraceLater, false);  // copying starts
+  const uint32_t total = min(c.later_count[c.gen & 1u], c.later_cap);
+  const int lane = threadIdx.x & 31;
+  const int cpr = c.row_bytes >> 4;
+  const uint32_t gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  constexpr int kRows = 4;
+  for (uint32_t base = gwarp * kRows; base < total; base += nwarps * kRows) {
+    for (int r = 0; r < kRows; ++r) {
+      const uint32_t i = base + r;
+      if (i >= total) break;
+      uint8_t* dst = c.later[i].dst;
+      if (!dst) continue;
+      const uint8_t* src = row_ptr(c, c.later[i].loc);
+      for (int ch = lane; ch < cpr; ch += 32) {
+        const uint4 v = src ? *reinterpret_cast<const uint4*>(src + ch * 16)
+                            : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(dst + ch * 16) = v;
+      }
+    }
+  }
+  if (threadIdx.x == 0) trace_mark(c.trace, kTraceLater, true);
 }
 
 template <int MAXI>
@@ -379,6 +475,19 @@ cudaError_t launch_t(const GatherCommon& c, const GatherItem* items, int n, bool
 }
 
 }  // namespace
+
+cudaError_t launch_gather_later(const GatherCommon& c, int ctas, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kLaterThreads);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_later_kernel, c);
+}
 
 cudaError_t gather_set_carveout() {
   const void* ks[] = {(const void*)gather_kernel<kGatherItemsSmall, 72>,

@@ -24,6 +24,7 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "dhs.h"
@@ -35,12 +36,21 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct MetaLayout {
-  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status, verdict, status;
+  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status, verdict;
+  size_t loc_ready, fill, later_count, status, later;
   size_t total;
 };
 
 inline int64_t pages_max_of(const dhs_pool_config& c) {
   return (c.max_rows_per_request + c.page_rows - 1) / c.page_rows;
+}
+
+inline int64_t fill_words_of(const dhs_pool_config& c) { return (c.hot_rows + 31) / 32; }
+
+// Fresh-row list entries: one resolved step's entries (Reuse layers beyond
+// that copy their fresh rows in their own tiles).
+inline int64_t later_cap_of(const dhs_pool_config& c) {
+  return std::max<int64_t>(1, (int64_t)c.max_requests * c.sources * c.max_queries * c.max_topk);
 }
 
 inline int64_t mcap_of(const dhs_pool_config& c) {
@@ -65,7 +75,11 @@ MetaLayout meta_layout(const dhs_pool_config& c) {
   m.miss_count = take(pairs * 4);
   m.pair_status = take(pairs * 4);
   m.verdict = take(pairs * 4);
+  m.loc_ready = take(pairs * 4);
+  m.fill = take(pairs * (size_t)fill_words_of(c) * 4);
+  m.later_count = take(2 * 4);
   m.status = take(64);
+  m.later = take((size_t)later_cap_of(c) * sizeof(dhs::LaterEntry));
   m.total = off;
   return m;
 }
@@ -143,6 +157,17 @@ struct dhs_pool {
   int early = 1;        // fused gathers copy step-1 rows before the resolve ends
   uint32_t* verdict = nullptr;  // [pairs] resolve verdicts for the fused gather
   uint32_t seq = 0;             // resolve launches so far
+  uint32_t* loc_ready = nullptr;  // [pairs] per-item "locations written" marks
+  uint32_t* fill = nullptr;       // [pairs][fill_words] slots the step's copy fills
+  uint32_t* later_count = nullptr;
+  dhs::LaterEntry* later = nullptr;
+  int64_t later_cap = 0;
+  int fill_words = 0;
+  uint32_t gen = 0;             // fused steps that launched a resolve
+  bool fused_resolved = false;  // the current fused step launched one
+  int fresh_list = -1;          // DHS_OPT_FRESH_LIST: -1 auto, 0 off, 1 on
+  int64_t complete_pages = 0;   // complete imported pages of admitted pairs
+  int sm_count = 0;
   unsigned long long* trace = nullptr;  // DHS_OPT_TRACE buffer, null = off
   // reusable launch tables
   std::vector<dhs::ResolveItem> ritems;
@@ -298,6 +323,9 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
       cudaSuccess)
     return DHS_ECUDA;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DHS_ECUDA;
   const size_t smem = max_resolve_smem(*cfg, false);
   if (smem + 1024 > (size_t)optin) return DHS_EINVAL;
   const size_t smem_u = max_resolve_smem(*cfg, true);
@@ -309,6 +337,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
   try {
     p->cfg = *cfg;
     p->union_ok = union_ok;
+    p->sm_count = sms;
     p->stream = (cudaStream_t)cfg->stream;
     p->device = dev;
     p->pairs = (int64_t)cfg->max_requests * cfg->sources;
@@ -325,6 +354,12 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->miss_count = (uint32_t*)(m + p->layout.miss_count);
     p->pair_status = (int32_t*)(m + p->layout.pair_status);
     p->verdict = (uint32_t*)(m + p->layout.verdict);
+    p->loc_ready = (uint32_t*)(m + p->layout.loc_ready);
+    p->fill = (uint32_t*)(m + p->layout.fill);
+    p->later_count = (uint32_t*)(m + p->layout.later_count);
+    p->later = (dhs::LaterEntry*)(m + p->layout.later);
+    p->later_cap = later_cap_of(*cfg);
+    p->fill_words = (int)fill_words_of(*cfg);
     p->status = (uint32_t*)(m + p->layout.status);
     p->ps.resize(p->pairs);
     p->map_host.assign((size_t)(p->pairs * p->pmax), -1);
@@ -354,7 +389,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
   if (e == cudaSuccess) e = cudaMemsetAsync(p->map, 0xFF, p->pairs * p->pmax * 4, p->stream);
   if (e == cudaSuccess)
     e = cudaMemsetAsync((uint8_t*)cfg->meta_dev + p->layout.miss_count, 0,
-                        p->layout.total - p->layout.miss_count, p->stream);
+                        p->layout.later - p->layout.miss_count, p->stream);
   if (e != cudaSuccess) {
     delete p;
     return DHS_ECUDA;
@@ -389,7 +424,34 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     pool->gather_impl = (int)value;
     return DHS_OK;
   }
+  if (key == DHS_OPT_FRESH_LIST) {
+    if (value < -1 || value > 1) return DHS_EINVAL;
+    pool->fresh_list = (int)value;
+    return DHS_OK;
+  }
   return DHS_EINVAL;
+}
+
+// Whether fused steps hand fresh rows to the list copied after the host-copy
+// grid (one launch more per step).  Auto: when more than a tenth of the
+// admitted complete pages are not optional-resident, so that host copies are
+// expected every step.
+static bool use_fresh_list(const dhs_pool* p) {
+  if (p->gather_impl != dhs::kGatherTma || !p->early) return false;
+  if (p->fresh_list >= 0) return p->fresh_list == 1;
+  return (p->complete_pages - p->used) * 10 > p->complete_pages;
+}
+
+int dhs_get_option(dhs_pool* pool, int32_t key, int64_t* value) {
+  if (!pool || !value) return DHS_EINVAL;
+  switch (key) {
+    case DHS_OPT_COPY_CTAS: *value = pool->copy_ctas; return DHS_OK;
+    case DHS_OPT_GATHER_IMPL: *value = pool->gather_impl; return DHS_OK;
+    case DHS_OPT_TRACE: *value = (int64_t)(uintptr_t)pool->trace; return DHS_OK;
+    case DHS_OPT_EARLY: *value = pool->early; return DHS_OK;
+    case DHS_OPT_FRESH_LIST: *value = use_fresh_list(pool) ? 1 : 0; return DHS_OK;
+    default: return DHS_EINVAL;
+  }
 }
 
 int dhs_admit(dhs_pool* p, int32_t req, int32_t src, void* host_rows, int64_t n_rows,
@@ -447,6 +509,7 @@ int dhs_admit(dhs_pool* p, int32_t req, int32_t src, void* host_rows, int64_t n_
   s.admitted = true;
   s.N = n_rows;
   s.L = n_rows;
+  p->complete_pages += n_rows >> p->page_shift;
   s.host = (uint8_t*)host_rows;
   s.host_dev = (uint8_t*)hdev;
   return DHS_OK;
@@ -482,6 +545,7 @@ int dhs_release(dhs_pool* p, int32_t req) {
   for (int32_t s = 0; s < p->cfg.sources; ++s) {
     const int64_t pair = (int64_t)req * p->cfg.sources + s;
     drop_pages(p, pair);
+    if (p->ps[pair].admitted) p->complete_pages -= p->ps[pair].N >> p->page_shift;
     p->ps[pair] = PairState();
   }
   const int64_t pair0 = (int64_t)req * p->cfg.sources;
@@ -577,7 +641,8 @@ static int validate_step(dhs_pool* p, const dhs_step* st, bool resolving) {
 // Launch resolve + host copy for every resolving item of a validated,
 // flushed step.  `apps` (may be null): appends folded into the resolve
 // kernel, one per pair listed in p->app_of_pair.
-static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* apps) {
+static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* apps,
+                        bool fused) {
   const dhs_pool_config& c = p->cfg;
   p->ritems.clear();
   p->citems.clear();
@@ -629,6 +694,13 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   rcm.tail = (uint8_t*)c.tail_dev;
   rcm.trace = p->trace;
   rcm.verdict = p->verdict;
+  p->fused_resolved = fused && !p->ritems.empty();
+  if (p->fused_resolved) ++p->gen;
+  rcm.loc_ready = p->loc_ready;
+  rcm.fill = p->fill;
+  rcm.fill_words = p->fill_words;
+  rcm.later_count = p->later_count;
+  rcm.gen = p->gen;
   dhs::CopyCommon ccm{};
   ccm.hot = (uint8_t*)c.hot_dev;
   ccm.miss_rows = p->miss_rows;
@@ -675,7 +747,7 @@ int dhs_resolve(dhs_pool* p, const dhs_step* st) {
   if (rc) return rc;
   if ((rc = enter(p))) return rc;
   if ((rc = flush(p))) return rc;
-  return resolve_impl(p, st, nullptr);
+  return resolve_impl(p, st, nullptr, false);
 }
 
 // Launch the gather for every item of a validated, flushed step.  `fused`:
@@ -701,6 +773,24 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   g.early = fused && p->early ? 1 : 0;
   g.verdict = p->verdict;
   g.trace = p->trace;
+  g.loc_ready = p->loc_ready;
+  g.fill = p->fill;
+  g.fill_words = p->fill_words;
+  g.B = c.hot_rows;
+  g.later_count = p->later_count;
+  g.later_cap = (uint32_t)std::min<int64_t>(p->later_cap, UINT32_MAX);
+  g.gen = p->gen;
+  // the step's resolved items publish their locations; gathers of them (and
+  // Reuse items handed the same location vector) may go before the grids end
+  const bool lr = fused && p->early && p->fused_resolved && p->gather_impl == dhs::kGatherTma;
+  g.later = lr && use_fresh_list(p) ? p->later : nullptr;
+  std::unordered_map<const void*, int64_t> loc_pair;
+  if (lr)
+    for (int32_t i = 0; i < st->n_items; ++i) {
+      const dhs_item& it = st->items[i];
+      if (!(it.flags & DHS_ITEM_GATHER_ONLY) && it.loc_dev)
+        loc_pair[it.loc_dev] = (int64_t)it.req * c.sources + it.src;
+    }
   p->gitems.clear();
   for (int32_t i = 0; i < st->n_items; ++i) {
     const dhs_item& it = st->items[i];
@@ -721,6 +811,14 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
       gi.L0 = p->l0_of_pair[pair];
       gi.seq = p->seq_of_pair[pair];
     }
+    if (lr) {
+      auto f = loc_pair.find(it.loc_dev);
+      if (f != loc_pair.end()) {
+        gi.pair = (int32_t)f->second;
+        gi.seq = p->seq_of_pair[f->second];
+        gi.flags |= dhs::kGiLocReady;
+      }
+    }
     p->gitems.push_back(gi);
   }
   const size_t ng = p->gitems.size();
@@ -740,6 +838,9 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
         cudaSuccess)
       return DHS_ECUDA;
   }
+  if (g.later && ng > 0 &&
+      dhs::launch_gather_later(g, 2 * std::max(1, p->sm_count), p->stream) != cudaSuccess)
+    return DHS_ECUDA;
   return DHS_OK;
 }
 
@@ -754,7 +855,10 @@ int dhs_gather(dhs_pool* p, const dhs_step* st) {
 int dhs_resolve_gather(dhs_pool* p, const dhs_step* st) {
   int rc = validate_step(p, st, false);
   if (rc) return rc;
-  if ((rc = dhs_resolve(p, st))) return rc;
+  if ((rc = validate_step(p, st, true))) return rc;
+  if ((rc = enter(p))) return rc;
+  if ((rc = flush(p))) return rc;
+  if ((rc = resolve_impl(p, st, nullptr, true))) return rc;
   return launch_gathers(p, st, true);
 }
 
@@ -803,7 +907,7 @@ int dhs_decode_step(dhs_pool* p, const dhs_append_item* apps, int32_t n_apps,
   for (int32_t i = 0; i < n_apps; ++i)
     if (apps[i].count > 0)
       p->app_of_pair[(int64_t)apps[i].req * c.sources + apps[i].src] = i;
-  rc = resolve_impl(p, st, apps);
+  rc = resolve_impl(p, st, apps, true);
   for (int32_t i = 0; i < n_apps; ++i)
     p->app_of_pair[(int64_t)apps[i].req * c.sources + apps[i].src] = -1;
   if (rc) return rc;

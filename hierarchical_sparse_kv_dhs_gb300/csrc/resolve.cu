@@ -219,6 +219,15 @@ __device__ __forceinline__ void publish(const ResolveCommon& c, int pair, uint32
                : "memory");
 }
 
+// Publish that an item's locations (and the decode rows it appended) are
+// written (thread 0 only, after a block barrier).
+__device__ __forceinline__ void publish_loc(const ResolveCommon& c, int pair) {
+  if (!c.loc_ready) return;
+  __threadfence();
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(c.loc_ready + pair),
+               "r"(c.seq & kSeqMask) : "memory");
+}
+
 // Write the failure result of one item: no state change.
 __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t code,
                           uint32_t flag) {
@@ -231,7 +240,9 @@ __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t
     for (int e = threadIdx.x; e < it.n; e += blockDim.x) it.loc[e] = kNoLoc;
   }
   if (threadIdx.x < 8 && it.counters) it.counters[threadIdx.x] = 0u;
+  __syncthreads();
   if (threadIdx.x == 0) {
+    publish_loc(c, it.pair);
     c.miss_count[it.pair] = 0u;
     c.pair_status[it.pair] = code;
     publish(c, it.pair, code == kErrRange ? kVerdictRange : kVerdictBudget);
@@ -274,6 +285,14 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   int32_t* tags = c.tags + (size_t)pair * B;
   uint32_t* stamps = c.stamps + (size_t)pair * B;
   const int32_t* map = c.map + (size_t)pair * c.Pmax;
+
+  // this step's fill marks start empty; the next fused step's fresh-row
+  // list starts empty (nothing reads either before this launch completes
+  // or, for the fill marks, before this item publishes its locations)
+  uint32_t* fill = c.fill ? c.fill + (size_t)pair * c.fill_words : nullptr;
+  if (fill)
+    for (int j = tid; j < c.fill_words; j += nt) fill[j] = 0u;
+  if (c.later_count && blockIdx.x == 0 && tid == 0) c.later_count[(c.gen & 1u) ^ 1u] = 0u;
 
   Smem s;
   carve(c.w64cap, c.qkcap, B, c.uni != 0, &s, smem_raw);
@@ -453,6 +472,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
           const int v = src[mr];
           const int32_t row = s.cand_row[i];
           evicted += tags[v] != -1;
+          if (fill) atomicOr(&fill[v >> 5], 1u << (v & 31));
           tags[v] = row;
           s.st[v] = step;
           s.slot_of[i] = (uint16_t)v;
@@ -506,6 +526,8 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
     }
     for (int u = (int)n_unique + tid; u < n; u += nt) it.loc[u] = kEndLoc;
   }
+  __syncthreads();
+  if (tid == 0) publish_loc(c, pair);
 
   if (m_miss) {
     uint32_t ev[4] = {evicted, 0u, 0u, 0u};

@@ -42,6 +42,7 @@ DHS_OPT_COPY_CTAS = 1
 DHS_OPT_GATHER_IMPL = 2
 DHS_OPT_TRACE = 3
 DHS_OPT_EARLY = 4
+DHS_OPT_FRESH_LIST = 5
 DHS_BUF_HOT, DHS_BUF_TAIL, DHS_BUF_OPT, DHS_BUF_META = range(4)
 
 _i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
@@ -97,6 +98,7 @@ def _load():
         "dhs_status": (ctypes.c_int, [_vp, P(_u32)]),
         "dhs_read_state": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp]),
         "dhs_set_option": (ctypes.c_int, [_vp, _i32, _i64]),
+        "dhs_get_option": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i64)]),
         "dhs_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
@@ -205,6 +207,12 @@ def dhs_status(h):
 
 def dhs_set_option(h, key, value):
     return lib.dhs_set_option(h, key, value)
+
+
+def dhs_get_option(h, key):
+    v = _i64(0)
+    rc = lib.dhs_get_option(h, key, ctypes.byref(v))
+    return rc, v.value
 
 
 def dhs_read_state(h, req, src, B, pages_max):
@@ -351,6 +359,11 @@ class Pool:
 
     def set_option(self, key, value):
         return check(dhs_set_option(self.h, key, value), "dhs_set_option")
+
+    def get_option(self, key):
+        rc, v = dhs_get_option(self.h, key)
+        check(rc, "dhs_get_option")
+        return v
 
     def read_state(self, req, src):
         return dhs_read_state(self.h, req, src, self.cfg.hot_rows, self.pages_max)

@@ -359,16 +359,28 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
                                      (default); 0 = 16-byte vector copy, 256
                                      threads per tile */
 /* Timeline: value = address of a device buffer of 8 uint64 (0 = off).  Each
- * kernel kind k (0 resolve, 1 host copy, 2 gather) atomically lowers buf[2k]
+ * kernel kind k (0 resolve, 1 host copy, 2 gather, 3 fresh-row copy) atomically
+ * lowers buf[2k]
  * to its earliest CTA start and raises buf[2k+1] to its latest CTA end
  * (%globaltimer, ns; the host copy's start is when its copying begins, after
  * it has waited for the resolve kernel); the caller initialises buf[2k] to
  * UINT64_MAX and buf[2k+1] to 0. */
 #define DHS_OPT_TRACE 3
-/* 1 (default): fused gathers copy step-1 rows while the resolve kernel runs;
- * 0: they wait for it first. */
+/* 1 (default): fused gathers copy step-1 rows while the resolve kernel runs,
+ * and every other row as soon as the resolve kernel has written its item's
+ * locations, except rows in hot slots this step's host copy fills; 0: they
+ * wait for the resolve and host-copy kernels first. */
 #define DHS_OPT_EARLY 4
+/* Fused steps (TMA gather): rows in hot slots that this step's host copy
+ * fills go to a device list copied by one more kernel after the copy, so
+ * gather tiles never wait for the copy.  -1 (default) = on when more than a
+ * tenth of the admitted complete pages are not optional-resident; 0 = off
+ * (such rows wait in their tile); 1 = on. */
+#define DHS_OPT_FRESH_LIST 5
 int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
+/* The value in effect (DHS_OPT_FRESH_LIST: 0 or 1, the auto rule resolved
+ * for the pool's current admissions).  DHS_EINVAL for an unknown key. */
+int dhs_get_option(dhs_pool *pool, int32_t key, int64_t *value);
 
 /* Static string for a DHS_* code. */
 const char *dhs_strerror(int code);

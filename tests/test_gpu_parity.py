@@ -36,7 +36,7 @@ def _as_u32(t):
 
 
 def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
-                gather_impl=0, patch=None, early=1, union=False):
+                gather_impl=0, patch=None, early=1, union=False, fresh=None):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
@@ -46,9 +46,11 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
     gpu = GpuRun(cfg, wl, gather_impl=gather_impl,
                  payload_requests=sampled if (big and sampled is not None) else None,
                  union=union)
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
     if not early:
-        from hierarchical_sparse_kv_dhs_gb300 import dhs
         gpu.pool.set_option(dhs.DHS_OPT_EARLY, 0)
+    if fresh is not None:
+        gpu.pool.set_option(dhs.DHS_OPT_FRESH_LIST, fresh)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
     orc = OracleRun(cfg, wl, requests=sampled, union=union)
     try:
@@ -167,6 +169,16 @@ UNION = [SMALL[1], SMALL[2], SMALL[4],
 def test_union_staging_bit_exact(cfg, mode):
     compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
                 union=True)
+
+
+@pytest.mark.parametrize("fresh", [0, 1])
+@pytest.mark.parametrize("cfg", [SMALL[1], SMALL[2], SMALL[4]], ids=["v3", "reuse", "evict"])
+def test_fresh_row_list_on_and_off(cfg, fresh):
+    """Rows in hot slots the step's host copy fills either wait in their gather
+    tile (0) or go to the list copied after the copy (1; the Reuse workload
+    overflows the list on its first step, so tiles also take the fallback)."""
+    compare_run(cfg, gather_impl=1, fresh=fresh)
+    compare_run(cfg, gather_impl=1, fresh=fresh, union=True)
 
 
 def test_union_staging_failures():
