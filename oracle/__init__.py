@@ -70,6 +70,14 @@ def lib() -> ctypes.CDLL:
             L.orc_append.argtypes = [vp, i32, i32, i32, vp]
             L.orc_resolve.restype = ctypes.c_int
             L.orc_resolve.argtypes = [vp, u32, i32, i32, i32, i32, vp, vp, vp]
+            L.orc_admit_device.restype = ctypes.c_int
+            L.orc_admit_device.argtypes = [vp, i32, i32, vp, i64, vp, vp]
+            L.orc_backup.restype = ctypes.c_int
+            L.orc_backup.argtypes = [vp, i64, vp]
+            L.orc_refill.restype = ctypes.c_int
+            L.orc_refill.argtypes = [vp, i64, vp]
+            L.orc_pending_backup.restype = i64
+            L.orc_pending_backup.argtypes = [vp]
             L.orc_resolve_union.restype = ctypes.c_int
             L.orc_resolve_union.argtypes = [vp, u32, i32, i32, i32, i32, vp, vp, vp, vp]
             L.orc_gather.restype = ctypes.c_int
@@ -123,6 +131,31 @@ class OraclePool:
         rc = lib().orc_admit(self._h, r, s, _p(host_rows), N, _p(mask),
                              ctypes.byref(d))
         return RC_NAMES[rc], d.value
+
+    def admit_device(self, r, s, N, mask=None, rows=None):
+        """Resident-first admission of rows held on the device (backup of the
+        resident pages deferred)."""
+        d = ctypes.c_int64(0)
+        if mask is not None:
+            mask = np.ascontiguousarray(mask, dtype=np.uint8)
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.uint16)
+            assert rows.size >= N * self.E
+        rc = lib().orc_admit_device(self._h, r, s, _p(rows), N, _p(mask), ctypes.byref(d))
+        return RC_NAMES[rc], d.value
+
+    def backup(self, max_pages):
+        n = ctypes.c_int64(0)
+        rc = lib().orc_backup(self._h, max_pages, ctypes.byref(n))
+        return RC_NAMES[rc], n.value
+
+    def refill(self, max_pages):
+        n = ctypes.c_int64(0)
+        rc = lib().orc_refill(self._h, max_pages, ctypes.byref(n))
+        return RC_NAMES[rc], n.value
+
+    def pending_backup(self):
+        return int(lib().orc_pending_backup(self._h))
 
     def reclaim(self, order, deficit):
         o = np.ascontiguousarray(order, dtype=np.int32)

@@ -77,10 +77,18 @@ typedef struct {
   uint16_t *host;     /* [max_rows][E]: this source's pinned-host copy */
   uint16_t *tail;     /* [T][E] */
   uint16_t *hot;      /* [B][E] */
+  /* resident-first admission from device rows: the imported rows as the
+   * device holds them (what a ready optional page contains); NULL when the
+   * source was admitted from its host copy */
+  uint16_t *imported;
+  uint8_t *backed;    /* [pages_max]: 1 = the host copy of the page is valid */
+  uint64_t *pend;     /* [pages_max]: backup order of a pending page, 0 = none */
 } orc_source;
 
 typedef struct {
   int32_t R, S, T, B, E, PR;
+  int32_t rr;         /* refill cursor: the next request visited */
+  uint64_t bseq;      /* pages put in backup order so far */
   int64_t max_rows, pages_max, capacity, reserve, used, first_free;
   int32_t *slot_pair; /* [capacity]: owning pair, -1 = free */
   int32_t *slot_page; /* [capacity]: page of the owner */
@@ -89,10 +97,14 @@ typedef struct {
 
 static void reset_source_state(const orc_pool *p, orc_source *s) {
   for (int32_t j = 0; j < p->B; ++j) { s->tags[j] = -1; s->stamps[j] = 0; }
-  for (int64_t q = 0; q < p->pages_max; ++q) s->page_slot[q] = -1;
+  for (int64_t q = 0; q < p->pages_max; ++q) {
+    s->page_slot[q] = -1;
+    s->backed[q] = 1;
+    s->pend[q] = 0;
+  }
   s->admitted = 0; s->tracked = 0; s->N = 0; s->L = 0;
-  free(s->host); free(s->tail); free(s->hot);
-  s->host = s->tail = s->hot = NULL;
+  free(s->host); free(s->tail); free(s->hot); free(s->imported);
+  s->host = s->tail = s->hot = s->imported = NULL;
 }
 
 void orc_pool_free(orc_pool *p) {
@@ -101,7 +113,8 @@ void orc_pool_free(orc_pool *p) {
     for (int64_t i = 0; i < (int64_t)p->R * p->S; ++i) {
       orc_source *s = &p->src[i];
       free(s->page_slot); free(s->tags); free(s->stamps);
-      free(s->host); free(s->tail); free(s->hot);
+      free(s->host); free(s->tail); free(s->hot); free(s->imported);
+      free(s->backed); free(s->pend);
     }
   }
   free(p->src); free(p->slot_pair); free(p->slot_page); free(p);
@@ -130,7 +143,12 @@ orc_pool *orc_pool_new(int32_t R, int32_t S, int32_t T, int32_t B, int32_t E,
     s->page_slot = (int32_t *)malloc(sizeof(int32_t) * (size_t)p->pages_max);
     s->tags = (int32_t *)malloc(sizeof(int32_t) * (size_t)B);
     s->stamps = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)B);
-    if (!s->page_slot || !s->tags || !s->stamps) { orc_pool_free(p); return NULL; }
+    s->backed = (uint8_t *)malloc((size_t)p->pages_max);
+    s->pend = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)p->pages_max);
+    if (!s->page_slot || !s->tags || !s->stamps || !s->backed || !s->pend) {
+      orc_pool_free(p);
+      return NULL;
+    }
     reset_source_state(p, s);
   }
   return p;
@@ -208,6 +226,133 @@ int orc_admit(orc_pool *p, int32_t r, int32_t s, const uint16_t *host_rows,
   return ORC_OK;
 }
 
+int orc_release(orc_pool *p, int32_t r);
+
+#define ORC_POISON 0xDEADu /* host rows whose backup has not happened yet */
+
+/*
+ * Resident-first admission of rows that are on the device ("Resident-first
+ * admission": a new request keeps its imported history on device and
+ * defers host backup while HBM is spare).  `rows` (N rows, NULL = metadata
+ * only) are the imported rows as the device holds them.  Pages are chosen
+ * and the capacity rule applied exactly as in orc_admit.  Every complete
+ * page marked in `mask` becomes a ready optional page whose host backup is
+ * deferred: it joins the backup order and its host rows are not valid yet.
+ * Every other imported row (pages left out, the incomplete last page) can
+ * only be served from host memory, so it is copied to the host now.
+ */
+int orc_admit_device(orc_pool *p, int32_t r, int32_t s, const uint16_t *rows,
+                     int64_t N, const uint8_t *mask, int64_t *deficit) {
+  orc_source *src = get_src(p, r, s);
+  if (deficit) *deficit = 0;
+  if (!src || N < 0 || N > p->max_rows) return ORC_EINVAL;
+  if (src->admitted) return ORC_ESTATE;
+  size_t E = (size_t)p->E;
+  uint16_t *imported = NULL;
+  if (rows) {
+    imported = (uint16_t *)malloc((size_t)N * E * 2 + 2);
+    if (!imported) return ORC_ENOMEM;
+    memcpy(imported, rows, (size_t)N * E * 2);
+  }
+  int rc = orc_admit(p, r, s, rows, N, mask, deficit);
+  if (rc != ORC_OK) {
+    free(imported);
+    return rc;
+  }
+  src->imported = imported;
+  for (int64_t q = 0; q < N / p->PR; ++q) {
+    if (src->page_slot[q] < 0) continue;
+    src->backed[q] = 0;
+    src->pend[q] = ++p->bseq;
+    if (src->host)
+      for (size_t i = 0; i < (size_t)p->PR * E; ++i)
+        src->host[(size_t)q * p->PR * E + i] = ORC_POISON;
+  }
+  return ORC_OK;
+}
+
+/* Copy one pending page's rows from the device copy to the host copy. */
+static void backup_page(orc_source *src, const orc_pool *p, int64_t q) {
+  if (src->host && src->imported) {
+    size_t n = (size_t)p->PR * p->E;
+    memcpy(src->host + (size_t)q * n, src->imported + (size_t)q * n, n * 2);
+  }
+  src->backed[q] = 1;
+  src->pend[q] = 0;
+}
+
+/*
+ * Back up at most max_pages pending pages, in backup order (admission order,
+ * pages ascending); *done = pages backed up.
+ */
+int orc_backup(orc_pool *p, int64_t max_pages, int64_t *done) {
+  if (done) *done = 0;
+  if (!p || max_pages < 0) return ORC_EINVAL;
+  int64_t n = 0;
+  while (n < max_pages) {
+    orc_source *best = NULL;
+    int64_t best_q = -1;
+    for (int64_t i = 0; i < (int64_t)p->R * p->S; ++i) {
+      orc_source *src = &p->src[i];
+      for (int64_t q = 0; q < p->pages_max; ++q)
+        if (src->pend[q] && (!best || src->pend[q] < best->pend[best_q])) {
+          best = src;
+          best_q = q;
+        }
+    }
+    if (!best) break;
+    backup_page(best, p, best_q);
+    n++;
+  }
+  if (done) *done = n;
+  return ORC_OK;
+}
+
+int64_t orc_pending_backup(const orc_pool *p) {
+  int64_t n = 0;
+  for (int64_t i = 0; p && i < (int64_t)p->R * p->S; ++i)
+    for (int64_t q = 0; q < p->pages_max; ++q) n += p->src[i].pend[q] != 0;
+  return n;
+}
+
+/*
+ * Bounded round-robin refill ("Reclamation and refill": refill uses bounded
+ * round-robin).  Requests are visited cyclically from the cursor; a visit
+ * to a request with a complete imported page that is not optional-resident
+ * makes its lowest (source, page) such page resident again (lowest free
+ * slot; the bytes come from the host copy, which such a page always has).
+ * It stops after max_pages pages, when the capacity rule (used <= capacity
+ * - reserve) leaves no room, or when a whole round of visits found nothing.
+ * The cursor keeps the next request to visit.  *filled = pages refilled.
+ */
+int orc_refill(orc_pool *p, int64_t max_pages, int64_t *filled) {
+  if (filled) *filled = 0;
+  if (!p || max_pages < 0) return ORC_EINVAL;
+  int64_t n = 0, idle = 0;
+  int32_t r = p->rr;
+  while (n < max_pages && p->used < p->capacity - p->reserve && idle < p->R) {
+    int found = 0;
+    for (int32_t s = 0; s < p->S && !found; ++s) {
+      orc_source *src = &p->src[(int64_t)r * p->S + s];
+      if (!src->admitted) continue;
+      for (int64_t q = 0; q < src->N / p->PR && !found; ++q) {
+        if (src->page_slot[q] >= 0) continue;
+        int64_t slot = lowest_free_slot(p);
+        p->slot_pair[slot] = (int32_t)((int64_t)r * p->S + s);
+        p->slot_page[slot] = (int32_t)q;
+        p->used += 1;
+        src->page_slot[q] = (int32_t)slot;
+        found = 1;
+      }
+    }
+    if (found) { n++; idle = 0; } else { idle++; }
+    r = (r + 1) % p->R;
+  }
+  p->rr = r;
+  if (filled) *filled = n;
+  return ORC_OK;
+}
+
 static int64_t request_pages(const orc_pool *p, int32_t r) {
   int64_t n = 0;
   for (int32_t s = 0; s < p->S; ++s) {
@@ -243,6 +388,8 @@ int orc_reclaim(orc_pool *p, const int32_t *order, int32_t n, int64_t deficit,
       orc_source *src = &p->src[(int64_t)r * p->S + s];
       for (int64_t q = 0; q < p->pages_max; ++q) {
         if (src->page_slot[q] < 0) continue;
+        /* a page is freed only after its host backup is complete */
+        if (!src->backed[q]) backup_page(src, p, q);
         free_slot(p, src->page_slot[q]);
         src->page_slot[q] = -1;
         got += 1;
@@ -495,7 +642,7 @@ int orc_gather(const orc_pool *p, const uint32_t *loc, int64_t n,
       const orc_source *o = &p->src[p->slot_pair[slot]];
       if (!o->tracked) return ORC_EINVAL;
       int64_t row = (int64_t)p->slot_page[slot] * p->PR + idx % p->PR;
-      from = o->host + (size_t)row * E;
+      from = (o->imported ? o->imported : o->host) + (size_t)row * E;
     } else if (tier == ORC_TIER_HOT) {
       int64_t pair = idx / p->B;
       if (pair >= pairs || !p->src[pair].tracked) return ORC_EINVAL;
@@ -557,6 +704,15 @@ int orc_check(const orc_pool *p, int32_t r, int32_t s) {
     if ((q + 1) * p->PR > src->N) return 5;
     if (sl >= p->capacity || p->slot_pair[sl] != pair || p->slot_page[sl] != q)
       return 6;
+  }
+  /* every row is either ready on the GPU or has a host copy */
+  for (int64_t q = 0; q < p->pages_max; ++q) {
+    if (src->page_slot[q] < 0 && !src->backed[q]) return 7;
+    if (src->backed[q] && src->pend[q]) return 8;
+    if (src->backed[q] && src->host && src->imported && (q + 1) * p->PR <= src->N &&
+        memcmp(src->host + (size_t)q * p->PR * p->E, src->imported + (size_t)q * p->PR * p->E,
+               (size_t)p->PR * p->E * 2) != 0)
+      return 9;
   }
   return 0;
 }

@@ -1,7 +1,8 @@
 """Parser and runner for the hand-worked traces under tests/golden.
 
-A trace is a list of commands (pool, admit, reclaim, release, used, pages,
-append, resolve) each followed by the values worked out by hand.  The runner
+A trace is a list of commands (pool, admit, admitdev, backup, refill,
+pending, hostok, reclaim, release, used, pages, append, resolve) each
+followed by the values worked out by hand.  The runner
 drives any implementation through a small adapter (the oracle, or the CUDA
 library through its C ABI) and checks every expected value, plus byte truth:
 each gathered row of a successful resolve equals the generator's payload of
@@ -66,6 +67,30 @@ def run_trace(name: str, api, elems: int | None = None):
             assert deficit == int(tok[7]), f"{where}: deficit {deficit} != {tok[7]}"
             if rc == 0:
                 lengths[(r, s)] = N
+        elif op == "admitdev":
+            r, s, N = map(int, tok[1:4])
+            m = tok[4]
+            mask = None if m == "*" else np.array([int(c) for c in m], np.uint8)
+            rows = dhs_workload.payload_rows(PAYLOAD_TAG, s, r, 0, N, E)
+            rc, deficit = api.admit_device(r, s, N, mask, rows)
+            assert tok[5] == "->"
+            assert rc == _rc(tok[6]), f"{where}: rc {rc} != {tok[6]}"
+            assert deficit == int(tok[7]), f"{where}: deficit {deficit} != {tok[7]}"
+            if rc == 0:
+                lengths[(r, s)] = N
+        elif op in ("backup", "refill"):
+            rc, n = getattr(api, op)(int(tok[1]))
+            assert tok[2] == "->"
+            assert rc == _rc(tok[3]), f"{where}: rc {rc} != {tok[3]}"
+            assert n == int(tok[4]), f"{where}: {op} {n} != {tok[4]}"
+        elif op == "pending":
+            got = api.pending_backup()
+            assert got == int(tok[1]), f"{where}: pending {got} != {tok[1]}"
+        elif op == "hostok":
+            r, s, row0, n = map(int, tok[1:5])
+            got = api.host_rows(r, s, row0, n)
+            want = dhs_workload.payload_rows(PAYLOAD_TAG, s, r, row0, n, E)
+            assert np.array_equal(got, want), f"{where}: host rows differ from payload"
         elif op == "reclaim":
             order = [] if tok[1] == "-" else [int(x) for x in tok[1].split(",")]
             rc, freed = api.reclaim(order, int(tok[2]))
@@ -132,6 +157,21 @@ class OracleAdapter:
 
     def admit(self, r, s, N, mask, host):
         return self.p.admit(r, s, N, mask, host)
+
+    def admit_device(self, r, s, N, mask, rows):
+        return self.p.admit_device(r, s, N, mask, rows)
+
+    def backup(self, n):
+        return self.p.backup(n)
+
+    def refill(self, n):
+        return self.p.refill(n)
+
+    def pending_backup(self):
+        return self.p.pending_backup()
+
+    def host_rows(self, r, s, row0, n):
+        return self.p.rows(r, s, 0, row0, n)
 
     def reclaim(self, order, deficit):
         return self.p.reclaim(order, deficit)

@@ -28,7 +28,7 @@ from oracle import OraclePool, decode
 from oracle.run import OracleRun
 
 TRACES = ["resolve_micro_b2.txt", "resolve_micro_b3_pairs.txt",
-          "admission_micro.txt"]
+          "admission_micro.txt", "backup_refill_micro.txt"]
 
 
 @pytest.mark.parametrize("trace", TRACES)
