@@ -24,6 +24,7 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <set>
 #include <unordered_map>
 #include <vector>
 
@@ -126,6 +127,8 @@ struct PairState {
   uint8_t* host = nullptr;      // caller's pinned host rows
   uint8_t* host_dev = nullptr;  // device-visible address of the same rows
   std::vector<int32_t> pending;  // resident pages whose bytes are not yet copied
+  std::vector<uint64_t> backup;  // per page: backup order while the host copy is
+                                 // deferred, 0 = backed (empty: all backed)
 };
 
 }  // namespace
@@ -167,6 +170,9 @@ struct dhs_pool {
   bool fused_resolved = false;  // the current fused step launched one
   int fresh_list = -1;          // DHS_OPT_FRESH_LIST: -1 auto, 0 off, 1 on
   int64_t complete_pages = 0;   // complete imported pages of admitted pairs
+  uint64_t bseq = 0;            // pages put in backup order so far
+  std::set<std::pair<uint64_t, int64_t>> backup_order;  // (order, pair * pmax + page)
+  int32_t rr = 0;               // refill cursor: the next request visited
   int sm_count = 0;
   unsigned long long* trace = nullptr;  // DHS_OPT_TRACE buffer, null = off
   // reusable launch tables
@@ -254,17 +260,45 @@ int64_t lowest_free_slot(dhs_pool* p) {
 }
 
 // Free every optional page of pair; returns pages freed.
-int64_t drop_pages(dhs_pool* p, int64_t pair) {
+// Device-to-host copy of one resident page whose backup was deferred.
+int backup_page(dhs_pool* p, int64_t pair, int64_t q) {
+  PairState& s = p->ps[pair];
+  const dhs_pool_config& c = p->cfg;
+  const size_t page_bytes = (size_t)c.page_rows * c.row_bytes;
+  const int32_t slot = p->map_host[pair * p->pmax + q];
+  cudaError_t e = cudaMemcpyAsync(s.host + (size_t)q * page_bytes,
+                                  (const uint8_t*)c.opt_dev + (size_t)slot * page_bytes,
+                                  page_bytes, cudaMemcpyDeviceToHost, p->stream);
+  if (e != cudaSuccess) return DHS_ECUDA;
+  p->backup_order.erase({s.backup[q], pair * p->pmax + q});
+  s.backup[q] = 0;
+  return DHS_OK;
+}
+
+// Free every optional page of pair; returns pages freed, or a negative DHS
+// code.  backup: pages whose host backup is still deferred are backed up
+// first (reclaim); a released request's pages need none.
+int64_t drop_pages(dhs_pool* p, int64_t pair, bool backup) {
   int32_t* pm = p->map_host.data() + pair * p->pmax;
+  PairState& s = p->ps[pair];
   int64_t n = 0;
   for (int64_t q = 0; q < p->pmax; ++q) {
     if (pm[q] < 0) continue;
+    if (!s.backup.empty() && s.backup[q]) {
+      if (backup) {
+        const int rc = backup_page(p, pair, q);
+        if (rc) return rc;
+      } else {
+        p->backup_order.erase({s.backup[q], pair * p->pmax + q});
+        s.backup[q] = 0;
+      }
+    }
     free_slot(p, pm[q]);
     pm[q] = -1;
     ++n;
   }
   if (n) mark_dirty(p, pair);
-  p->ps[pair].pending.clear();
+  s.pending.clear();
   return n;
 }
 
@@ -515,6 +549,153 @@ int dhs_admit(dhs_pool* p, int32_t req, int32_t src, void* host_rows, int64_t n_
   return DHS_OK;
 }
 
+int dhs_admit_device(dhs_pool* p, int32_t req, int32_t src, const void* dev_rows,
+                     void* host_rows, int64_t n_rows, const uint8_t* mask,
+                     int64_t* deficit) {
+  if (deficit) *deficit = 0;
+  if (!p || req < 0 || req >= p->cfg.max_requests || src < 0 || src >= p->cfg.sources)
+    return DHS_EINVAL;
+  const dhs_pool_config& c = p->cfg;
+  if (n_rows < 0 || n_rows > c.max_rows_per_request || !host_rows) return DHS_EINVAL;
+  if (n_rows > 0 && !dev_rows) return DHS_EINVAL;
+  const int64_t pair = (int64_t)req * c.sources + src;
+  PairState& s = p->ps[pair];
+  if (s.admitted) return DHS_ESTATE;
+  int rc = enter(p);
+  if (rc) return rc;
+  void* hdev = nullptr;
+  if (cudaHostGetDevicePointer(&hdev, host_rows, 0) != cudaSuccess || !hdev) {
+    cudaGetLastError();
+    return DHS_EINVAL;
+  }
+  const int64_t complete = n_rows / c.page_rows;
+  int64_t want = 0;
+  for (int64_t q = 0; q < complete; ++q) want += (!mask || mask[q]) ? 1 : 0;
+  const int64_t usable = c.optional_pages - c.admission_reserve_pages;
+  if (p->used + want > usable) {
+    if (deficit) *deficit = p->used + want - usable;
+    return DHS_EWOULDWAIT;
+  }
+  // the copies are enqueued now; the page map reaches the device at the next
+  // flush, after them in stream order
+  const int64_t T = c.tail_rows, rb = c.row_bytes, PR = c.page_rows;
+  const size_t page_bytes = (size_t)PR * rb;
+  const uint8_t* dsrc = (const uint8_t*)dev_rows;
+  uint8_t* hdst = (uint8_t*)host_rows;
+  auto copy = [&](void* dst, const void* from, size_t bytes, cudaMemcpyKind kind) {
+    return cudaMemcpyAsync(dst, from, bytes, kind, p->stream) == cudaSuccess;
+  };
+  // tail ring <- rows [max(0, N-T), N)
+  for (int64_t row = std::max<int64_t>(0, n_rows - T); row < n_rows;) {
+    const int64_t slot = row % T;
+    const int64_t run = std::min(n_rows - row, T - slot);
+    if (!copy((uint8_t*)c.tail_dev + ((size_t)pair * T + slot) * rb, dsrc + (size_t)row * rb,
+              run * rb, cudaMemcpyDeviceToDevice))
+      return DHS_ECUDA;
+    row += run;
+  }
+  int32_t* pm = p->map_host.data() + pair * p->pmax;
+  s.backup.assign((size_t)p->pmax, 0);
+  for (int64_t q = 0; q < complete; ++q) {
+    if (mask && !mask[q]) continue;
+    const int64_t slot = lowest_free_slot(p);
+    p->slot_pair[slot] = (int32_t)pair;
+    p->slot_page[slot] = (int32_t)q;
+    p->used += 1;
+    pm[q] = (int32_t)slot;
+    s.backup[q] = ++p->bseq;
+    p->backup_order.insert({s.backup[q], pair * p->pmax + q});
+  }
+  // resident pages: device to device, runs of consecutive pages and slots;
+  // every other imported row: device to host now, runs of consecutive rows
+  for (int64_t q = 0; q < complete;) {
+    int64_t run = 1;
+    if (pm[q] >= 0) {
+      while (q + run < complete && pm[q + run] == pm[q] + run) ++run;
+      if (!copy((uint8_t*)c.opt_dev + (size_t)pm[q] * page_bytes, dsrc + q * page_bytes,
+                run * page_bytes, cudaMemcpyDeviceToDevice))
+        return DHS_ECUDA;
+    } else {
+      while (q + run < complete && pm[q + run] < 0) ++run;
+      if (!copy(hdst + q * page_bytes, dsrc + q * page_bytes, run * page_bytes,
+                cudaMemcpyDeviceToHost))
+        return DHS_ECUDA;
+    }
+    q += run;
+  }
+  if (n_rows > complete * PR &&
+      !copy(hdst + complete * page_bytes, dsrc + complete * page_bytes,
+            (size_t)(n_rows - complete * PR) * rb, cudaMemcpyDeviceToHost))
+    return DHS_ECUDA;
+  if (want) mark_dirty(p, pair);
+  s.admitted = true;
+  s.N = n_rows;
+  s.L = n_rows;
+  p->complete_pages += complete;
+  s.host = (uint8_t*)host_rows;
+  s.host_dev = (uint8_t*)hdev;
+  return DHS_OK;
+}
+
+int dhs_backup(dhs_pool* p, int64_t max_pages, int64_t* done) {
+  if (done) *done = 0;
+  if (!p || max_pages < 0) return DHS_EINVAL;
+  int rc = enter(p);
+  if (rc) return rc;
+  int64_t n = 0;
+  while (n < max_pages && !p->backup_order.empty()) {
+    const int64_t key = p->backup_order.begin()->second;
+    if ((rc = backup_page(p, key / p->pmax, key % p->pmax))) return rc;
+    ++n;
+  }
+  if (done) *done = n;
+  return DHS_OK;
+}
+
+int64_t dhs_pending_backup(const dhs_pool* p) {
+  return p ? (int64_t)p->backup_order.size() : -1;
+}
+
+int dhs_refill(dhs_pool* p, int64_t max_pages, int64_t* filled) {
+  if (filled) *filled = 0;
+  if (!p || max_pages < 0) return DHS_EINVAL;
+  const dhs_pool_config& c = p->cfg;
+  const int64_t usable = c.optional_pages - c.admission_reserve_pages;
+  int64_t n = 0, idle = 0;
+  int32_t r = p->rr;
+  while (n < max_pages && p->used < usable && idle < c.max_requests) {
+    bool found = false;
+    for (int32_t src = 0; src < c.sources && !found; ++src) {
+      const int64_t pair = (int64_t)r * c.sources + src;
+      PairState& s = p->ps[pair];
+      if (!s.admitted) continue;
+      int32_t* pm = p->map_host.data() + pair * p->pmax;
+      for (int64_t q = 0; q < s.N / c.page_rows && !found; ++q) {
+        if (pm[q] >= 0) continue;
+        const int64_t slot = lowest_free_slot(p);
+        p->slot_pair[slot] = (int32_t)pair;
+        p->slot_page[slot] = (int32_t)q;
+        p->used += 1;
+        pm[q] = (int32_t)slot;
+        s.pending.push_back((int32_t)q);  // copied from the host copy at flush
+        p->any_pending = true;
+        mark_dirty(p, pair);
+        found = true;
+      }
+    }
+    if (found) {
+      ++n;
+      idle = 0;
+    } else {
+      ++idle;
+    }
+    r = (r + 1) % c.max_requests;
+  }
+  p->rr = r;
+  if (filled) *filled = n;
+  return DHS_OK;
+}
+
 int dhs_reclaim(dhs_pool* p, const int32_t* order, int32_t n, int64_t deficit,
                 int64_t* freed) {
   if (freed) *freed = 0;
@@ -529,10 +710,15 @@ int dhs_reclaim(dhs_pool* p, const int32_t* order, int32_t n, int64_t deficit,
     avail += request_pages(p, order[i]);
   }
   if (avail < deficit) return DHS_EWOULDWAIT;
+  int rc = enter(p);
+  if (rc) return rc;
   int64_t got = 0;
   for (int32_t i = 0; i < n && got < deficit; ++i)
-    for (int32_t s = 0; s < p->cfg.sources; ++s)
-      got += drop_pages(p, (int64_t)order[i] * p->cfg.sources + s);
+    for (int32_t s = 0; s < p->cfg.sources; ++s) {
+      const int64_t k = drop_pages(p, (int64_t)order[i] * p->cfg.sources + s, true);
+      if (k < 0) return (int)k;
+      got += k;
+    }
   if (freed) *freed = got;
   return DHS_OK;
 }
@@ -544,7 +730,7 @@ int dhs_release(dhs_pool* p, int32_t req) {
   const int64_t B = p->cfg.hot_rows;
   for (int32_t s = 0; s < p->cfg.sources; ++s) {
     const int64_t pair = (int64_t)req * p->cfg.sources + s;
-    drop_pages(p, pair);
+    drop_pages(p, pair, false);
     if (p->ps[pair].admitted) p->complete_pages -= p->ps[pair].N >> p->page_shift;
     p->ps[pair] = PairState();
   }

@@ -88,6 +88,10 @@ def _load():
         "dhs_admit": (ctypes.c_int, [_vp, _i32, _i32, _vp, _i64, _vp, P(_i64)]),
         "dhs_reclaim": (ctypes.c_int, [_vp, _vp, _i32, _i64, P(_i64)]),
         "dhs_release": (ctypes.c_int, [_vp, _i32]),
+        "dhs_admit_device": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _i64, _vp, P(_i64)]),
+        "dhs_backup": (ctypes.c_int, [_vp, _i64, P(_i64)]),
+        "dhs_pending_backup": (_i64, [_vp]),
+        "dhs_refill": (ctypes.c_int, [_vp, _i64, P(_i64)]),
         "dhs_pool_used": (_i64, [_vp]),
         "dhs_flush": (ctypes.c_int, [_vp]),
         "dhs_append": (ctypes.c_int, [_vp, P(dhs_append_item), _i32]),
@@ -161,6 +165,28 @@ def dhs_reclaim(h, order, deficit):
 
 def dhs_release(h, req):
     return lib.dhs_release(h, req)
+
+
+def dhs_admit_device(h, req, src, dev_ptr, host_ptr, n_rows, mask=None):
+    d = _i64(0)
+    m = None
+    if mask is not None:
+        mask = np.ascontiguousarray(mask, np.uint8)
+        m = mask.ctypes.data
+    rc = lib.dhs_admit_device(h, req, src, dev_ptr, host_ptr, n_rows, m, ctypes.byref(d))
+    return rc, d.value
+
+
+def dhs_backup(h, max_pages):
+    n = _i64(0)
+    rc = lib.dhs_backup(h, max_pages, ctypes.byref(n))
+    return rc, n.value
+
+
+def dhs_refill(h, max_pages):
+    n = _i64(0)
+    rc = lib.dhs_refill(h, max_pages, ctypes.byref(n))
+    return rc, n.value
 
 
 def dhs_pool_used(h):
@@ -335,6 +361,18 @@ class Pool:
 
     def release(self, req):
         return dhs_release(self.h, req)
+
+    def admit_device(self, req, src, dev_ptr, host_ptr, n_rows, mask=None):
+        return dhs_admit_device(self.h, req, src, dev_ptr, host_ptr, n_rows, mask)
+
+    def backup(self, max_pages):
+        return dhs_backup(self.h, max_pages)
+
+    def refill(self, max_pages):
+        return dhs_refill(self.h, max_pages)
+
+    def pending_backup(self):
+        return int(lib.dhs_pending_backup(self.h))
 
     def used(self):
         return dhs_pool_used(self.h)

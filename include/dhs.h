@@ -179,6 +179,54 @@ int dhs_reclaim(dhs_pool *pool, const int32_t *order, int32_t n,
  * caches, forget its host rows.  Errors: DHS_EINVAL, DHS_ECUDA. */
 int dhs_release(dhs_pool *pool, int32_t req);
 
+/*
+ * Resident-first admission of rows that are on the device ("Resident-first
+ * admission": a new request keeps its imported history on device and defers
+ * host backup while HBM is spare).  dev_rows: device memory, rows
+ * [0, n_rows) of row_bytes each (e.g. the prefill's output), read only by
+ * copies this call enqueues on the pool's stream (reuse it after the stream
+ * has passed them).  host_rows: as for dhs_admit, but its imported rows need
+ * not be written yet.  Pages are chosen and the capacity rule applied as in
+ * dhs_admit.  This call enqueues: the tail ring fill and the resident pages'
+ * copies from dev_rows (device to device), and the copy to host_rows of
+ * every other imported row -- pages left out and the incomplete last page,
+ * which only the host can serve (device to host).  The resident pages' own
+ * host backup is deferred: they enter the backup order (admission order,
+ * pages ascending), see dhs_backup; until then their host rows are not
+ * valid.  Errors: as dhs_admit.
+ */
+int dhs_admit_device(dhs_pool *pool, int32_t req, int32_t src, const void *dev_rows,
+                     void *host_rows, int64_t n_rows, const uint8_t *resident_page_mask,
+                     int64_t *deficit_pages);
+
+/*
+ * Deferred host backup: enqueue the device-to-host copies of at most
+ * max_pages pages in backup order; *done = pages backed up.  dhs_reclaim
+ * backs up a reclaimed page that is still pending before freeing its slot
+ * ("pages are freed only after host backup completes and earlier readers
+ * finish"): the copy is ordered on the pool's stream after every earlier
+ * reader and before any later copy into the slot.  Released requests' pages
+ * need no backup.  Errors: DHS_EINVAL, DHS_ECUDA.
+ */
+int dhs_backup(dhs_pool *pool, int64_t max_pages, int64_t *done);
+
+/* Pages whose host backup is still deferred. */
+int64_t dhs_pending_backup(const dhs_pool *pool);
+
+/*
+ * Bounded round-robin refill ("Reclamation and refill": refill uses bounded
+ * round-robin).  Requests are visited cyclically from a cursor that starts
+ * at request 0; a visit to a request with a complete imported page that is
+ * not optional-resident makes its lowest (source, page) such page resident
+ * again in the lowest free slot, its bytes copied from the host copy (which
+ * every non-resident page has) before the next device call observes it.
+ * Stops after max_pages pages, when used reaches optional_pages -
+ * admission_reserve_pages, or when a whole round of visits found nothing;
+ * the cursor keeps the next request to visit.  *filled = pages refilled.
+ * Errors: DHS_EINVAL.
+ */
+int dhs_refill(dhs_pool *pool, int64_t max_pages, int64_t *filled);
+
 /* Optional pages in use (host metadata). */
 int64_t dhs_pool_used(const dhs_pool *pool);
 

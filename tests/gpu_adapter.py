@@ -34,8 +34,38 @@ class GpuAdapter:
             self.lengths[(r, s)] = N
         return dhs.RC_NAMES[rc], d
 
+    def admit_device(self, r, s, N, mask, rows):
+        off = self._host_off(r, s)
+        # the host copy starts empty: only this call's copies and later
+        # backups may fill it
+        self.host.array[off: off + self.max_rows * self.rb] = 0
+        dev = torch.from_numpy(np.ascontiguousarray(rows).view(np.int16).copy()).cuda()
+        rc, d = self.pool.admit_device(r, s, dev.data_ptr(), self.host.ptr + off, N, mask)
+        torch.cuda.synchronize()  # dev is read by the copies just enqueued
+        if rc == 0:
+            self.lengths[(r, s)] = N
+        return dhs.RC_NAMES[rc], d
+
+    def backup(self, n):
+        rc, k = self.pool.backup(n)
+        torch.cuda.synchronize()
+        return dhs.RC_NAMES[rc], k
+
+    def refill(self, n):
+        rc, k = self.pool.refill(n)
+        return dhs.RC_NAMES[rc], k
+
+    def pending_backup(self):
+        return self.pool.pending_backup()
+
+    def host_rows(self, r, s, row0, n):
+        torch.cuda.synchronize()
+        off = self._host_off(r, s) + row0 * self.rb
+        return self.host.array[off: off + n * self.rb].view(np.uint16).reshape(n, self.E).copy()
+
     def reclaim(self, order, deficit):
         rc, f = self.pool.reclaim(order, deficit)
+        torch.cuda.synchronize()
         return dhs.RC_NAMES[rc], f
 
     def release(self, r):

@@ -119,10 +119,21 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
 # ------------------------------------------------------------ golden traces
 
 @pytest.mark.parametrize("trace", ["resolve_micro_b2.txt", "resolve_micro_b3_pairs.txt",
-                                   "admission_micro.txt"])
+                                   "admission_micro.txt", "backup_refill_micro.txt"])
 def test_golden_trace_gpu(trace):
     from gpu_adapter import GpuAdapter
     run_trace(trace, GpuAdapter(), elems=8)  # 16-byte rows
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_admission_sequences_match_oracle(seed):
+    """Device admission, deferred backup, reclaim, release, refill, appends
+    and resolves in random order: the library and the oracle agree on every
+    result, page map and host row, and every gathered row is its payload."""
+    from admission_seq import run_sequence
+    from fixture_runner import OracleAdapter
+    from gpu_adapter import GpuAdapter
+    run_sequence([OracleAdapter(), GpuAdapter()], seed, reserve=seed % 3)
 
 
 # ------------------------------------------------------------ small, every output

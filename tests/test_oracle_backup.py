@@ -158,3 +158,12 @@ def test_round_robin_closed_form(oracle_lib, k):
     for i, r in enumerate(order):
         want[r] = k // R + (1 if i < k % R else 0)
     assert np.array_equal(got, want), (got, want)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_lockstep_driver_on_the_oracle(oracle_lib, gen_lib, seed):
+    """The lockstep driver the GPU parity test uses, run on the oracle alone
+    (its own checks: bookkeeping, host rows, payload bytes)."""
+    from admission_seq import run_sequence
+    from fixture_runner import OracleAdapter
+    run_sequence([OracleAdapter()], seed, reserve=seed % 3)
