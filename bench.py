@@ -80,6 +80,8 @@ def parse():
     ap.add_argument("--no-hugepages", action="store_true")
     ap.add_argument("--union", action="store_true",
                     help="union verification staging (DHS_ITEM_UNION)")
+    ap.add_argument("--experiment", default=None, choices=["loadstep"],
+                    help="run an experiment instead of the benchmark (one JSON line)")
     return ap.parse_args()
 
 
@@ -385,8 +387,51 @@ def measure_e2e(run, cycle, steps, dev, stream):
             "steps": steps, "seconds": dt}
 
 
+def run_loadstep(args):
+    """The load-step on/off experiment through the C ABI: host-fetched
+    fraction of unique selected rows per phase with optional residency on
+    and off, decode-step device time per phase, and the admission
+    machinery's copy rates (device admission, deferred backup, refill)."""
+    import torch
+    from dhs_workload.loadstep import LOADSTEP, phase_fractions, run
+    from hierarchical_sparse_kv_dhs_gb300.runner import LoadStepGpu
+    cfg = LOADSTEP
+    out = {"experiment": "loadstep", "data": "synthetic",
+           "config": {"slots": cfg.slots, "low_load_requests": cfg.low,
+                      "sources": cfg.sources, "history_rows": cfg.history,
+                      "topk": cfg.topk, "hot_rows": cfg.hot, "tail_rows": cfg.tail,
+                      "optional_pages": cfg.capacity,
+                      "steps": [cfg.steps_low, cfg.steps_burst, cfg.steps_drain],
+                      "refill_pages_per_step": cfg.refill_per_step,
+                      "backup_pages_per_step": cfg.backup_per_step}}
+    for mode in ("on", "off"):
+        g = LoadStepGpu(cfg.topk)
+        recs = run(g, cfg, residency=(mode == "on"))
+        fr = phase_fractions(recs)
+        step_us = {}
+        for ph in ("low", "burst", "drain"):
+            ts = [t for t, x in zip(g.times["step"], recs) if x["phase"] == ph]
+            step_us[ph] = statistics.median(ts) * 1e6 if ts else None
+        rates = {k: (g.bytes[k] / sum(g.times[k]) / 1e9) if g.times[k] else None
+                 for k in ("admit", "backup", "refill")}
+        out[mode] = {"host_fraction": fr, "step_us_median": step_us,
+                     "copy_gbs": rates,
+                     "pages_moved": {k: g.bytes[k] // (cfg.page_rows * cfg.row_elems * 2)
+                                     for k in ("backup", "refill")},
+                     "resident_pages_end_of_phase": {
+                         ph: [x for x in recs if x["phase"] == ph][-1]["resident_pages"]
+                         for ph in ("low", "burst", "drain")}}
+        g.close()
+        del g
+        torch.cuda.empty_cache()
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
+    if args.experiment == "loadstep":
+        run_loadstep(args)
+        return
     from dhs_workload.configs import CONFIGS
     cfg = CONFIGS[args.config]
     if args.impl == "reference":

@@ -112,6 +112,19 @@ cudaError_t resolve_set_smem_limit(size_t bytes);
 cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,
                            int n_items, size_t smem, cudaStream_t stream);
 
+// ------------------------------------------------------------ page moves
+// Whole optional pages between the optional arena and the pinned host copy
+// (refill and admission host -> device, deferred backup device -> host), as
+// one launch over a list of pages instead of one copy call per page.
+struct PageMove {
+  const uint8_t* src;  // device-visible addresses (mapped host or device)
+  uint8_t* dst;
+};
+constexpr int kPageMovesMax = 1024;  // per launch (kernel parameter space)
+constexpr int kPageMoveThreads = 512;
+cudaError_t launch_page_moves(const PageMove* moves, int n, int page_bytes, int ctas,
+                              cudaStream_t stream);
+
 // ------------------------------------------------------------ host copy (d)
 constexpr int kCopyThreads = 512;
 constexpr int kCopyItemsMax = 256;

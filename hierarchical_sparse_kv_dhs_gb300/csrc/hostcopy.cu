@@ -8,6 +8,8 @@
 // can be overridden for sweeps.  Each warp keeps up to four 1152-byte rows
 // in flight (12 x 16-byte loads per lane) so the link sees enough
 // outstanding requests to cover its latency.
+#include <algorithm>
+
 #include "dhs_internal.h"
 
 namespace dhs {
@@ -152,7 +154,63 @@ cudaError_t launch_t(const CopyCommon& c, const CopyItem* items, int n, int ctas
   return cudaLaunchKernelEx(&cfg, hostcopy_kernel<MAXI, false>, P);
 }
 
+// ---------------------------------------------------------------- page moves
+
+struct PageMoveParams {
+  int32_t n;
+  int32_t page_bytes;
+  PageMove m[kPageMovesMax];
+};
+
+// Grid-stride over the 16-byte chunks of every listed page; each thread
+// keeps four chunks in flight so the link sees enough outstanding requests
+// (one side of every move is mapped host memory).
+__global__ void __launch_bounds__(kPageMoveThreads)
+    page_move_kernel(const __grid_constant__ PageMoveParams P) {
+  const uint32_t cpp = (uint32_t)P.page_bytes >> 4;  // chunks per page
+  const uint32_t total = (uint32_t)P.n * cpp;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  constexpr int kIn = 4;
+  for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < total;
+       base += stride * kIn) {
+    uint4 v[kIn];
+#pragma unroll
+    for (int u = 0; u < kIn; ++u) {
+      const uint32_t ch = base + u * stride;
+      if (ch < total) {
+        const uint32_t pg = ch / cpp, c = ch - pg * cpp;
+        v[u] = __ldcs(reinterpret_cast<const uint4*>(P.m[pg].src) + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kIn; ++u) {
+      const uint32_t ch = base + u * stride;
+      if (ch < total) {
+        const uint32_t pg = ch / cpp, c = ch - pg * cpp;
+        __stcs(reinterpret_cast<uint4*>(P.m[pg].dst) + c, v[u]);
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_page_moves(const PageMove* moves, int n, int page_bytes, int ctas,
+                              cudaStream_t stream) {
+  for (int b = 0; b < n; b += kPageMovesMax) {
+    PageMoveParams P;
+    P.n = std::min(kPageMovesMax, n - b);
+    P.page_bytes = page_bytes;
+    for (int i = 0; i < P.n; ++i) P.m[i] = moves[b + i];
+    const int64_t chunks = (int64_t)P.n * (page_bytes >> 4);
+    const int64_t need = (chunks + kPageMoveThreads - 1) / kPageMoveThreads;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, need));
+    page_move_kernel<<<grid, kPageMoveThreads, 0, stream>>>(P);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 cudaError_t hostcopy_set_carveout() {
   cudaError_t e = cudaFuncSetAttribute(hostcopy_kernel<kCopyItemsMax, true>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);

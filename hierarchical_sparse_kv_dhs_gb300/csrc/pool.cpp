@@ -184,11 +184,17 @@ struct dhs_pool {
   std::vector<int32_t> app_of_pair;  // decode step: append item of each pair, -1 = none
   std::vector<int64_t> l0_of_pair;   // length of each resolved pair before this step's append
   std::vector<uint32_t> seq_of_pair; // resolve launch that last resolved each pair
+  std::vector<dhs::PageMove> moves;  // page list of the next page-move launch
 };
 
 namespace {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? DHS_OK : DHS_ECUDA; }
+
+// Pages small enough for the page-move kernel's 32-bit chunk arithmetic.
+bool small_pages(const dhs_pool* p) {
+  return (int64_t)p->cfg.page_rows * p->cfg.row_bytes <= ((int64_t)1 << 24);
+}
 
 int enter(dhs_pool* p) {
   int cur = -1;
@@ -208,28 +214,39 @@ int flush(dhs_pool* p) {
   const dhs_pool_config& c = p->cfg;
   const size_t page_bytes = (size_t)c.page_rows * c.row_bytes;
   if (p->any_pending) {
+    p->moves.clear();
     for (int64_t pair = 0; pair < p->pairs; ++pair) {
       PairState& s = p->ps[pair];
       if (s.pending.empty()) continue;
       std::sort(s.pending.begin(), s.pending.end());
       const int32_t* pm = p->map_host.data() + pair * p->pmax;
-      size_t i = 0;
-      while (i < s.pending.size()) {
-        const int32_t page = s.pending[i];
-        const int32_t slot = pm[page];
-        size_t run = 1;
-        while (i + run < s.pending.size() && s.pending[i + run] == page + (int32_t)run &&
-               pm[page + run] == slot + (int32_t)run)
-          ++run;
-        cudaError_t e = cudaMemcpyAsync((uint8_t*)c.opt_dev + (size_t)slot * page_bytes,
-                                        s.host + (size_t)page * page_bytes, run * page_bytes,
-                                        cudaMemcpyHostToDevice, p->stream);
-        if (e != cudaSuccess) return DHS_ECUDA;
-        i += run;
+      if (!small_pages(p)) {  // pages too large for the page kernel: copy runs
+        size_t i = 0;
+        while (i < s.pending.size()) {
+          const int32_t page = s.pending[i];
+          const int32_t slot = pm[page];
+          size_t run = 1;
+          while (i + run < s.pending.size() && s.pending[i + run] == page + (int32_t)run &&
+                 pm[page + run] == slot + (int32_t)run)
+            ++run;
+          cudaError_t e = cudaMemcpyAsync((uint8_t*)c.opt_dev + (size_t)slot * page_bytes,
+                                          s.host + (size_t)page * page_bytes, run * page_bytes,
+                                          cudaMemcpyHostToDevice, p->stream);
+          if (e != cudaSuccess) return DHS_ECUDA;
+          i += run;
+        }
+      } else {
+        for (int32_t page : s.pending)
+          p->moves.push_back({s.host_dev + (size_t)page * page_bytes,
+                              (uint8_t*)c.opt_dev + (size_t)pm[page] * page_bytes});
       }
       s.pending.clear();
     }
     p->any_pending = false;
+    if (!p->moves.empty() &&
+        dhs::launch_page_moves(p->moves.data(), (int)p->moves.size(), (int)page_bytes,
+                               2 * std::max(1, p->sm_count), p->stream) != cudaSuccess)
+      return DHS_ECUDA;
   }
   if (p->dirty_hi >= 0) {
     const size_t off = (size_t)p->dirty_lo * p->pmax;
@@ -260,19 +277,34 @@ int64_t lowest_free_slot(dhs_pool* p) {
 }
 
 // Free every optional page of pair; returns pages freed.
-// Device-to-host copy of one resident page whose backup was deferred.
+// Queue the device-to-host copy of one resident page whose backup was
+// deferred (p->moves; launched by run_moves) and mark it backed.
 int backup_page(dhs_pool* p, int64_t pair, int64_t q) {
   PairState& s = p->ps[pair];
   const dhs_pool_config& c = p->cfg;
   const size_t page_bytes = (size_t)c.page_rows * c.row_bytes;
   const int32_t slot = p->map_host[pair * p->pmax + q];
-  cudaError_t e = cudaMemcpyAsync(s.host + (size_t)q * page_bytes,
-                                  (const uint8_t*)c.opt_dev + (size_t)slot * page_bytes,
-                                  page_bytes, cudaMemcpyDeviceToHost, p->stream);
-  if (e != cudaSuccess) return DHS_ECUDA;
+  const uint8_t* from = (const uint8_t*)c.opt_dev + (size_t)slot * page_bytes;
+  if (small_pages(p)) {
+    p->moves.push_back({from, s.host_dev + (size_t)q * page_bytes});
+  } else if (cudaMemcpyAsync(s.host + (size_t)q * page_bytes, from, page_bytes,
+                             cudaMemcpyDeviceToHost, p->stream) != cudaSuccess) {
+    return DHS_ECUDA;
+  }
   p->backup_order.erase({s.backup[q], pair * p->pmax + q});
   s.backup[q] = 0;
   return DHS_OK;
+}
+
+// Launch the queued page moves (in stream order, before anything enqueued
+// after this call -- in particular before a freed slot is written again).
+int run_moves(dhs_pool* p) {
+  if (p->moves.empty()) return DHS_OK;
+  const int pb = (int)((int64_t)p->cfg.page_rows * p->cfg.row_bytes);
+  cudaError_t e = dhs::launch_page_moves(p->moves.data(), (int)p->moves.size(), pb,
+                                         2 * std::max(1, p->sm_count), p->stream);
+  p->moves.clear();
+  return e == cudaSuccess ? DHS_OK : DHS_ECUDA;
 }
 
 // Free every optional page of pair; returns pages freed, or a negative DHS
@@ -495,13 +527,15 @@ int dhs_admit(dhs_pool* p, int32_t req, int32_t src, void* host_rows, int64_t n_
     return DHS_EINVAL;
   const dhs_pool_config& c = p->cfg;
   if (n_rows < 0 || n_rows > c.max_rows_per_request || !host_rows) return DHS_EINVAL;
+  if ((uintptr_t)host_rows % 16) return DHS_EINVAL;  // rows move in 16-byte chunks
   const int64_t pair = (int64_t)req * c.sources + src;
   PairState& s = p->ps[pair];
   if (s.admitted) return DHS_ESTATE;
   int rc = enter(p);
   if (rc) return rc;
   void* hdev = nullptr;
-  if (cudaHostGetDevicePointer(&hdev, host_rows, 0) != cudaSuccess || !hdev) {
+  if (cudaHostGetDevicePointer(&hdev, host_rows, 0) != cudaSuccess || !hdev ||
+      (uintptr_t)hdev % 16) {
     cudaGetLastError();  // clear the sticky-free error state
     return DHS_EINVAL;
   }
@@ -558,13 +592,15 @@ int dhs_admit_device(dhs_pool* p, int32_t req, int32_t src, const void* dev_rows
   const dhs_pool_config& c = p->cfg;
   if (n_rows < 0 || n_rows > c.max_rows_per_request || !host_rows) return DHS_EINVAL;
   if (n_rows > 0 && !dev_rows) return DHS_EINVAL;
+  if ((uintptr_t)host_rows % 16) return DHS_EINVAL;
   const int64_t pair = (int64_t)req * c.sources + src;
   PairState& s = p->ps[pair];
   if (s.admitted) return DHS_ESTATE;
   int rc = enter(p);
   if (rc) return rc;
   void* hdev = nullptr;
-  if (cudaHostGetDevicePointer(&hdev, host_rows, 0) != cudaSuccess || !hdev) {
+  if (cudaHostGetDevicePointer(&hdev, host_rows, 0) != cudaSuccess || !hdev ||
+      (uintptr_t)hdev % 16) {
     cudaGetLastError();
     return DHS_EINVAL;
   }
@@ -642,12 +678,14 @@ int dhs_backup(dhs_pool* p, int64_t max_pages, int64_t* done) {
   if (!p || max_pages < 0) return DHS_EINVAL;
   int rc = enter(p);
   if (rc) return rc;
+  p->moves.clear();
   int64_t n = 0;
   while (n < max_pages && !p->backup_order.empty()) {
     const int64_t key = p->backup_order.begin()->second;
     if ((rc = backup_page(p, key / p->pmax, key % p->pmax))) return rc;
     ++n;
   }
+  if ((rc = run_moves(p))) return rc;
   if (done) *done = n;
   return DHS_OK;
 }
@@ -712,6 +750,7 @@ int dhs_reclaim(dhs_pool* p, const int32_t* order, int32_t n, int64_t deficit,
   if (avail < deficit) return DHS_EWOULDWAIT;
   int rc = enter(p);
   if (rc) return rc;
+  p->moves.clear();
   int64_t got = 0;
   for (int32_t i = 0; i < n && got < deficit; ++i)
     for (int32_t s = 0; s < p->cfg.sources; ++s) {
@@ -719,6 +758,7 @@ int dhs_reclaim(dhs_pool* p, const int32_t* order, int32_t n, int64_t deficit,
       if (k < 0) return (int)k;
       got += k;
     }
+  if ((rc = run_moves(p))) return rc;  // backups before any reuse of the slots
   if (freed) *freed = got;
   return DHS_OK;
 }

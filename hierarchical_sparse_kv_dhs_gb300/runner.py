@@ -192,3 +192,119 @@ class GpuRun:
     def close(self):
         self.pool.close()
         self.host.close()
+
+
+class LoadStepGpu:
+    """The load-step schedule (dhs_workload.loadstep.run) over the C ABI with
+    every step as one batched dhs_decode_step, timed with CUDA events on the
+    pool's stream: decode steps, device admissions, deferred backups and
+    refills (whose host-to-device copies are enqueued by the dhs_flush the
+    refill is followed by)."""
+
+    def __init__(self, max_topk: int, device="cuda"):
+        self.k = max_topk
+        self.device = torch.device(device)
+        if self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        torch.cuda.set_device(self.device)
+        self.times = {"step": [], "admit": [], "backup": [], "refill": []}
+        self.bytes = {"admit": 0, "backup": 0, "refill": 0}
+
+    def _timed(self, kind, fn, nbytes=0):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        out = fn()
+        e1.record()
+        e1.synchronize()
+        self.times[kind].append(e0.elapsed_time(e1) / 1e3)
+        if kind in self.bytes:
+            self.bytes[kind] += nbytes
+        return out
+
+    def new_pool(self, R, S, T, B, E, PR, max_rows, cap, reserve):
+        self.R, self.S, self.E, self.PR = R, S, E, PR
+        self.rb = E * 2
+        self.max_rows = max_rows
+        self.pool = dhs.Pool(max_requests=R, sources=S, row_bytes=self.rb, page_rows=PR,
+                             tail_rows=T, hot_rows=B, max_queries=1, max_topk=self.k,
+                             max_rows_per_request=max_rows, optional_pages=cap,
+                             admission_reserve_pages=reserve, device=self.device)
+        self.host = dhs.HostRows(R * S * max_rows * self.rb, hugepages=False)
+        dev = self.device
+        self.sel = torch.zeros((R * S, self.k), dtype=torch.int32, device=dev)
+        self.loc = torch.zeros((R * S, self.k), dtype=torch.int32, device=dev)
+        self.cnt = torch.zeros((R * S, 8), dtype=torch.int32, device=dev)
+        self.stg = torch.empty((R * S, self.k, E), dtype=torch.int16, device=dev)
+        self.app = torch.zeros((R * S, E), dtype=torch.int16, device=dev)
+
+    def _host_ptr(self, r, s):
+        return self.host.ptr + (r * self.S + s) * self.max_rows * self.rb
+
+    def admit_device(self, r, s, N, mask, rows):
+        dev = torch.from_numpy(np.ascontiguousarray(rows).view(np.int16)).to(self.device)
+        torch.cuda.synchronize(self.device)
+        rc, d = self._timed("admit", lambda: self.pool.admit_device(
+            r, s, dev.data_ptr(), self._host_ptr(r, s), N, mask), N * self.rb)
+        return dhs.RC_NAMES[rc], d
+
+    def release(self, r):
+        return dhs.RC_NAMES[self.pool.release(r)]
+
+    def reclaim(self, order, deficit):
+        rc, f = self.pool.reclaim(order, deficit)
+        return dhs.RC_NAMES[rc], f
+
+    def refill(self, n):
+        rc, k = self.pool.refill(n)
+        if k:
+            self._timed("refill", lambda: dhs.check(self.pool.flush(), "dhs_flush"),
+                        k * self.PR * self.rb)
+        return dhs.RC_NAMES[rc], k
+
+    def backup(self, n):
+        rc, k = self._timed("backup", lambda: self.pool.backup(n))
+        if k:
+            self.bytes["backup"] += k * self.PR * self.rb
+        else:
+            self.times["backup"].pop()
+        return dhs.RC_NAMES[rc], k
+
+    def used(self):
+        return self.pool.used()
+
+    def pending_backup(self):
+        return self.pool.pending_backup()
+
+    def decode_step(self, step, work):
+        apps, items = [], []
+        for i, (r, s, row, sel) in enumerate(work):
+            p = r * self.S + s
+            self.app[p].copy_(torch.from_numpy(np.ascontiguousarray(row[0]).view(np.int16)))
+            self.sel[p].copy_(torch.from_numpy(np.ascontiguousarray(sel, np.int32)))
+            a = dhs.dhs_append_item()
+            a.req, a.src, a.count, a.rows_dev = r, s, 1, self.app[p].data_ptr()
+            apps.append(a)
+            it = dhs.dhs_item()
+            it.req, it.src, it.queries, it.topk = r, s, 1, len(sel)
+            it.sel_dev, it.loc_dev = self.sel[p].data_ptr(), self.loc[p].data_ptr()
+            it.counters_dev, it.staging_dev = self.cnt[p].data_ptr(), self.stg[p].data_ptr()
+            items.append(it)
+        arr = (dhs.dhs_append_item * len(apps))(*apps)
+        st, keep = dhs.make_step(step, items)
+        torch.cuda.synchronize(self.device)
+        self._timed("step", lambda: dhs.check(
+            dhs.lib.dhs_decode_step(self.pool.h, arr, len(apps), ctypes.byref(st)),
+            "dhs_decode_step"))
+        rc, flags = self.pool.status()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} flags {flags}")
+        cnt = self.cnt.cpu().numpy().view(np.uint32)
+        loc = self.loc.cpu().numpy().view(np.uint32)
+        return [(0, loc[r * self.S + s, : len(sel)], cnt[r * self.S + s])
+                for (r, s, _, sel) in work]
+
+    def close(self):
+        torch.cuda.synchronize(self.device)
+        self.pool.close()
+        self.host.close()

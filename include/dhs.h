@@ -144,7 +144,8 @@ void dhs_pool_destroy(dhs_pool *pool);
 /*
  * Admit (req, src) with n_rows imported rows ("Resident-first admission").
  * host_rows: caller-owned pinned + mapped host memory (cudaHostAlloc or
- * cudaHostRegister with the mapped flag) holding rows [0, n_rows) and room
+ * cudaHostRegister with the mapped flag), 16-byte aligned, holding rows
+ * [0, n_rows) and room
  * for max_rows_per_request rows (appended rows are written through to it);
  * it must outlive the admission.  resident_page_mask: one byte per complete
  * page (n_rows / page_rows of them), nonzero = keep on device; NULL = all

@@ -136,6 +136,39 @@ def test_admission_sequences_match_oracle(seed):
     run_sequence([OracleAdapter(), GpuAdapter()], seed, reserve=seed % 3)
 
 
+@pytest.mark.parametrize("residency", [True, False])
+def test_loadstep_matches_oracle(residency):
+    """The load-step schedule (admission pressure rising and draining, with
+    reclaim, deferred backup and refill) through the library and the
+    oracle: every step's results, locations and counters agree, and every
+    gathered row on the GPU is its payload."""
+    from dhs_workload.loadstep import LOADSTEP_SMALL, LoadStepInputs, run
+    from fixture_runner import OracleAdapter
+    from gpu_adapter import GpuAdapter
+    cfg = LOADSTEP_SMALL
+    got, want = {}, {}
+
+    def keep(into):
+        return lambda step, res: into.__setitem__(step, res)
+
+    gpu = GpuAdapter(max_queries=1, max_topk=cfg.topk)
+    rec_g = run(gpu, cfg, residency, LoadStepInputs(cfg), keep(got))
+    rec_o = run(OracleAdapter(), cfg, residency, LoadStepInputs(cfg), keep(want))
+    assert rec_g == rec_o
+    inputs = LoadStepInputs(cfg)
+    for step in want:
+        for (r, s, rc, loc, cnt, sel), (r2, s2, rc2, loc2, cnt2, _) in zip(want[step], got[step]):
+            assert (r, s, rc) == (r2, s2, rc2)
+            assert np.array_equal(np.asarray(loc).ravel(), np.asarray(loc2).ravel()), (step, r, s)
+            assert np.array_equal(np.asarray(cnt), np.asarray(cnt2)), (step, r, s)
+    # byte truth of the last step's gathers on the GPU
+    step = max(got)
+    for r, s, rc, loc, cnt, sel in got[step]:
+        st = gpu.gather(np.asarray(loc).ravel())
+        for e in range(0, len(sel), 7):
+            assert np.array_equal(st[e], inputs.rows(r, s, int(sel[e]), 1)[0]), (r, s, e)
+
+
 # ------------------------------------------------------------ small, every output
 
 SMALL = [
@@ -283,3 +316,25 @@ def test_c128_full_size_sampled():
 
 def test_long_full_size_sampled():
     compare_run(LONG, sampled=[0, 31], check_all_bytes=False)
+
+
+def test_admission_rejects_misaligned_host_rows():
+    """Rows move between HBM and the host copy in 16-byte chunks: a host
+    copy that is not 16-byte aligned is refused, for both admissions."""
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    pool = dhs.Pool(max_requests=2, sources=1, row_bytes=16, page_rows=4, tail_rows=2,
+                    hot_rows=4, max_queries=1, max_topk=4, max_rows_per_request=16,
+                    optional_pages=4)
+    host = dhs.HostRows(4096)
+    dev = torch.zeros(16 * 8, dtype=torch.int16, device="cuda")
+    try:
+        rc, _ = pool.admit(0, 0, host.ptr + 8, 8, None)
+        assert rc == dhs.DHS_EINVAL
+        rc, _ = pool.admit_device(0, 0, dev.data_ptr(), host.ptr + 8, 8, None)
+        assert rc == dhs.DHS_EINVAL
+        rc, _ = pool.admit_device(0, 0, dev.data_ptr(), host.ptr, 8, None)
+        assert rc == 0
+        torch.cuda.synchronize()
+    finally:
+        pool.close()
+        host.close()
