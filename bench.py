@@ -78,9 +78,11 @@ def parse():
     ap.add_argument("--kernel-steps", type=int, default=500)
     ap.add_argument("--trace-steps", type=int, default=100)
     ap.add_argument("--no-hugepages", action="store_true")
+    ap.add_argument("--gemm", type=int, default=4096,
+                    help="--experiment prefetch: per-layer compute, an n x n x n bf16 GEMM")
     ap.add_argument("--union", action="store_true",
                     help="union verification staging (DHS_ITEM_UNION)")
-    ap.add_argument("--experiment", default=None, choices=["loadstep"],
+    ap.add_argument("--experiment", default=None, choices=["loadstep", "prefetch"],
                     help="run an experiment instead of the benchmark (one JSON line)")
     return ap.parse_args()
 
@@ -427,10 +429,82 @@ def run_loadstep(args):
     print(json.dumps(out), flush=True)
 
 
+def run_prefetch(args, cfg):
+    """Per-layer decode with the caller's compute between layers (a bf16
+    GEMM standing in for each layer's attention + MLP), two schedules over
+    the same steps from the same pool state:
+      serial    per layer: resolve, gather, compute (pool stream);
+      prefetch  layer 0 resolved on the pool stream, every later resolving
+                layer by dhs_prefetch on a side stream at step start; per
+                layer: gather, compute.
+    Device time per step from CUDA events on the pool stream."""
+    import torch
+    from dhs_workload.configs import Workload
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    wl = Workload(cfg)
+    run = GpuRun(cfg, wl)
+    n = args.gemm
+    A = torch.randn(n, n, device="cuda", dtype=torch.bfloat16)
+    B = torch.randn(n, n, device="cuda", dtype=torch.bfloat16)
+    C = torch.empty(n, n, device="cuda", dtype=torch.bfloat16)
+    layers = list(range(len(run.layers)))
+    resolving = [l for l, (kind, _) in enumerate(run.layers) if kind == "resolve"]
+
+    def serial(step):
+        run.append(step)
+        for l in layers:
+            if l in resolving:
+                run.resolve_layer(step, l)
+            run.gather_layer(step, l)
+            torch.mm(A, B, out=C)
+
+    def prefetch(step):
+        run.append(step)
+        run.resolve_layer(step, layers[0])
+        if len(resolving) > 1:
+            run.prefetch_layers(step, resolving[1:])
+        for l in layers:
+            run.gather_layer(step, l)
+            torch.mm(A, B, out=C)
+
+    def compute_only():
+        for _ in layers:
+            torch.mm(A, B, out=C)
+
+    out = {"experiment": "prefetch", "config": workload_desc(cfg), "gemm": [n, n, n],
+           "layers": len(layers), "resolving_layers": len(resolving)}
+    for name, fn in (("serial", serial), ("prefetch", prefetch), ("compute_only", None)):
+        run.reset()
+        torch.cuda.synchronize()
+        ts = []
+        for step in range(1, cfg.total_steps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            if fn is None:
+                compute_only()
+            else:
+                fn(step)
+            e1.record()
+            e1.synchronize()
+            if step > cfg.warmup_steps + 2:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        rc, flags = run.status()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} flags {flags}")
+        out[name + "_us_median"] = statistics.median(ts)
+    out["hidden_us"] = out["serial_us_median"] - out["prefetch_us_median"]
+    run.close()
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     if args.experiment == "loadstep":
         run_loadstep(args)
+        return
+    if args.experiment == "prefetch":
+        from dhs_workload.configs import CONFIGS
+        run_prefetch(args, CONFIGS[args.config])
         return
     from dhs_workload.configs import CONFIGS
     cfg = CONFIGS[args.config]

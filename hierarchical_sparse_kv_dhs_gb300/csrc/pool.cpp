@@ -185,6 +185,15 @@ struct dhs_pool {
   std::vector<int64_t> l0_of_pair;   // length of each resolved pair before this step's append
   std::vector<uint32_t> seq_of_pair; // resolve launch that last resolved each pair
   std::vector<dhs::PageMove> moves;  // page list of the next page-move launch
+  // dhs_prefetch: resolves enqueued on a caller's side stream; the pool's
+  // stream waits for them before its next device work
+  cudaEvent_t ev_main = nullptr, ev_prefetch = nullptr;
+  bool prefetch_pending = false;
+  std::vector<uint8_t> pf_pair;  // pairs resolved by the outstanding prefetch
+  ~dhs_pool() {
+    if (ev_main) cudaEventDestroy(ev_main);
+    if (ev_prefetch) cudaEventDestroy(ev_prefetch);
+  }
 };
 
 namespace {
@@ -196,11 +205,41 @@ bool small_pages(const dhs_pool* p) {
   return (int64_t)p->cfg.page_rows * p->cfg.row_bytes <= ((int64_t)1 << 24);
 }
 
+// Every call that enqueues device work starts here: the pool's device, and
+// the pool's stream ordered after an outstanding dhs_prefetch.
 int enter(dhs_pool* p) {
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return DHS_ECUDA;
   if (cur != p->device && cudaSetDevice(p->device) != cudaSuccess) return DHS_ECUDA;
+  if (p->prefetch_pending) {
+    if (cudaStreamWaitEvent(p->stream, p->ev_prefetch, 0) != cudaSuccess) return DHS_ECUDA;
+    p->prefetch_pending = false;
+    std::fill(p->pf_pair.begin(), p->pf_pair.end(), 0);
+  }
   return DHS_OK;
+}
+
+// enter() for a resolve or gather of `st`: the outstanding prefetch is
+// joined only if the step touches one of its pairs (a gather-only item may
+// read any pair's rows, so it always joins); a step on other pairs runs
+// alongside it -- their metadata, hot slots and miss lists are disjoint.
+int enter_step(dhs_pool* p, const dhs_step* st) {
+  // pending page copies or map uploads (the flush that follows) also join
+  bool join = p->any_pending || p->dirty_hi >= 0;
+  if (p->prefetch_pending && !join) {
+    const dhs_pool_config& c = p->cfg;
+    for (int32_t i = 0; i < st->n_items && !join; ++i) {
+      const dhs_item& it = st->items[i];
+      join = (it.flags & DHS_ITEM_GATHER_ONLY) ||
+             p->pf_pair[(size_t)it.req * c.sources + it.src];
+    }
+  }
+  if (join) return enter(p);
+  const bool pending = p->prefetch_pending;
+  p->prefetch_pending = false;  // device selection only
+  const int rc = enter(p);
+  p->prefetch_pending = pending;
+  return rc;
 }
 
 void mark_dirty(dhs_pool* p, int64_t pair) {
@@ -435,6 +474,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->app_of_pair.assign((size_t)p->pairs, -1);
     p->l0_of_pair.assign((size_t)p->pairs, 0);
     p->seq_of_pair.assign((size_t)p->pairs, 0);
+    p->pf_pair.assign((size_t)p->pairs, 0);
   } catch (...) {
     delete p;
     return DHS_ENOMEM;
@@ -444,7 +484,9 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     delete p;
     return DHS_ECUDA;
   }
-  if (dhs::gather_set_smem_limit(cfg->row_bytes) != cudaSuccess) {
+  if (dhs::gather_set_smem_limit(cfg->row_bytes) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_main, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_prefetch, cudaEventDisableTiming) != cudaSuccess) {
     delete p;
     return DHS_ECUDA;
   }
@@ -968,10 +1010,38 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   return DHS_OK;
 }
 
-int dhs_resolve(dhs_pool* p, const dhs_step* st) {
+int dhs_prefetch(dhs_pool* p, const dhs_step* st, void* side_stream) {
+  if (!p || !side_stream) return DHS_EINVAL;
   int rc = validate_step(p, st, true);
   if (rc) return rc;
   if ((rc = enter(p))) return rc;
+  // pending page copies and map uploads, then everything the pool's stream
+  // holds so far (earlier gathers still reading hot slots), come first
+  if ((rc = flush(p))) return rc;
+  cudaStream_t side = (cudaStream_t)side_stream;
+  if (cudaEventRecord(p->ev_main, p->stream) != cudaSuccess ||
+      cudaStreamWaitEvent(side, p->ev_main, 0) != cudaSuccess)
+    return DHS_ECUDA;
+  cudaStream_t main = p->stream;
+  p->stream = side;
+  rc = resolve_impl(p, st, nullptr, false);
+  p->stream = main;
+  // whatever was enqueued on the side stream is joined before the pool's next
+  // device work, even if the call failed part way
+  if (cudaEventRecord(p->ev_prefetch, side) != cudaSuccess) return DHS_ECUDA;
+  p->prefetch_pending = true;
+  for (int32_t i = 0; i < st->n_items; ++i) {
+    const dhs_item& it = st->items[i];
+    if (!(it.flags & DHS_ITEM_GATHER_ONLY))
+      p->pf_pair[(size_t)it.req * p->cfg.sources + it.src] = 1;
+  }
+  return rc;
+}
+
+int dhs_resolve(dhs_pool* p, const dhs_step* st) {
+  int rc = validate_step(p, st, true);
+  if (rc) return rc;
+  if ((rc = enter_step(p, st))) return rc;
   if ((rc = flush(p))) return rc;
   return resolve_impl(p, st, nullptr, false);
 }
@@ -1073,7 +1143,7 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
 int dhs_gather(dhs_pool* p, const dhs_step* st) {
   int rc = validate_step(p, st, false);
   if (rc) return rc;
-  if ((rc = enter(p))) return rc;
+  if ((rc = enter_step(p, st))) return rc;
   if ((rc = flush(p))) return rc;
   return launch_gathers(p, st, false);
 }

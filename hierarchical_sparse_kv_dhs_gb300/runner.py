@@ -118,7 +118,7 @@ class GpuRun:
     def _build_descriptors(self):
         c = self.cfg
         Q, k, rb = c.queries, c.topk, c.row_bytes
-        self._steps, self._appends = [], []
+        self._steps, self._appends, self._layer_steps = [], [], []
         loc0 = self.loc.data_ptr()
         cnt0 = self.counters.data_ptr()
         stg0 = self.staging.data_ptr()
@@ -140,6 +140,8 @@ class GpuRun:
                     it.staging_dev = stg0 + ((r * len(self.layers) + layer) * Q * k) * rb
                     items.append(it)
             self._steps.append(dhs.make_step(step, items))
+            nl = len(self.layers)
+            self._layer_steps.append([dhs.make_step(step, items[l::nl]) for l in range(nl)])
             apps = []
             for i, (r, s) in enumerate((r, s) for r in range(c.requests)
                                        for s in range(c.sources)):
@@ -165,9 +167,49 @@ class GpuRun:
         st, _ = self._steps[step - 1]
         dhs.check(dhs.lib.dhs_gather(self.pool.h, ctypes.byref(st)), "dhs_gather")
 
+    def side_stream(self):
+        if getattr(self, "_side", None) is None:
+            self._side = torch.cuda.Stream(self.device)
+        return self._side
+
+    def prefetch(self, step):
+        """Resolve every layer of the step on the side stream (dhs_prefetch)."""
+        st, _ = self._steps[step - 1]
+        dhs.check(dhs.lib.dhs_prefetch(self.pool.h, ctypes.byref(st),
+                                       ctypes.c_void_p(self.side_stream().cuda_stream)),
+                  "dhs_prefetch")
+
+    def prefetch_layers(self, step, layers):
+        """dhs_prefetch of the given layers' items (one step descriptor)."""
+        key = (step, tuple(layers))
+        cache = self.__dict__.setdefault("_pf_cache", {})
+        if key not in cache:
+            items = [it for l in layers for it in self._layer_steps[step - 1][l][1]
+                     [: self._layer_steps[step - 1][l][0].n_items]]
+            cache[key] = dhs.make_step(step, items)
+        st, _ = cache[key]
+        dhs.check(dhs.lib.dhs_prefetch(self.pool.h, ctypes.byref(st),
+                                       ctypes.c_void_p(self.side_stream().cuda_stream)),
+                  "dhs_prefetch")
+
+    def resolve_layer(self, step, layer):
+        st, _ = self._layer_steps[step - 1][layer]
+        dhs.check(dhs.lib.dhs_resolve(self.pool.h, ctypes.byref(st)), "dhs_resolve")
+
+    def gather_layer(self, step, layer):
+        st, _ = self._layer_steps[step - 1][layer]
+        dhs.check(dhs.lib.dhs_gather(self.pool.h, ctypes.byref(st)), "dhs_gather")
+
     def step(self, step, fused=True):
         """One decode step: append, then resolve + gather every layer -- one
-        dhs_decode_step call, or dhs_append, dhs_resolve, dhs_gather."""
+        dhs_decode_step call (fused=True), dhs_append, dhs_resolve and
+        dhs_gather (False), or dhs_append, dhs_prefetch on a side stream and
+        dhs_gather ("prefetch")."""
+        if fused == "prefetch":
+            self.append(step)
+            self.prefetch(step)
+            self.gather(step)
+            return
         if not fused:
             self.append(step)
             self.resolve(step)

@@ -330,6 +330,19 @@ typedef struct {
 int dhs_resolve(dhs_pool *pool, const dhs_step *step);
 
 /*
+ * dhs_resolve on a caller's side stream ("Model-specific reuse": layers that
+ * share sparse indices but keep distinct payloads have their positions
+ * prefetched).  The resolve and host-copy kernels are enqueued on
+ * side_stream (a cudaStream_t of the pool's device) after everything the
+ * pool's stream holds so far; the pool's stream waits for them before its
+ * next device work (the next dhs_gather, for instance), while work the
+ * caller enqueues on its own streams in between -- the previous layer's
+ * compute -- overlaps them.  Results are those of dhs_resolve.  Errors: as
+ * dhs_resolve, plus DHS_EINVAL for a null side_stream.
+ */
+int dhs_prefetch(dhs_pool *pool, const dhs_step *step, void *side_stream);
+
+/*
  * Gather: staging_dev[q][i] = the row at loc_dev[q][i] for every item
  * (resolved or gather-only); DHS_NO_LOC rows become zeros and DHS_END_LOC
  * entries are skipped (staging untouched).  staging_dev must

@@ -196,9 +196,10 @@ IMPLS = {"vec": 0, "tma": 1}
 
 @pytest.mark.parametrize("cfg", SMALL, ids=[c.name for c in SMALL])
 @pytest.mark.parametrize("mode", ["fused-vec", "fused-tma", "split-vec", "split-tma",
-                                  "fused-tma-late", "fused-vec-late"])
+                                  "fused-tma-late", "fused-vec-late", "prefetch-tma"])
 def test_small_configs_bit_exact(cfg, mode):
-    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
+    fused = "prefetch" if mode.startswith("prefetch") else mode.startswith("fused")
+    compare_run(cfg, fused=fused, gather_impl=IMPLS[mode.split("-")[1]],
                 early=0 if mode.endswith("late") else 1)
 
 
@@ -223,6 +224,39 @@ def test_fresh_row_list_on_and_off(cfg, fresh):
     overflows the list on its first step, so tiles also take the fallback)."""
     compare_run(cfg, gather_impl=1, fresh=fresh)
     compare_run(cfg, gather_impl=1, fresh=fresh, union=True)
+
+
+def test_prefetch_per_layer_pipeline_matches_oracle():
+    """Every layer resolved on a side stream at step start (dhs_prefetch),
+    then each layer gathered on its own just before it is needed, with other
+    work on the pool's stream in between: the same results as the oracle."""
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    from oracle.run import OracleRun
+    cfg = SMALL[2]  # three sources sharing a selection, three Reuse layers
+    wl = Workload(cfg)
+    gpu = GpuRun(cfg, wl)
+    orc = OracleRun(cfg, wl)
+    filler = torch.empty(1 << 24, dtype=torch.uint8, device="cuda")
+    try:
+        for step in range(1, cfg.total_steps + 1):
+            gpu.append(step)
+            # layer 0 on the pool's stream, the other resolving layers on the
+            # side stream; layer 0's gather runs alongside their resolve
+            gpu.resolve_layer(step, 0)
+            gpu.prefetch_layers(step, list(range(1, cfg.sources)))
+            for layer in range(len(gpu.layers)):
+                filler.add_(1)  # the caller's work between layers
+                gpu.gather_layer(step, layer)
+            res = orc.step(step)
+            assert gpu.status() == (0, 0)
+            loc = _as_u32(gpu.loc)
+            for r in range(cfg.requests):
+                assert np.array_equal(loc[r], res[r]["loc"]), (step, r)
+                stg = gpu.staging[r].cpu().view(torch.int16).numpy().view(np.uint16)
+                assert np.array_equal(stg, res[r]["staging"]), (step, r)
+    finally:
+        gpu.close()
+        orc.pool.close()
 
 
 def test_union_staging_failures():
