@@ -194,6 +194,8 @@ struct GatherCommon {
   uint32_t* later_count;      // [2]
   uint32_t later_cap;
   uint32_t gen;
+  int32_t tpc;                // TMA gather: consecutive tiles per CTA (>= 1)
+  int32_t pad;
 };
 
 // Each kernel file sets its kernels' shared-memory carveout to the maximum,

@@ -312,15 +312,9 @@ __global__ void __launch_bounds__(kTmaThreads)
   extern __shared__ __align__(128) uint8_t s_rows[];  // [32][row_bytes]
   __shared__ __align__(8) uint64_t s_bar;
   const GatherCommon& c = P.c;
-  const int tile = blockIdx.x;
-  const GatherItem& it = P.items[find_item(P, tile)];
-  const int e0 = (tile - it.tile0) * kGatherTileRows;
-  const int ne = min(kGatherTileRows, it.n - e0);
   const int lane = threadIdx.x;
   const uint32_t rb = (uint32_t)c.row_bytes;
   uint8_t* my_row = s_rows + (size_t)lane * rb;
-  uint8_t* dst = it.staging + ((size_t)e0 + lane) * rb;
-  const bool early = c.early && it.sel != nullptr;
   asm volatile("griddepcontrol.launch_dependents;");
   if (lane == 0) {
     trace_mark(c.trace, kTraceGather, false);
@@ -329,9 +323,10 @@ __global__ void __launch_bounds__(kTmaThreads)
   __syncwarp();
   uint32_t parity = 0;
   bool stored = false, ok = true, waited = false;
+  uint8_t* dst = nullptr;
 
-  // Move entry `lane` (src: row address, nullptr = zeros) when `mine`;
-  // false if the bounded wait gave up.
+  // Move entry `lane` (src: row address, nullptr = zeros) to `dst` when
+  // `mine`; false if the bounded wait gave up.
   auto move = [&](bool mine, const uint8_t* src) -> bool {
     const bool load = mine && src != nullptr;
     const unsigned lmask = __ballot_sync(0xFFFFFFFFu, load);
@@ -360,55 +355,72 @@ __global__ void __launch_bounds__(kTmaThreads)
     return true;
   };
 
-  const uint32_t v0 = early ? ld_verdict(&c.verdict[it.pair]) : 0u;
-  const uint8_t* src = nullptr;
-  if (early && lane < ne) src = step1_ptr(c, it, it.sel[e0 + lane]);
-  bool deferred = lane < ne && src == nullptr;
-  if (early) {
-    ok = move(src != nullptr, src);  // rows resolved in step 1
-    if (ok && item_verdict(c, it, v0, &waited) != kVerdictOk) {
-      // the item failed: every entry becomes zeros; a row stored above must
-      // be fully written (and its shared-memory copy read) before it is
-      // overwritten
-      if (stored) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-      ok = move(lane < ne, nullptr);
-      deferred = false;
+  // c.tpc consecutive tiles per CTA (one by default)
+  for (int t = 0; t < c.tpc && ok; ++t) {
+    const int tile = blockIdx.x * c.tpc + t;
+    if (tile >= c.n_tiles) break;
+    // the previous tile's stores must have read its rows out of shared memory
+    if (stored) {
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      stored = false;
     }
-  }
-  const bool lr = c.early && (it.flags & kGiLocReady) && !waited;
-  if (ok && __any_sync(0xFFFFFFFFu, deferred) && lr && wait_loc_ready(c, it)) {
-    // the item's locations are out: every row but the fresh ones (hot slots
-    // the host copy is still filling) can move now
-    const uint32_t l = deferred ? ld_relaxed(&it.loc[e0 + lane]) : kEndLoc;
-    const bool fresh = deferred && fresh_loc(c, l);
-    const bool now = deferred && l != kEndLoc && !fresh;
-    ok = move(now, now ? row_ptr(c, l) : nullptr);
-    bool later = fresh;
-    if (c.later) {  // hand the fresh rows to the list copied after the copy grid
-      const unsigned fm = __ballot_sync(0xFFFFFFFFu, fresh);
-      uint32_t base = 0;
-      if (lane == 0 && fm) base = atomicAdd(&c.later_count[c.gen & 1u], (uint32_t)__popc(fm));
-      base = __shfl_sync(0xFFFFFFFFu, base, 0);
-      const uint32_t cnt = (uint32_t)__popc(fm);
-      const bool fits = (uint64_t)base + cnt <= c.later_cap;
-      const uint32_t slot = base + (uint32_t)__popc(fm & ((1u << lane) - 1u));
-      if (fresh && fits) {
-        c.later[slot].dst = dst;
-        c.later[slot].loc = l;
-        later = false;
-      } else if (fresh && slot < c.later_cap) {
-        c.later[slot].dst = nullptr;  // the list is full: the tile copies it
+    const GatherItem& it = P.items[find_item(P, tile)];
+    const int e0 = (tile - it.tile0) * kGatherTileRows;
+    const int ne = min(kGatherTileRows, it.n - e0);
+    dst = it.staging + ((size_t)e0 + lane) * rb;
+    const bool early = c.early && it.sel != nullptr;
+
+    const uint32_t v0 = early ? ld_verdict(&c.verdict[it.pair]) : 0u;
+    const uint8_t* src = nullptr;
+    if (early && lane < ne) src = step1_ptr(c, it, it.sel[e0 + lane]);
+    bool deferred = lane < ne && src == nullptr;
+    if (early) {
+      ok = move(src != nullptr, src);  // rows resolved in step 1
+      if (ok && item_verdict(c, it, v0, &waited) != kVerdictOk) {
+        // the item failed: every entry becomes zeros; a row stored above must
+        // be fully written (and its shared-memory copy read) before it is
+        // overwritten
+        if (stored) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        ok = move(lane < ne, nullptr);
+        deferred = false;
       }
     }
-    deferred = later;
-  }
-  if (ok && __any_sync(0xFFFFFFFFu, deferred)) {
-    // rows that needed the hot cache (or no early phase): wait for the
-    // resolve / host-copy grids (a no-op without programmatic dependent launch)
-    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
-    const uint32_t l = deferred ? it.loc[e0 + lane] : kEndLoc;
-    const bool live = l != kEndLoc;  // past a union list: nothing to write
-    ok = move(live, live ? row_ptr(c, l) : nullptr);
+    const bool lr = c.early && (it.flags & kGiLocReady) && !waited;
+    if (ok && __any_sync(0xFFFFFFFFu, deferred) && lr && wait_loc_ready(c, it)) {
+      // the item's locations are out: every row but the fresh ones (hot slots
+      // the host copy is still filling) can move now
+      const uint32_t l = deferred ? ld_relaxed(&it.loc[e0 + lane]) : kEndLoc;
+      const bool fresh = deferred && fresh_loc(c, l);
+      const bool now = deferred && l != kEndLoc && !fresh;
+      ok = move(now, now ? row_ptr(c, l) : nullptr);
+      bool later = fresh;
+      if (c.later) {  // hand the fresh rows to the list copied after the copy grid
+        const unsigned fm = __ballot_sync(0xFFFFFFFFu, fresh);
+        uint32_t base = 0;
+        if (lane == 0 && fm) base = atomicAdd(&c.later_count[c.gen & 1u], (uint32_t)__popc(fm));
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+        const uint32_t cnt = (uint32_t)__popc(fm);
+        const bool fits = (uint64_t)base + cnt <= c.later_cap;
+        const uint32_t slot = base + (uint32_t)__popc(fm & ((1u << lane) - 1u));
+        if (fresh && fits) {
+          c.later[slot].dst = dst;
+          c.later[slot].loc = l;
+          later = false;
+        } else if (fresh && slot < c.later_cap) {
+          c.later[slot].dst = nullptr;  // the list is full: the tile copies it
+        }
+      }
+      deferred = later;
+    }
+    if (ok && __any_sync(0xFFFFFFFFu, deferred)) {
+      // rows that needed the hot cache (or no early phase): wait for the
+      // resolve / host-copy grids (a no-op without programmatic dependent launch)
+      if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+      const uint32_t l = deferred ? it.loc[e0 + lane] : kEndLoc;
+      const bool live = l != kEndLoc;  // past a union list: nothing to write
+      ok = move(live, live ? row_ptr(c, l) : nullptr);
+    }
   }
   // shared memory must outlive the stores' reads
   if (stored) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -465,6 +477,7 @@ cudaError_t launch_t(const GatherCommon& c, const GatherItem* items, int n, bool
     cfg.numAttrs = 1;
   }
   if (impl == kGatherTma) {
+    cfg.gridDim = dim3((unsigned)((c.n_tiles + c.tpc - 1) / c.tpc));
     cfg.blockDim = dim3(kTmaThreads);
     cfg.dynamicSmemBytes = (size_t)kGatherTileRows * c.row_bytes;
     return cudaLaunchKernelEx(&cfg, gather_tma_kernel<MAXI>, P);

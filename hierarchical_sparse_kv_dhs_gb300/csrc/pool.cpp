@@ -157,6 +157,7 @@ struct dhs_pool {
   int copy_ctas = 0;
   bool union_ok = false;  // the union staging plan fits in shared memory
   int gather_impl = dhs::kGatherTma;
+  int gather_tpc = 1;   // DHS_OPT_GATHER_TPC
   int early = 1;        // fused gathers copy step-1 rows before the resolve ends
   uint32_t* verdict = nullptr;  // [pairs] resolve verdicts for the fused gather
   uint32_t seq = 0;             // resolve launches so far
@@ -537,6 +538,11 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     pool->fresh_list = (int)value;
     return DHS_OK;
   }
+  if (key == DHS_OPT_GATHER_TPC) {
+    if (value < 1 || value > 64) return DHS_EINVAL;
+    pool->gather_tpc = (int)value;
+    return DHS_OK;
+  }
   return DHS_EINVAL;
 }
 
@@ -558,6 +564,7 @@ int dhs_get_option(dhs_pool* pool, int32_t key, int64_t* value) {
     case DHS_OPT_TRACE: *value = (int64_t)(uintptr_t)pool->trace; return DHS_OK;
     case DHS_OPT_EARLY: *value = pool->early; return DHS_OK;
     case DHS_OPT_FRESH_LIST: *value = use_fresh_list(pool) ? 1 : 0; return DHS_OK;
+    case DHS_OPT_GATHER_TPC: *value = pool->gather_tpc; return DHS_OK;
     default: return DHS_EINVAL;
   }
 }
@@ -1076,6 +1083,7 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   g.later_count = p->later_count;
   g.later_cap = (uint32_t)std::min<int64_t>(p->later_cap, UINT32_MAX);
   g.gen = p->gen;
+  g.tpc = p->gather_tpc;
   // the step's resolved items publish their locations; gathers of them (and
   // Reuse items handed the same location vector) may go before the grids end
   const bool lr = fused && p->early && p->fused_resolved && p->gather_impl == dhs::kGatherTma;

@@ -439,6 +439,8 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
  * tenth of the admitted complete pages are not optional-resident; 0 = off
  * (such rows wait in their tile); 1 = on. */
 #define DHS_OPT_FRESH_LIST 5
+/* TMA gather: consecutive 32-entry tiles per CTA, 1 (default) .. 64. */
+#define DHS_OPT_GATHER_TPC 6
 int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
 /* The value in effect (DHS_OPT_FRESH_LIST: 0 or 1, the auto rule resolved
  * for the pool's current admissions).  DHS_EINVAL for an unknown key. */

@@ -36,7 +36,7 @@ def _as_u32(t):
 
 
 def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
-                gather_impl=0, patch=None, early=1, union=False, fresh=None):
+                gather_impl=0, patch=None, early=1, union=False, fresh=None, tpc=None):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
@@ -51,6 +51,8 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
         gpu.pool.set_option(dhs.DHS_OPT_EARLY, 0)
     if fresh is not None:
         gpu.pool.set_option(dhs.DHS_OPT_FRESH_LIST, fresh)
+    if tpc is not None:
+        gpu.pool.set_option(dhs.DHS_OPT_GATHER_TPC, tpc)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
     orc = OracleRun(cfg, wl, requests=sampled, union=union)
     try:
@@ -214,6 +216,17 @@ UNION = [SMALL[1], SMALL[2], SMALL[4],
 def test_union_staging_bit_exact(cfg, mode):
     compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
                 union=True)
+
+
+@pytest.mark.parametrize("tpc", [2, 5])
+@pytest.mark.parametrize("cfg", [SMALL[1], SMALL[2], SMALL[4]], ids=["v3", "reuse", "evict"])
+def test_gather_tiles_per_cta(cfg, tpc):
+    """Several consecutive tiles per TMA gather CTA (tiles of different items
+    in one CTA, a ragged last CTA): same results, fused and split, both
+    staging layouts."""
+    compare_run(cfg, gather_impl=1, tpc=tpc)
+    compare_run(cfg, gather_impl=1, tpc=tpc, fused=False)
+    compare_run(cfg, gather_impl=1, tpc=tpc, union=True)
 
 
 @pytest.mark.parametrize("fresh", [0, 1])
