@@ -635,6 +635,15 @@ def main():
                "kind": "oracle",
                "sample": f"{n} decode steps of the same workload (all requests, "
                          f"{n * entries} rows, {dt:.1f} s timed), {ot.threads} threads"}
+        # the same oracle on one thread, a shorter sample
+        ot1 = OracleTimer(cfg, wl, threads=1, union=args.union)
+        dt1, n1 = 0.0, 0
+        while dt1 < args.cpu_seconds / 2:
+            dt1 += ot1.step()
+            n1 += 1
+        ot1.close()
+        cpu["single_thread_value"] = n1 * entries / dt1
+        cpu["single_thread_sample"] = f"{n1} decode steps, {dt1:.1f} s timed, 1 thread"
 
     peaks = {}
     try:
