@@ -125,7 +125,13 @@ LONG = Config("long", 5, requests=32, sources=3, history=512000, tail=256,
               hot=8192, topk=2048, steps=16, residency=0.2, reuse_layers=3,
               shared_selection=True)
 
-CONFIGS = {c.name: c for c in (TINY, C8, C64, C128, LONG)}
+# host-copy profiling case: nothing optional-resident, so every selected row
+# outside the tail is a hot-cache hit or a host fetch (1.2 GB pinned region,
+# about 0.25 GB on the device)
+MISS = Config("miss", 6, requests=16, sources=2, history=32768, tail=256, hot=4096,
+              topk=2048, steps=16, residency=0.0)
+
+CONFIGS = {c.name: c for c in (TINY, C8, C64, C128, LONG, MISS)}
 
 
 class Workload:

@@ -4,8 +4,9 @@
 // Reads the missing rows straight out of mapped pinned host memory over
 // NVLink-C2C into their victim hot-cache slots.  The pages note that the
 // copy kernel scales from 4 to 32 thread blocks with batch size; the grid
-// here is chosen by the host the same way (clamp(requests / 4, 4, 32)) and
-// can be overridden for sweeps.  Each warp keeps up to four 1152-byte rows
+// here scales the same way up to 32 blocks but never goes below 16
+// (clamp(requests / 4, 16, 32)): fewer rows in flight leave the host link
+// idle on GB300.  It can be overridden for sweeps.  Each warp keeps up to four 1152-byte rows
 // in flight (12 x 16-byte loads per lane) so the link sees enough
 // outstanding requests to cover its latency.
 #include <algorithm>
