@@ -349,11 +349,12 @@ def traced_pass(run, cycle, steps, dev, flush_l2):
 
 
 def measure_e2e(run, cycle, steps, dev, stream):
-    """The metric through the C ABI for `steps` further decode steps: each
-    step's selections and decode rows are copied in from pinned host memory,
-    the step runs, and its locations + counters are read back into pinned
-    host memory (wall clock; synchronised per step, as a caller reading its
-    result is)."""
+    """The metric through the C ABI with host buffers for `steps` further
+    decode steps: each is one dhs_decode_step_host call that copies the
+    step's selections and decode rows in from pinned host memory, runs the
+    step, copies its locations + counters (+ union indices) back to pinned
+    host memory and synchronises (wall clock around the call, the copies
+    inside it)."""
     import torch
     T = run.cfg.total_steps
     sel_host = [run.sel[s].cpu().pin_memory() for s in range(T)]
@@ -362,6 +363,17 @@ def measure_e2e(run, cycle, steps, dev, stream):
     cnt_host = torch.empty(run.counters.shape, dtype=run.counters.dtype).pin_memory()
     idx_host = (torch.empty(run.index.shape, dtype=run.index.dtype).pin_memory()
                 if run.index is not None else None)  # union staging: entry -> row
+
+    def span(dst, src):
+        return (dst.data_ptr(), src.data_ptr(), src.numel() * src.element_size())
+
+    outs = [span(loc_host, run.loc), span(cnt_host, run.counters)]
+    if idx_host is not None:
+        outs.append(span(idx_host, run.index))
+    # the call's arguments for every step of the cycle, built once as a caller would
+    io = [run.host_io(s, [span(run.sel[s - 1], sel_host[s - 1]),
+                          span(run.app_rows[s - 1], rows_host[s - 1])], outs)
+          for s in range(1, T + 1)]
     torch.cuda.synchronize(dev)
     dt = 0.0
     for _ in range(steps):
@@ -371,22 +383,15 @@ def measure_e2e(run, cycle, steps, dev, stream):
             s = cycle.next()
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        run.sel[s - 1].copy_(sel_host[s - 1], non_blocking=True)
-        run.app_rows[s - 1].copy_(rows_host[s - 1], non_blocking=True)
-        run.step(s)
-        loc_host.copy_(run.loc, non_blocking=True)
-        cnt_host.copy_(run.counters, non_blocking=True)
-        if idx_host is not None:
-            idx_host.copy_(run.index, non_blocking=True)
-        stream.synchronize()
+        run.step_host(s, io=io[s - 1])
         dt += time.perf_counter() - t0
     h2d = sel_host[0].numel() * 4 + rows_host[0].numel() * 2
-    d2h = loc_host.numel() * 4 + cnt_host.numel() * 4
-    if idx_host is not None:
-        d2h += idx_host.numel() * 4
+    d2h = sum(o[2] for o in outs)
     return {"value": run.cfg.entries_per_step * steps / dt, "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": steps, "seconds": dt}
+            "steps": steps, "seconds": dt,
+            "path": "dhs_decode_step_host: H2D copies, decode step, D2H copies, "
+                    "stream synchronise -- one C ABI call per step"}
 
 
 def run_loadstep(args):

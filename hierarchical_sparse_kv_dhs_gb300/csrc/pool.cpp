@@ -1227,6 +1227,29 @@ int dhs_decode_step(dhs_pool* p, const dhs_append_item* apps, int32_t n_apps,
   return launch_gathers(p, st, true);
 }
 
+int dhs_decode_step_host(dhs_pool* p, const dhs_copy* in, int32_t n_in,
+                         const dhs_append_item* apps, int32_t n_apps, const dhs_step* st,
+                         const dhs_copy* out, int32_t n_out) {
+  if (!p || n_in < 0 || n_out < 0 || (n_in > 0 && !in) || (n_out > 0 && !out))
+    return DHS_EINVAL;
+  for (int32_t i = 0; i < n_in; ++i)
+    if (in[i].bytes && (!in[i].dst || !in[i].src)) return DHS_EINVAL;
+  for (int32_t i = 0; i < n_out; ++i)
+    if (out[i].bytes && (!out[i].dst || !out[i].src)) return DHS_EINVAL;
+  int rc = enter(p);
+  if (rc) return rc;
+  for (int32_t i = 0; i < n_in; ++i)
+    if (in[i].bytes && cudaMemcpyAsync(in[i].dst, in[i].src, in[i].bytes,
+                                       cudaMemcpyHostToDevice, p->stream) != cudaSuccess)
+      return DHS_ECUDA;
+  if ((rc = dhs_decode_step(p, apps, n_apps, st))) return rc;
+  for (int32_t i = 0; i < n_out; ++i)
+    if (out[i].bytes && cudaMemcpyAsync(out[i].dst, out[i].src, out[i].bytes,
+                                        cudaMemcpyDeviceToHost, p->stream) != cudaSuccess)
+      return DHS_ECUDA;
+  return cudaStreamSynchronize(p->stream) == cudaSuccess ? DHS_OK : DHS_ECUDA;
+}
+
 int dhs_status(dhs_pool* p, uint32_t* flags) {
   if (flags) *flags = 0;
   if (!p) return DHS_EINVAL;

@@ -71,6 +71,10 @@ class dhs_item(ctypes.Structure):
                 ("index_dev", _vp)]
 
 
+class dhs_copy(ctypes.Structure):
+    _fields_ = [("dst", _vp), ("src", _vp), ("bytes", ctypes.c_size_t)]
+
+
 class dhs_step(ctypes.Structure):
     _fields_ = [("step", _u32), ("n_items", _i32), ("items", ctypes.POINTER(dhs_item))]
 
@@ -90,6 +94,7 @@ def _load():
         "dhs_reclaim": (ctypes.c_int, [_vp, _vp, _i32, _i64, P(_i64)]),
         "dhs_release": (ctypes.c_int, [_vp, _i32]),
         "dhs_prefetch": (ctypes.c_int, [_vp, _vp, _vp]),
+        "dhs_decode_step_host": (ctypes.c_int, [_vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32]),
         "dhs_admit_device": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _i64, _vp, P(_i64)]),
         "dhs_backup": (ctypes.c_int, [_vp, _i64, P(_i64)]),
         "dhs_pending_backup": (_i64, [_vp]),

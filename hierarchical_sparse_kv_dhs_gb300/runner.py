@@ -220,6 +220,21 @@ class GpuRun:
         dhs.check(dhs.lib.dhs_decode_step(self.pool.h, arr, n, ctypes.byref(st)),
                   "dhs_decode_step")
 
+    def host_io(self, step, ins, outs):
+        """Prebuilt arguments of dhs_decode_step_host for `step`: `ins` /
+        `outs` are lists of (dst, src, bytes) host<->device copies."""
+        arr, n = self._appends[step - 1]
+        st, _ = self._steps[step - 1]
+        cin = (dhs.dhs_copy * max(1, len(ins)))(*[dhs.dhs_copy(*c) for c in ins])
+        cout = (dhs.dhs_copy * max(1, len(outs)))(*[dhs.dhs_copy(*c) for c in outs])
+        return (self.pool.h, cin, len(ins), arr, n, ctypes.byref(st), cout, len(outs))
+
+    def step_host(self, step, ins=None, outs=None, io=None):
+        """dhs_decode_step_host with prebuilt `io` (host_io) or with ins/outs;
+        returns after the outputs have landed in host memory."""
+        io = io or self.host_io(step, ins, outs)
+        dhs.check(dhs.lib.dhs_decode_step_host(*io), "dhs_decode_step_host")
+
     def reset(self):
         """Release every request and admit it again: the pool returns to its
         state before step 1 (stream-ordered; no synchronisation)."""

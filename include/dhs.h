@@ -397,6 +397,28 @@ int dhs_resolve_gather(dhs_pool *pool, const dhs_step *step);
 int dhs_decode_step(dhs_pool *pool, const dhs_append_item *appends, int32_t n_appends,
                     const dhs_step *step);
 
+/* One contiguous copy between host and device memory (see
+ * dhs_decode_step_host).  Host memory should be pinned for the copies to be
+ * asynchronous. */
+typedef struct {
+  void *dst;
+  const void *src;
+  size_t bytes;
+} dhs_copy;
+
+/*
+ * dhs_decode_step with its inputs and outputs in host memory: enqueue the
+ * n_in host-to-device copies (the step's selections and decode rows, into
+ * the device buffers its items and appends name), the decode step, the
+ * n_out device-to-host copies (locations, counters), then synchronise the
+ * pool's stream; on return the outputs are in host memory.  One
+ * cudaMemcpyAsync per copy on the pool's stream.  Errors: as
+ * dhs_decode_step, DHS_EINVAL for a copy with a null pointer, DHS_ECUDA.
+ */
+int dhs_decode_step_host(dhs_pool *pool, const dhs_copy *in, int32_t n_in,
+                         const dhs_append_item *appends, int32_t n_appends,
+                         const dhs_step *step, const dhs_copy *out, int32_t n_out);
+
 /*
  * Synchronise the pool's stream, read and clear the sticky device status.
  * *flags (may be NULL) receives DHS_STATUS_* bits.  Returns DHS_OK when no

@@ -385,3 +385,35 @@ def test_admission_rejects_misaligned_host_rows():
     finally:
         pool.close()
         host.close()
+
+
+def test_decode_step_host_matches_device_path():
+    """dhs_decode_step_host (host selections and decode rows in, host
+    locations and counters out, one call) gives what the device-side
+    dhs_decode_step leaves in device memory."""
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    cfg = SMALL[1]  # verify block of 3 queries, ragged k, appends of 1-4 rows
+    wl = Workload(cfg)
+    a, b = GpuRun(cfg, wl), GpuRun(cfg, wl)
+    try:
+        loc_h = torch.empty(b.loc.shape, dtype=b.loc.dtype).pin_memory()
+        cnt_h = torch.empty(b.counters.shape, dtype=b.counters.dtype).pin_memory()
+        for step in range(1, cfg.total_steps + 1):
+            sel_h = b.sel[step - 1].cpu().pin_memory()
+            rows_h = b.app_rows[step - 1].cpu().pin_memory()
+            b.sel[step - 1].zero_()  # the call must bring the inputs in itself
+            b.app_rows[step - 1].zero_()
+            a.step(step)
+
+            def span(dst, src):
+                return (dst.data_ptr(), src.data_ptr(), src.numel() * src.element_size())
+
+            b.step_host(step, [span(b.sel[step - 1], sel_h), span(b.app_rows[step - 1], rows_h)],
+                        [span(loc_h, b.loc), span(cnt_h, b.counters)])
+            torch.cuda.synchronize()
+            assert torch.equal(loc_h, a.loc.cpu()) and torch.equal(cnt_h, a.counters.cpu())
+            assert torch.equal(a.staging.view(torch.int16), b.staging.view(torch.int16))
+        assert a.status() == (0, 0) and b.status() == (0, 0)
+    finally:
+        a.close()
+        b.close()
