@@ -17,6 +17,8 @@ struct AppendParams {
   AppendCommon c;
   AppendItem items[MAXI];
 };
+// kernel parameter space holds at most 32764 bytes
+static_assert(sizeof(AppendParams<kAppendItemsMax>) <= 32764, "append item table too large");
 
 template <int MAXI>
 __global__ void __launch_bounds__(kAppendThreads)

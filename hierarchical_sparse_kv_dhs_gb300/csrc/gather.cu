@@ -34,6 +34,8 @@ struct GatherParams {
   GatherCommon c;
   GatherItem items[MAXI];
 };
+// kernel parameter space holds at most 32764 bytes
+static_assert(sizeof(GatherParams<kGatherItemsLarge>) <= 32764, "gather item table too large");
 
 __device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
   uint4 v;

@@ -21,6 +21,8 @@ struct CopyParams {
   CopyCommon c;
   CopyItem items[MAXI];
 };
+// kernel parameter space holds at most 32764 bytes
+static_assert(sizeof(CopyParams<kCopyItemsMax>) <= 32764, "copy item table too large");
 
 __device__ __forceinline__ uint4 ld_sys(const uint8_t* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
@@ -162,6 +164,7 @@ struct PageMoveParams {
   int32_t page_bytes;
   PageMove m[kPageMovesMax];
 };
+static_assert(sizeof(PageMoveParams) <= 32764, "page list too large");
 
 // Grid-stride over the 16-byte chunks of every listed page; each thread
 // keeps four chunks in flight so the link sees enough outstanding requests

@@ -258,6 +258,8 @@ struct ResolveParams {
   ResolveCommon c;
   ResolveItem items[MAXI];
 };
+// kernel parameter space holds at most 32764 bytes
+static_assert(sizeof(ResolveParams<kResolveItemsLarge>) <= 32764, "resolve item table too large");
 
 template <int MAXI>
 __global__ void __launch_bounds__(kResolveThreads, 1)

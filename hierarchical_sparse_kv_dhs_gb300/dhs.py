@@ -272,9 +272,9 @@ class HostRows:
         self.nbytes = max(int(nbytes), 4096)
         self._mm = mmap.mmap(-1, self.nbytes)
         if hugepages and hasattr(mmap, "MADV_HUGEPAGE"):
-            # 2 MB host pages: the GPU reads missing rows straight from this
-            # memory at random offsets, and large pages keep its address
-            # translations cached across tens of GB
+            # ask for transparent huge pages (the GPU reads missing rows from
+            # this memory at random offsets); where the kernel grants none the
+            # advice changes nothing
             try:
                 self._mm.madvise(mmap.MADV_HUGEPAGE)
             except OSError:
