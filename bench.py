@@ -441,7 +441,9 @@ def run_prefetch(args, cfg):
       serial    per layer: resolve, gather, compute (pool stream);
       prefetch  layer 0 resolved on the pool stream, every later resolving
                 layer by dhs_prefetch on a side stream at step start; per
-                layer: gather, compute.
+                layer: gather, compute;
+      pipelined as prefetch, with every gather on a second stream
+                (dhs_gather_on), overlapping the previous layer's compute.
     Device time per step from CUDA events on the pool stream."""
     import torch
     from dhs_workload.configs import Workload
@@ -472,13 +474,31 @@ def run_prefetch(args, cfg):
             run.gather_layer(step, l)
             torch.mm(A, B, out=C)
 
+    gs = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+
+    def pipelined(step):
+        # prefetch, and every layer's gather on a second stream so that it
+        # overlaps the previous layer's compute
+        run.append(step)
+        run.resolve_layer(step, layers[0])
+        if len(resolving) > 1:
+            run.prefetch_layers(step, resolving[1:])
+        for l in layers:
+            run.gather_layer(step, l, stream=gs)
+            ev = torch.cuda.Event()
+            ev.record(gs)
+            main.wait_event(ev)
+            torch.mm(A, B, out=C)
+
     def compute_only():
         for _ in layers:
             torch.mm(A, B, out=C)
 
     out = {"experiment": "prefetch", "config": workload_desc(cfg), "gemm": [n, n, n],
            "layers": len(layers), "resolving_layers": len(resolving)}
-    for name, fn in (("serial", serial), ("prefetch", prefetch), ("compute_only", None)):
+    for name, fn in (("serial", serial), ("prefetch", prefetch), ("pipelined", pipelined),
+                     ("compute_only", None)):
         run.reset()
         torch.cuda.synchronize()
         ts = []
@@ -498,6 +518,7 @@ def run_prefetch(args, cfg):
             raise RuntimeError(f"device status {rc} flags {flags}")
         out[name + "_us_median"] = statistics.median(ts)
     out["hidden_us"] = out["serial_us_median"] - out["prefetch_us_median"]
+    out["hidden_pipelined_us"] = out["serial_us_median"] - out["pipelined_us_median"]
     run.close()
     print(json.dumps(out), flush=True)
 

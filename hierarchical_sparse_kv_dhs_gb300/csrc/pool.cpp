@@ -190,10 +190,17 @@ struct dhs_pool {
   // stream waits for them before its next device work
   cudaEvent_t ev_main = nullptr, ev_prefetch = nullptr;
   bool prefetch_pending = false;
+  bool join_gathers = true;  // enter(): also join gathers on other streams
   std::vector<uint8_t> pf_pair;  // pairs resolved by the outstanding prefetch
+  // dhs_gather_on: gathers on callers' streams read rows the pool's next
+  // resolve / append / admission may change; one event per such call,
+  // joined (and recycled) by the pool's next call that can change rows
+  std::vector<cudaEvent_t> ev_free, ev_gathers;
   ~dhs_pool() {
     if (ev_main) cudaEventDestroy(ev_main);
     if (ev_prefetch) cudaEventDestroy(ev_prefetch);
+    for (cudaEvent_t e : ev_free) cudaEventDestroy(e);
+    for (cudaEvent_t e : ev_gathers) cudaEventDestroy(e);
   }
 };
 
@@ -226,6 +233,12 @@ int enter(dhs_pool* p) {
     p->prefetch_pending = false;
     std::fill(p->pf_pair.begin(), p->pf_pair.end(), 0);
   }
+  if (!p->join_gathers) return DHS_OK;
+  for (cudaEvent_t e : p->ev_gathers) {
+    if (cudaStreamWaitEvent(p->stream, e, 0) != cudaSuccess) return DHS_ECUDA;
+    p->ev_free.push_back(e);
+  }
+  p->ev_gathers.clear();
   return DHS_OK;
 }
 
@@ -1157,12 +1170,55 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   return DHS_OK;
 }
 
+// enter_step() for a gather: gathers only read rows, so gathers still
+// running on other streams need not be joined.
+int enter_gather(dhs_pool* p, const dhs_step* st) {
+  p->join_gathers = false;
+  const int rc = enter_step(p, st);
+  p->join_gathers = true;
+  return rc;
+}
+
 int dhs_gather(dhs_pool* p, const dhs_step* st) {
   int rc = validate_step(p, st, false);
   if (rc) return rc;
-  if ((rc = enter_step(p, st))) return rc;
+  if ((rc = enter_gather(p, st))) return rc;
   if ((rc = flush(p))) return rc;
   return launch_gathers(p, st, false);
+}
+
+int dhs_gather_on(dhs_pool* p, const dhs_step* st, void* stream) {
+  if (!p || !stream) return DHS_EINVAL;
+  int rc = validate_step(p, st, false);
+  if (rc) return rc;
+  if ((rc = enter_gather(p, st))) return rc;
+  if ((rc = flush(p))) return rc;
+  cudaStream_t other = (cudaStream_t)stream;
+  cudaEvent_t done = nullptr;
+  if (!p->ev_free.empty()) {
+    done = p->ev_free.back();
+    p->ev_free.pop_back();
+  } else if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) != cudaSuccess) {
+    return DHS_ECUDA;
+  }
+  // after everything the pool's stream holds (resolves, copies, appends)
+  if (cudaEventRecord(p->ev_main, p->stream) != cudaSuccess ||
+      cudaStreamWaitEvent(other, p->ev_main, 0) != cudaSuccess) {
+    p->ev_free.push_back(done);
+    return DHS_ECUDA;
+  }
+  cudaStream_t main = p->stream;
+  p->stream = other;
+  rc = launch_gathers(p, st, false);
+  p->stream = main;
+  // joined before the pool's next call that can change rows, even if the
+  // launch failed part way
+  if (cudaEventRecord(done, other) != cudaSuccess) {
+    p->ev_free.push_back(done);
+    return DHS_ECUDA;
+  }
+  p->ev_gathers.push_back(done);
+  return rc;
 }
 
 int dhs_resolve_gather(dhs_pool* p, const dhs_step* st) {

@@ -196,9 +196,15 @@ class GpuRun:
         st, _ = self._layer_steps[step - 1][layer]
         dhs.check(dhs.lib.dhs_resolve(self.pool.h, ctypes.byref(st)), "dhs_resolve")
 
-    def gather_layer(self, step, layer):
+    def gather_layer(self, step, layer, stream=None):
+        """dhs_gather of one layer, or dhs_gather_on `stream` (torch stream)."""
         st, _ = self._layer_steps[step - 1][layer]
-        dhs.check(dhs.lib.dhs_gather(self.pool.h, ctypes.byref(st)), "dhs_gather")
+        if stream is None:
+            dhs.check(dhs.lib.dhs_gather(self.pool.h, ctypes.byref(st)), "dhs_gather")
+        else:
+            dhs.check(dhs.lib.dhs_gather_on(self.pool.h, ctypes.byref(st),
+                                            ctypes.c_void_p(stream.cuda_stream)),
+                      "dhs_gather_on")
 
     def step(self, step, fused=True):
         """One decode step: append, then resolve + gather every layer -- one

@@ -378,6 +378,18 @@ int dhs_gather(dhs_pool *pool, const dhs_step *step);
 int dhs_resolve_noalloc(dhs_pool *pool, const dhs_step *step);
 
 /*
+ * dhs_gather enqueued on a caller's stream (a cudaStream_t of the pool's
+ * device) instead of the pool's: it runs after everything the pool's stream
+ * holds so far, and the pool's next call that can change rows (resolve,
+ * append, admission, reclaim, release, ...) waits for it.  With two staging
+ * buffers this lets a layer's gather overlap the previous layer's compute;
+ * the caller orders its own consumers after the gather on `stream`.
+ * Results are those of dhs_gather.  Errors: as dhs_gather, plus DHS_EINVAL
+ * for a null stream.
+ */
+int dhs_gather_on(dhs_pool *pool, const dhs_step *step, void *stream);
+
+/*
  * dhs_resolve followed by dhs_gather on the same step, with the same results.
  * The kernels overlap (programmatic dependent launch): rows that resolve in
  * step 1 (tail, ready optional page) are copied into staging while the

@@ -272,6 +272,45 @@ def test_prefetch_per_layer_pipeline_matches_oracle():
         orc.pool.close()
 
 
+def test_gathers_on_a_second_stream_match_oracle():
+    """The pipelined schedule: layer 0 resolved on the pool's stream, the
+    other resolving layers prefetched on a side stream, every layer gathered
+    on a second stream (dhs_gather_on) while the caller's work for the
+    previous layer runs on the pool's stream; then the next step's appends
+    and resolves on the pool's stream (which must wait for those gathers)."""
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    from oracle.run import OracleRun
+    cfg = SMALL[2]
+    wl = Workload(cfg)
+    gpu = GpuRun(cfg, wl)
+    orc = OracleRun(cfg, wl)
+    g = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    filler = torch.empty(1 << 24, dtype=torch.uint8, device="cuda")
+    try:
+        for step in range(1, cfg.total_steps + 1):
+            gpu.append(step)
+            gpu.resolve_layer(step, 0)
+            gpu.prefetch_layers(step, list(range(1, cfg.sources)))
+            for layer in range(len(gpu.layers)):
+                gpu.gather_layer(step, layer, stream=g)
+                ev = torch.cuda.Event()
+                ev.record(g)
+                main.wait_event(ev)  # the layer's consumer after its gather
+                filler.add_(1)
+            res = orc.step(step)
+            torch.cuda.synchronize()
+            assert gpu.status() == (0, 0)
+            loc = _as_u32(gpu.loc)
+            for r in range(cfg.requests):
+                assert np.array_equal(loc[r], res[r]["loc"]), (step, r)
+                stg = gpu.staging[r].cpu().view(torch.int16).numpy().view(np.uint16)
+                assert np.array_equal(stg, res[r]["staging"]), (step, r)
+    finally:
+        gpu.close()
+        orc.pool.close()
+
+
 def test_union_staging_failures():
     # an out-of-range row and budget overflows: empty union lists
     cfg = TINY.scaled(name="ubudget", tag=50, requests=2, sources=1, hot=16, topk=64,
