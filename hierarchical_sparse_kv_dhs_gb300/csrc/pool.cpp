@@ -939,7 +939,7 @@ static int validate_step(dhs_pool* p, const dhs_step* st, bool resolving) {
 // flushed step.  `apps` (may be null): appends folded into the resolve
 // kernel, one per pair listed in p->app_of_pair.
 static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* apps,
-                        bool fused) {
+                        bool fused, const dhs::NoallocScratch* scr = nullptr) {
   const dhs_pool_config& c = p->cfg;
   p->ritems.clear();
   p->citems.clear();
@@ -976,9 +976,11 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   rcm.tags = p->tags;
   rcm.stamps = p->stamps;
   rcm.map = p->map;
-  rcm.miss_rows = p->miss_rows;
-  rcm.miss_slots = p->miss_slots;
-  rcm.miss_count = p->miss_count;
+  // miss lists: the pool's metadata, or the fixed scratch of
+  // dhs_resolve_noalloc
+  rcm.miss_rows = scr ? scr->miss_rows : p->miss_rows;
+  rcm.miss_slots = scr ? scr->miss_slots : p->miss_slots;
+  rcm.miss_count = scr ? scr->miss_count : p->miss_count;
   rcm.pair_status = p->pair_status;
   rcm.status = p->status;
   rcm.T = c.tail_rows;
@@ -1000,9 +1002,9 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   rcm.gen = p->gen;
   dhs::CopyCommon ccm{};
   ccm.hot = (uint8_t*)c.hot_dev;
-  ccm.miss_rows = p->miss_rows;
-  ccm.miss_slots = p->miss_slots;
-  ccm.miss_count = p->miss_count;
+  ccm.miss_rows = rcm.miss_rows;
+  ccm.miss_slots = rcm.miss_slots;
+  ccm.miss_count = rcm.miss_count;
   ccm.B = c.hot_rows;
   ccm.Mcap = (int32_t)p->mcap;
   ccm.row_bytes = c.row_bytes;
@@ -1367,76 +1369,5 @@ extern "C" int dhs_resolve_noalloc(dhs_pool* p, const dhs_step* st) {
   dhs::NoallocScratch scr{};
   if (dhs::noalloc_scratch(&scr) != cudaSuccess) return DHS_ECUDA;
   if ((rc = flush(p))) return rc;
-  const dhs_pool_config& c = p->cfg;
-  std::vector<dhs::ResolveItem> ritems;
-  std::vector<dhs::CopyItem> citems;
-  for (int32_t i = 0; i < st->n_items; ++i) {
-    const dhs_item& it = st->items[i];
-    if (it.flags & DHS_ITEM_GATHER_ONLY) continue;
-    const int64_t pair = (int64_t)it.req * c.sources + it.src;
-    const PairState& s = p->ps[pair];
-    dhs::ResolveItem r{};
-    r.sel = it.sel_dev;
-    r.loc = it.loc_dev;
-    r.counters = it.counters_dev;
-    r.index = (it.flags & DHS_ITEM_UNION) ? it.index_dev : nullptr;
-    r.L = s.L;
-    r.N = s.N;
-    r.pair = (int32_t)pair;
-    r.n = it.queries * it.topk;
-    ritems.push_back(r);
-    dhs::CopyItem ci{};
-    ci.host = s.host_dev;
-    ci.pair = (int32_t)pair;
-    citems.push_back(ci);
-  }
-  dhs::ResolveCommon rcm{};
-  rcm.tags = p->tags;
-  rcm.stamps = p->stamps;
-  rcm.map = p->map;
-  rcm.miss_rows = scr.miss_rows;
-  rcm.miss_slots = scr.miss_slots;
-  rcm.miss_count = scr.miss_count;
-  rcm.pair_status = p->pair_status;
-  rcm.status = p->status;
-  rcm.T = c.tail_rows;
-  rcm.B = c.hot_rows;
-  rcm.Pmax = (int32_t)p->pmax;
-  rcm.Mcap = (int32_t)p->mcap;
-  rcm.page_shift = p->page_shift;
-  rcm.step = st->step;
-  dhs::CopyCommon ccm{};
-  ccm.hot = (uint8_t*)c.hot_dev;
-  ccm.miss_rows = scr.miss_rows;
-  ccm.miss_slots = scr.miss_slots;
-  ccm.miss_count = scr.miss_count;
-  ccm.B = c.hot_rows;
-  ccm.Mcap = (int32_t)p->mcap;
-  ccm.row_bytes = c.row_bytes;
-  const size_t nr = ritems.size();
-  for (size_t b = 0; b < nr; b += dhs::kResolveItemsLarge) {
-    const int n = (int)std::min<size_t>(dhs::kResolveItemsLarge, nr - b);
-    int64_t wmax = 0, qmax = 0, requests = 0, last_req = -1;
-    bool uni = false;
-    for (int i = 0; i < n; ++i) {
-      const dhs::ResolveItem& r = ritems[b + i];
-      uni |= r.index != nullptr;
-      wmax = std::max<int64_t>(wmax, (r.L + 63) / 64);
-      qmax = std::max<int64_t>(qmax, std::min<int64_t>(r.n, r.L));
-      const int64_t req = r.pair / c.sources;
-      if (req != last_req) ++requests;
-      last_req = req;
-    }
-    rcm.w64cap = (int32_t)wmax;
-    rcm.qkcap = (int32_t)qmax;
-    rcm.uni = uni ? 1 : 0;
-    const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni);
-    if (dhs::launch_resolve(rcm, ritems.data() + b, n, smem, p->stream) != cudaSuccess)
-      return DHS_ECUDA;
-    int ctas = p->copy_ctas;
-    if (ctas <= 0) ctas = default_copy_ctas(requests);
-    if (dhs::launch_hostcopy(ccm, citems.data() + b, n, ctas, true, p->stream) != cudaSuccess)
-      return DHS_ECUDA;
-  }
-  return DHS_OK;
+  return resolve_impl(p, st, nullptr, false, &scr);
 }
