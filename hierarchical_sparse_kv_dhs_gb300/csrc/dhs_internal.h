@@ -142,6 +142,9 @@ struct CopyCommon {
   const uint32_t* miss_count;
   int32_t B, Mcap, row_bytes, n_items;
   unsigned long long* trace;  // null = off
+  const uint32_t* loc_ready;  // [pairs] the resolve launch's per-item marks, null = none
+  uint32_t seq;               // that launch's sequence number
+  int32_t pad;
 };
 
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,

@@ -3,12 +3,11 @@
 //
 // Reads the missing rows straight out of mapped pinned host memory over
 // NVLink-C2C into their victim hot-cache slots.  The pages note that the
-// copy kernel scales from 4 to 32 thread blocks with batch size; the grid
-// here scales the same way up to 32 blocks but never goes below 16
-// (clamp(requests / 4, 16, 32)): fewer rows in flight leave the host link
-// idle on GB300.  It can be overridden for sweeps.  Each warp keeps up to four 1152-byte rows
-// in flight (12 x 16-byte loads per lane) so the link sees enough
-// outstanding requests to cover its latency.
+// copy kernel scales from 4 to 32 thread blocks with batch size; on GB300
+// fewer than about 16 blocks leave the host link idle, so the grid is the
+// upper end, 32 blocks, whatever the batch (overridable for sweeps).  Each
+// warp keeps up to four 1152-byte rows in flight (12 x 16-byte loads per
+// lane) so the link sees enough outstanding requests to cover its latency.
 #include <algorithm>
 
 #include "dhs_internal.h"
@@ -31,105 +30,135 @@ __device__ __forceinline__ uint4 ld_sys(const uint8_t* p) {
 constexpr int kRowsPerWarp = 4;
 constexpr int kChunksPerLane = 3;  // rows up to 96 x 16 = 1536 bytes
 
+constexpr uint32_t kReadyPolls = 1u << 20;
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Copy the miss rows of the launch's items.  CTA b owns items b, b + gridDim,
+// ...  An item's miss list (rows ascending, victim slots) is complete once
+// the resolve kernel has published the item's locations (loc_ready == seq,
+// after a fence), so the CTA does not wait for the whole resolve grid: it
+// takes, in order, every owned item whose mark is out as one batch (waiting,
+// bounded, only when none is), and its warps copy the batch's rows as one
+// flat list, four rows per warp in flight.  A poll that runs out falls back
+// to waiting for the resolve grid.
+constexpr int kBatchMax = 64;
+
 template <int MAXI, bool kSmallRow>
 __global__ void __launch_bounds__(kCopyThreads)
     hostcopy_kernel(const __grid_constant__ CopyParams<MAXI> P) {
-  __shared__ uint32_t s_pre[MAXI + 1];
-  __shared__ uint32_t s_scr[33];
+  __shared__ int s_n, s_next, s_wait;
+  __shared__ int s_item[kBatchMax];
+  __shared__ uint32_t s_pre[kBatchMax + 1];
   const CopyCommon& c = P.c;
   const int tid = threadIdx.x, lane = tid & 31;
-  const int n_items = c.n_items;
-
-  // The gather may be launched now; the miss lists are read only after the
-  // resolve grid has finished writing them.
+  // the gather may be launched now
   asm volatile("griddepcontrol.launch_dependents;");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0) trace_mark(c.trace, kTraceCopy, false);  // the copy phase starts
-
-  // prefix of the per-item miss counts (n_items <= blockDim.x)
-  const uint32_t mine = tid < n_items ? c.miss_count[P.items[tid].pair] : 0u;
-  {
-    const int warp = tid >> 5, nw = blockDim.x >> 5;
-    uint32_t v = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
-      if (lane >= o) v += t;
-    }
-    if (lane == 31) s_scr[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t w = lane < nw ? s_scr[lane] : 0u;
-      uint32_t wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        uint32_t t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-        if (lane >= o) wi += t;
-      }
-      if (lane < nw) s_scr[lane] = wi - w;
-    }
-    __syncthreads();
-    if (tid < n_items) s_pre[tid + 1] = s_scr[warp] + v;
-    if (tid == 0) s_pre[0] = 0u;
-    __syncthreads();
-  }
-  const uint32_t total = s_pre[n_items];
-  if (total == 0) {
-    if (tid == 0) trace_mark(c.trace, kTraceCopy, true);
-    return;
-  }
-
   const int rb = c.row_bytes;
   const int cpr = rb >> 4;
-  const uint32_t gwarp = (blockIdx.x * blockDim.x + tid) >> 5;
-  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (uint32_t base = gwarp * kRowsPerWarp; base < total; base += nwarps * kRowsPerWarp) {
-    const uint8_t* src[kRowsPerWarp];
-    uint8_t* dst[kRowsPerWarp];
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const uint32_t i = base + r;
-      src[r] = nullptr;
-      dst[r] = nullptr;
-      if (i < total) {
-        int lo = 0, hi = n_items - 1;  // last item with s_pre[item] <= i
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (s_pre[mid] <= i) lo = mid; else hi = mid - 1;
+  const uint32_t warp = (uint32_t)tid >> 5, nwarps = blockDim.x >> 5;
+  const uint32_t want = c.seq & kSeqMask;
+  bool waited = c.loc_ready == nullptr, traced = false;
+  if (waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+  int next = blockIdx.x;
+  for (;;) {
+    if (tid == 0) {  // the next batch: owned items whose miss lists are out
+      int n = 0, j = next, need_wait = 0;
+      uint32_t acc = 0;
+      while (j < c.n_items && n < kBatchMax) {
+        const uint32_t* mark = c.loc_ready + P.items[j].pair;
+        bool ok = waited || ld_acquire_u32(mark) == want;
+        for (uint32_t i = 0; !ok && n == 0 && i < kReadyPolls; ++i) {
+          __nanosleep(256);
+          ok = ld_acquire_u32(mark) == want;
         }
-        const CopyItem& it = P.items[lo];
-        const uint32_t mi = i - s_pre[lo];
-        const size_t off = (size_t)it.pair * c.Mcap + mi;
-        const int32_t row = c.miss_rows[off];
-        const int32_t slot = c.miss_slots[off];
-        src[r] = it.host + (size_t)row * rb;
-        dst[r] = c.hot + ((size_t)it.pair * c.B + slot) * rb;
+        if (!ok) {
+          need_wait = n == 0;
+          break;
+        }
+        s_item[n] = j;
+        s_pre[n] = acc;
+        acc += c.miss_count[P.items[j].pair];
+        ++n;
+        j += gridDim.x;
       }
+      s_pre[n] = acc;
+      s_n = n;
+      s_next = j;
+      s_wait = need_wait;
     }
-    if (kSmallRow) {
-      uint4 v[kRowsPerWarp][kChunksPerLane];
+    __syncthreads();
+    if (s_wait) {  // a mark never came: wait for the resolve grid, then go on
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+      __syncthreads();
+      continue;
+    }
+    const int n = s_n, nxt = s_next;
+    if (n == 0) break;
+    if (!waited)  // each thread's own acquire of the batch's marks
+      for (int b = 0; b < n; ++b) (void)ld_acquire_u32(c.loc_ready + P.items[s_item[b]].pair);
+    if (tid == 0 && !traced) {
+      trace_mark(c.trace, kTraceCopy, false);  // copying starts
+      traced = true;
+    }
+    const uint32_t total = s_pre[n];
+    for (uint32_t base = warp * kRowsPerWarp; base < total; base += nwarps * kRowsPerWarp) {
+      const uint8_t* src[kRowsPerWarp];
+      uint8_t* dst[kRowsPerWarp];
 #pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-        for (int q = 0; q < kChunksPerLane; ++q) {
-          const int ch = lane + 32 * q;
-          if (src[r] && ch < cpr) v[r][q] = ld_sys(src[r] + ch * 16);
-        }
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-        for (int q = 0; q < kChunksPerLane; ++q) {
-          const int ch = lane + 32 * q;
-          if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
-        }
-    } else {
       for (int r = 0; r < kRowsPerWarp; ++r) {
-        if (!src[r]) continue;
-        for (int ch = lane; ch < cpr; ch += 32)
-          *reinterpret_cast<uint4*>(dst[r] + ch * 16) = ld_sys(src[r] + ch * 16);
+        const uint32_t i = base + r;
+        src[r] = nullptr;
+        dst[r] = nullptr;
+        if (i < total) {
+          int lo = 0, hi = n - 1;  // last batch entry with s_pre <= i
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_pre[mid] <= i) lo = mid; else hi = mid - 1;
+          }
+          const CopyItem& it = P.items[s_item[lo]];
+          const size_t off = (size_t)it.pair * c.Mcap + (i - s_pre[lo]);
+          const int32_t row = c.miss_rows[off];
+          const int32_t slot = c.miss_slots[off];
+          src[r] = it.host + (size_t)row * rb;
+          dst[r] = c.hot + ((size_t)it.pair * c.B + slot) * rb;
+        }
+      }
+      if (kSmallRow) {
+        uint4 v[kRowsPerWarp][kChunksPerLane];
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+          for (int q = 0; q < kChunksPerLane; ++q) {
+            const int ch = lane + 32 * q;
+            if (src[r] && ch < cpr) v[r][q] = ld_sys(src[r] + ch * 16);
+          }
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+          for (int q = 0; q < kChunksPerLane; ++q) {
+            const int ch = lane + 32 * q;
+            if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
+          }
+      } else {
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+          if (!src[r]) continue;
+          for (int ch = lane; ch < cpr; ch += 32)
+            *reinterpret_cast<uint4*>(dst[r] + ch * 16) = ld_sys(src[r] + ch * 16);
+        }
       }
     }
+    __syncthreads();  // the batch tables are rebuilt
+    next = nxt;
   }
+  // this grid completes only after the resolve grid (the gather and the
+  // fresh-row copy rely on that)
+  if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
   if (tid == 0) trace_mark(c.trace, kTraceCopy, true);
 }

@@ -208,14 +208,14 @@ namespace {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? DHS_OK : DHS_ECUDA; }
 
-// Host-copy grid: the pages' scaling with batch (requests / 4, up to 32
-// blocks) with a floor of 16 blocks -- 1024 rows in flight, about the
-// bytes the host link needs in flight at its bandwidth and latency (on the
-// miss-heavy workload 4 blocks reach 78 GB/s, 8 reach 130, 16 reach 188 and
-// 32 reach 198 of the 211 GB/s pinned host-to-device peak).
-int default_copy_ctas(int64_t requests) {
-  return (int)std::min<int64_t>(32, std::max<int64_t>(16, requests / 4));
-}
+// Host-copy grid: the upper end of the pages' 4-to-32-block scaling.  On
+// GB300 the host link needs about 1024 rows in flight (16 blocks x 16 warps x
+// 4 rows); below that the copy is latency-bound (miss-heavy workload: 4
+// blocks 78 GB/s, 8 130, 16 188, 32 198 of the 211 GB/s pinned peak), and in
+// same-box runs 32 blocks were as fast as or faster than 16 on every
+// workload with misses (warm steps: C64 1969 vs 2066 us, C128 640 vs 627,
+// miss-heavy 147 vs 152), so the grid does not shrink with the batch.
+int default_copy_ctas(int64_t /*requests*/) { return 32; }
 
 // Pages small enough for the page-move kernel's 32-bit chunk arithmetic.
 bool small_pages(const dhs_pool* p) {
@@ -1027,6 +1027,8 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     rcm.qkcap = (int32_t)qmax;
     rcm.seq = ++p->seq & dhs::kSeqMask;
     if (rcm.seq == 0) rcm.seq = p->seq = 1;  // 0 never matches a published verdict
+    ccm.loc_ready = rcm.loc_ready;  // the copy starts on each item once it is resolved
+    ccm.seq = rcm.seq;
     for (int i = 0; i < n; ++i) p->seq_of_pair[p->ritems[b + i].pair] = rcm.seq;
     rcm.uni = uni ? 1 : 0;
     const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni);

@@ -242,9 +242,9 @@ __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t
   if (threadIdx.x < 8 && it.counters) it.counters[threadIdx.x] = 0u;
   __syncthreads();
   if (threadIdx.x == 0) {
-    publish_loc(c, it.pair);
-    c.miss_count[it.pair] = 0u;
+    c.miss_count[it.pair] = 0u;  // before the mark: the host copy reads it then
     c.pair_status[it.pair] = code;
+    publish_loc(c, it.pair);
     publish(c, it.pair, code == kErrRange ? kVerdictRange : kVerdictBudget);
     atomicOr(c.status, flag);
     trace_mark(c.trace, kTraceResolve, true);
@@ -529,7 +529,13 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
     for (int u = (int)n_unique + tid; u < n; u += nt) it.loc[u] = kEndLoc;
   }
   __syncthreads();
-  if (tid == 0) publish_loc(c, pair);
+  if (tid == 0) {
+    // everything the host copy and the gather read of this item -- miss
+    // lists, fill marks, locations, appended rows -- is written before the mark
+    c.miss_count[pair] = m_miss;
+    c.pair_status[pair] = 0;
+    publish_loc(c, pair);
+  }
 
   if (m_miss) {
     uint32_t ev[4] = {evicted, 0u, 0u, 0u};
@@ -547,8 +553,6 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
       it.counters[6] = scan_max;
       it.counters[7] = evicted;
     }
-    c.miss_count[pair] = m_miss;
-    c.pair_status[pair] = 0;
     trace_mark(c.trace, kTraceResolve, true);
   }
 }

@@ -450,7 +450,7 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
                    uint32_t *stamps, int32_t *page_slot, int64_t *info);
 
 /* Tunables (performance only; results do not depend on them). */
-#define DHS_OPT_COPY_CTAS 1 /* host-copy CTAs; 0 = clamp(requests/4, 16, 32) */
+#define DHS_OPT_COPY_CTAS 1 /* host-copy CTAs; 0 = 32 */
 #define DHS_OPT_GATHER_IMPL 2 /* 1 = TMA bulk copy, one warp per 32-row tile
                                      (default); 0 = 16-byte vector copy, 256
                                      threads per tile */
