@@ -78,3 +78,23 @@ def test_null_arguments(dhs):
     assert dhs.lib.dhs_flush(None) == dhs.DHS_EINVAL
     assert dhs.lib.dhs_pool_used(None) == -1
     dhs.lib.dhs_pool_destroy(None)
+    # every other entry point refuses a null pool before touching a device
+    n64 = ctypes.c_int64(0)
+    E = dhs.DHS_EINVAL
+    assert dhs.lib.dhs_admit(None, 0, 0, None, 0, None, ctypes.byref(n64)) == E
+    assert dhs.lib.dhs_admit_device(None, 0, 0, None, None, 0, None, ctypes.byref(n64)) == E
+    assert dhs.lib.dhs_reclaim(None, None, 0, 0, ctypes.byref(n64)) == E
+    assert dhs.lib.dhs_release(None, 0) == E
+    assert dhs.lib.dhs_backup(None, 1, ctypes.byref(n64)) == E
+    assert dhs.lib.dhs_refill(None, 1, ctypes.byref(n64)) == E
+    assert dhs.lib.dhs_pending_backup(None) == -1
+    assert dhs.lib.dhs_append(None, None, 0) == E
+    for fn in ("dhs_resolve", "dhs_gather", "dhs_resolve_gather", "dhs_resolve_noalloc"):
+        assert getattr(dhs.lib, fn)(None, None) == E, fn
+    assert dhs.lib.dhs_decode_step(None, None, 0, None) == E
+    assert dhs.lib.dhs_decode_step_host(None, None, 0, None, 0, None, None, 0) == E
+    assert dhs.lib.dhs_prefetch(None, None, None) == E
+    assert dhs.lib.dhs_gather_on(None, None, None) == E
+    assert dhs.lib.dhs_set_option(None, dhs.DHS_OPT_EARLY, 1) == E
+    assert dhs.lib.dhs_get_option(None, dhs.DHS_OPT_EARLY, ctypes.byref(n64)) == E
+    assert dhs.lib.dhs_read_state(None, 0, 0, None, None, None, None) == E
