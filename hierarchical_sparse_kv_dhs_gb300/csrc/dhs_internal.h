@@ -216,7 +216,9 @@ cudaError_t launch_gather(const GatherCommon& c, const GatherItem* items,
 cudaError_t launch_gather_later(const GatherCommon& c, int ctas, cudaStream_t stream);
 
 // Raise the TMA gather's dynamic shared-memory limit for a row size.
-cudaError_t gather_set_smem_limit(int row_bytes);
+// *tma_ok: whether the TMA gather's 32-row tile of this row size fits in
+// `optin` bytes of shared memory per block (else only the vector gather runs).
+cudaError_t gather_set_smem_limit(int row_bytes, int optin, bool* tma_ok);
 
 // ------------------------------------------------------------ append (A0)
 constexpr int kAppendThreads = 256;

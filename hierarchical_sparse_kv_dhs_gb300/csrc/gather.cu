@@ -24,6 +24,8 @@
 // overflow) as soon as it is decided; after its early copies a tile reads its
 // item's verdict -- or waits for the resolve grid if it is not out yet -- and
 // a failed item's rows become zeros, exactly as its locations say.
+#include <algorithm>
+
 #include "dhs_internal.h"
 
 namespace dhs {
@@ -519,14 +521,16 @@ cudaError_t gather_set_carveout() {
   return cudaSuccess;
 }
 
-cudaError_t gather_set_smem_limit(int row_bytes) {
+cudaError_t gather_set_smem_limit(int row_bytes, int optin, bool* tma_ok) {
   const int bytes = kGatherTileRows * row_bytes;
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute((const void*)gather_tma_kernel<kGatherItemsSmall>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute((const void*)gather_tma_kernel<kGatherItemsLarge>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  *tma_ok = bytes + 1024 <= optin;  // 1 KB for the kernel's static shared memory
+  if (!*tma_ok || bytes <= 48 * 1024) return cudaSuccess;
+  for (const void* f : {(const void*)gather_tma_kernel<kGatherItemsSmall>,
+                        (const void*)gather_tma_kernel<kGatherItemsLarge>}) {
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_gather(const GatherCommon& c, const GatherItem* items, int n_items,

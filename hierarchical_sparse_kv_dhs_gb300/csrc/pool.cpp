@@ -157,6 +157,7 @@ struct dhs_pool {
   int copy_ctas = 0;
   bool union_ok = false;  // the union staging plan fits in shared memory
   int gather_impl = dhs::kGatherTma;
+  bool tma_ok = true;  // the TMA gather's tile fits the row size
   int gather_tpc = 1;   // DHS_OPT_GATHER_TPC
   int early = 1;        // fused gathers copy step-1 rows before the resolve ends
   uint32_t* verdict = nullptr;  // [pairs] resolve verdicts for the fused gather
@@ -465,6 +466,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
   try {
     p->cfg = *cfg;
     p->union_ok = union_ok;
+    p->gather_impl = dhs::kGatherTma;
     p->sm_count = sms;
     p->stream = (cudaStream_t)cfg->stream;
     p->device = dev;
@@ -507,12 +509,13 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     delete p;
     return DHS_ECUDA;
   }
-  if (dhs::gather_set_smem_limit(cfg->row_bytes) != cudaSuccess ||
+  if (dhs::gather_set_smem_limit(cfg->row_bytes, optin, &p->tma_ok) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->ev_main, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->ev_prefetch, cudaEventDisableTiming) != cudaSuccess) {
     delete p;
     return DHS_ECUDA;
   }
+  if (!p->tma_ok) p->gather_impl = dhs::kGatherVector;  // rows too large to stage a tile
   // empty hot caches (tag -1, stamp 0), no ready pages, zero counts/status
   cudaError_t e = cudaMemsetAsync(p->tags, 0xFF, p->pairs * cfg->hot_rows * 4, p->stream);
   if (e == cudaSuccess)
@@ -551,7 +554,8 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     return DHS_OK;
   }
   if (key == DHS_OPT_GATHER_IMPL) {
-    if (value != dhs::kGatherVector && value != dhs::kGatherTma) return DHS_EINVAL;
+    if (value != dhs::kGatherVector && !(value == dhs::kGatherTma && pool->tma_ok))
+      return DHS_EINVAL;
     pool->gather_impl = (int)value;
     return DHS_OK;
   }
@@ -572,8 +576,10 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
 // grid (one launch more per step).  Auto: when more than a tenth of the
 // admitted complete pages are not optional-resident, so that host copies are
 // expected every step.
+static bool tma_gather(const dhs_pool* p) { return p->gather_impl == dhs::kGatherTma; }
+
 static bool use_fresh_list(const dhs_pool* p) {
-  if (p->gather_impl != dhs::kGatherTma || !p->early) return false;
+  if (!tma_gather(p) || !p->early) return false;
   if (p->fresh_list >= 0) return p->fresh_list == 1;
   return (p->complete_pages - p->used) * 10 > p->complete_pages;
 }
@@ -1112,7 +1118,7 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   g.tpc = p->gather_tpc;
   // the step's resolved items publish their locations; gathers of them (and
   // Reuse items handed the same location vector) may go before the grids end
-  const bool lr = fused && p->early && p->fused_resolved && p->gather_impl == dhs::kGatherTma;
+  const bool lr = fused && p->early && p->fused_resolved && tma_gather(p);
   g.later = lr && use_fresh_list(p) ? p->later : nullptr;
   std::unordered_map<const void*, int64_t> loc_pair;
   if (lr)

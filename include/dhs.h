@@ -453,7 +453,8 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
 #define DHS_OPT_COPY_CTAS 1 /* host-copy CTAs; 0 = 32 */
 #define DHS_OPT_GATHER_IMPL 2 /* 1 = TMA bulk copy, one warp per 32-row tile
                                      (default); 0 = 16-byte vector copy, 256
-                                     threads per tile */
+                                     threads per tile (the only one for rows
+                                     too large to stage 32 of them) */
 /* Timeline: value = address of a device buffer of 8 uint64 (0 = off).  Each
  * kernel kind k (0 resolve, 1 host copy, 2 gather, 3 fresh-row copy) atomically
  * lowers buf[2k]
