@@ -456,3 +456,21 @@ def test_decode_step_host_matches_device_path():
     finally:
         a.close()
         b.close()
+
+
+def test_rows_too_large_for_a_tma_tile_use_the_vector_gather():
+    """8 KB rows: 32 of them do not fit in a block's shared memory, so the
+    pool refuses the TMA gather and runs the vector gather, bit-exact."""
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    cfg = TINY.scaled(name="bigrows", tag=51, row_elems=4096, history=1024, tail=16,
+                      hot=128, topk=64, steps=4, requests=2)
+    gpu = GpuRun(cfg, Workload(cfg))
+    try:
+        assert gpu.pool.get_option(dhs.DHS_OPT_GATHER_IMPL) == 0
+        with pytest.raises(Exception):
+            gpu.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, 1)
+    finally:
+        gpu.close()
+    compare_run(cfg, gather_impl=0)
+    compare_run(cfg, gather_impl=0, fused=False)
