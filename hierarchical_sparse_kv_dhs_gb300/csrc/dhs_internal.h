@@ -75,7 +75,8 @@ struct ResolveItem {
   uint8_t* app_host;        // device-visible pointer of the pair's host rows
   int64_t app_L0;           // length before the append
   int32_t app_count;
-  int32_t pad;
+  int32_t stage;   // list, per miss, the entries that selected it (host copy
+                   // writes them into staging)
   int32_t* index;  // union staging: [n] union rank of each entry; null = per-query
 };
 
@@ -105,6 +106,10 @@ struct ResolveCommon {
   uint32_t* later_count; // [2] fresh-row list lengths; the launch zeroes [gen ^ 1]
   int32_t fill_words;
   uint32_t gen;          // fused-step generation (parity picks the list counter)
+  int32_t* miss_off;     // [pairs][Mcap + 1] per miss: first entry in miss_ent
+  int32_t* miss_ent;     // [pairs][ent_cap] staging entries of the misses
+  int32_t ent_cap;
+  int32_t pad3;
 };
 
 size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni);
@@ -131,6 +136,7 @@ constexpr int kCopyItemsMax = 256;
 
 struct CopyItem {
   const uint8_t* host;  // device-visible pointer of the pair's pinned host rows
+  uint8_t* staging;     // also write each miss row to its staging entries; null = no
   int32_t pair;
   int32_t pad;
 };
@@ -144,7 +150,9 @@ struct CopyCommon {
   unsigned long long* trace;  // null = off
   const uint32_t* loc_ready;  // [pairs] the resolve launch's per-item marks, null = none
   uint32_t seq;               // that launch's sequence number
-  int32_t pad;
+  int32_t ent_cap;
+  const int32_t* miss_off;    // [pairs][Mcap + 1] (items with staging)
+  const int32_t* miss_ent;    // [pairs][ent_cap]
 };
 
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,
@@ -173,6 +181,8 @@ struct GatherItem {
 // The item's locations are those of a pair resolved by the preceding resolve
 // launch of the same fused step, published through loc_ready[pair] == seq.
 constexpr uint32_t kGiLocReady = 1u;
+// The host copy writes the item's fresh rows into its staging itself.
+constexpr uint32_t kGiStaged = 2u;
 
 struct GatherCommon {
   const uint8_t* tail;

@@ -397,20 +397,21 @@ __global__ void __launch_bounds__(kTmaThreads)
       const bool fresh = deferred && fresh_loc(c, l);
       const bool now = deferred && l != kEndLoc && !fresh;
       ok = move(now, now ? row_ptr(c, l) : nullptr);
-      bool later = fresh;
+      // the host copy writes a staged item's fresh rows into staging itself
+      bool later = fresh && !(it.flags & kGiStaged);
       if (c.later) {  // hand the fresh rows to the list copied after the copy grid
-        const unsigned fm = __ballot_sync(0xFFFFFFFFu, fresh);
+        const unsigned fm = __ballot_sync(0xFFFFFFFFu, later);
         uint32_t base = 0;
         if (lane == 0 && fm) base = atomicAdd(&c.later_count[c.gen & 1u], (uint32_t)__popc(fm));
         base = __shfl_sync(0xFFFFFFFFu, base, 0);
         const uint32_t cnt = (uint32_t)__popc(fm);
         const bool fits = (uint64_t)base + cnt <= c.later_cap;
         const uint32_t slot = base + (uint32_t)__popc(fm & ((1u << lane) - 1u));
-        if (fresh && fits) {
+        if (later && fits) {
           c.later[slot].dst = dst;
           c.later[slot].loc = l;
           later = false;
-        } else if (fresh && slot < c.later_cap) {
+        } else if (later && slot < c.later_cap) {
           c.later[slot].dst = nullptr;  // the list is full: the tile copies it
         }
       }

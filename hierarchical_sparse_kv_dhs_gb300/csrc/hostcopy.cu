@@ -110,11 +110,19 @@ __global__ void __launch_bounds__(kCopyThreads)
     for (uint32_t base = warp * kRowsPerWarp; base < total; base += nwarps * kRowsPerWarp) {
       const uint8_t* src[kRowsPerWarp];
       uint8_t* dst[kRowsPerWarp];
+      // staging entries of the row (items whose host copy stages): the
+      // entries e0 .. e1 of the item's miss_ent list, written at stg + e * rb
+      uint8_t* stg[kRowsPerWarp];
+      const int32_t* ents[kRowsPerWarp];
+      int32_t e0[kRowsPerWarp], e1[kRowsPerWarp];
 #pragma unroll
       for (int r = 0; r < kRowsPerWarp; ++r) {
         const uint32_t i = base + r;
         src[r] = nullptr;
         dst[r] = nullptr;
+        stg[r] = nullptr;
+        ents[r] = nullptr;
+        e0[r] = e1[r] = 0;
         if (i < total) {
           int lo = 0, hi = n - 1;  // last batch entry with s_pre <= i
           while (lo < hi) {
@@ -122,11 +130,19 @@ __global__ void __launch_bounds__(kCopyThreads)
             if (s_pre[mid] <= i) lo = mid; else hi = mid - 1;
           }
           const CopyItem& it = P.items[s_item[lo]];
-          const size_t off = (size_t)it.pair * c.Mcap + (i - s_pre[lo]);
+          const uint32_t mi = i - s_pre[lo];
+          const size_t off = (size_t)it.pair * c.Mcap + mi;
           const int32_t row = c.miss_rows[off];
           const int32_t slot = c.miss_slots[off];
           src[r] = it.host + (size_t)row * rb;
           dst[r] = c.hot + ((size_t)it.pair * c.B + slot) * rb;
+          if (it.staging) {
+            const int32_t* mo = c.miss_off + (size_t)it.pair * (c.Mcap + 1);
+            stg[r] = it.staging;
+            ents[r] = c.miss_ent + (size_t)it.pair * c.ent_cap;
+            e0[r] = mo[mi];
+            e1[r] = mo[mi + 1];
+          }
         }
       }
       if (kSmallRow) {
@@ -139,17 +155,30 @@ __global__ void __launch_bounds__(kCopyThreads)
             if (src[r] && ch < cpr) v[r][q] = ld_sys(src[r] + ch * 16);
           }
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r)
+        for (int r = 0; r < kRowsPerWarp; ++r) {
 #pragma unroll
           for (int q = 0; q < kChunksPerLane; ++q) {
             const int ch = lane + 32 * q;
             if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
           }
+          for (int k = e0[r]; k < e1[r]; ++k) {  // the same bytes to its staging entries
+            uint8_t* to = stg[r] + (size_t)ents[r][k] * rb;
+#pragma unroll
+            for (int q = 0; q < kChunksPerLane; ++q) {
+              const int ch = lane + 32 * q;
+              if (ch < cpr) *reinterpret_cast<uint4*>(to + ch * 16) = v[r][q];
+            }
+          }
+        }
       } else {
         for (int r = 0; r < kRowsPerWarp; ++r) {
           if (!src[r]) continue;
-          for (int ch = lane; ch < cpr; ch += 32)
-            *reinterpret_cast<uint4*>(dst[r] + ch * 16) = ld_sys(src[r] + ch * 16);
+          for (int ch = lane; ch < cpr; ch += 32) {
+            const uint4 v = ld_sys(src[r] + ch * 16);
+            *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v;
+            for (int k = e0[r]; k < e1[r]; ++k)
+              *reinterpret_cast<uint4*>(stg[r] + (size_t)ents[r][k] * rb + ch * 16) = v;
+          }
         }
       }
     }

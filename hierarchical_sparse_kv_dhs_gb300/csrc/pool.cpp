@@ -38,7 +38,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct MetaLayout {
   size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status, verdict;
-  size_t loc_ready, fill, later_count, status, later;
+  size_t loc_ready, fill, later_count, status, later, miss_off, miss_ent;
   size_t total;
 };
 
@@ -52,6 +52,11 @@ inline int64_t fill_words_of(const dhs_pool_config& c) { return (c.hot_rows + 31
 // that copy their fresh rows in their own tiles).
 inline int64_t later_cap_of(const dhs_pool_config& c) {
   return std::max<int64_t>(1, (int64_t)c.max_requests * c.sources * c.max_queries * c.max_topk);
+}
+
+// Staging entries one resolve of a (request, source) can list.
+inline int64_t ent_cap_of(const dhs_pool_config& c) {
+  return std::max<int64_t>(1, (int64_t)c.max_queries * c.max_topk);
 }
 
 inline int64_t mcap_of(const dhs_pool_config& c) {
@@ -81,6 +86,8 @@ MetaLayout meta_layout(const dhs_pool_config& c) {
   m.later_count = take(2 * 4);
   m.status = take(64);
   m.later = take((size_t)later_cap_of(c) * sizeof(dhs::LaterEntry));
+  m.miss_off = take(pairs * (size_t)(mcap_of(c) + 1) * 4);
+  m.miss_ent = take(pairs * (size_t)ent_cap_of(c) * 4);
   m.total = off;
   return m;
 }
@@ -176,6 +183,11 @@ struct dhs_pool {
   std::set<std::pair<uint64_t, int64_t>> backup_order;  // (order, pair * pmax + page)
   int32_t rr = 0;               // refill cursor: the next request visited
   int sm_count = 0;
+  int32_t* miss_off = nullptr;  // [pairs][Mcap + 1] staging entries of each miss
+  int32_t* miss_ent = nullptr;  // [pairs][ent_cap]
+  int64_t ent_cap = 0;
+  int stage_misses = 1;         // DHS_OPT_STAGE_MISSES
+  std::vector<uint8_t> staged_pair;  // the host copy stages this pair's misses this step
   unsigned long long* trace = nullptr;  // DHS_OPT_TRACE buffer, null = off
   // reusable launch tables
   std::vector<dhs::ResolveItem> ritems;
@@ -490,6 +502,9 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->later = (dhs::LaterEntry*)(m + p->layout.later);
     p->later_cap = later_cap_of(*cfg);
     p->fill_words = (int)fill_words_of(*cfg);
+    p->miss_off = (int32_t*)(m + p->layout.miss_off);
+    p->miss_ent = (int32_t*)(m + p->layout.miss_ent);
+    p->ent_cap = ent_cap_of(*cfg);
     p->status = (uint32_t*)(m + p->layout.status);
     p->ps.resize(p->pairs);
     p->map_host.assign((size_t)(p->pairs * p->pmax), -1);
@@ -500,6 +515,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->l0_of_pair.assign((size_t)p->pairs, 0);
     p->seq_of_pair.assign((size_t)p->pairs, 0);
     p->pf_pair.assign((size_t)p->pairs, 0);
+    p->staged_pair.assign((size_t)p->pairs, 0);
   } catch (...) {
     delete p;
     return DHS_ENOMEM;
@@ -564,6 +580,11 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     pool->fresh_list = (int)value;
     return DHS_OK;
   }
+  if (key == DHS_OPT_STAGE_MISSES) {
+    if (value < 0 || value > 1) return DHS_EINVAL;
+    pool->stage_misses = (int)value;
+    return DHS_OK;
+  }
   if (key == DHS_OPT_GATHER_TPC) {
     if (value < 1 || value > 64) return DHS_EINVAL;
     pool->gather_tpc = (int)value;
@@ -593,6 +614,7 @@ int dhs_get_option(dhs_pool* pool, int32_t key, int64_t* value) {
     case DHS_OPT_EARLY: *value = pool->early; return DHS_OK;
     case DHS_OPT_FRESH_LIST: *value = use_fresh_list(pool) ? 1 : 0; return DHS_OK;
     case DHS_OPT_GATHER_TPC: *value = pool->gather_tpc; return DHS_OK;
+    case DHS_OPT_STAGE_MISSES: *value = pool->stage_misses; return DHS_OK;
     default: return DHS_EINVAL;
   }
 }
@@ -972,9 +994,16 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     r.N = s.N;
     r.pair = (int32_t)pair;
     r.n = it.queries * it.topk;
+    // fused steps: the host copy writes the misses into the item's staging,
+    // and its gather leaves them out
+    const bool stage = fused && !scr && p->stage_misses && tma_gather(p) && p->early &&
+                       it.staging_dev != nullptr && r.n > 0;
+    r.stage = stage ? 1 : 0;
+    p->staged_pair[pair] = stage ? 1 : 0;
     p->ritems.push_back(r);
     dhs::CopyItem ci{};
     ci.host = s.host_dev;
+    ci.staging = stage ? (uint8_t*)it.staging_dev : nullptr;
     ci.pair = (int32_t)pair;
     p->citems.push_back(ci);
   }
@@ -1006,11 +1035,17 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   rcm.fill_words = p->fill_words;
   rcm.later_count = p->later_count;
   rcm.gen = p->gen;
+  rcm.miss_off = p->miss_off;
+  rcm.miss_ent = p->miss_ent;
+  rcm.ent_cap = (int32_t)p->ent_cap;
   dhs::CopyCommon ccm{};
   ccm.hot = (uint8_t*)c.hot_dev;
   ccm.miss_rows = rcm.miss_rows;
   ccm.miss_slots = rcm.miss_slots;
   ccm.miss_count = rcm.miss_count;
+  ccm.miss_off = p->miss_off;
+  ccm.miss_ent = p->miss_ent;
+  ccm.ent_cap = (int32_t)p->ent_cap;
   ccm.B = c.hot_rows;
   ccm.Mcap = (int32_t)p->mcap;
   ccm.row_bytes = c.row_bytes;
@@ -1153,6 +1188,9 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
         gi.pair = (int32_t)f->second;
         gi.seq = p->seq_of_pair[f->second];
         gi.flags |= dhs::kGiLocReady;
+        // the resolved item itself (not a Reuse item sharing its locations)
+        if (!(it.flags & DHS_ITEM_GATHER_ONLY) && p->staged_pair[f->second])
+          gi.flags |= dhs::kGiStaged;
       }
     }
     p->gitems.push_back(gi);

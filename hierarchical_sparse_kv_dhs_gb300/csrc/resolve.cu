@@ -478,6 +478,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
           tags[v] = row;
           s.st[v] = step;
           s.slot_of[i] = (uint16_t)v;
+          s.cand_row[i] = ~(int32_t)mr;  // from here on: miss index of candidate i
           mrows[mr] = row;
           mslots[mr] = v;
           ++mr;
@@ -528,10 +529,61 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
     }
     for (int u = (int)n_unique + tid; u < n; u += nt) it.loc[u] = kEndLoc;
   }
+  // ---- staging entries of each miss (the host copy writes them): entries
+  // grouped by miss index, CSR in miss_off / miss_ent.  After the stamp
+  // commit the working stamps serve as per-miss counters, then cursors.
+  if (it.stage && m_miss) {
+    int32_t* off = c.miss_off + (size_t)pair * (c.Mcap + 1);
+    int32_t* ent = c.miss_ent + (size_t)pair * c.ent_cap;
+    // miss index of the entry's row, or -1 when the row is not a miss
+    auto miss_of = [&](int32_t row) -> int32_t {
+      if ((int64_t)row >= t0) return -1;
+      const uint64_t m = s.bm[row >> 6];
+      const uint64_t bit = 1ull << (row & 63);
+      if (!(m & bit)) return -1;
+      const int32_t v = s.cand_row[s.wpre[row >> 6] + (uint32_t)__popcll(m & (bit - 1ull))];
+      return v < 0 ? ~v : -1;
+    };
+    __syncthreads();
+    for (uint32_t j = tid; j < m_miss; j += nt) s.st[j] = 0u;
+    __syncthreads();
+    if (!uni) {
+      for (int e = tid; e < n; e += nt) {
+        const int32_t mi = miss_of(it.sel[e]);
+        if (mi >= 0) atomicAdd(&s.st[mi], 1u);
+      }
+    } else {  // one staging row per distinct row
+      for (int w = tid; w < W; w += nt)
+        for (uint64_t m = s.ubm[w]; m; m &= m - 1) {
+          const int32_t mi = miss_of((w << 6) + __ffsll((long long)m) - 1);
+          if (mi >= 0) atomicAdd(&s.st[mi], 1u);
+        }
+    }
+    __syncthreads();
+    const uint32_t total = block_scan_array(s.st, (int)m_miss, scratch);
+    for (uint32_t j = tid; j < m_miss; j += nt) off[j] = (int32_t)s.st[j];
+    if (tid == 0) off[m_miss] = (int32_t)total;
+    __syncthreads();
+    if (!uni) {
+      for (int e = tid; e < n; e += nt) {
+        const int32_t mi = miss_of(it.sel[e]);
+        if (mi >= 0) ent[atomicAdd(&s.st[mi], 1u)] = e;
+      }
+    } else {
+      for (int w = tid; w < W; w += nt) {
+        uint32_t u = s.upre[w];
+        for (uint64_t m = s.ubm[w]; m; m &= m - 1, ++u) {
+          const int32_t mi = miss_of((w << 6) + __ffsll((long long)m) - 1);
+          if (mi >= 0) ent[atomicAdd(&s.st[mi], 1u)] = (int32_t)u;
+        }
+      }
+    }
+  }
   __syncthreads();
   if (tid == 0) {
     // everything the host copy and the gather read of this item -- miss
-    // lists, fill marks, locations, appended rows -- is written before the mark
+    // lists, staging entries, fill marks, locations, appended rows -- is
+    // written before the mark
     c.miss_count[pair] = m_miss;
     c.pair_status[pair] = 0;
     publish_loc(c, pair);

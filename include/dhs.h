@@ -476,6 +476,11 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
 #define DHS_OPT_FRESH_LIST 5
 /* TMA gather: consecutive 32-entry tiles per CTA, 1 (default) .. 64. */
 #define DHS_OPT_GATHER_TPC 6
+/* Fused steps (TMA gather, early copies on): 1 (default) = the host copy
+ * writes each row it fetches into the hot cache and into every staging
+ * entry of the resolved item that selected it, and the gather leaves those
+ * rows out; 0 = the gather copies them from the hot cache after the copy. */
+#define DHS_OPT_STAGE_MISSES 7
 int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
 /* The value in effect (DHS_OPT_FRESH_LIST: 0 or 1, the auto rule resolved
  * for the pool's current admissions).  DHS_EINVAL for an unknown key. */

@@ -36,7 +36,8 @@ def _as_u32(t):
 
 
 def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
-                gather_impl=0, patch=None, early=1, union=False, fresh=None, tpc=None):
+                gather_impl=0, patch=None, early=1, union=False, fresh=None, tpc=None,
+                stage=None):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
@@ -53,6 +54,8 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
         gpu.pool.set_option(dhs.DHS_OPT_FRESH_LIST, fresh)
     if tpc is not None:
         gpu.pool.set_option(dhs.DHS_OPT_GATHER_TPC, tpc)
+    if stage is not None:
+        gpu.pool.set_option(dhs.DHS_OPT_STAGE_MISSES, stage)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
     orc = OracleRun(cfg, wl, requests=sampled, union=union)
     try:
@@ -216,6 +219,17 @@ UNION = [SMALL[1], SMALL[2], SMALL[4],
 def test_union_staging_bit_exact(cfg, mode):
     compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
                 union=True)
+
+
+@pytest.mark.parametrize("cfg", [SMALL[1], SMALL[2], SMALL[4], UNION[3]],
+                         ids=["v3", "reuse", "evict", "v8"])
+def test_misses_staged_by_the_host_copy_or_not(cfg):
+    """Fused steps: the host copy writes the rows it fetches into the
+    resolved items' staging (default), or leaves them to the gather."""
+    for stage in (1, 0):
+        compare_run(cfg, gather_impl=1, stage=stage)
+        compare_run(cfg, gather_impl=1, stage=stage, union=True)
+        compare_run(cfg, gather_impl=1, stage=stage, fresh=0)
 
 
 @pytest.mark.parametrize("tpc", [2, 5])
