@@ -164,12 +164,12 @@ class OracleTimer:
         self.threads = threads or min(n, cores)
         self.runs = [OracleRun(cfg, wl, requests=reqs[i::self.threads], union=union)
                      for i in range(self.threads)]
+        self.cycle = Cycle(cfg, self._reset)
 
     @property
     def rows_per_step(self):
         """Selected rows the sampled requests resolve + gather per step."""
         return self.cfg.entries_per_step * self.sampled // self.cfg.requests
-        self.cycle = Cycle(cfg, self._reset)
 
     def _reset(self):
         for r in self.runs:
