@@ -32,7 +32,8 @@
  *   last-use step stamps, empty slots (tag -1, stamp 0) first, smallest
  *   (stamp, slot) evicted, misses handled in ascending row order, slots hit
  *   or filled in this step protected; a step that needs more victims than
- *   unprotected slots fails with EBUDGET and changes nothing; duplicates in
+ *   unprotected slots fails with EBUDGET and changes nothing (its step-1
+ *   rows keep their locations, every other entry has none); duplicates in
  *   a selection share one location and count once; a verify block is one
  *   step; optional slots are allocated lowest-free-first, pages ascending.
  *
@@ -456,10 +457,30 @@ static int64_t find_sorted(const int32_t *u, int64_t n, int32_t v) {
 }
 
 /*
+ * Step 1 of Resolution for one row of (r, s): the mutable tail holds rows
+ * [L-T, L) at ring slot row mod T; else the ready optional-history map
+ * (complete imported pages only, "Memory split").  The row's location, or
+ * ORC_NO_LOC when step 1 does not hold it (or the row is outside [0, L)).
+ */
+static uint32_t step1_location(const orc_pool *p, const orc_source *src,
+                               int64_t pair, int64_t row) {
+  const int64_t L = src->L, N = src->N, T = p->T, PR = p->PR;
+  if (row < 0 || row >= L) return ORC_NO_LOC;
+  if (row >= L - T) return (ORC_TIER_TAIL << 30) | (uint32_t)(pair * T + row % T);
+  int64_t page = row / PR;
+  if ((page + 1) * PR <= N && src->page_slot[page] >= 0)
+    return (ORC_TIER_OPT << 30) |
+           (uint32_t)((int64_t)src->page_slot[page] * PR + row % PR);
+  return ORC_NO_LOC;
+}
+
+/*
  * Resolve the Q x k selection `sel` of (r, s) at `step` (>= 1) into `loc`
  * (Q*k) and `counters` (8).  On ORC_ERANGE (a row outside [0, L)) or
- * ORC_EBUDGET (more misses than unprotected hot slots) nothing changes,
- * every location is ORC_NO_LOC and every counter 0.
+ * ORC_EBUDGET (more misses than unprotected hot slots) nothing changes and
+ * every counter is 0; step 1 reads no state that resolution changes, so the
+ * entries it resolves keep their locations and every other entry is
+ * ORC_NO_LOC.
  */
 int orc_resolve(orc_pool *p, uint32_t step, int32_t r, int32_t s, int32_t Q,
                 int32_t k, const int32_t *sel, uint32_t *loc,
@@ -469,11 +490,13 @@ int orc_resolve(orc_pool *p, uint32_t step, int32_t r, int32_t s, int32_t Q,
   if (!src->admitted) return ORC_ESTATE;
   int64_t n = (int64_t)Q * k;
   const int64_t pair = (int64_t)r * p->S + s;
-  const int64_t L = src->L, N = src->N, T = p->T, B = p->B, PR = p->PR;
+  const int64_t L = src->L, B = p->B;
   for (int c = 0; c < 8; ++c) counters[c] = 0;
-  for (int64_t e = 0; e < n; ++e) loc[e] = ORC_NO_LOC;
   for (int64_t e = 0; e < n; ++e)
-    if (sel[e] < 0 || (int64_t)sel[e] >= L) return ORC_ERANGE;
+    if (sel[e] < 0 || (int64_t)sel[e] >= L) {
+      for (int64_t f = 0; f < n; ++f) loc[f] = step1_location(p, src, pair, sel[f]);
+      return ORC_ERANGE;
+    }
 
   /* all verify queries together: sorted union of the selected rows */
   int32_t *U = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n + 1));
@@ -495,18 +518,11 @@ int orc_resolve(orc_pool *p, uint32_t step, int32_t r, int32_t s, int32_t Q,
   int64_t n_miss = 0;
   for (int64_t u = 0; u < nu; ++u) {
     int64_t row = U[u];
-    /* step 1a: the mutable tail holds rows [L-T, L) at row mod T */
-    if (row >= L - T) {
-      where[u] = (ORC_TIER_TAIL << 30) | (uint32_t)(pair * T + row % T);
-      c_tail++;
-      continue;
-    }
-    /* step 1b: the ready optional-history map (complete imported pages) */
-    int64_t page = row / PR;
-    if ((page + 1) * PR <= N && src->page_slot[page] >= 0) {
-      where[u] = (ORC_TIER_OPT << 30) |
-                 (uint32_t)((int64_t)src->page_slot[page] * PR + row % PR);
-      c_opt++;
+    /* step 1: the tail, then the ready optional-history map */
+    uint32_t l1 = step1_location(p, src, pair, row);
+    if (l1 != ORC_NO_LOC) {
+      where[u] = l1;
+      if ((l1 >> 30) == ORC_TIER_TAIL) c_tail++; else c_opt++;
       continue;
     }
     /* step 2: scan of the hot cache, bounded by B */
@@ -528,6 +544,7 @@ int orc_resolve(orc_pool *p, uint32_t step, int32_t r, int32_t s, int32_t Q,
   int64_t avail = 0;
   for (int64_t j = 0; j < B; ++j) avail += st[j] != step;
   if (n_miss > avail) {
+    for (int64_t e = 0; e < n; ++e) loc[e] = step1_location(p, src, pair, sel[e]);
     free(U); free(where); free(miss); free(st);
     return ORC_EBUDGET;
   }

@@ -74,10 +74,22 @@ class BrutePool:
         pair = r * self.S + s
         L, N, T, B, PR = st["L"], st["N"], self.T, self.B, self.PR
         n = len(sel_rows)
-        if any(x < 0 or x >= L for x in sel_rows):
-            return "erange", [NO_LOC] * n, [0] * 8
-        union = sorted(set(sel_rows))
         tail_rows = set(range(max(0, L - T), L))
+
+        def step1_only():  # a failed step: locations of what step 1 holds
+            out = []
+            for row in sel_rows:
+                if row in tail_rows:
+                    out.append(_loc(0, pair * T + row % T))
+                elif 0 <= row < L and row // PR in st["ready"] and (row // PR + 1) * PR <= N:
+                    out.append(_loc(1, st["ready"][row // PR] * PR + row % PR))
+                else:
+                    out.append(NO_LOC)
+            return out
+
+        if any(x < 0 or x >= L for x in sel_rows):
+            return "erange", step1_only(), [0] * 8
+        union = sorted(set(sel_rows))
         where, pending, touched = {}, [], set()
         c = dict(tail=0, opt=0, hot=0, host=0, scan=0, ev=0)
         for row in union:
@@ -100,7 +112,7 @@ class BrutePool:
         use = [step if j in touched else st["last_use"][j] for j in range(B)]
         free = sorted((use[j], j) for j in range(B) if use[j] != step)
         if len(pending) > len(free):
-            return "ebudget", [NO_LOC] * n, [0] * 8
+            return "ebudget", step1_only(), [0] * 8
         for row, (_, j) in zip(pending, free):
             old = st["slot_row"][j]
             if old is not None:

@@ -172,6 +172,13 @@ def test_range_and_tail_boundary(oracle_lib):
     for bad in ([[N]], [[-1]], [[0, N + 3]]):
         rc, loc, cnt = p.resolve(1, 0, 0, np.array(bad, np.int32))
         assert rc == "erange" and (loc == oracle.NO_LOC).all() and not cnt.any()
+    # a failed step still locates what step 1 holds: the tail row and the row
+    # on resident page 3, not row 0 (page 0 absent) nor the out-of-range row
+    rc, loc, cnt = p.resolve(1, 0, 0, np.array([[N - 1, N, 3 * 64 + 5, 0]], np.int32))
+    assert rc == "erange" and not cnt.any()
+    tier, idx = decode(loc.ravel()[[0, 2]])
+    assert tier.tolist() == [0, 1] and idx.tolist() == [(N - 1) % T, 0 * 64 + 5]
+    assert (loc.ravel()[[1, 3]] == oracle.NO_LOC).all()
     # row L-T is tail; L-T-1 lies in resident page 3 -> optional
     rc, loc, cnt = p.resolve(1, 0, 0, np.array([[N - T, N - T - 1, N - 1]], np.int32))
     assert rc == 0
