@@ -21,11 +21,9 @@ constexpr uint32_t kStatusEtimeout = 8u;
 constexpr int32_t kErrRange = -5, kErrBudget = -4;  // DHS_ERANGE, DHS_EBUDGET
 constexpr int kMaxHotRows = 16384;
 
-// Per-item verdicts the resolve kernel publishes as soon as they are decided
-// (read by the fused gather): ((launch sequence & kSeqMask) << kVerdictShift)
-// | code.
-constexpr uint32_t kVerdictOk = 1u, kVerdictRange = 2u, kVerdictBudget = 3u;
-constexpr uint32_t kVerdictShift = 3u, kVerdictCodeMask = 7u, kSeqMask = 0x1FFFFFFFu;
+// Sequence numbers of resolve launches as published in loc_ready marks (never
+// 0, which is what a zeroed mark holds).
+constexpr uint32_t kSeqMask = 0x1FFFFFFFu;
 
 // Optional timeline (DHS_OPT_TRACE): per kernel kind, the earliest CTA start
 // and the latest CTA end in %globaltimer nanoseconds.
@@ -98,7 +96,6 @@ struct ResolveCommon {
   int32_t row_bytes;
   uint8_t* tail;         // tail arena (appends folded into the launch)
   unsigned long long* trace;  // null = off
-  uint32_t* verdict;     // [pairs] published verdicts, null = none
   uint32_t seq;          // sequence number of this launch
   int32_t uni;           // shared-memory plan includes the union bitmap
   uint32_t* loc_ready;   // [pairs] seq once the item's locations are written; null = off
@@ -161,7 +158,16 @@ cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,
 // ------------------------------------------------------------ gather (e)
 constexpr int kGatherThreads = 256;
 constexpr int kGatherVector = 0, kGatherTma = 1;  // DHS_OPT_GATHER_IMPL values
-constexpr int kGatherTileRows = 32;
+constexpr int kGatherTileRows = 32;  // entries per tile of the vector gather
+// TMA gather tile: kTmaWarps warps per CTA, each moving kTmaWarpRows entries
+// under its own mbarrier (lanes past them idle).  A warp's bulk stores wait
+// only for its own rows, not for the slowest row of the whole tile.
+constexpr int kTmaWarpRows = 8;
+constexpr int kTmaWarps = 2;
+constexpr int kTmaTileRows = kTmaWarpRows * kTmaWarps;
+constexpr int gather_tile_rows(int impl) {
+  return impl == kGatherTma ? kTmaTileRows : kGatherTileRows;
+}
 constexpr int kLaterThreads = 512;
 constexpr int kGatherItemsLarge = 384, kGatherItemsSmall = 64;
 
@@ -197,7 +203,6 @@ struct GatherCommon {
   int32_t n_tiles;
   int32_t T, Pmax, page_shift;
   int32_t early;             // copy step-1 rows before waiting for the resolve grid
-  const uint32_t* verdict;   // [pairs] verdicts published by the resolve kernel
   unsigned long long* trace;  // null = off
   const uint32_t* loc_ready;  // [pairs] (kGiLocReady items)
   const uint32_t* fill;       // [pairs][fill_words]
@@ -226,7 +231,7 @@ cudaError_t launch_gather(const GatherCommon& c, const GatherItem* items,
 cudaError_t launch_gather_later(const GatherCommon& c, int ctas, cudaStream_t stream);
 
 // Raise the TMA gather's dynamic shared-memory limit for a row size.
-// *tma_ok: whether the TMA gather's 32-row tile of this row size fits in
+// *tma_ok: whether the TMA gather's 16-row tile of this row size fits in
 // `optin` bytes of shared memory per block (else only the vector gather runs).
 cudaError_t gather_set_smem_limit(int row_bytes, int optin, bool* tma_ok);
 

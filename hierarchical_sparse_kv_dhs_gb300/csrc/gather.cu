@@ -5,13 +5,15 @@
 // location vector.  This is the byte-dominant step of the decode path
 // (1152 bytes read + 1152 written per entry against 4 bytes of location), a
 // pure HBM copy, so it is built for memory-level parallelism, not arithmetic.
-// One CTA per tile of 32 entries of one item; two implementations:
-//   * TMA (default): one warp per tile; lane e moves entry e with one bulk
-//     copy (cp.async.bulk) global -> shared, completion counted on an
-//     mbarrier, then one bulk copy shared -> staging.  No row byte passes
-//     through registers; six 36 KB tiles stay in flight per SM.
-//   * vector: 256 threads per tile, 9 x 16-byte loads in flight per thread,
-//     consecutive threads on consecutive 16-byte chunks (full-line coalesced).
+// One CTA per tile of entries of one item; two implementations:
+//   * TMA (default): 16 entries per CTA, split between two warps of 8; lane
+//     e of a warp moves its entry with one bulk copy (cp.async.bulk) global
+//     -> shared, completion counted on the warp's own mbarrier, then one bulk
+//     copy shared -> staging.  No row byte passes through registers; eleven
+//     18 KB tiles stay in flight per SM.
+//   * vector: 256 threads per tile of 32 entries, 9 x 16-byte loads in flight
+//     per thread, consecutive threads on consecutive 16-byte chunks
+//     (full-line coalesced).
 //
 // Early phase (fused resolve + gather).  A row that resolves in step 1 of
 // "Resolution" -- the tail (row >= L - T) or a ready optional page -- has a
@@ -19,11 +21,10 @@
 // which the resolve kernel of the same step changes.  The fused launch
 // (programmatic dependent launch) therefore copies those rows while the
 // resolve kernel still runs, and only tiles with rows that need the hot cache
-// wait (griddepcontrol.wait) for the resolve / host-copy grids.  The resolve
-// kernel publishes each item's verdict (resolved / row out of range / budget
-// overflow) as soon as it is decided; after its early copies a tile reads its
-// item's verdict -- or waits for the resolve grid if it is not out yet -- and
-// a failed item's rows become zeros, exactly as its locations say.
+// wait for the item's locations (or the resolve / host-copy grids).  Step-1
+// rows never wait for the item's outcome: a failed resolution still gives
+// them their locations (it changes no state they depend on), and every other
+// entry of a failed item has none, so its rows become zeros.
 #include <algorithm>
 
 #include "dhs_internal.h"
@@ -44,15 +45,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
-  return v;
-}
-
-// A verdict guards no other data (it only decides whether a tile's rows
-// become zeros), so a relaxed load suffices and does not hold back the
-// address loads issued after it.
-__device__ __forceinline__ uint32_t ld_verdict(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
@@ -136,29 +128,13 @@ __device__ __forceinline__ const uint8_t* step1_ptr(const GatherCommon& c,
   return c.opt + (size_t)idx * c.row_bytes;
 }
 
-// Verdict of an early item's resolution (kVerdictOk / kVerdictRange /
-// kVerdictBudget).  `v` was read when the CTA started (in parallel with its
-// address loads); if it was not published then, read it again, and if it is
-// still not out, wait for the resolve grid (*waited = true) and read it.
-// Every thread of the CTA calls it and gets the same result.
-__device__ __forceinline__ uint32_t item_verdict(const GatherCommon& c, const GatherItem& it,
-                                                 uint32_t v, bool* waited) {
-  const uint32_t want = it.seq & kSeqMask;
-  if ((v >> kVerdictShift) != want) v = ld_verdict(&c.verdict[it.pair]);
-  if ((v >> kVerdictShift) != want) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    *waited = true;
-    v = ld_verdict(&c.verdict[it.pair]);
-  }
-  return v & kVerdictCodeMask;
-}
-
 // End of a gather CTA.  The gather grid must not complete before the resolve
 // / host-copy grids it overlaps (stream order for whatever follows), so its
 // last block waits for them; every other CTA leaves as soon as its rows are
 // written.
 __device__ __forceinline__ void end_grid(const GatherCommon& c) {
   if (blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (c.trace) __syncthreads();  // the CTA's end is its last warp's end
   if (threadIdx.x == 0) trace_mark(c.trace, kTraceGather, true);
 }
 
@@ -223,7 +199,6 @@ __global__ void __launch_bounds__(kGatherThreads)
   if (tid == 0) trace_mark(c.trace, kTraceGather, false);
 
   // phase 0: rows resolved in step 1 (fused launch only)
-  const uint32_t v0 = early ? ld_verdict(&c.verdict[it.pair]) : 0u;
   int deferred = 0;
   if (tid < ne) {
     const uint8_t* p = early ? step1_ptr(c, it, it.sel[e0 + tid]) : nullptr;
@@ -232,25 +207,11 @@ __global__ void __launch_bounds__(kGatherThreads)
     deferred = p == nullptr;
   }
   const int any_deferred = __syncthreads_or(deferred);
-  bool waited = false;
-  if (early) {
-    copy_tile<CPR>(c, dst, s_src, s_phase, ne, 0);
-    if (item_verdict(c, it, v0, &waited) != kVerdictOk) {
-      // the item failed: every entry becomes zeros (each 16-byte chunk is
-      // rewritten by the thread that wrote it above)
-      __syncthreads();
-      if (tid < ne) s_src[tid] = nullptr;
-      __syncthreads();
-      copy_tile<CPR>(c, dst, s_src, s_phase, ne, 0);
-      copy_tile<CPR>(c, dst, s_src, s_phase, ne, 1);
-      end_grid(c);
-      return;
-    }
-  }
+  if (early) copy_tile<CPR>(c, dst, s_src, s_phase, ne, 0);
   if (any_deferred) {
     // rows that needed the hot cache (or no early phase): wait for the
     // resolve / host-copy grids (a no-op without programmatic dependent launch)
-    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid < ne && s_phase[tid] == 1) {
       const uint32_t l = it.loc[e0 + tid];
       if (l == kEndLoc) s_phase[tid] = 2;  // past a union list: nothing to write
@@ -264,7 +225,7 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 // ---------------------------------------------------------------- TMA variant
 
-constexpr int kTmaThreads = 32;
+constexpr int kTmaThreads = 32 * kTmaWarps;
 constexpr uint32_t kWaitPolls = 1u << 26;  // bounded mbarrier wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -313,17 +274,17 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uin
 template <int MAXI>
 __global__ void __launch_bounds__(kTmaThreads)
     gather_tma_kernel(const __grid_constant__ GatherParams<MAXI> P) {
-  extern __shared__ __align__(128) uint8_t s_rows[];  // [32][row_bytes]
-  __shared__ __align__(8) uint64_t s_bar;
+  extern __shared__ __align__(128) uint8_t s_rows[];  // [kTmaTileRows][row_bytes]
+  __shared__ __align__(8) uint64_t s_bars[kTmaWarps];
   const GatherCommon& c = P.c;
-  const int lane = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rb = (uint32_t)c.row_bytes;
-  uint8_t* my_row = s_rows + (size_t)lane * rb;
+  uint64_t& s_bar = s_bars[warp];
+  // lanes past the warp's rows hold none (their entries never exist)
+  uint8_t* my_row = s_rows + (size_t)(warp * kTmaWarpRows + min(lane, kTmaWarpRows - 1)) * rb;
   asm volatile("griddepcontrol.launch_dependents;");
-  if (lane == 0) {
-    trace_mark(c.trace, kTraceGather, false);
-    mbar_init(&s_bar, 1);
-  }
+  if (threadIdx.x == 0) trace_mark(c.trace, kTraceGather, false);
+  if (lane == 0) mbar_init(&s_bar, 1);
   __syncwarp();
   uint32_t parity = 0;
   bool stored = false, ok = true, waited = false;
@@ -369,26 +330,17 @@ __global__ void __launch_bounds__(kTmaThreads)
       stored = false;
     }
     const GatherItem& it = P.items[find_item(P, tile)];
-    const int e0 = (tile - it.tile0) * kGatherTileRows;
-    const int ne = min(kGatherTileRows, it.n - e0);
+    // this warp's entries of the tile (none past the end of the item)
+    const int e0 = (tile - it.tile0) * kTmaTileRows + warp * kTmaWarpRows;
+    const int ne = min(kTmaWarpRows, it.n - e0);
+    if (ne <= 0) continue;
     dst = it.staging + ((size_t)e0 + lane) * rb;
     const bool early = c.early && it.sel != nullptr;
 
-    const uint32_t v0 = early ? ld_verdict(&c.verdict[it.pair]) : 0u;
     const uint8_t* src = nullptr;
     if (early && lane < ne) src = step1_ptr(c, it, it.sel[e0 + lane]);
     bool deferred = lane < ne && src == nullptr;
-    if (early) {
-      ok = move(src != nullptr, src);  // rows resolved in step 1
-      if (ok && item_verdict(c, it, v0, &waited) != kVerdictOk) {
-        // the item failed: every entry becomes zeros; a row stored above must
-        // be fully written (and its shared-memory copy read) before it is
-        // overwritten
-        if (stored) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        ok = move(lane < ne, nullptr);
-        deferred = false;
-      }
-    }
+    if (early) ok = move(src != nullptr, src);  // rows resolved in step 1
     const bool lr = c.early && (it.flags & kGiLocReady) && !waited;
     if (ok && __any_sync(0xFFFFFFFFu, deferred) && lr && wait_loc_ready(c, it)) {
       // the item's locations are out: every row but the fresh ones (hot slots
@@ -484,7 +436,7 @@ cudaError_t launch_t(const GatherCommon& c, const GatherItem* items, int n, bool
   if (impl == kGatherTma) {
     cfg.gridDim = dim3((unsigned)((c.n_tiles + c.tpc - 1) / c.tpc));
     cfg.blockDim = dim3(kTmaThreads);
-    cfg.dynamicSmemBytes = (size_t)kGatherTileRows * c.row_bytes;
+    cfg.dynamicSmemBytes = (size_t)kTmaTileRows * c.row_bytes;
     return cudaLaunchKernelEx(&cfg, gather_tma_kernel<MAXI>, P);
   }
   cfg.blockDim = dim3(kGatherThreads);
@@ -523,7 +475,7 @@ cudaError_t gather_set_carveout() {
 }
 
 cudaError_t gather_set_smem_limit(int row_bytes, int optin, bool* tma_ok) {
-  const int bytes = kGatherTileRows * row_bytes;
+  const int bytes = kTmaTileRows * row_bytes;
   *tma_ok = bytes + 1024 <= optin;  // 1 KB for the kernel's static shared memory
   if (!*tma_ok || bytes <= 48 * 1024) return cudaSuccess;
   for (const void* f : {(const void*)gather_tma_kernel<kGatherItemsSmall>,

@@ -37,7 +37,7 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct MetaLayout {
-  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status, verdict;
+  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status;
   size_t loc_ready, fill, later_count, status, later, miss_off, miss_ent;
   size_t total;
 };
@@ -80,7 +80,6 @@ MetaLayout meta_layout(const dhs_pool_config& c) {
   m.miss_slots = take(pairs * (size_t)mcap_of(c) * 4);
   m.miss_count = take(pairs * 4);
   m.pair_status = take(pairs * 4);
-  m.verdict = take(pairs * 4);
   m.loc_ready = take(pairs * 4);
   m.fill = take(pairs * (size_t)fill_words_of(c) * 4);
   m.later_count = take(2 * 4);
@@ -167,7 +166,6 @@ struct dhs_pool {
   bool tma_ok = true;  // the TMA gather's tile fits the row size
   int gather_tpc = 1;   // DHS_OPT_GATHER_TPC
   int early = 1;        // fused gathers copy step-1 rows before the resolve ends
-  uint32_t* verdict = nullptr;  // [pairs] resolve verdicts for the fused gather
   uint32_t seq = 0;             // resolve launches so far
   uint32_t* loc_ready = nullptr;  // [pairs] per-item "locations written" marks
   uint32_t* fill = nullptr;       // [pairs][fill_words] slots the step's copy fills
@@ -495,7 +493,6 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->miss_slots = (int32_t*)(m + p->layout.miss_slots);
     p->miss_count = (uint32_t*)(m + p->layout.miss_count);
     p->pair_status = (int32_t*)(m + p->layout.pair_status);
-    p->verdict = (uint32_t*)(m + p->layout.verdict);
     p->loc_ready = (uint32_t*)(m + p->layout.loc_ready);
     p->fill = (uint32_t*)(m + p->layout.fill);
     p->later_count = (uint32_t*)(m + p->layout.later_count);
@@ -1027,7 +1024,6 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   rcm.row_bytes = c.row_bytes;
   rcm.tail = (uint8_t*)c.tail_dev;
   rcm.trace = p->trace;
-  rcm.verdict = p->verdict;
   p->fused_resolved = fused && !p->ritems.empty();
   if (p->fused_resolved) ++p->gen;
   rcm.loc_ready = p->loc_ready;
@@ -1067,7 +1063,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     rcm.w64cap = (int32_t)wmax;
     rcm.qkcap = (int32_t)qmax;
     rcm.seq = ++p->seq & dhs::kSeqMask;
-    if (rcm.seq == 0) rcm.seq = p->seq = 1;  // 0 never matches a published verdict
+    if (rcm.seq == 0) rcm.seq = p->seq = 1;  // 0 never matches a published mark
     ccm.loc_ready = rcm.loc_ready;  // the copy starts on each item once it is resolved
     ccm.seq = rcm.seq;
     for (int i = 0; i < n; ++i) p->seq_of_pair[p->ritems[b + i].pair] = rcm.seq;
@@ -1141,7 +1137,6 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   g.Pmax = (int32_t)p->pmax;
   g.page_shift = p->page_shift;
   g.early = fused && p->early ? 1 : 0;
-  g.verdict = p->verdict;
   g.trace = p->trace;
   g.loc_ready = p->loc_ready;
   g.fill = p->fill;
@@ -1196,13 +1191,14 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
     p->gitems.push_back(gi);
   }
   const size_t ng = p->gitems.size();
+  const int tile_rows = dhs::gather_tile_rows(p->gather_impl);
   for (size_t b = 0; b < ng; b += dhs::kGatherItemsLarge) {
     const int n = (int)std::min<size_t>(dhs::kGatherItemsLarge, ng - b);
     int64_t tiles = 0;
     for (int i = 0; i < n; ++i) {
       dhs::GatherItem& gi = p->gitems[b + i];
       gi.tile0 = (int32_t)tiles;
-      tiles += (gi.n + dhs::kGatherTileRows - 1) / dhs::kGatherTileRows;
+      tiles += (gi.n + tile_rows - 1) / tile_rows;
     }
     if (tiles > INT32_MAX) return DHS_EINVAL;
     g.n_tiles = (int32_t)tiles;

@@ -211,14 +211,6 @@ __device__ __forceinline__ uint64_t opt_mask(int w, int64_t N, const int32_t* ma
   return m;
 }
 
-// Publish an item's verdict for the fused gather (thread 0 only).
-__device__ __forceinline__ void publish(const ResolveCommon& c, int pair, uint32_t code) {
-  if (!c.verdict) return;
-  const uint32_t v = ((c.seq & kSeqMask) << kVerdictShift) | code;
-  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(c.verdict + pair), "r"(v)
-               : "memory");
-}
-
 // Publish that an item's locations (and the decode rows it appended) are
 // written (thread 0 only, after a block barrier).
 __device__ __forceinline__ void publish_loc(const ResolveCommon& c, int pair) {
@@ -228,7 +220,12 @@ __device__ __forceinline__ void publish_loc(const ResolveCommon& c, int pair) {
                "r"(c.seq & kSeqMask) : "memory");
 }
 
-// Write the failure result of one item: no state change.
+// Write the failure result of one item: no state change, zero counters.
+// Step 1 of "Resolution" reads no state that resolution changes, so the
+// entries it resolves keep their locations (the tail, or a ready page of the
+// optional map) and every other entry gets none; the fused gather copies
+// step-1 rows without waiting for the outcome.  A union item gets an empty
+// list.
 __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t code,
                           uint32_t flag) {
   if (it.index) {  // union staging: an empty union list
@@ -237,7 +234,23 @@ __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t
       it.index[e] = -1;
     }
   } else {
-    for (int e = threadIdx.x; e < it.n; e += blockDim.x) it.loc[e] = kNoLoc;
+    const int64_t L = it.L, N = it.N, T = c.T;
+    const int ps = c.page_shift;
+    const int32_t* map = c.map + (size_t)it.pair * c.Pmax;
+    for (int e = threadIdx.x; e < it.n; e += blockDim.x) {
+      const int32_t row = it.sel[e];
+      uint32_t l = kNoLoc;
+      if (row >= 0 && (int64_t)row < L) {
+        const int64_t page = (int64_t)row >> ps;
+        if ((int64_t)row >= L - T) {
+          l = (kTierTail << 30) | (uint32_t)((int64_t)it.pair * T + (int64_t)row % T);
+        } else if (((page + 1) << ps) <= N && map[page] >= 0) {
+          l = (kTierOpt << 30) |
+              (uint32_t)(((int64_t)map[page] << ps) + (row & ((1 << ps) - 1)));
+        }
+      }
+      it.loc[e] = l;
+    }
   }
   if (threadIdx.x < 8 && it.counters) it.counters[threadIdx.x] = 0u;
   __syncthreads();
@@ -245,7 +258,6 @@ __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t
     c.miss_count[it.pair] = 0u;  // before the mark: the host copy reads it then
     c.pair_status[it.pair] = code;
     publish_loc(c, it.pair);
-    publish(c, it.pair, code == kErrRange ? kVerdictRange : kVerdictBudget);
     atomicOr(c.status, flag);
     trace_mark(c.trace, kTraceResolve, true);
   }
@@ -320,13 +332,22 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   for (int w = tid; w < W; w += nt) s.bm[w] = 0ull;
   if (tid == 0) s_bad = 0;
   __syncthreads();
-  for (int e = tid; e < n; e += nt) {
-    const int32_t row = it.sel[e];
-    if (row < 0 || (int64_t)row >= L) {
-      s_bad = 1;
-    } else {
-      atomicOr((unsigned long long*)&s.bm[row >> 6], 1ull << (row & 63));
-    }
+  // Selections cluster (a recency window, sorted top-k lists), so many lanes
+  // of a warp set bits of the same 64-row word: the lanes of each word OR
+  // their bits together first and one of them updates the word, instead of
+  // up to 32 contending shared-memory atomics per word.
+  for (int e0 = 0; e0 < n; e0 += nt) {  // block-uniform trip count: full warps
+    const int e = e0 + tid;
+    const int32_t row = e < n ? it.sel[e] : -1;
+    const bool ok = row >= 0 && (int64_t)row < L;
+    if (e < n && !ok) s_bad = 1;
+    const int word = ok ? (row >> 6) : -1;
+    const unsigned grp = __match_any_sync(0xFFFFFFFFu, word);
+    const uint64_t bit = ok ? 1ull << (row & 63) : 0ull;
+    const uint32_t lo = __reduce_or_sync(grp, (uint32_t)bit);
+    const uint32_t hi = __reduce_or_sync(grp, (uint32_t)(bit >> 32));
+    if (ok && (tid & 31) == __ffs(grp) - 1)
+      atomicOr((unsigned long long*)&s.bm[word], ((unsigned long long)hi << 32) | lo);
   }
   __syncthreads();
   if (s_bad) {
@@ -359,7 +380,6 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   block_sum4(cnt, scratch);
   const uint32_t n_unique = cnt[0], n_tail = cnt[1], n_opt = cnt[2];
   const uint32_t C = cnt[3];  // rows left for the hot cache (block-uniform)
-  if (C == 0 && tid == 0) publish(c, pair, kVerdictOk);  // nothing can fail now
   if (uni) block_scan_array(s.upre, W, scratch);  // union ranks
 
   uint32_t hits = 0u, m_miss = 0u, scan_max = 0u, evicted = 0u;
@@ -420,7 +440,6 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
       fail_item(c, it, kErrBudget, kStatusEbudget);
       return;
     }
-    if (tid == 0) publish(c, pair, kVerdictOk);
 
     // ---- step 3 victims: the m smallest (stamp, slot) among unprotected slots
     if (m_miss) {

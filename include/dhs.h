@@ -19,9 +19,12 @@
  *   - Errors found on the device (a selected row outside [0, L), more missing
  *     rows than unprotected hot slots, a gather location outside its arena)
  *     cannot be returned by the launching call: they leave the affected
- *     (request, source) unchanged for that step, write DHS_NO_LOC to all its
- *     locations (a union item: DHS_END_LOC, index -1) and zero to its
- *     counters, and set a sticky flag read by dhs_status().
+ *     (request, source) unchanged for that step, zero its counters and set a
+ *     sticky flag read by dhs_status().  Its entries that step 1 of
+ *     "Resolution" resolves (the tail, or a ready page of the optional map:
+ *     a lookup that changes no state) keep their locations; every other
+ *     entry gets DHS_NO_LOC (a union item: an empty list, DHS_END_LOC and
+ *     index -1).
  *   - A pool is not thread-safe: calls on one pool must not overlap.
  *   - Ownership: the caller owns every device buffer (the four arenas,
  *     selections, location vectors, staging, counters, appended rows) and
@@ -325,7 +328,8 @@ typedef struct {
  * get their bytes copied from pinned host memory, and become hot.  Writes
  * loc_dev and counters_dev.  Items must name distinct (req, src) pairs.
  * Errors (synchronous): DHS_EINVAL, DHS_ESTATE, DHS_ECUDA; device-side
- * DHS_ERANGE / DHS_EBUDGET go to dhs_status().
+ * DHS_ERANGE / DHS_EBUDGET go to dhs_status() (the item keeps only its
+ * step-1 locations, see above).
  */
 int dhs_resolve(dhs_pool *pool, const dhs_step *step);
 
@@ -451,10 +455,10 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
 
 /* Tunables (performance only; results do not depend on them). */
 #define DHS_OPT_COPY_CTAS 1 /* host-copy CTAs; 0 = 32 */
-#define DHS_OPT_GATHER_IMPL 2 /* 1 = TMA bulk copy, one warp per 32-row tile
-                                     (default); 0 = 16-byte vector copy, 256
-                                     threads per tile (the only one for rows
-                                     too large to stage 32 of them) */
+#define DHS_OPT_GATHER_IMPL 2 /* 1 = TMA bulk copy, 16-row tiles of two
+                                     warps (default); 0 = 16-byte vector copy,
+                                     256 threads per 32-row tile (the only one
+                                     for rows too large to stage 16 of them) */
 /* Timeline: value = address of a device buffer of 8 uint64 (0 = off).  Each
  * kernel kind k (0 resolve, 1 host copy, 2 gather, 3 fresh-row copy) atomically
  * lowers buf[2k]
@@ -474,7 +478,7 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
  * tenth of the admitted complete pages are not optional-resident; 0 = off
  * (such rows wait in their tile); 1 = on. */
 #define DHS_OPT_FRESH_LIST 5
-/* TMA gather: consecutive 32-entry tiles per CTA, 1 (default) .. 64. */
+/* TMA gather: consecutive 16-entry tiles per CTA, 1 (default) .. 64. */
 #define DHS_OPT_GATHER_TPC 6
 /* Fused steps (TMA gather, early copies on): 1 (default) = the host copy
  * writes each row it fetches into the hot cache and into every staging

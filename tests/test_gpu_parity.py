@@ -48,8 +48,8 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
                  payload_requests=sampled if (big and sampled is not None) else None,
                  union=union)
     from hierarchical_sparse_kv_dhs_gb300 import dhs
-    if not early:
-        gpu.pool.set_option(dhs.DHS_OPT_EARLY, 0)
+    if early != 1:
+        gpu.pool.set_option(dhs.DHS_OPT_EARLY, early)
     if fresh is not None:
         gpu.pool.set_option(dhs.DHS_OPT_FRESH_LIST, fresh)
     if tpc is not None:
@@ -340,19 +340,23 @@ def _bad_row(wl):
     sel[2, 1, 0, 0, 5] = wl.length(1, 3)
 
 
-@pytest.mark.parametrize("mode", ["fused-vec", "fused-tma", "split-vec", "split-tma"])
-def test_out_of_range_row_zeroes_the_item(mode):
+@pytest.mark.parametrize("mode", ["fused-vec", "fused-tma", "split-vec", "split-tma",
+                                  "fused-tma-late"])
+def test_out_of_range_row_keeps_only_step1_rows(mode):
+    """The failed item's step-1 rows are gathered, every other entry is zeros."""
     cfg = TINY.scaled(name="range", tag=46, requests=2, sources=2, steps=4, residency=0.6)
     compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
-                patch=_bad_row)
+                patch=_bad_row, early=0 if mode.endswith("late") else 1)
 
 
-@pytest.mark.parametrize("mode", ["fused-vec", "fused-tma"])
-def test_budget_overflow_zeroes_the_item(mode):
-    # 16 hot slots, no residency: most steps need more victims than slots
+@pytest.mark.parametrize("mode", ["fused-vec", "fused-tma", "split-tma", "fused-tma-late"])
+def test_budget_overflow_keeps_only_step1_rows(mode):
+    # 16 hot slots, 40 % residency: most steps need more victims than slots,
+    # and their items still hold step-1 rows
     cfg = TINY.scaled(name="budget", tag=47, requests=2, sources=1, hot=16, topk=64,
-                      residency=0.0, steps=4)
-    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]])
+                      residency=0.4, steps=4)
+    compare_run(cfg, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
+                early=0 if mode.endswith("late") else 1)
 
 
 # ------------------------------------------------------------ full size
@@ -472,12 +476,28 @@ def test_decode_step_host_matches_device_path():
         b.close()
 
 
+def test_large_rows_take_the_tma_gather_with_opt_in_shared_memory():
+    """4 KB rows: a 16-entry TMA tile needs 64 KB of shared memory (past the
+    48 KB default), which the pool opts in to; bit-exact in every mode."""
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    cfg = TINY.scaled(name="rows4k", tag=52, row_elems=2048, history=1024, tail=16,
+                      hot=128, topk=64, steps=4, requests=2)
+    gpu = GpuRun(cfg, Workload(cfg))
+    try:
+        assert gpu.pool.get_option(dhs.DHS_OPT_GATHER_IMPL) == 1
+    finally:
+        gpu.close()
+    compare_run(cfg, gather_impl=1)
+    compare_run(cfg, gather_impl=1, fused=False)
+
+
 def test_rows_too_large_for_a_tma_tile_use_the_vector_gather():
-    """8 KB rows: 32 of them do not fit in a block's shared memory, so the
+    """16 KB rows: a 16-entry tile of them does not fit in a block's shared memory, so the
     pool refuses the TMA gather and runs the vector gather, bit-exact."""
     from hierarchical_sparse_kv_dhs_gb300 import dhs
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
-    cfg = TINY.scaled(name="bigrows", tag=51, row_elems=4096, history=1024, tail=16,
+    cfg = TINY.scaled(name="bigrows", tag=51, row_elems=8192, history=1024, tail=16,
                       hot=128, topk=64, steps=4, requests=2)
     gpu = GpuRun(cfg, Workload(cfg))
     try:
