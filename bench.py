@@ -642,6 +642,29 @@ def main():
     gather_ms = [e[1].elapsed_time(e[2]) for e in ev2]
     resolve_ms = [e[0].elapsed_time(e[1]) for e in ev2]
 
+    # Context for the gather's roofline, timed the same way (flush, events):
+    # a contiguous device copy of the staging bytes, and one trivial launch
+    ctx_n = min(K2, 100)
+    src_b = torch.empty(cfg.entries_per_step * cfg.row_bytes, dtype=torch.uint8, device=dev)
+    dst_b = torch.empty_like(src_b)
+    tiny = torch.zeros(1, dtype=torch.int32, device=dev)
+    ctx = {}
+    for name, fn in (("contiguous_copy_us", lambda: dst_b.copy_(src_b)),
+                     ("empty_launch_us", lambda: tiny.fill_(0))):
+        evc = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ctx_n)]
+        for i in range(ctx_n):
+            flush_l2()
+            evc[i][0].record(stream)
+            fn()
+            evc[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        ctx[name] = statistics.median(e[0].elapsed_time(e[1]) * 1e3 for e in evc)
+    ctx["contiguous_copy_GBps"] = 2 * src_b.numel() / (ctx["contiguous_copy_us"] * 1e3)
+    ctx["what"] = (f"cudaMemcpyAsync device-to-device of {src_b.numel()} contiguous bytes "
+                   "(the step's staging bytes) and a 1-element fill, medians of "
+                   f"{ctx_n}, L2 flushed before each")
+    del src_b, dst_b
+
     trace_info = traced_pass(run, cycle, min(K, args.trace_steps), dev, flush_l2)
     h2d = h2d_peak_gbs(dev)
     link = None
@@ -722,7 +745,8 @@ def main():
                      "peak_source": f"hbm_gbs {peak_src} (copy, read+write bytes)",
                      "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
                      "timed": f"{K2} launches, CUDA events around dhs_gather "
-                              "(L2 flushed before each step)"},
+                              "(L2 flushed before each step)",
+                     "context": ctx},
         "host_link": link,
         "cpu_baseline": cpu,
         "e2e": e2e,
