@@ -332,22 +332,28 @@ __global__ void __launch_bounds__(kResolveThreads, 1)
   for (int w = tid; w < W; w += nt) s.bm[w] = 0ull;
   if (tid == 0) s_bad = 0;
   __syncthreads();
-  // Selections cluster (a recency window, sorted top-k lists), so many lanes
-  // of a warp set bits of the same 64-row word: the lanes of each word OR
-  // their bits together first and one of them updates the word, instead of
-  // up to 32 contending shared-memory atomics per word.
-  for (int e0 = 0; e0 < n; e0 += nt) {  // block-uniform trip count: full warps
-    const int e = e0 + tid;
-    const int32_t row = e < n ? it.sel[e] : -1;
-    const bool ok = row >= 0 && (int64_t)row < L;
-    if (e < n && !ok) s_bad = 1;
-    const int word = ok ? (row >> 6) : -1;
-    const unsigned grp = __match_any_sync(0xFFFFFFFFu, word);
-    const uint64_t bit = ok ? 1ull << (row & 63) : 0ull;
-    const uint32_t lo = __reduce_or_sync(grp, (uint32_t)bit);
-    const uint32_t hi = __reduce_or_sync(grp, (uint32_t)(bit >> 32));
-    if (ok && (tid & 31) == __ffs(grp) - 1)
-      atomicOr((unsigned long long*)&s.bm[word], ((unsigned long long)hi << 32) | lo);
+  // Each thread ORs the bits of four consecutive entries into a register and
+  // updates shared memory once per 64-row word they touch.  Selections
+  // cluster (a recency window, sorted top-k lists), so this is usually one
+  // atomic per four entries instead of one per entry, many on the same word.
+  for (int b = tid * 4; b < n; b += nt * 4) {
+    uint64_t acc = 0ull;
+    int cur = -1;
+    for (int j = 0; j < 4 && b + j < n; ++j) {
+      const int32_t row = it.sel[b + j];
+      if (row < 0 || (int64_t)row >= L) {
+        s_bad = 1;
+        continue;
+      }
+      const int w = row >> 6;
+      if (w != cur) {
+        if (cur >= 0) atomicOr((unsigned long long*)&s.bm[cur], (unsigned long long)acc);
+        cur = w;
+        acc = 0ull;
+      }
+      acc |= 1ull << (row & 63);
+    }
+    if (cur >= 0) atomicOr((unsigned long long*)&s.bm[cur], (unsigned long long)acc);
   }
   __syncthreads();
   if (s_bad) {
