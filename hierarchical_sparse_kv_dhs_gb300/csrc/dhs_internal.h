@@ -57,8 +57,15 @@ __device__ __forceinline__ void trace_mark(unsigned long long* trace, int kind, 
 #endif
 
 // ------------------------------------------------------------ resolve (a-c)
-constexpr int kResolveThreads = 1024;
 constexpr int kResolveItemsLarge = 256, kResolveItemsSmall = 32;
+// Threads per resolve CTA (one CTA per item).  A launch of at most
+// kResolveItemsSmall items leaves most SMs to the gather that overlaps it,
+// and its CTAs share their SMs with that gather: 512 threads there.  Larger
+// launches fill the GPU, and each item's copy starts when it is resolved:
+// 1024 threads there.
+constexpr int resolve_threads(int max_items) {
+  return max_items <= kResolveItemsSmall ? 512 : 1024;
+}
 
 struct ResolveItem {
   const int32_t* sel;   // [n] selected rows (Q*k, verify queries back to back)

@@ -274,7 +274,7 @@ struct ResolveParams {
 static_assert(sizeof(ResolveParams<kResolveItemsLarge>) <= 32764, "resolve item table too large");
 
 template <int MAXI>
-__global__ void __launch_bounds__(kResolveThreads, 1)
+__global__ void __launch_bounds__(resolve_threads(MAXI), 1)
     resolve_kernel(const __grid_constant__ ResolveParams<MAXI> P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint32_t scratch[4 * 33];
@@ -641,7 +641,7 @@ cudaError_t launch_t(const ResolveCommon& c, const ResolveItem* items, int n,
   P.c = c;
   P.c.n_items = n;
   for (int i = 0; i < n; ++i) P.items[i] = items[i];
-  resolve_kernel<MAXI><<<n, kResolveThreads, smem, stream>>>(P);
+  resolve_kernel<MAXI><<<n, resolve_threads(MAXI), smem, stream>>>(P);
   return cudaGetLastError();
 }
 
