@@ -69,6 +69,14 @@ def test_invalid_geometry_rejected_on_host(dhs, field, value):
                                    ctypes.byref(h)) == dhs.DHS_EINVAL
 
 
+def test_hot_cache_size_limit(dhs):
+    """16384 hot slots per (request, source) is the largest B the resolve
+    kernel's 16-bit slot lists take."""
+    out = (ctypes.c_size_t * 4)()
+    assert dhs.lib.dhs_pool_bytes(ctypes.byref(_cfg(dhs, hot_rows=16384)), out) == 0
+    assert dhs.lib.dhs_pool_bytes(ctypes.byref(_cfg(dhs, hot_rows=16385)), out) == dhs.DHS_EINVAL
+
+
 def test_null_arguments(dhs):
     assert dhs.lib.dhs_pool_create(None, None) == dhs.DHS_EINVAL
     h = ctypes.c_void_p()

@@ -476,6 +476,19 @@ def test_decode_step_host_matches_device_path():
         b.close()
 
 
+MAXHOT = TINY.scaled(name="maxhot", tag=53, requests=1, sources=1, hot=16384, history=65536,
+                     topk=4096, residency=0.0, steps=10, window=4096, frac_recent=0.3,
+                     zipf_s=0.6, row_elems=64)
+
+
+@pytest.mark.parametrize("mode", ["fused-tma", "split-vec", "fused-tma-union"])
+def test_largest_hot_cache_fills_and_evicts(mode):
+    """B at its maximum (16384 slots): about 4000 misses a step fill the hot
+    cache by step 5, and from step 6 every step evicts ~1900 rows."""
+    compare_run(MAXHOT, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
+                union=mode.endswith("union"))
+
+
 def test_large_rows_take_the_tma_gather_with_opt_in_shared_memory():
     """4 KB rows: a 16-entry TMA tile needs 64 KB of shared memory (past the
     48 KB default), which the pool opts in to; bit-exact in every mode."""
