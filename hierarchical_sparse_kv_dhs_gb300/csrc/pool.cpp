@@ -1327,9 +1327,9 @@ int dhs_decode_step(dhs_pool* p, const dhs_append_item* apps, int32_t n_apps,
   return launch_gathers(p, st, true);
 }
 
-int dhs_decode_step_host(dhs_pool* p, const dhs_copy* in, int32_t n_in,
-                         const dhs_append_item* apps, int32_t n_apps, const dhs_step* st,
-                         const dhs_copy* out, int32_t n_out) {
+int dhs_decode_step_host_async(dhs_pool* p, const dhs_copy* in, int32_t n_in,
+                               const dhs_append_item* apps, int32_t n_apps,
+                               const dhs_step* st, const dhs_copy* out, int32_t n_out) {
   if (!p || n_in < 0 || n_out < 0 || (n_in > 0 && !in) || (n_out > 0 && !out))
     return DHS_EINVAL;
   for (int32_t i = 0; i < n_in; ++i)
@@ -1347,6 +1347,14 @@ int dhs_decode_step_host(dhs_pool* p, const dhs_copy* in, int32_t n_in,
     if (out[i].bytes && cudaMemcpyAsync(out[i].dst, out[i].src, out[i].bytes,
                                         cudaMemcpyDeviceToHost, p->stream) != cudaSuccess)
       return DHS_ECUDA;
+  return DHS_OK;
+}
+
+int dhs_decode_step_host(dhs_pool* p, const dhs_copy* in, int32_t n_in,
+                         const dhs_append_item* apps, int32_t n_apps, const dhs_step* st,
+                         const dhs_copy* out, int32_t n_out) {
+  const int rc = dhs_decode_step_host_async(p, in, n_in, apps, n_apps, st, out, n_out);
+  if (rc) return rc;
   return cudaStreamSynchronize(p->stream) == cudaSuccess ? DHS_OK : DHS_ECUDA;
 }
 

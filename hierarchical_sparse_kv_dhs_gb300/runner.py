@@ -43,6 +43,19 @@ class _Admit:
         return dhs.RC_NAMES[rc], f
 
 
+def _align16(n: int) -> int:
+    return (n + 15) // 16 * 16
+
+
+def _field(block, offset: int, dtype, shape):
+    """A typed view of bytes [offset, ...) of a uint8 block: of each row of a
+    2-D block ([steps][bytes]), or of a 1-D block."""
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    if block.dim() == 2:
+        return block[:, offset:offset + n].view(dtype).view(block.shape[0], *shape)
+    return block[offset:offset + n].view(dtype).view(*shape)
+
+
 class GpuRun:
     def __init__(self, cfg: Config, wl: Workload | None = None, device="cuda",
                  host_threads=None, gather_impl=None, payload_requests=None,
@@ -86,17 +99,29 @@ class GpuRun:
         dev = self.device
         Q, k = c.queries, c.topk
         sel = self.wl.selections()
-        self.sel = torch.from_numpy(sel).to(dev)
-        self.loc = torch.empty((c.requests, c.sources, Q, k), dtype=torch.int32, device=dev)
-        self.counters = torch.zeros((c.requests, c.sources, 8), dtype=torch.int32, device=dev)
-        self.index = (torch.empty((c.requests, c.sources, Q, k), dtype=torch.int32, device=dev)
-                      if union else None)
+        a_hi = c.append_hi
+        # Each step's inputs lie in one block (selections, then appended rows)
+        # and the step's outputs in another (locations, counters, union
+        # indices), so that a caller with host buffers moves each with a
+        # single copy.
+        sel_b = _align16(sel[0].nbytes)
+        rows_shape = (c.pairs, a_hi, c.row_elems)
+        in_b = sel_b + _align16(int(np.prod(rows_shape)) * 2)
+        self.step_in = torch.zeros((c.total_steps, in_b), dtype=torch.uint8, device=dev)
+        self.sel = _field(self.step_in, 0, torch.int32, sel.shape[1:])
+        self.sel.copy_(torch.from_numpy(sel))
+        # appended rows of every step
+        self.app_rows = _field(self.step_in, sel_b, torch.int16, rows_shape)
+        loc_shape, cnt_shape = (c.requests, c.sources, Q, k), (c.requests, c.sources, 8)
+        loc_b = _align16(int(np.prod(loc_shape)) * 4)
+        cnt_b = _align16(int(np.prod(cnt_shape)) * 4)
+        self.step_out = torch.zeros(loc_b + cnt_b + (loc_b if union else 0),
+                                    dtype=torch.uint8, device=dev)
+        self.loc = _field(self.step_out, 0, torch.int32, loc_shape)
+        self.counters = _field(self.step_out, loc_b, torch.int32, cnt_shape)
+        self.index = _field(self.step_out, loc_b + cnt_b, torch.int32, loc_shape) if union else None
         self.staging = torch.empty((c.requests, len(self.layers), Q, k, c.row_elems),
                                    dtype=torch.bfloat16, device=dev)
-        # appended rows of every step
-        a_hi = c.append_hi
-        self.app_rows = torch.zeros((c.total_steps, c.pairs, a_hi, c.row_elems),
-                                    dtype=torch.int16, device=dev)
         pairs = [(r, s) for r in range(c.requests) for s in range(c.sources)]
         for step in range(1, c.total_steps + 1):
             _, rows = self.wl.appended_rows(step, pairs)
@@ -235,11 +260,15 @@ class GpuRun:
         cout = (dhs.dhs_copy * max(1, len(outs)))(*[dhs.dhs_copy(*c) for c in outs])
         return (self.pool.h, cin, len(ins), arr, n, ctypes.byref(st), cout, len(outs))
 
-    def step_host(self, step, ins=None, outs=None, io=None):
+    def step_host(self, step, ins=None, outs=None, io=None, wait=True):
         """dhs_decode_step_host with prebuilt `io` (host_io) or with ins/outs;
-        returns after the outputs have landed in host memory."""
+        returns after the outputs have landed in host memory, or (wait=False,
+        dhs_decode_step_host_async) once everything is enqueued."""
         io = io or self.host_io(step, ins, outs)
-        dhs.check(dhs.lib.dhs_decode_step_host(*io), "dhs_decode_step_host")
+        if wait:
+            dhs.check(dhs.lib.dhs_decode_step_host(*io), "dhs_decode_step_host")
+        else:
+            dhs.check(dhs.lib.dhs_decode_step_host_async(*io), "dhs_decode_step_host_async")
 
     def reset(self):
         """Release every request and admit it again: the pool returns to its

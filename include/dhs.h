@@ -436,6 +436,19 @@ int dhs_decode_step_host(dhs_pool *pool, const dhs_copy *in, int32_t n_in,
                          const dhs_step *step, const dhs_copy *out, int32_t n_out);
 
 /*
+ * dhs_decode_step_host without the final synchronisation: it returns once
+ * the copies and the step are enqueued on the pool's stream.  The caller
+ * waits for that stream (an event recorded on it after the call) before it
+ * reads the outputs or reuses the input buffers, and may enqueue the next
+ * step meanwhile, so that the host prepares step s+1 while the device runs
+ * step s.  Errors: as dhs_decode_step_host (device-side errors go to
+ * dhs_status).
+ */
+int dhs_decode_step_host_async(dhs_pool *pool, const dhs_copy *in, int32_t n_in,
+                               const dhs_append_item *appends, int32_t n_appends,
+                               const dhs_step *step, const dhs_copy *out, int32_t n_out);
+
+/*
  * Synchronise the pool's stream, read and clear the sticky device status.
  * *flags (may be NULL) receives DHS_STATUS_* bits.  Returns DHS_OK when no
  * flag was set, else DHS_ERANGE (ERANGE or ELOC), DHS_EBUDGET or

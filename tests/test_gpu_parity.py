@@ -476,6 +476,51 @@ def test_decode_step_host_matches_device_path():
         b.close()
 
 
+def test_decode_step_host_async_pipelined_matches_device_path():
+    """dhs_decode_step_host_async with step s+1 enqueued before step s's
+    outputs are read (two host output sets) gives what the device-side
+    dhs_decode_step leaves in device memory, step by step."""
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    cfg = SMALL[1]
+    wl = Workload(cfg)
+    a, b = GpuRun(cfg, wl), GpuRun(cfg, wl)
+    try:
+        def span(dst, src):
+            return (dst.data_ptr(), src.data_ptr(), src.numel() * src.element_size())
+
+        outs = [(torch.empty(b.loc.shape, dtype=b.loc.dtype).pin_memory(),
+                 torch.empty(b.counters.shape, dtype=b.counters.dtype).pin_memory())
+                for _ in range(2)]
+        ins = [(b.sel[s].cpu().pin_memory(), b.app_rows[s].cpu().pin_memory())
+               for s in range(cfg.total_steps)]
+        b.sel.zero_()  # the calls must bring the inputs in themselves
+        b.app_rows.zero_()
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        want = []
+        for step in range(1, cfg.total_steps + 1):
+            a.step(step)
+            want.append((a.loc.cpu(), a.counters.cpu(), a.staging.clone()))
+        for step in range(1, cfg.total_steps + 1):
+            j = (step - 1) % 2
+            sel_h, rows_h = ins[step - 1]
+            b.step_host(step, [span(b.sel[step - 1], sel_h), span(b.app_rows[step - 1], rows_h)],
+                        [span(outs[j][0], b.loc), span(outs[j][1], b.counters)], wait=False)
+            done[j].record(torch.cuda.current_stream())
+            if step > 1:
+                done[1 - j].synchronize()
+                loc_w, cnt_w, _ = want[step - 2]
+                assert torch.equal(outs[1 - j][0], loc_w) and torch.equal(outs[1 - j][1], cnt_w)
+        done[(cfg.total_steps - 1) % 2].synchronize()
+        loc_w, cnt_w, stg_w = want[-1]
+        last = outs[(cfg.total_steps - 1) % 2]
+        assert torch.equal(last[0], loc_w) and torch.equal(last[1], cnt_w)
+        assert torch.equal(stg_w.view(torch.int16), b.staging.view(torch.int16))
+        assert a.status() == (0, 0) and b.status() == (0, 0)
+    finally:
+        a.close()
+        b.close()
+
+
 MAXHOT = TINY.scaled(name="maxhot", tag=53, requests=1, sources=1, hot=16384, history=65536,
                      topk=4096, residency=0.0, steps=10, window=4096, frac_recent=0.3,
                      zipf_s=0.6, row_elems=64)
