@@ -366,34 +366,36 @@ def traced_pass(run, cycle, steps, dev, flush_l2):
 def measure_e2e(run, cycle, steps, dev, stream):
     """The metric through the C ABI with host buffers for `steps` further
     decode steps.  Each step copies its selections and decode rows in from
-    pinned host memory, runs, and copies its locations + counters (+ union
-    indices) back to pinned host memory, all inside the timed region.
+    pinned host memory (one block), runs, and copies its locations +
+    counters (+ union indices) back to pinned host memory (one block), all
+    inside the timed region.
 
-    value: pipelined as a serving loop runs it -- dhs_decode_step_host_async
-    enqueues step s+1 before the host waits for step s's outputs (an event on
-    the pool's stream) and reads them; outputs alternate between two host
-    buffer sets.  Wall clock over runs of consecutive steps (a workload's
-    pool reset between cycles is outside it).
+    value: pipelined as a serving loop runs it.  dhs_decode_step_host_async
+    puts each step's input copy on an input stream and its output copy on an
+    output stream, so step s+1's inputs come in and step s-1's outputs go out
+    while step s runs; the host waits for step s-1's outputs (an event) and
+    reads its counters after enqueuing step s.  Device output blocks and host
+    output buffers alternate between two sets.  Wall clock over runs of
+    consecutive steps (a workload's pool reset between cycles is outside it).
     sync_value: one blocking dhs_decode_step_host call per step, wall clock
     around each call."""
     import numpy as np
     import torch
     T = run.cfg.total_steps
-    # the step's inputs (selections, decode rows) and outputs (locations,
-    # counters, union indices) each lie in one block: one copy each way
     in_host = [run.step_in[s].cpu().pin_memory() for s in range(T)]
+    blocks = [run.step_out, run.second_outputs()]
 
     def span(dst, src):
         return (dst.data_ptr(), src.data_ptr(), src.numel() * src.element_size())
 
     cnt_off = run.counters.data_ptr() - run.step_out.data_ptr()
-    sets = []  # two sets of host outputs
-    for _ in range(2):
-        out_h = torch.empty(run.step_out.shape, dtype=torch.uint8).pin_memory()
+    sets = []  # host outputs of each device output block
+    for blk in blocks:
+        out_h = torch.empty(blk.shape, dtype=torch.uint8).pin_memory()
         cnt_h = out_h[cnt_off:cnt_off + run.counters.numel() * 4].view(torch.int32)
-        sets.append((cnt_h.view(run.counters.shape).numpy(), [span(out_h, run.step_out)], out_h))
+        sets.append((cnt_h.view(run.counters.shape).numpy(), [span(out_h, blk)], out_h))
     # the calls' arguments for every step of the cycle, built once as a caller would
-    io = [[run.host_io(s, [span(run.step_in[s - 1], in_host[s - 1])], sets[b][1])
+    io = [[run.host_io(s, [span(run.step_in[s - 1], in_host[s - 1])], sets[b][1], alt=b == 1)
            for s in range(1, T + 1)] for b in range(2)]
 
     def next_timed():
@@ -413,7 +415,9 @@ def measure_e2e(run, cycle, steps, dev, stream):
         run.step_host(s, io=io[0][s - 1])
         sync_dt += time.perf_counter() - t0
     # pipelined: runs of consecutive steps up to the end of the cycle
-    done = [torch.cuda.Event(), torch.cuda.Event()]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    kern_done = [torch.cuda.Event(), torch.cuda.Event()]  # the step's kernels, per set
+    out_done = [torch.cuda.Event(), torch.cuda.Event()]   # its output copy, per set
     dt, n, seen = 0.0, 0, 0
     while n < steps:
         seg = [next_timed()]
@@ -422,29 +426,35 @@ def measure_e2e(run, cycle, steps, dev, stream):
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for j, s in enumerate(seg):
-            run.step_host(s, io=io[j % 2][s - 1], wait=False)
-            done[j % 2].record(stream)
+            b = j % 2
+            if j >= 2:  # set b was last used two steps ago
+                s_in.wait_event(kern_done[b])
+                stream.wait_event(out_done[b])
+            run.step_host(s, io=io[b][s - 1], wait=False, in_stream=s_in, out_stream=s_out)
+            kern_done[b].record(stream)
+            out_done[b].record(s_out)
             if j:  # the previous step's outputs are in host memory: read them
-                done[(j - 1) % 2].synchronize()
-                seen += int(sets[(j - 1) % 2][0][..., 0].sum(dtype=np.int64))
-        done[(len(seg) - 1) % 2].synchronize()
-        seen += int(sets[(len(seg) - 1) % 2][0][..., 0].sum(dtype=np.int64))
+                out_done[1 - b].synchronize()
+                seen += int(sets[1 - b][0][..., 0].sum(dtype=np.int64))
+        last = (len(seg) - 1) % 2
+        out_done[last].synchronize()
+        seen += int(sets[last][0][..., 0].sum(dtype=np.int64))
         dt += time.perf_counter() - t0
         n += len(seg)
+    torch.cuda.synchronize(dev)
     c = run.cfg
     want = steps * c.requests * c.sources * c.queries * c.topk
     if seen != want:  # counters[0] = entries each resolved (request, source) took
         raise RuntimeError(f"e2e outputs: {seen} entries counted, {want} expected")
-    h2d = in_host[0].numel()
-    d2h = run.step_out.numel()
-    return {"value": run.cfg.entries_per_step * steps / dt, "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+    return {"value": c.entries_per_step * steps / dt, "unit": UNIT,
+            "h2d_bytes_per_step": int(in_host[0].numel()),
+            "d2h_bytes_per_step": int(run.step_out.numel()),
             "steps": steps, "seconds": dt,
-            "sync_value": run.cfg.entries_per_step * steps / sync_dt,
-            "path": "dhs_decode_step_host_async per step (H2D copies, decode step, D2H "
-                    "copies), the next step enqueued before the host waits for and "
-                    "reads the previous step's outputs; sync_value: blocking "
-                    "dhs_decode_step_host, one call per step"}
+            "sync_value": c.entries_per_step * steps / sync_dt,
+            "path": "dhs_decode_step_host_async per step: input copy on an input stream, "
+                    "step, output copy on an output stream (two output sets), the "
+                    "previous step's outputs waited for and read after each call; "
+                    "sync_value: blocking dhs_decode_step_host, one call per step"}
 
 
 def run_loadstep(args):

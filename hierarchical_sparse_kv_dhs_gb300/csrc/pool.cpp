@@ -200,6 +200,9 @@ struct dhs_pool {
   // dhs_prefetch: resolves enqueued on a caller's side stream; the pool's
   // stream waits for them before its next device work
   cudaEvent_t ev_main = nullptr, ev_prefetch = nullptr;
+  // dhs_decode_step_host_async on callers' copy streams: the step waits for
+  // the inputs (ev_in), the outputs' copies wait for the step (ev_step)
+  cudaEvent_t ev_in = nullptr, ev_step = nullptr;
   bool prefetch_pending = false;
   bool join_gathers = true;  // enter(): also join gathers on other streams
   std::vector<uint8_t> pf_pair;  // pairs resolved by the outstanding prefetch
@@ -210,6 +213,8 @@ struct dhs_pool {
   ~dhs_pool() {
     if (ev_main) cudaEventDestroy(ev_main);
     if (ev_prefetch) cudaEventDestroy(ev_prefetch);
+    if (ev_in) cudaEventDestroy(ev_in);
+    if (ev_step) cudaEventDestroy(ev_step);
     for (cudaEvent_t e : ev_free) cudaEventDestroy(e);
     for (cudaEvent_t e : ev_gathers) cudaEventDestroy(e);
   }
@@ -524,7 +529,9 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
   }
   if (dhs::gather_set_smem_limit(cfg->row_bytes, optin, &p->tma_ok) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->ev_main, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&p->ev_prefetch, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventCreateWithFlags(&p->ev_prefetch, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_in, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_step, cudaEventDisableTiming) != cudaSuccess) {
     delete p;
     return DHS_ECUDA;
   }
@@ -1328,8 +1335,9 @@ int dhs_decode_step(dhs_pool* p, const dhs_append_item* apps, int32_t n_apps,
 }
 
 int dhs_decode_step_host_async(dhs_pool* p, const dhs_copy* in, int32_t n_in,
-                               const dhs_append_item* apps, int32_t n_apps,
-                               const dhs_step* st, const dhs_copy* out, int32_t n_out) {
+                               void* in_stream, const dhs_append_item* apps, int32_t n_apps,
+                               const dhs_step* st, const dhs_copy* out, int32_t n_out,
+                               void* out_stream) {
   if (!p || n_in < 0 || n_out < 0 || (n_in > 0 && !in) || (n_out > 0 && !out))
     return DHS_EINVAL;
   for (int32_t i = 0; i < n_in; ++i)
@@ -1338,14 +1346,24 @@ int dhs_decode_step_host_async(dhs_pool* p, const dhs_copy* in, int32_t n_in,
     if (out[i].bytes && (!out[i].dst || !out[i].src)) return DHS_EINVAL;
   int rc = enter(p);
   if (rc) return rc;
+  cudaStream_t sin = in_stream ? (cudaStream_t)in_stream : p->stream;
+  cudaStream_t sout = out_stream ? (cudaStream_t)out_stream : p->stream;
   for (int32_t i = 0; i < n_in; ++i)
     if (in[i].bytes && cudaMemcpyAsync(in[i].dst, in[i].src, in[i].bytes,
-                                       cudaMemcpyHostToDevice, p->stream) != cudaSuccess)
+                                       cudaMemcpyHostToDevice, sin) != cudaSuccess)
       return DHS_ECUDA;
+  if (sin != p->stream && n_in > 0 &&
+      (cudaEventRecord(p->ev_in, sin) != cudaSuccess ||
+       cudaStreamWaitEvent(p->stream, p->ev_in, 0) != cudaSuccess))
+    return DHS_ECUDA;
   if ((rc = dhs_decode_step(p, apps, n_apps, st))) return rc;
+  if (sout != p->stream && n_out > 0 &&
+      (cudaEventRecord(p->ev_step, p->stream) != cudaSuccess ||
+       cudaStreamWaitEvent(sout, p->ev_step, 0) != cudaSuccess))
+    return DHS_ECUDA;
   for (int32_t i = 0; i < n_out; ++i)
     if (out[i].bytes && cudaMemcpyAsync(out[i].dst, out[i].src, out[i].bytes,
-                                        cudaMemcpyDeviceToHost, p->stream) != cudaSuccess)
+                                        cudaMemcpyDeviceToHost, sout) != cudaSuccess)
       return DHS_ECUDA;
   return DHS_OK;
 }
@@ -1353,7 +1371,8 @@ int dhs_decode_step_host_async(dhs_pool* p, const dhs_copy* in, int32_t n_in,
 int dhs_decode_step_host(dhs_pool* p, const dhs_copy* in, int32_t n_in,
                          const dhs_append_item* apps, int32_t n_apps, const dhs_step* st,
                          const dhs_copy* out, int32_t n_out) {
-  const int rc = dhs_decode_step_host_async(p, in, n_in, apps, n_apps, st, out, n_out);
+  const int rc = dhs_decode_step_host_async(p, in, n_in, nullptr, apps, n_apps, st, out,
+                                            n_out, nullptr);
   if (rc) return rc;
   return cudaStreamSynchronize(p->stream) == cudaSuccess ? DHS_OK : DHS_ECUDA;
 }

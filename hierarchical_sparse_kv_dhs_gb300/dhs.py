@@ -97,8 +97,8 @@ def _load():
         "dhs_prefetch": (ctypes.c_int, [_vp, _vp, _vp]),
         "dhs_gather_on": (ctypes.c_int, [_vp, _vp, _vp]),
         "dhs_decode_step_host": (ctypes.c_int, [_vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32]),
-        "dhs_decode_step_host_async": (ctypes.c_int,
-                                       [_vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32]),
+        "dhs_decode_step_host_async": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _i32, _vp,
+                                                      _vp, _i32, _vp]),
         "dhs_admit_device": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _i64, _vp, P(_i64)]),
         "dhs_backup": (ctypes.c_int, [_vp, _i64, P(_i64)]),
         "dhs_pending_backup": (_i64, [_vp]),

@@ -140,14 +140,14 @@ class GpuRun:
         return a.view(np.uint16).reshape(n, c.row_elems)
 
     # ---------------------------------------------------------- descriptors
-    def _build_descriptors(self):
+    def _make_steps(self, loc, counters, index):
+        """Step descriptors of every step with outputs in `loc`, `counters`
+        (and union `index`): one dhs_step per step and one per layer."""
         c = self.cfg
         Q, k, rb = c.queries, c.topk, c.row_bytes
-        self._steps, self._appends, self._layer_steps = [], [], []
-        loc0 = self.loc.data_ptr()
-        cnt0 = self.counters.data_ptr()
+        steps, layer_steps = [], []
+        loc0, cnt0 = loc.data_ptr(), counters.data_ptr()
         stg0 = self.staging.data_ptr()
-        nsel = 1 if c.shared_selection else c.sources
         for step in range(1, c.total_steps + 1):
             items = []
             for r in range(c.requests):
@@ -157,16 +157,24 @@ class GpuRun:
                     it.flags = dhs.DHS_ITEM_GATHER_ONLY if kind == "reuse" else 0
                     if self.union and kind != "reuse":
                         it.flags |= dhs.DHS_ITEM_UNION
-                        it.index_dev = self.index[r, s].data_ptr()
+                        it.index_dev = index[r, s].data_ptr()
                     ss = 0 if c.shared_selection else s
                     it.sel_dev = self.sel[step - 1, r, ss].data_ptr()
                     it.loc_dev = loc0 + ((r * c.sources + s) * Q * k) * 4
                     it.counters_dev = cnt0 + (r * c.sources + s) * 32
                     it.staging_dev = stg0 + ((r * len(self.layers) + layer) * Q * k) * rb
                     items.append(it)
-            self._steps.append(dhs.make_step(step, items))
+            steps.append(dhs.make_step(step, items))
             nl = len(self.layers)
-            self._layer_steps.append([dhs.make_step(step, items[l::nl]) for l in range(nl)])
+            layer_steps.append([dhs.make_step(step, items[l::nl]) for l in range(nl)])
+        return steps, layer_steps
+
+    def _build_descriptors(self):
+        c = self.cfg
+        self._steps, self._layer_steps = self._make_steps(self.loc, self.counters, self.index)
+        self._steps_alt = None
+        self._appends = []
+        for step in range(1, c.total_steps + 1):
             apps = []
             for i, (r, s) in enumerate((r, s) for r in range(c.requests)
                                        for s in range(c.sources)):
@@ -177,7 +185,21 @@ class GpuRun:
                 apps.append(a)
             arr = (dhs.dhs_append_item * len(apps))(*apps)
             self._appends.append((arr, len(apps)))
-        del nsel
+
+    def second_outputs(self):
+        """A second output block (locations, counters, union indices) laid out
+        as step_out, and step descriptors that write it: a pipelined caller
+        alternates the two while one block's copy to the host is in flight."""
+        if self._steps_alt is None:
+            self.step_out_alt = torch.zeros_like(self.step_out)
+            off = lambda t: t.data_ptr() - self.step_out.data_ptr()
+            view = lambda t: self.step_out_alt[off(t):off(t) + t.numel() * 4].view(
+                torch.int32).view(t.shape)
+            self.loc_alt, self.counters_alt = view(self.loc), view(self.counters)
+            self.index_alt = view(self.index) if self.index is not None else None
+            self._steps_alt, _ = self._make_steps(self.loc_alt, self.counters_alt,
+                                                  self.index_alt)
+        return self.step_out_alt
 
     # ---------------------------------------------------------- stepping
     def append(self, step):
@@ -251,24 +273,31 @@ class GpuRun:
         dhs.check(dhs.lib.dhs_decode_step(self.pool.h, arr, n, ctypes.byref(st)),
                   "dhs_decode_step")
 
-    def host_io(self, step, ins, outs):
+    def host_io(self, step, ins, outs, alt=False):
         """Prebuilt arguments of dhs_decode_step_host for `step`: `ins` /
-        `outs` are lists of (dst, src, bytes) host<->device copies."""
+        `outs` are lists of (dst, src, bytes) host<->device copies; `alt`:
+        the step writes the second output block (second_outputs)."""
         arr, n = self._appends[step - 1]
-        st, _ = self._steps[step - 1]
+        st, _ = (self._steps_alt if alt else self._steps)[step - 1]
         cin = (dhs.dhs_copy * max(1, len(ins)))(*[dhs.dhs_copy(*c) for c in ins])
         cout = (dhs.dhs_copy * max(1, len(outs)))(*[dhs.dhs_copy(*c) for c in outs])
         return (self.pool.h, cin, len(ins), arr, n, ctypes.byref(st), cout, len(outs))
 
-    def step_host(self, step, ins=None, outs=None, io=None, wait=True):
+    def step_host(self, step, ins=None, outs=None, io=None, wait=True, in_stream=None,
+                  out_stream=None):
         """dhs_decode_step_host with prebuilt `io` (host_io) or with ins/outs;
         returns after the outputs have landed in host memory, or (wait=False,
-        dhs_decode_step_host_async) once everything is enqueued."""
+        dhs_decode_step_host_async) once everything is enqueued, the copies on
+        `in_stream` / `out_stream` (torch streams; None = the pool's)."""
         io = io or self.host_io(step, ins, outs)
         if wait:
             dhs.check(dhs.lib.dhs_decode_step_host(*io), "dhs_decode_step_host")
-        else:
-            dhs.check(dhs.lib.dhs_decode_step_host_async(*io), "dhs_decode_step_host_async")
+            return
+        h, cin, nin, arr, n, st, cout, nout = io
+        sin = ctypes.c_void_p(in_stream.cuda_stream if in_stream is not None else None)
+        sout = ctypes.c_void_p(out_stream.cuda_stream if out_stream is not None else None)
+        dhs.check(dhs.lib.dhs_decode_step_host_async(h, cin, nin, sin, arr, n, st, cout, nout,
+                                                     sout), "dhs_decode_step_host_async")
 
     def reset(self):
         """Release every request and admit it again: the pool returns to its

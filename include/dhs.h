@@ -436,17 +436,26 @@ int dhs_decode_step_host(dhs_pool *pool, const dhs_copy *in, int32_t n_in,
                          const dhs_step *step, const dhs_copy *out, int32_t n_out);
 
 /*
- * dhs_decode_step_host without the final synchronisation: it returns once
- * the copies and the step are enqueued on the pool's stream.  The caller
- * waits for that stream (an event recorded on it after the call) before it
- * reads the outputs or reuses the input buffers, and may enqueue the next
- * step meanwhile, so that the host prepares step s+1 while the device runs
- * step s.  Errors: as dhs_decode_step_host (device-side errors go to
- * dhs_status).
+ * dhs_decode_step_host without the final synchronisation, for a pipelined
+ * caller: it returns once everything is enqueued.
+ *   - The n_in host-to-device copies go on `in_stream` (a cudaStream_t; NULL
+ *     = the pool's stream) with no other ordering: the caller makes that
+ *     stream wait until earlier work is done with the input buffers.  The
+ *     step waits for them.
+ *   - The step runs on the pool's stream, after everything already on it.
+ *   - The n_out device-to-host copies go on `out_stream` (NULL = the pool's
+ *     stream) after the step.  The caller waits for them (an event it records
+ *     on that stream) before it reads the outputs, and makes the pool's
+ *     stream wait for them before a later step writes the same device
+ *     buffers: the pool does not track readers of the caller's buffers.
+ * With separate streams and alternating buffers, step s+1's inputs come in
+ * and step s-1's outputs go out while step s runs.  Errors: as
+ * dhs_decode_step_host (device-side errors go to dhs_status).
  */
 int dhs_decode_step_host_async(dhs_pool *pool, const dhs_copy *in, int32_t n_in,
-                               const dhs_append_item *appends, int32_t n_appends,
-                               const dhs_step *step, const dhs_copy *out, int32_t n_out);
+                               void *in_stream, const dhs_append_item *appends,
+                               int32_t n_appends, const dhs_step *step,
+                               const dhs_copy *out, int32_t n_out, void *out_stream);
 
 /*
  * Synchronise the pool's stream, read and clear the sticky device status.

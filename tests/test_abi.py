@@ -101,7 +101,8 @@ def test_null_arguments(dhs):
         assert getattr(dhs.lib, fn)(None, None) == E, fn
     assert dhs.lib.dhs_decode_step(None, None, 0, None) == E
     assert dhs.lib.dhs_decode_step_host(None, None, 0, None, 0, None, None, 0) == E
-    assert dhs.lib.dhs_decode_step_host_async(None, None, 0, None, 0, None, None, 0) == E
+    assert dhs.lib.dhs_decode_step_host_async(None, None, 0, None, None, 0, None, None, 0,
+                                              None) == E
     assert dhs.lib.dhs_prefetch(None, None, None) == E
     assert dhs.lib.dhs_gather_on(None, None, None) == E
     assert dhs.lib.dhs_set_option(None, dhs.DHS_OPT_EARLY, 1) == E

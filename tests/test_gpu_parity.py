@@ -476,10 +476,13 @@ def test_decode_step_host_matches_device_path():
         b.close()
 
 
-def test_decode_step_host_async_pipelined_matches_device_path():
+@pytest.mark.parametrize("streams", [False, True])
+def test_decode_step_host_async_pipelined_matches_device_path(streams):
     """dhs_decode_step_host_async with step s+1 enqueued before step s's
-    outputs are read (two host output sets) gives what the device-side
-    dhs_decode_step leaves in device memory, step by step."""
+    outputs are read (two host output sets; with `streams`, the input and
+    output copies on their own streams and two device output blocks, as the
+    bench's e2e runs it) gives what the device-side dhs_decode_step leaves
+    in device memory, step by step."""
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     cfg = SMALL[1]
     wl = Workload(cfg)
@@ -488,33 +491,47 @@ def test_decode_step_host_async_pipelined_matches_device_path():
         def span(dst, src):
             return (dst.data_ptr(), src.data_ptr(), src.numel() * src.element_size())
 
-        outs = [(torch.empty(b.loc.shape, dtype=b.loc.dtype).pin_memory(),
-                 torch.empty(b.counters.shape, dtype=b.counters.dtype).pin_memory())
-                for _ in range(2)]
-        ins = [(b.sel[s].cpu().pin_memory(), b.app_rows[s].cpu().pin_memory())
-               for s in range(cfg.total_steps)]
-        b.sel.zero_()  # the calls must bring the inputs in themselves
-        b.app_rows.zero_()
-        done = [torch.cuda.Event(), torch.cuda.Event()]
+        blocks = [b.step_out, b.second_outputs() if streams else b.step_out]
+        cnt_off = b.counters.data_ptr() - b.step_out.data_ptr()
+        loc_n, cnt_n = b.loc.numel() * 4, b.counters.numel() * 4
+        outs = [torch.empty(blk.shape, dtype=torch.uint8).pin_memory() for blk in blocks]
+        ins = [b.step_in[s].cpu().pin_memory() for s in range(cfg.total_steps)]
+        b.step_in.zero_()  # the calls must bring the inputs in themselves
         want = []
         for step in range(1, cfg.total_steps + 1):
             a.step(step)
             want.append((a.loc.cpu(), a.counters.cpu(), a.staging.clone()))
+        pool_stream = torch.cuda.current_stream()
+        s_in = torch.cuda.Stream() if streams else None
+        s_out = torch.cuda.Stream() if streams else None
+        kern_done = [torch.cuda.Event(), torch.cuda.Event()]
+        out_done = [torch.cuda.Event(), torch.cuda.Event()]
+
+        def check(j, step):
+            o = outs[j]
+            loc_w, cnt_w, _ = want[step - 1]
+            assert torch.equal(o[:loc_n].view(torch.int32).view(loc_w.shape), loc_w), step
+            assert torch.equal(o[cnt_off:cnt_off + cnt_n].view(torch.int32).view(cnt_w.shape),
+                               cnt_w), step
+
         for step in range(1, cfg.total_steps + 1):
             j = (step - 1) % 2
-            sel_h, rows_h = ins[step - 1]
-            b.step_host(step, [span(b.sel[step - 1], sel_h), span(b.app_rows[step - 1], rows_h)],
-                        [span(outs[j][0], b.loc), span(outs[j][1], b.counters)], wait=False)
-            done[j].record(torch.cuda.current_stream())
+            if step > 2 and streams:
+                s_in.wait_event(kern_done[j])
+                pool_stream.wait_event(out_done[j])
+            io = b.host_io(step, [span(b.step_in[step - 1], ins[step - 1])],
+                           [span(outs[j], blocks[j])], alt=streams and j == 1)
+            b.step_host(step, io=io, wait=False, in_stream=s_in, out_stream=s_out)
+            kern_done[j].record(pool_stream)
+            out_done[j].record(s_out if streams else pool_stream)
             if step > 1:
-                done[1 - j].synchronize()
-                loc_w, cnt_w, _ = want[step - 2]
-                assert torch.equal(outs[1 - j][0], loc_w) and torch.equal(outs[1 - j][1], cnt_w)
-        done[(cfg.total_steps - 1) % 2].synchronize()
-        loc_w, cnt_w, stg_w = want[-1]
-        last = outs[(cfg.total_steps - 1) % 2]
-        assert torch.equal(last[0], loc_w) and torch.equal(last[1], cnt_w)
-        assert torch.equal(stg_w.view(torch.int16), b.staging.view(torch.int16))
+                out_done[1 - j].synchronize()
+                check(1 - j, step - 1)
+        last = (cfg.total_steps - 1) % 2
+        out_done[last].synchronize()
+        check(last, cfg.total_steps)
+        torch.cuda.synchronize()
+        assert torch.equal(want[-1][2].view(torch.int16), b.staging.view(torch.int16))
         assert a.status() == (0, 0) and b.status() == (0, 0)
     finally:
         a.close()
