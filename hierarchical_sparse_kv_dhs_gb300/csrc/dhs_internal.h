@@ -208,6 +208,7 @@ struct GatherCommon {
   uint32_t* status;
   int32_t n_items;
   int32_t n_tiles;
+  int32_t item_tiles;         // tiles of every item when all items have as many, else 0
   int32_t T, Pmax, page_shift;
   int32_t early;             // copy step-1 rows before waiting for the resolve grid
   unsigned long long* trace;  // null = off

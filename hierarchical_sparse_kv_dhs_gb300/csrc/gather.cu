@@ -86,6 +86,7 @@ __device__ __forceinline__ bool fresh_loc(const GatherCommon& c, uint32_t loc) {
 
 template <int MAXI>
 __device__ __forceinline__ int find_item(const GatherParams<MAXI>& P, int tile) {
+  if (P.c.item_tiles > 0) return tile / P.c.item_tiles;  // equal items: no search
   int lo = 0, hi = P.c.n_items - 1;  // last item whose first tile <= tile
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;

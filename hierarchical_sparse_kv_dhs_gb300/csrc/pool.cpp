@@ -1201,14 +1201,17 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   const int tile_rows = dhs::gather_tile_rows(p->gather_impl);
   for (size_t b = 0; b < ng; b += dhs::kGatherItemsLarge) {
     const int n = (int)std::min<size_t>(dhs::kGatherItemsLarge, ng - b);
-    int64_t tiles = 0;
+    int64_t tiles = 0, per = -1;
     for (int i = 0; i < n; ++i) {
       dhs::GatherItem& gi = p->gitems[b + i];
       gi.tile0 = (int32_t)tiles;
-      tiles += (gi.n + tile_rows - 1) / tile_rows;
+      const int64_t t = (gi.n + tile_rows - 1) / tile_rows;
+      per = i == 0 ? t : (per == t ? per : 0);
+      tiles += t;
     }
     if (tiles > INT32_MAX) return DHS_EINVAL;
     g.n_tiles = (int32_t)tiles;
+    g.item_tiles = (int32_t)std::max<int64_t>(per, 0);
     // only the first gather launch directly follows the resolve launches
     if (dhs::launch_gather(g, p->gitems.data() + b, n, fused && b == 0, p->gather_impl,
                           p->stream) !=
