@@ -202,7 +202,6 @@ struct GatherCommon {
   const uint8_t* opt;
   const uint8_t* hot;
   const int32_t* map;          // [pairs][Pmax] page map (early phase)
-  const int32_t* pair_status;  // resolve status per pair (early phase)
   uint32_t tail_rows, opt_rows, hot_rows;  // arena sizes in rows
   int32_t row_bytes;
   uint32_t* status;

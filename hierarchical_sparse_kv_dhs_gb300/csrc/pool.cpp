@@ -1134,7 +1134,6 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   g.opt = (const uint8_t*)c.opt_dev;
   g.hot = (const uint8_t*)c.hot_dev;
   g.map = p->map;
-  g.pair_status = p->pair_status;
   g.tail_rows = (uint32_t)(p->pairs * c.tail_rows);
   g.opt_rows = (uint32_t)(c.optional_pages * c.page_rows);
   g.hot_rows = (uint32_t)(p->pairs * c.hot_rows);
