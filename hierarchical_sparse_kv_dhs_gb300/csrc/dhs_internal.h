@@ -106,6 +106,7 @@ struct ResolveCommon {
   uint32_t seq;          // sequence number of this launch
   int32_t uni;           // shared-memory plan includes the union bitmap
   uint32_t* loc_ready;   // [pairs] seq once the item's locations are written; null = off
+  uint32_t* copy_ready;  // [pairs] seq once its miss lists (and staging entries) are written
   uint32_t* fill;        // [pairs][fill_words] hot slots filled by this step's copy
   uint32_t* later_count; // [2] fresh-row list lengths; the launch zeroes [gen ^ 1]
   int32_t fill_words;
@@ -152,7 +153,7 @@ struct CopyCommon {
   const uint32_t* miss_count;
   int32_t B, Mcap, row_bytes, n_items;
   unsigned long long* trace;  // null = off
-  const uint32_t* loc_ready;  // [pairs] the resolve launch's per-item marks, null = none
+  const uint32_t* ready;      // [pairs] the resolve launch's copy_ready marks, null = none
   uint32_t seq;               // that launch's sequence number
   int32_t ent_cap;
   const int32_t* miss_off;    // [pairs][Mcap + 1] (items with staging)

@@ -39,9 +39,10 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 }
 
 // Copy the miss rows of the launch's items.  CTA b owns items b, b + gridDim,
-// ...  An item's miss list (rows ascending, victim slots) is complete once
-// the resolve kernel has published the item's locations (loc_ready == seq,
-// after a fence), so the CTA does not wait for the whole resolve grid: it
+// ...  An item's miss list (rows ascending, victim slots, staging entries)
+// is complete once the resolve kernel has published its copy_ready mark
+// (== seq, after a fence; before the item's locations are written), so the
+// CTA does not wait for the whole resolve grid: it
 // takes, in order, every owned item whose mark is out as one batch (waiting,
 // bounded, only when none is), and its warps copy the batch's rows as one
 // flat list, four rows per warp in flight.  A poll that runs out falls back
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(kCopyThreads)
   const int cpr = rb >> 4;
   const uint32_t warp = (uint32_t)tid >> 5, nwarps = blockDim.x >> 5;
   const uint32_t want = c.seq & kSeqMask;
-  bool waited = c.loc_ready == nullptr, traced = false;
+  bool waited = c.ready == nullptr, traced = false;
   if (waited) asm volatile("griddepcontrol.wait;" ::: "memory");
   int next = blockIdx.x;
   for (;;) {
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(kCopyThreads)
       int n = 0, j = next, need_wait = 0;
       uint32_t acc = 0;
       while (j < c.n_items && n < kBatchMax) {
-        const uint32_t* mark = c.loc_ready + P.items[j].pair;
+        const uint32_t* mark = c.ready + P.items[j].pair;
         bool ok = waited || ld_acquire_u32(mark) == want;
         for (uint32_t i = 0; !ok && n == 0 && i < kReadyPolls; ++i) {
           __nanosleep(256);
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kCopyThreads)
     const int n = s_n, nxt = s_next;
     if (n == 0) break;
     if (!waited)  // each thread's own acquire of the batch's marks
-      for (int b = 0; b < n; ++b) (void)ld_acquire_u32(c.loc_ready + P.items[s_item[b]].pair);
+      for (int b = 0; b < n; ++b) (void)ld_acquire_u32(c.ready + P.items[s_item[b]].pair);
     if (tid == 0 && !traced) {
       trace_mark(c.trace, kTraceCopy, false);  // copying starts
       traced = true;

@@ -38,7 +38,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct MetaLayout {
   size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status;
-  size_t loc_ready, fill, later_count, status, later, miss_off, miss_ent;
+  size_t loc_ready, copy_ready, fill, later_count, status, later, miss_off, miss_ent;
   size_t total;
 };
 
@@ -81,6 +81,7 @@ MetaLayout meta_layout(const dhs_pool_config& c) {
   m.miss_count = take(pairs * 4);
   m.pair_status = take(pairs * 4);
   m.loc_ready = take(pairs * 4);
+  m.copy_ready = take(pairs * 4);
   m.fill = take(pairs * (size_t)fill_words_of(c) * 4);
   m.later_count = take(2 * 4);
   m.status = take(64);
@@ -168,6 +169,7 @@ struct dhs_pool {
   int early = 1;        // fused gathers copy step-1 rows before the resolve ends
   uint32_t seq = 0;             // resolve launches so far
   uint32_t* loc_ready = nullptr;  // [pairs] per-item "locations written" marks
+  uint32_t* copy_ready = nullptr; // [pairs] per-item "miss lists written" marks
   uint32_t* fill = nullptr;       // [pairs][fill_words] slots the step's copy fills
   uint32_t* later_count = nullptr;
   dhs::LaterEntry* later = nullptr;
@@ -499,6 +501,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->miss_count = (uint32_t*)(m + p->layout.miss_count);
     p->pair_status = (int32_t*)(m + p->layout.pair_status);
     p->loc_ready = (uint32_t*)(m + p->layout.loc_ready);
+    p->copy_ready = (uint32_t*)(m + p->layout.copy_ready);
     p->fill = (uint32_t*)(m + p->layout.fill);
     p->later_count = (uint32_t*)(m + p->layout.later_count);
     p->later = (dhs::LaterEntry*)(m + p->layout.later);
@@ -1034,6 +1037,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   p->fused_resolved = fused && !p->ritems.empty();
   if (p->fused_resolved) ++p->gen;
   rcm.loc_ready = p->loc_ready;
+  rcm.copy_ready = p->copy_ready;
   rcm.fill = p->fill;
   rcm.fill_words = p->fill_words;
   rcm.later_count = p->later_count;
@@ -1071,7 +1075,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     rcm.qkcap = (int32_t)qmax;
     rcm.seq = ++p->seq & dhs::kSeqMask;
     if (rcm.seq == 0) rcm.seq = p->seq = 1;  // 0 never matches a published mark
-    ccm.loc_ready = rcm.loc_ready;  // the copy starts on each item once it is resolved
+    ccm.ready = rcm.copy_ready;  // the copy starts on each item once its misses are listed
     ccm.seq = rcm.seq;
     for (int i = 0; i < n; ++i) p->seq_of_pair[p->ritems[b + i].pair] = rcm.seq;
     rcm.uni = uni ? 1 : 0;

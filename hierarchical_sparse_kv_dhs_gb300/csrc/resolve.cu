@@ -220,6 +220,15 @@ __device__ __forceinline__ void publish_loc(const ResolveCommon& c, int pair) {
                "r"(c.seq & kSeqMask) : "memory");
 }
 
+// Publish that an item's miss count, miss lists and staging entries are
+// written (thread 0 only, after a block barrier): its host copy may start.
+__device__ __forceinline__ void publish_copy(const ResolveCommon& c, int pair) {
+  if (!c.copy_ready) return;
+  __threadfence();
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(c.copy_ready + pair),
+               "r"(c.seq & kSeqMask) : "memory");
+}
+
 // Write the failure result of one item: no state change, zero counters.
 // Step 1 of "Resolution" reads no state that resolution changes, so the
 // entries it resolves keep their locations (the tail, or a ready page of the
@@ -255,8 +264,9 @@ __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t
   if (threadIdx.x < 8 && it.counters) it.counters[threadIdx.x] = 0u;
   __syncthreads();
   if (threadIdx.x == 0) {
-    c.miss_count[it.pair] = 0u;  // before the mark: the host copy reads it then
+    c.miss_count[it.pair] = 0u;  // before the marks: the host copy reads it then
     c.pair_status[it.pair] = code;
+    publish_copy(c, it.pair);
     publish_loc(c, it.pair);
     atomicOr(c.status, flag);
     trace_mark(c.trace, kTraceResolve, true);
@@ -517,43 +527,6 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
       if (s.st[j] == step) stamps[j] = step;
   }
 
-  // ---- location vector
-  const int ps = c.page_shift;
-  const int64_t pmask = ((int64_t)1 << ps) - 1;
-  auto loc_of = [&](int32_t row) -> uint32_t {
-    if ((int64_t)row >= t0)
-      return (kTierTail << 30) | (uint32_t)((int64_t)pair * T + (int64_t)row % T);
-    const uint64_t m = s.bm[row >> 6];  // rows that went to the hot cache
-    const uint64_t bit = 1ull << (row & 63);
-    if (m & bit) {
-      const uint32_t r = s.wpre[row >> 6] + (uint32_t)__popcll(m & (bit - 1ull));
-      return (kTierHot << 30) | (uint32_t)((int64_t)pair * B + s.slot_of[r]);
-    }
-    const int32_t slot = map[row >> ps];
-    return (kTierOpt << 30) | (uint32_t)(((int64_t)slot << ps) + (row & pmask));
-  };
-  if (!uni) {
-    for (int e = tid; e < n; e += nt) it.loc[e] = loc_of(it.sel[e]);
-  } else {
-    // union staging: each entry's rank among the distinct rows, the distinct
-    // rows' locations in ascending row order, then the end marker
-    for (int e = tid; e < n; e += nt) {
-      const int32_t row = it.sel[e];
-      const uint64_t bit = 1ull << (row & 63);
-      it.index[e] = (int32_t)(s.upre[row >> 6] +
-                              (uint32_t)__popcll(s.ubm[row >> 6] & (bit - 1ull)));
-    }
-    for (int w = tid; w < W; w += nt) {
-      uint64_t m = s.ubm[w];
-      uint32_t u = s.upre[w];
-      while (m) {
-        const int b = __ffsll((long long)m) - 1;
-        m &= m - 1;
-        it.loc[u++] = loc_of((w << 6) + b);
-      }
-    }
-    for (int u = (int)n_unique + tid; u < n; u += nt) it.loc[u] = kEndLoc;
-  }
   // ---- staging entries of each miss (the host copy writes them): entries
   // grouped by miss index, CSR in miss_off / miss_ent.  After the stamp
   // commit the working stamps serve as per-miss counters, then cursors.
@@ -606,10 +579,53 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
   }
   __syncthreads();
   if (tid == 0) {
-    // everything the host copy and the gather read of this item -- miss
-    // lists, staging entries, fill marks, locations, appended rows -- is
-    // written before the mark
+    // the miss count, miss lists and staging entries are written: the host
+    // copy of this item may start while its locations are being written
     c.miss_count[pair] = m_miss;
+    publish_copy(c, pair);
+  }
+
+  // ---- location vector
+  const int ps = c.page_shift;
+  const int64_t pmask = ((int64_t)1 << ps) - 1;
+  auto loc_of = [&](int32_t row) -> uint32_t {
+    if ((int64_t)row >= t0)
+      return (kTierTail << 30) | (uint32_t)((int64_t)pair * T + (int64_t)row % T);
+    const uint64_t m = s.bm[row >> 6];  // rows that went to the hot cache
+    const uint64_t bit = 1ull << (row & 63);
+    if (m & bit) {
+      const uint32_t r = s.wpre[row >> 6] + (uint32_t)__popcll(m & (bit - 1ull));
+      return (kTierHot << 30) | (uint32_t)((int64_t)pair * B + s.slot_of[r]);
+    }
+    const int32_t slot = map[row >> ps];
+    return (kTierOpt << 30) | (uint32_t)(((int64_t)slot << ps) + (row & pmask));
+  };
+  if (!uni) {
+    for (int e = tid; e < n; e += nt) it.loc[e] = loc_of(it.sel[e]);
+  } else {
+    // union staging: each entry's rank among the distinct rows, the distinct
+    // rows' locations in ascending row order, then the end marker
+    for (int e = tid; e < n; e += nt) {
+      const int32_t row = it.sel[e];
+      const uint64_t bit = 1ull << (row & 63);
+      it.index[e] = (int32_t)(s.upre[row >> 6] +
+                              (uint32_t)__popcll(s.ubm[row >> 6] & (bit - 1ull)));
+    }
+    for (int w = tid; w < W; w += nt) {
+      uint64_t m = s.ubm[w];
+      uint32_t u = s.upre[w];
+      while (m) {
+        const int b = __ffsll((long long)m) - 1;
+        m &= m - 1;
+        it.loc[u++] = loc_of((w << 6) + b);
+      }
+    }
+    for (int u = (int)n_unique + tid; u < n; u += nt) it.loc[u] = kEndLoc;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // everything the gather reads of this item -- locations, fill marks,
+    // appended rows -- is written before the mark
     c.pair_status[pair] = 0;
     publish_loc(c, pair);
   }
