@@ -23,9 +23,9 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <new>
 #include <set>
-#include <unordered_map>
 #include <vector>
 
 #include "dhs.h"
@@ -193,6 +193,17 @@ struct dhs_pool {
   std::vector<dhs::ResolveItem> ritems;
   std::vector<dhs::CopyItem> citems;
   std::vector<dhs::GatherItem> gitems;
+  // gathers of a fused step: the resolved items' location vectors, sorted,
+  // to find which pair (if any) published a gather item's locations
+  struct LocKey {
+    const void* loc;
+    int32_t order;  // item index: of equal vectors the last one counts
+    int64_t pair;
+    bool operator<(const LocKey& o) const {
+      return loc != o.loc ? std::less<const void*>()(loc, o.loc) : order < o.order;
+    }
+  };
+  std::vector<LocKey> loc_keys;
   std::vector<dhs::AppendItem> aitems;
   std::vector<uint8_t> seen;
   std::vector<int32_t> app_of_pair;  // decode step: append item of each pair, -1 = none
@@ -1160,13 +1171,22 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   // Reuse items handed the same location vector) may go before the grids end
   const bool lr = fused && p->early && p->fused_resolved && tma_gather(p);
   g.later = lr && use_fresh_list(p) ? p->later : nullptr;
-  std::unordered_map<const void*, int64_t> loc_pair;
-  if (lr)
+  p->loc_keys.clear();
+  if (lr) {
     for (int32_t i = 0; i < st->n_items; ++i) {
       const dhs_item& it = st->items[i];
       if (!(it.flags & DHS_ITEM_GATHER_ONLY) && it.loc_dev)
-        loc_pair[it.loc_dev] = (int64_t)it.req * c.sources + it.src;
+        p->loc_keys.push_back({it.loc_dev, i, (int64_t)it.req * c.sources + it.src});
     }
+    std::sort(p->loc_keys.begin(), p->loc_keys.end());
+  }
+  // pair whose resolve published `loc`, or -1
+  auto loc_pair = [&](const void* loc) -> int64_t {
+    auto f = std::upper_bound(p->loc_keys.begin(), p->loc_keys.end(),
+                              dhs_pool::LocKey{loc, INT32_MAX, 0});
+    if (f == p->loc_keys.begin() || (f - 1)->loc != loc) return -1;
+    return (f - 1)->pair;
+  };
   p->gitems.clear();
   for (int32_t i = 0; i < st->n_items; ++i) {
     const dhs_item& it = st->items[i];
@@ -1187,16 +1207,13 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
       gi.L0 = p->l0_of_pair[pair];
       gi.seq = p->seq_of_pair[pair];
     }
-    if (lr) {
-      auto f = loc_pair.find(it.loc_dev);
-      if (f != loc_pair.end()) {
-        gi.pair = (int32_t)f->second;
-        gi.seq = p->seq_of_pair[f->second];
-        gi.flags |= dhs::kGiLocReady;
-        // the resolved item itself (not a Reuse item sharing its locations)
-        if (!(it.flags & DHS_ITEM_GATHER_ONLY) && p->staged_pair[f->second])
-          gi.flags |= dhs::kGiStaged;
-      }
+    const int64_t lp = lr ? loc_pair(it.loc_dev) : -1;
+    if (lp >= 0) {
+      gi.pair = (int32_t)lp;
+      gi.seq = p->seq_of_pair[lp];
+      gi.flags |= dhs::kGiLocReady;
+      // the resolved item itself (not a Reuse item sharing its locations)
+      if (!(it.flags & DHS_ITEM_GATHER_ONLY) && p->staged_pair[lp]) gi.flags |= dhs::kGiStaged;
     }
     p->gitems.push_back(gi);
   }
