@@ -138,6 +138,7 @@ cudaError_t launch_page_moves(const PageMove* moves, int n, int page_bytes, int 
 // ------------------------------------------------------------ host copy (d)
 constexpr int kCopyThreads = 512;
 constexpr int kCopyItemsMax = 256;
+constexpr int kCopyItemsSmall = 32;  // a smaller parameter table for small steps
 
 struct CopyItem {
   const uint8_t* host;  // device-visible pointer of the pair's pinned host rows

@@ -276,15 +276,24 @@ cudaError_t launch_page_moves(const PageMove* moves, int n, int page_bytes, int 
 }
 
 cudaError_t hostcopy_set_carveout() {
-  cudaError_t e = cudaFuncSetAttribute(hostcopy_kernel<kCopyItemsMax, true>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(hostcopy_kernel<kCopyItemsMax, false>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  for (const void* k : {(const void*)hostcopy_kernel<kCopyItemsMax, true>,
+                        (const void*)hostcopy_kernel<kCopyItemsMax, false>,
+                        (const void*)hostcopy_kernel<kCopyItemsSmall, true>,
+                        (const void*)hostcopy_kernel<kCopyItemsSmall, false>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items, int n_items,
                             int ctas, bool pdl, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
   if (n_items > kCopyItemsMax || n_items > kCopyThreads) return cudaErrorInvalidValue;
+  // the whole table travels with every launch: a small one for small steps
+  if (n_items <= kCopyItemsSmall)
+    return launch_t<kCopyItemsSmall>(c, items, n_items, ctas, pdl, stream);
   return launch_t<kCopyItemsMax>(c, items, n_items, ctas, pdl, stream);
 }
 
