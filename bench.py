@@ -777,7 +777,9 @@ def main():
         os.path.join(ROOT, "profiles", f"gather_{cfg.name}_traffic.json"))
     n_resolve = -(-cfg.requests * cfg.sources // 256)
     n_gather = -(-cfg.requests * cfg.layers // 384)
-    fresh = run.pool.get_option(dhs.DHS_OPT_FRESH_LIST)
+    # the fresh-row list copy launches only for gather-only (Reuse) items the
+    # host copy does not write itself: beyond three per resolved item
+    fresh = int(run.pool.get_option(dhs.DHS_OPT_FRESH_LIST) and cfg.reuse_layers > 3)
     # append folded into resolve; resolve + host copy per chunk, the gathers,
     # and the fresh-row list copy when it is on
     launches = K * (2 * n_resolve + n_gather + fresh)

@@ -140,11 +140,16 @@ constexpr int kCopyThreads = 512;
 constexpr int kCopyItemsMax = 256;
 constexpr int kCopyItemsSmall = 32;  // a smaller parameter table for small steps
 
+// Gather-only (Reuse) items handed an item's location vector whose staging
+// the host copy also writes, per item; further ones take the fresh-row list.
+constexpr int kCopyShareMax = 3;
+
 struct CopyItem {
   const uint8_t* host;  // device-visible pointer of the pair's pinned host rows
   uint8_t* staging;     // also write each miss row to its staging entries; null = no
   int32_t pair;
-  int32_t pad;
+  int32_t nshare;       // staging buffers of gather-only items sharing the locations
+  uint8_t* share[kCopyShareMax];  // (the same entries, the same row layout)
 };
 
 struct CopyCommon {

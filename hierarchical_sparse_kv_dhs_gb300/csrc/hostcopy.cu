@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kCopyThreads)
       // entries e0 .. e1 of the item's miss_ent list, written at stg + e * rb
       uint8_t* stg[kRowsPerWarp];
       const int32_t* ents[kRowsPerWarp];
-      int32_t e0[kRowsPerWarp], e1[kRowsPerWarp];
+      int32_t e0[kRowsPerWarp], e1[kRowsPerWarp], itm[kRowsPerWarp];
 #pragma unroll
       for (int r = 0; r < kRowsPerWarp; ++r) {
         const uint32_t i = base + r;
@@ -124,13 +124,15 @@ __global__ void __launch_bounds__(kCopyThreads)
         stg[r] = nullptr;
         ents[r] = nullptr;
         e0[r] = e1[r] = 0;
+        itm[r] = 0;
         if (i < total) {
           int lo = 0, hi = n - 1;  // last batch entry with s_pre <= i
           while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (s_pre[mid] <= i) lo = mid; else hi = mid - 1;
           }
-          const CopyItem& it = P.items[s_item[lo]];
+          itm[r] = s_item[lo];
+          const CopyItem& it = P.items[itm[r]];
           const uint32_t mi = i - s_pre[lo];
           const size_t off = (size_t)it.pair * c.Mcap + mi;
           const int32_t row = c.miss_rows[off];
@@ -162,23 +164,34 @@ __global__ void __launch_bounds__(kCopyThreads)
             const int ch = lane + 32 * q;
             if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
           }
-          for (int k = e0[r]; k < e1[r]; ++k) {  // the same bytes to its staging entries
-            uint8_t* to = stg[r] + (size_t)ents[r][k] * rb;
+          // the same bytes to its staging entries, in the item's staging and
+          // in that of the gather-only items sharing its locations
+          const int ns = stg[r] ? P.items[itm[r]].nshare : 0;
+          for (int k = e0[r]; k < e1[r]; ++k) {
+            const size_t eo = (size_t)ents[r][k] * rb;
+            for (int j = -1; j < ns; ++j) {
+              uint8_t* to = (j < 0 ? stg[r] : P.items[itm[r]].share[j]) + eo;
 #pragma unroll
-            for (int q = 0; q < kChunksPerLane; ++q) {
-              const int ch = lane + 32 * q;
-              if (ch < cpr) *reinterpret_cast<uint4*>(to + ch * 16) = v[r][q];
+              for (int q = 0; q < kChunksPerLane; ++q) {
+                const int ch = lane + 32 * q;
+                if (ch < cpr) *reinterpret_cast<uint4*>(to + ch * 16) = v[r][q];
+              }
             }
           }
         }
       } else {
         for (int r = 0; r < kRowsPerWarp; ++r) {
           if (!src[r]) continue;
+          const int ns = stg[r] ? P.items[itm[r]].nshare : 0;
           for (int ch = lane; ch < cpr; ch += 32) {
             const uint4 v = ld_sys(src[r] + ch * 16);
             *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v;
-            for (int k = e0[r]; k < e1[r]; ++k)
-              *reinterpret_cast<uint4*>(stg[r] + (size_t)ents[r][k] * rb + ch * 16) = v;
+            for (int k = e0[r]; k < e1[r]; ++k) {
+              const size_t eo = (size_t)ents[r][k] * rb + ch * 16;
+              *reinterpret_cast<uint4*>(stg[r] + eo) = v;
+              for (int j = 0; j < ns; ++j)
+                *reinterpret_cast<uint4*>(P.items[itm[r]].share[j] + eo) = v;
+            }
           }
         }
       }

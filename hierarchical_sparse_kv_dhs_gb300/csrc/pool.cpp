@@ -188,6 +188,8 @@ struct dhs_pool {
   int64_t ent_cap = 0;
   int stage_misses = 1;         // DHS_OPT_STAGE_MISSES
   std::vector<uint8_t> staged_pair;  // the host copy stages this pair's misses this step
+  std::vector<uint8_t> staged_item;  // per item of the step: a gather-only item whose
+                                     // staging the host copy writes too
   unsigned long long* trace = nullptr;  // DHS_OPT_TRACE buffer, null = off
   // reusable launch tables
   std::vector<dhs::ResolveItem> ritems;
@@ -1025,6 +1027,23 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     ci.pair = (int32_t)pair;
     p->citems.push_back(ci);
   }
+  // gather-only (Reuse) items handed a staged item's location vector, with
+  // the same entries: the host copy writes their fetched rows too
+  p->staged_item.assign((size_t)st->n_items, 0);
+  for (int32_t i = 0; i < st->n_items; ++i) {
+    const dhs_item& it = st->items[i];
+    if (!(it.flags & DHS_ITEM_GATHER_ONLY) || !it.staging_dev || !it.loc_dev) continue;
+    for (size_t k = 0; k < p->ritems.size(); ++k) {
+      dhs::CopyItem& ci = p->citems[k];
+      if (p->ritems[k].loc != it.loc_dev) continue;
+      if (ci.staging && p->ritems[k].n == it.queries * it.topk &&
+          ci.nshare < dhs::kCopyShareMax) {
+        ci.share[ci.nshare++] = (uint8_t*)it.staging_dev;
+        p->staged_item[i] = 1;
+      }
+      break;
+    }
+  }
   dhs::ResolveCommon rcm{};
   rcm.tags = p->tags;
   rcm.stamps = p->stamps;
@@ -1213,7 +1232,10 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
       gi.seq = p->seq_of_pair[lp];
       gi.flags |= dhs::kGiLocReady;
       // the resolved item itself (not a Reuse item sharing its locations)
-      if (!(it.flags & DHS_ITEM_GATHER_ONLY) && p->staged_pair[lp]) gi.flags |= dhs::kGiStaged;
+      if (it.flags & DHS_ITEM_GATHER_ONLY ? (i < (int32_t)p->staged_item.size() &&
+                                             p->staged_item[i])
+                                          : p->staged_pair[lp] != 0)
+        gi.flags |= dhs::kGiStaged;
     }
     p->gitems.push_back(gi);
   }
@@ -1238,7 +1260,13 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
         cudaSuccess)
       return DHS_ECUDA;
   }
-  if (g.later && ng > 0 &&
+  // the fresh-row list copy runs only when some tile can list a row: an
+  // item that waits on published locations and whose fetched rows the host
+  // copy does not write itself
+  bool listing = false;
+  for (const dhs::GatherItem& gi : p->gitems)
+    listing |= (gi.flags & dhs::kGiLocReady) && !(gi.flags & dhs::kGiStaged);
+  if (g.later && listing &&
       dhs::launch_gather_later(g, 2 * std::max(1, p->sm_count), p->stream) != cudaSuccess)
     return DHS_ECUDA;
   return DHS_OK;

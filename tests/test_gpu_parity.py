@@ -221,11 +221,18 @@ def test_union_staging_bit_exact(cfg, mode):
                 union=True)
 
 
-@pytest.mark.parametrize("cfg", [SMALL[1], SMALL[2], SMALL[4], UNION[3]],
-                         ids=["v3", "reuse", "evict", "v8"])
+# five Reuse layers on one location vector: the host copy writes the fetched
+# rows of three of them, the other two take the fresh-row list
+REUSE5 = TINY.scaled(name="reuse5", tag=54, requests=2, sources=2, reuse_layers=5,
+                     shared_selection=True, residency=0.2, steps=6, hot=700)
+
+
+@pytest.mark.parametrize("cfg", [SMALL[1], SMALL[2], SMALL[4], UNION[3], REUSE5],
+                         ids=["v3", "reuse", "evict", "v8", "reuse5"])
 def test_misses_staged_by_the_host_copy_or_not(cfg):
     """Fused steps: the host copy writes the rows it fetches into the
-    resolved items' staging (default), or leaves them to the gather."""
+    resolved items' staging and that of up to three Reuse items sharing
+    their locations (default), or leaves them to the gather."""
     for stage in (1, 0):
         compare_run(cfg, gather_impl=1, stage=stage)
         compare_run(cfg, gather_impl=1, stage=stage, union=True)
