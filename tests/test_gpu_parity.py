@@ -545,6 +545,70 @@ def test_decode_step_host_async_pipelined_matches_device_path(streams):
         b.close()
 
 
+def test_degenerate_steps():
+    """Through the C ABI: an empty step (no items, no appends) changes
+    nothing in any entry point; an item with k = 0 resolves nothing (zero
+    counters); steps of gather-only items gather without resolving, fused or
+    not; ordinary steps around them still match the oracle."""
+    import ctypes
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    from oracle.run import OracleRun
+    cfg = TINY.scaled(name="degen", tag=56, requests=2, sources=1, steps=3, residency=0.5)
+    wl = Workload(cfg)
+    gpu, orc = GpuRun(cfg, wl), OracleRun(cfg, wl)
+    h = gpu.pool.h
+
+    def check(step):
+        res = orc.step(step)
+        for r in range(cfg.requests):
+            assert np.array_equal(gpu.loc[r].cpu().numpy().view(np.uint32), res[r]["loc"])
+            assert np.array_equal(gpu.counters[r].cpu().numpy().view(np.uint32),
+                                  res[r]["counters"])
+            stg = gpu.staging[r].cpu().view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(stg, res[r]["staging"])
+
+    try:
+        empty, _keep = dhs.make_step(1, [])
+        for fn in (dhs.lib.dhs_resolve, dhs.lib.dhs_gather, dhs.lib.dhs_resolve_gather):
+            assert fn(h, ctypes.byref(empty)) == 0
+        assert dhs.lib.dhs_decode_step(h, None, 0, ctypes.byref(empty)) == 0
+        # k = 0
+        cnt = torch.full((8,), 7, dtype=torch.int32, device="cuda")
+        it = dhs.dhs_item()
+        it.req, it.src, it.queries, it.topk = 0, 0, 1, 0
+        it.sel_dev, it.loc_dev = gpu.sel[0, 0, 0].data_ptr(), gpu.loc[0, 0].data_ptr()
+        it.counters_dev, it.staging_dev = cnt.data_ptr(), gpu.staging[0, 0].data_ptr()
+        st0, _keep0 = dhs.make_step(1, [it])
+        assert dhs.lib.dhs_resolve_gather(h, ctypes.byref(st0)) == 0
+        torch.cuda.synchronize()
+        assert gpu.status() == (0, 0) and not cnt.cpu().any()
+        gpu.step(1)
+        check(1)
+        # gather-only items on step 1's locations, into other staging
+        other = torch.zeros_like(gpu.staging)
+        items = []
+        for r in range(cfg.requests):
+            g = dhs.dhs_item()
+            g.req, g.src, g.queries, g.topk = r, 0, cfg.queries, cfg.topk
+            g.flags = dhs.DHS_ITEM_GATHER_ONLY
+            g.loc_dev, g.staging_dev = gpu.loc[r, 0].data_ptr(), other[r, 0].data_ptr()
+            items.append(g)
+        stg, _keepg = dhs.make_step(1, items)
+        for fn in (dhs.lib.dhs_gather, dhs.lib.dhs_resolve_gather):
+            other.zero_()
+            assert fn(h, ctypes.byref(stg)) == 0
+            torch.cuda.synchronize()
+            assert torch.equal(other.view(torch.int16), gpu.staging.view(torch.int16))
+        for step in (2, 3):
+            gpu.step(step)
+            check(step)
+        assert gpu.status() == (0, 0)
+    finally:
+        gpu.close()
+        orc.pool.close()
+
+
 MAXHOT = TINY.scaled(name="maxhot", tag=53, requests=1, sources=1, hot=16384, history=65536,
                      topk=4096, residency=0.0, steps=10, window=4096, frac_recent=0.3,
                      zipf_s=0.6, row_elems=64)
