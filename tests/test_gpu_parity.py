@@ -609,6 +609,18 @@ def test_degenerate_steps():
         orc.pool.close()
 
 
+# 400 (request, source) pairs: two resolve and copy launches (at most 256
+# items each) and two gather launches (at most 384 items each) per step
+MANY = TINY.scaled(name="many", tag=57, requests=200, sources=2, history=512, tail=16,
+                   hot=96, topk=48, steps=4, residency=0.3)
+
+
+@pytest.mark.parametrize("mode", ["fused-tma", "split-vec", "fused-tma-union"])
+def test_steps_of_several_launches_per_kernel(mode):
+    compare_run(MANY, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
+                union=mode.endswith("union"))
+
+
 MAXHOT = TINY.scaled(name="maxhot", tag=53, requests=1, sources=1, hot=16384, history=65536,
                      topk=4096, residency=0.0, steps=10, window=4096, frac_recent=0.3,
                      zipf_s=0.6, row_elems=64)
