@@ -190,13 +190,14 @@ struct GatherItem {
   uint8_t* staging;
   const int32_t* sel;  // non-null: a resolved item whose step-1 rows may be copied early
   int64_t L, N;        // length and imported rows of the item's source
-  int64_t L0;          // rows >= L0 were appended by this launch: never early
+  int64_t L0;          // rows >= L0 were appended by this launch
+  const uint8_t* app;  // their bytes ([L - L0][row_bytes], the append's source), or
+                       // null: rows >= L0 are then never early
   int32_t n;           // entries
   int32_t tile0;       // first tile of this item in the launch
   int32_t pair;        // req * S + src (resolved items)
   uint32_t seq;        // sequence number of the resolve launch that resolved it
   uint32_t flags;      // kGiLocReady
-  int32_t pad;
 };
 // The item's locations are those of a pair resolved by the preceding resolve
 // launch of the same fused step, published through loc_ready[pair] == seq.

@@ -112,11 +112,16 @@ __device__ __forceinline__ const uint8_t* row_ptr(const GatherCommon& c, uint32_
 }
 
 // Step-1 row address of `row` of an item, or nullptr if the row needs the
-// hot cache, was appended by this launch, or is out of range (which the
-// resolve kernel reports).
+// hot cache or is out of range (which the resolve kernel reports).  A row
+// appended by this launch is in the tail once the resolve kernel has written
+// it there; until then the same bytes are in the append's source rows.
 __device__ __forceinline__ const uint8_t* step1_ptr(const GatherCommon& c,
                                                     const GatherItem& it, int32_t row) {
-  if (row < 0 || (int64_t)row >= it.L0) return nullptr;
+  if (row < 0) return nullptr;
+  if ((int64_t)row >= it.L0) {
+    if (!it.app || (int64_t)row >= it.L) return nullptr;
+    return it.app + (size_t)((int64_t)row - it.L0) * c.row_bytes;
+  }
   const int64_t T = c.T;
   if ((int64_t)row >= it.L - T)
     return c.tail + ((size_t)it.pair * T + (size_t)((int64_t)row % T)) * c.row_bytes;

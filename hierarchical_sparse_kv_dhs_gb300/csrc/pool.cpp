@@ -210,6 +210,7 @@ struct dhs_pool {
   std::vector<uint8_t> seen;
   std::vector<int32_t> app_of_pair;  // decode step: append item of each pair, -1 = none
   std::vector<int64_t> l0_of_pair;   // length of each resolved pair before this step's append
+  std::vector<const uint8_t*> app_of_pair_rows;  // its appended rows' source, or null
   std::vector<uint32_t> seq_of_pair; // resolve launch that last resolved each pair
   std::vector<dhs::PageMove> moves;  // page list of the next page-move launch
   // dhs_prefetch: resolves enqueued on a caller's side stream; the pool's
@@ -531,6 +532,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->seen.assign((size_t)p->pairs, 0);
     p->app_of_pair.assign((size_t)p->pairs, -1);
     p->l0_of_pair.assign((size_t)p->pairs, 0);
+    p->app_of_pair_rows.assign((size_t)p->pairs, nullptr);
     p->seq_of_pair.assign((size_t)p->pairs, 0);
     p->pf_pair.assign((size_t)p->pairs, 0);
     p->staged_pair.assign((size_t)p->pairs, 0);
@@ -998,6 +1000,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     PairState& s = p->ps[pair];
     dhs::ResolveItem r{};
     p->l0_of_pair[pair] = s.L;
+    p->app_of_pair_rows[pair] = nullptr;
     if (apps && p->app_of_pair[pair] >= 0) {
       const dhs_append_item& a = apps[p->app_of_pair[pair]];
       r.app_rows = (const uint8_t*)a.rows_dev;
@@ -1005,6 +1008,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
       r.app_L0 = s.L;
       r.app_count = a.count;
       s.L += a.count;
+      p->app_of_pair_rows[pair] = (const uint8_t*)a.rows_dev;
     }
     r.sel = it.sel_dev;
     r.loc = it.loc_dev;
@@ -1224,6 +1228,7 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
       gi.L = p->ps[pair].L;
       gi.N = p->ps[pair].N;
       gi.L0 = p->l0_of_pair[pair];
+      gi.app = p->app_of_pair_rows[pair];
       gi.seq = p->seq_of_pair[pair];
     }
     const int64_t lp = lr ? loc_pair(it.loc_dev) : -1;
