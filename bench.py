@@ -43,6 +43,9 @@ METRIC = ("selected KV rows resolved+gathered/sec and GB/s vs HBM & host-link "
           "roofline")
 UNIT = "rows/s"
 GATHER_WRITE_BYTES_PER_ENTRY = 1152 + 4  # staging row write + location read
+# host-buffer pipeline depth: output sets a serving loop cycles through (the
+# host reads step s-2's outputs after enqueuing step s)
+E2E_SETS = 3
 
 
 def gather_alg_bytes(cfg, wl, step, union=False):
@@ -77,6 +80,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--kernel-steps", type=int, default=500)
     ap.add_argument("--trace-steps", type=int, default=100)
+    ap.add_argument("--b2b-steps", type=int, default=200,
+                    help="consecutive fused steps timed without L2 flushes (breakdown)")
     ap.add_argument("--no-hugepages", action="store_true")
     ap.add_argument("--gemm", type=int, default=4096,
                     help="--experiment prefetch: per-layer compute, an n x n x n bf16 GEMM")
@@ -363,6 +368,36 @@ def traced_pass(run, cycle, steps, dev, flush_l2):
             "copy_gbs": (host_b / copy_s / 1e9) if copy_s else None}
 
 
+def back_to_back(run, cycle, steps, dev, stream):
+    """Device time per step of consecutive fused steps with no L2 flush
+    between them (not the headline): CUDA events around each run of
+    consecutive steps of a cycle.  Each step's gather then also writes back
+    the previous step's staging lines still dirty in L2, which the flushed
+    timing moves into the flush, and each step's first kernel starts only
+    after the previous step's gather has drained."""
+    import torch
+    T = run.cfg.total_steps
+    total_ms, n = 0.0, 0
+    while n < steps:
+        s = cycle.next()
+        while not cycle.timed(s):
+            run.step(s)
+            s = cycle.next()
+        seg = [s]
+        while len(seg) < steps - n and seg[-1] < T:
+            seg.append(cycle.next())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for s in seg:
+            run.step(s)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms += e0.elapsed_time(e1)
+        n += len(seg)
+    return total_ms * 1e3 / n
+
+
 def measure_e2e(run, cycle, steps, dev, stream):
     """The metric through the C ABI with host buffers for `steps` further
     decode steps.  Each step copies its selections and decode rows in from
@@ -372,18 +407,24 @@ def measure_e2e(run, cycle, steps, dev, stream):
 
     value: pipelined as a serving loop runs it.  dhs_decode_step_host_async
     puts each step's input copy on an input stream and its output copy on an
-    output stream, so step s+1's inputs come in and step s-1's outputs go out
-    while step s runs; the host waits for step s-1's outputs (an event) and
-    reads its counters after enqueuing step s.  Device output blocks and host
-    output buffers alternate between two sets.  Wall clock over runs of
-    consecutive steps (a workload's pool reset between cycles is outside it).
+    output stream, so inputs come in and earlier steps' outputs go out while
+    a step runs.  Device output blocks and host output buffers cycle through
+    E2E_SETS sets; after enqueuing step s the host waits for step
+    s - (E2E_SETS - 1)'s outputs (an event) and reads its counters, so the
+    host's own work per step overlaps the device's instead of following it.
+    A set is rewritten only after the host has read its previous outputs, and
+    every step has its own device input block, so no device-side waits are
+    needed.  Wall clock over runs of consecutive steps (a workload's pool
+    reset between cycles is outside it), all of a run's outputs read inside
+    it.
     sync_value: one blocking dhs_decode_step_host call per step, wall clock
     around each call."""
     import numpy as np
     import torch
     T = run.cfg.total_steps
     in_host = [run.step_in[s].cpu().pin_memory() for s in range(T)]
-    blocks = [run.step_out, run.second_outputs()]
+    D = E2E_SETS
+    blocks = [run.output_block(i) for i in range(D)]
 
     def span(dst, src):
         return (dst.data_ptr(), src.data_ptr(), src.numel() * src.element_size())
@@ -395,8 +436,8 @@ def measure_e2e(run, cycle, steps, dev, stream):
         cnt_h = out_h[cnt_off:cnt_off + run.counters.numel() * 4].view(torch.int32)
         sets.append((cnt_h.view(run.counters.shape).numpy(), [span(out_h, blk)], out_h))
     # the calls' arguments for every step of the cycle, built once as a caller would
-    io = [[run.host_io(s, [span(run.step_in[s - 1], in_host[s - 1])], sets[b][1], alt=b == 1)
-           for s in range(1, T + 1)] for b in range(2)]
+    io = [[run.host_io(s, [span(run.step_in[s - 1], in_host[s - 1])], sets[b][1], out_set=b)
+           for s in range(1, T + 1)] for b in range(D)]
 
     def next_timed():
         s = cycle.next()
@@ -416,8 +457,7 @@ def measure_e2e(run, cycle, steps, dev, stream):
         sync_dt += time.perf_counter() - t0
     # pipelined: runs of consecutive steps up to the end of the cycle
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    kern_done = [torch.cuda.Event(), torch.cuda.Event()]  # the step's kernels, per set
-    out_done = [torch.cuda.Event(), torch.cuda.Event()]   # its output copy, per set
+    out_done = [torch.cuda.Event() for _ in range(D)]  # each set's output copy
     dt, n, seen = 0.0, 0, 0
     while n < steps:
         seg = [next_timed()]
@@ -426,19 +466,16 @@ def measure_e2e(run, cycle, steps, dev, stream):
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for j, s in enumerate(seg):
-            b = j % 2
-            if j >= 2:  # set b was last used two steps ago
-                s_in.wait_event(kern_done[b])
-                stream.wait_event(out_done[b])
+            b = j % D  # its last outputs (step j - D) were read at iteration j - 1
             run.step_host(s, io=io[b][s - 1], wait=False, in_stream=s_in, out_stream=s_out)
-            kern_done[b].record(stream)
             out_done[b].record(s_out)
-            if j:  # the previous step's outputs are in host memory: read them
-                out_done[1 - b].synchronize()
-                seen += int(sets[1 - b][0][..., 0].sum(dtype=np.int64))
-        last = (len(seg) - 1) % 2
-        out_done[last].synchronize()
-        seen += int(sets[last][0][..., 0].sum(dtype=np.int64))
+            if j >= D - 1:  # step j - (D - 1)'s outputs are in host memory: read them
+                k = (j - (D - 1)) % D
+                out_done[k].synchronize()
+                seen += int(sets[k][0][..., 0].sum(dtype=np.int64))
+        for j in range(max(0, len(seg) - (D - 1)), len(seg)):
+            out_done[j % D].synchronize()
+            seen += int(sets[j % D][0][..., 0].sum(dtype=np.int64))
         dt += time.perf_counter() - t0
         n += len(seg)
     torch.cuda.synchronize(dev)
@@ -451,9 +488,9 @@ def measure_e2e(run, cycle, steps, dev, stream):
             "d2h_bytes_per_step": int(run.step_out.numel()),
             "steps": steps, "seconds": dt,
             "sync_value": c.entries_per_step * steps / sync_dt,
-            "path": "dhs_decode_step_host_async per step: input copy on an input stream, "
-                    "step, output copy on an output stream (two output sets), the "
-                    "previous step's outputs waited for and read after each call; "
+            "path": f"dhs_decode_step_host_async per step: input copy on an input stream, "
+                    f"step, output copy on an output stream ({D} output sets); after "
+                    f"enqueuing step s, step s-{D - 1}'s outputs waited for and read; "
                     "sync_value: blocking dhs_decode_step_host, one call per step"}
 
 
@@ -689,6 +726,7 @@ def main():
     torch.cuda.synchronize(dev)
     gather_ms = [e[1].elapsed_time(e[2]) for e in ev2]
     resolve_ms = [e[0].elapsed_time(e[1]) for e in ev2]
+    b2b_us = back_to_back(run, cycle, args.b2b_steps, dev, stream) if args.b2b_steps else None
 
     # Context for the gather's roofline, timed the same way (flush, events):
     # a contiguous device copy of the staging bytes, and one trivial launch
@@ -812,6 +850,8 @@ def main():
             "h2d_peak_gbs": h2d,
             "split_append_resolve_hostcopy_ms": sum(resolve_ms) / K2,
             "split_gather_ms": sum(gather_ms) / K2,
+            "back_to_back_us_per_step": b2b_us,
+            "back_to_back_rows_per_s": entries / (b2b_us * 1e-6) if b2b_us else None,
             "wall_s_timed_region": t_wall1 - t_wall0,
             "last_step_unique_rows": tiers,
             "last_step_host_bytes": host_rows * cfg.row_bytes,

@@ -172,7 +172,7 @@ class GpuRun:
     def _build_descriptors(self):
         c = self.cfg
         self._steps, self._layer_steps = self._make_steps(self.loc, self.counters, self.index)
-        self._steps_alt = None
+        self._outs = [(self.step_out, self._steps)]
         self._appends = []
         for step in range(1, c.total_steps + 1):
             apps = []
@@ -186,20 +186,19 @@ class GpuRun:
             arr = (dhs.dhs_append_item * len(apps))(*apps)
             self._appends.append((arr, len(apps)))
 
-    def second_outputs(self):
-        """A second output block (locations, counters, union indices) laid out
-        as step_out, and step descriptors that write it: a pipelined caller
-        alternates the two while one block's copy to the host is in flight."""
-        if self._steps_alt is None:
-            self.step_out_alt = torch.zeros_like(self.step_out)
+    def output_block(self, i):
+        """Output block `i` (locations, counters, union indices) laid out as
+        step_out (block 0), with step descriptors that write it (host_io's
+        `out_set`): a pipelined caller cycles through several blocks while
+        earlier blocks' copies to the host are in flight."""
+        while len(self._outs) <= i:
+            blk = torch.zeros_like(self.step_out)
             off = lambda t: t.data_ptr() - self.step_out.data_ptr()
-            view = lambda t: self.step_out_alt[off(t):off(t) + t.numel() * 4].view(
-                torch.int32).view(t.shape)
-            self.loc_alt, self.counters_alt = view(self.loc), view(self.counters)
-            self.index_alt = view(self.index) if self.index is not None else None
-            self._steps_alt, _ = self._make_steps(self.loc_alt, self.counters_alt,
-                                                  self.index_alt)
-        return self.step_out_alt
+            view = lambda t: blk[off(t):off(t) + t.numel() * 4].view(torch.int32).view(t.shape)
+            steps, _ = self._make_steps(view(self.loc), view(self.counters),
+                                        view(self.index) if self.index is not None else None)
+            self._outs.append((blk, steps))
+        return self._outs[i][0]
 
     # ---------------------------------------------------------- stepping
     def append(self, step):
@@ -273,12 +272,13 @@ class GpuRun:
         dhs.check(dhs.lib.dhs_decode_step(self.pool.h, arr, n, ctypes.byref(st)),
                   "dhs_decode_step")
 
-    def host_io(self, step, ins, outs, alt=False):
+    def host_io(self, step, ins, outs, out_set=0):
         """Prebuilt arguments of dhs_decode_step_host for `step`: `ins` /
-        `outs` are lists of (dst, src, bytes) host<->device copies; `alt`:
-        the step writes the second output block (second_outputs)."""
+        `outs` are lists of (dst, src, bytes) host<->device copies; the step
+        writes output block `out_set` (output_block)."""
         arr, n = self._appends[step - 1]
-        st, _ = (self._steps_alt if alt else self._steps)[step - 1]
+        self.output_block(out_set)
+        st, _ = self._outs[out_set][1][step - 1]
         cin = (dhs.dhs_copy * max(1, len(ins)))(*[dhs.dhs_copy(*c) for c in ins])
         cout = (dhs.dhs_copy * max(1, len(outs)))(*[dhs.dhs_copy(*c) for c in outs])
         return (self.pool.h, cin, len(ins), arr, n, ctypes.byref(st), cout, len(outs))

@@ -485,11 +485,11 @@ def test_decode_step_host_matches_device_path():
 
 @pytest.mark.parametrize("streams", [False, True])
 def test_decode_step_host_async_pipelined_matches_device_path(streams):
-    """dhs_decode_step_host_async with step s+1 enqueued before step s's
-    outputs are read (two host output sets; with `streams`, the input and
-    output copies on their own streams and two device output blocks, as the
-    bench's e2e runs it) gives what the device-side dhs_decode_step leaves
-    in device memory, step by step."""
+    """dhs_decode_step_host_async with later steps enqueued before step s's
+    outputs are read (two host output sets; with `streams`, three, the input
+    and output copies on their own streams and three device output blocks,
+    as the bench's e2e runs it) gives what the device-side dhs_decode_step
+    leaves in device memory, step by step."""
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     cfg = SMALL[1]
     wl = Workload(cfg)
@@ -498,7 +498,11 @@ def test_decode_step_host_async_pipelined_matches_device_path(streams):
         def span(dst, src):
             return (dst.data_ptr(), src.data_ptr(), src.numel() * src.element_size())
 
-        blocks = [b.step_out, b.second_outputs() if streams else b.step_out]
+        # host output sets; step s's outputs are read after step s+D-1 is
+        # enqueued.  Without streams every copy is on the pool's stream, which
+        # orders the one device output block's reuse.
+        D = 3 if streams else 2
+        blocks = [b.output_block(i if streams else 0) for i in range(D)]
         cnt_off = b.counters.data_ptr() - b.step_out.data_ptr()
         loc_n, cnt_n = b.loc.numel() * 4, b.counters.numel() * 4
         outs = [torch.empty(blk.shape, dtype=torch.uint8).pin_memory() for blk in blocks]
@@ -511,8 +515,7 @@ def test_decode_step_host_async_pipelined_matches_device_path(streams):
         pool_stream = torch.cuda.current_stream()
         s_in = torch.cuda.Stream() if streams else None
         s_out = torch.cuda.Stream() if streams else None
-        kern_done = [torch.cuda.Event(), torch.cuda.Event()]
-        out_done = [torch.cuda.Event(), torch.cuda.Event()]
+        out_done = [torch.cuda.Event() for _ in range(D)]
 
         def check(j, step):
             o = outs[j]
@@ -521,22 +524,20 @@ def test_decode_step_host_async_pipelined_matches_device_path(streams):
             assert torch.equal(o[cnt_off:cnt_off + cnt_n].view(torch.int32).view(cnt_w.shape),
                                cnt_w), step
 
-        for step in range(1, cfg.total_steps + 1):
-            j = (step - 1) % 2
-            if step > 2 and streams:
-                s_in.wait_event(kern_done[j])
-                pool_stream.wait_event(out_done[j])
+        T = cfg.total_steps
+        for step in range(1, T + 1):
+            j = (step - 1) % D  # set j's last outputs (step - D) are already read
             io = b.host_io(step, [span(b.step_in[step - 1], ins[step - 1])],
-                           [span(outs[j], blocks[j])], alt=streams and j == 1)
+                           [span(outs[j], blocks[j])], out_set=j if streams else 0)
             b.step_host(step, io=io, wait=False, in_stream=s_in, out_stream=s_out)
-            kern_done[j].record(pool_stream)
             out_done[j].record(s_out if streams else pool_stream)
-            if step > 1:
-                out_done[1 - j].synchronize()
-                check(1 - j, step - 1)
-        last = (cfg.total_steps - 1) % 2
-        out_done[last].synchronize()
-        check(last, cfg.total_steps)
+            if step >= D:
+                r = step - (D - 1)
+                out_done[(r - 1) % D].synchronize()
+                check((r - 1) % D, r)
+        for r in range(max(1, T - D + 2), T + 1):
+            out_done[(r - 1) % D].synchronize()
+            check((r - 1) % D, r)
         torch.cuda.synchronize()
         assert torch.equal(want[-1][2].view(torch.int16), b.staging.view(torch.int16))
         assert a.status() == (0, 0) and b.status() == (0, 0)
