@@ -21,9 +21,11 @@ constexpr uint32_t kStatusEtimeout = 8u;
 constexpr int32_t kErrRange = -5, kErrBudget = -4;  // DHS_ERANGE, DHS_EBUDGET
 constexpr int kMaxHotRows = 16384;
 
-// Sequence numbers of resolve launches as published in loc_ready marks (never
-// 0, which is what a zeroed mark holds).
+// Sequence numbers of resolve launches as published in loc_ready / copy_ready
+// marks (never 0, which is what a zeroed mark holds).
 constexpr uint32_t kSeqMask = 0x1FFFFFFFu;
+// copy_ready mark bit: the item has no misses, so its copy reads nothing of it
+constexpr uint32_t kMarkNoMiss = 0x20000000u;
 
 // Optional timeline (DHS_OPT_TRACE): per kernel kind, the earliest CTA start
 // and the latest CTA end in %globaltimer nanoseconds.
@@ -80,8 +82,9 @@ struct ResolveItem {
   uint8_t* app_host;        // device-visible pointer of the pair's host rows
   int64_t app_L0;           // length before the append
   int32_t app_count;
-  int32_t stage;   // list, per miss, the entries that selected it (host copy
-                   // writes them into staging)
+  int16_t stage;       // list, per miss, the entries that selected it (host
+                       // copy writes them into staging)
+  int16_t loc_shared;  // a gather-only item of the launch reads `loc` too
   int32_t* index;  // union staging: [n] union rank of each entry; null = per-query
 };
 

@@ -72,10 +72,12 @@ __global__ void __launch_bounds__(kCopyThreads)
       uint32_t acc = 0;
       while (j < c.n_items && n < kBatchMax) {
         const uint32_t* mark = c.ready + P.items[j].pair;
-        bool ok = waited || ld_acquire_u32(mark) == want;
+        uint32_t v = waited ? 0u : ld_acquire_u32(mark);
+        bool ok = waited || (v & kSeqMask) == want;
         for (uint32_t i = 0; !ok && n == 0 && i < kReadyPolls; ++i) {
           __nanosleep(256);
-          ok = ld_acquire_u32(mark) == want;
+          v = ld_acquire_u32(mark);
+          ok = (v & kSeqMask) == want;
         }
         if (!ok) {
           need_wait = n == 0;
@@ -83,7 +85,8 @@ __global__ void __launch_bounds__(kCopyThreads)
         }
         s_item[n] = j;
         s_pre[n] = acc;
-        acc += c.miss_count[P.items[j].pair];
+        // an item whose mark says "no misses" has written nothing to read
+        acc += (v & kMarkNoMiss) ? 0u : c.miss_count[P.items[j].pair];
         ++n;
         j += gridDim.x;
       }

@@ -1031,21 +1031,24 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     ci.pair = (int32_t)pair;
     p->citems.push_back(ci);
   }
-  // gather-only (Reuse) items handed a staged item's location vector, with
-  // the same entries: the host copy writes their fetched rows too
+  // gather-only (Reuse) items handed a resolved item's location vector: the
+  // resolved item publishes its locations for them, and when it is staged
+  // with the same entries, the host copy writes their fetched rows too
   p->staged_item.assign((size_t)st->n_items, 0);
   for (int32_t i = 0; i < st->n_items; ++i) {
     const dhs_item& it = st->items[i];
-    if (!(it.flags & DHS_ITEM_GATHER_ONLY) || !it.staging_dev || !it.loc_dev) continue;
+    if (!(it.flags & DHS_ITEM_GATHER_ONLY) || !it.loc_dev) continue;
+    bool first = true;
     for (size_t k = 0; k < p->ritems.size(); ++k) {
       dhs::CopyItem& ci = p->citems[k];
       if (p->ritems[k].loc != it.loc_dev) continue;
-      if (ci.staging && p->ritems[k].n == it.queries * it.topk &&
+      p->ritems[k].loc_shared = 1;
+      if (first && it.staging_dev && ci.staging && p->ritems[k].n == it.queries * it.topk &&
           ci.nshare < dhs::kCopyShareMax) {
         ci.share[ci.nshare++] = (uint8_t*)it.staging_dev;
         p->staged_item[i] = 1;
       }
-      break;
+      first = false;
     }
   }
   dhs::ResolveCommon rcm{};

@@ -222,11 +222,15 @@ __device__ __forceinline__ void publish_loc(const ResolveCommon& c, int pair) {
 
 // Publish that an item's miss count, miss lists and staging entries are
 // written (thread 0 only, after a block barrier): its host copy may start.
-__device__ __forceinline__ void publish_copy(const ResolveCommon& c, int pair) {
+// An item without misses says so in the mark itself; the copy then reads
+// nothing the item wrote, so the mark needs no fence (a fence waits for the
+// block's earlier writes, microseconds while the gather fills the memory
+// system).
+__device__ __forceinline__ void publish_copy(const ResolveCommon& c, int pair, bool none) {
   if (!c.copy_ready) return;
-  __threadfence();
+  if (!none) __threadfence();
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(c.copy_ready + pair),
-               "r"(c.seq & kSeqMask) : "memory");
+               "r"((c.seq & kSeqMask) | (none ? kMarkNoMiss : 0u)) : "memory");
 }
 
 // Write the failure result of one item: no state change, zero counters.
@@ -266,7 +270,7 @@ __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t
   if (threadIdx.x == 0) {
     c.miss_count[it.pair] = 0u;  // before the marks: the host copy reads it then
     c.pair_status[it.pair] = code;
-    publish_copy(c, it.pair);
+    publish_copy(c, it.pair, true);
     publish_loc(c, it.pair);
     atomicOr(c.status, flag);
     trace_mark(c.trace, kTraceResolve, true);
@@ -582,7 +586,7 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
     // the miss count, miss lists and staging entries are written: the host
     // copy of this item may start while its locations are being written
     c.miss_count[pair] = m_miss;
-    publish_copy(c, pair);
+    publish_copy(c, pair, m_miss == 0);
   }
 
   // ---- location vector
@@ -624,10 +628,13 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
   }
   __syncthreads();
   if (tid == 0) {
-    // everything the gather reads of this item -- locations, fill marks,
-    // appended rows -- is written before the mark
     c.pair_status[pair] = 0;
-    publish_loc(c, pair);
+    // everything the gather reads of this item -- locations, fill marks,
+    // appended rows -- is written before the mark.  Only tiles with rows that
+    // step 1 leaves open (hot-cache rows, a union list, a gather-only item
+    // reading this vector) wait for it; without such rows nothing does, and
+    // the mark and its fence are left out.
+    if (C != 0u || uni || it.loc_shared) publish_loc(c, pair);
   }
 
   if (m_miss) {
