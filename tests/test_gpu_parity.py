@@ -239,6 +239,39 @@ def test_misses_staged_by_the_host_copy_or_not(cfg):
         compare_run(cfg, gather_impl=1, stage=stage, fresh=0)
 
 
+# fully resident: every resolved item's rows resolve in step 1, so an item
+# publishes its location mark only because Reuse items read its vector
+RESIDENT_REUSE = TINY.scaled(name="resident_reuse", tag=55, requests=2, sources=2,
+                             reuse_layers=3, shared_selection=True, residency=1.0, steps=6)
+
+
+def test_location_mark_of_step1_only_items_read_by_reuse_items():
+    """An item whose rows all resolve in step 1 leaves its location mark out
+    unless a gather-only item of the launch reads its vector.  Here Reuse
+    items read such vectors: the results are bit-exact, and no step waits
+    for a gather tile's bounded poll to run out (about a second) before it
+    falls back to waiting for the grids."""
+    import time
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    cfg = RESIDENT_REUSE
+    compare_run(cfg, gather_impl=1)
+    run = GpuRun(cfg, Workload(cfg), gather_impl=1)
+    try:
+        worst = 0.0
+        for step in range(1, cfg.total_steps + 1):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            run.step(step)
+            torch.cuda.synchronize()
+            if step > 1:
+                worst = max(worst, time.perf_counter() - t0)
+            # no hot-cache hits or misses: every row resolved in step 1
+            assert int(run.counters[..., 4:6].sum()) == 0, step
+        assert worst < 0.1, worst
+    finally:
+        run.close()
+
+
 @pytest.mark.parametrize("tpc", [2, 5])
 @pytest.mark.parametrize("cfg", [SMALL[1], SMALL[2], SMALL[4]], ids=["v3", "reuse", "evict"])
 def test_gather_tiles_per_cta(cfg, tpc):
