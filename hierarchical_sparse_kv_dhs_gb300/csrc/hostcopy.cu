@@ -203,8 +203,10 @@ __global__ void __launch_bounds__(kCopyThreads)
     next = nxt;
   }
   // this grid completes only after the resolve grid (the gather and the
-  // fresh-row copy rely on that)
-  if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // fresh-row copy rely on that): its last block waits for it.  The others
+  // leave once their items are copied; each holds a whole SM's registers
+  // (512 threads x 128), which the gather can use as soon as it is gone.
+  if (!waited && blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
   if (tid == 0) trace_mark(c.trace, kTraceCopy, true);
 }
