@@ -519,8 +519,8 @@ def test_decode_step_host_matches_device_path():
 @pytest.mark.parametrize("streams", [False, True])
 def test_decode_step_host_async_pipelined_matches_device_path(streams):
     """dhs_decode_step_host_async with later steps enqueued before step s's
-    outputs are read (two host output sets; with `streams`, three, the input
-    and output copies on their own streams and three device output blocks,
+    outputs are read (two host output sets; with `streams`, four, the input
+    and output copies on their own streams and four device output blocks,
     as the bench's e2e runs it) gives what the device-side dhs_decode_step
     leaves in device memory, step by step."""
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
@@ -534,7 +534,7 @@ def test_decode_step_host_async_pipelined_matches_device_path(streams):
         # host output sets; step s's outputs are read after step s+D-1 is
         # enqueued.  Without streams every copy is on the pool's stream, which
         # orders the one device output block's reuse.
-        D = 3 if streams else 2
+        D = 4 if streams else 2
         blocks = [b.output_block(i if streams else 0) for i in range(D)]
         cnt_off = b.counters.data_ptr() - b.step_out.data_ptr()
         loc_n, cnt_n = b.loc.numel() * 4, b.counters.numel() * 4
