@@ -231,7 +231,8 @@ struct GatherCommon {
   uint32_t later_cap;
   uint32_t gen;
   int32_t tpc;                // TMA gather: consecutive tiles per CTA (>= 1)
-  int32_t pad;
+  int32_t read_once;          // no row of the launch is read twice (one query per item,
+                              // no gather-only item): bulk loads hint L2 evict-first
 };
 
 // Each kernel file sets its kernels' shared-memory carveout to the maximum,

@@ -1213,6 +1213,12 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
     if (f == p->loc_keys.begin() || (f - 1)->loc != loc) return -1;
     return (f - 1)->pair;
   };
+  // Rows read once: verify queries and Reuse items read their rows again,
+  // from L2 when the first read left them there
+  g.read_once = 1;
+  for (int32_t i = 0; i < st->n_items; ++i)
+    if (st->items[i].queries > 1 || (st->items[i].flags & DHS_ITEM_GATHER_ONLY))
+      g.read_once = 0;
   p->gitems.clear();
   for (int32_t i = 0; i < st->n_items; ++i) {
     const dhs_item& it = st->items[i];
