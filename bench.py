@@ -833,6 +833,10 @@ def main():
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"hbm_gbs {peak_src} (copy, read+write bytes)",
                      "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
+                     "traffic_note": "DRAM bytes inside one launch (ncu): every row is read "
+                                     "from DRAM, but staging rows still in L2 when the "
+                                     "launch ends are written back after it, by the next "
+                                     "step's traffic or the flush",
                      "timed": f"{K2} launches, CUDA events around dhs_gather "
                               "(L2 flushed before each step)",
                      "context": ctx},
