@@ -20,8 +20,11 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "dhs_oracle.c")
-_LIB_PATH = os.path.join(_HERE, "liborc.so")
+# DHS_ORACLE_SRC names another copy of dhs_oracle.c to build and load instead
+# (the mutation harness in tests/ plants one mistake per copy); its library
+# is built beside it.
+_SRC = os.environ.get("DHS_ORACLE_SRC") or os.path.join(_HERE, "dhs_oracle.c")
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(_SRC)), "liborc.so")
 _lib = None
 _lock = threading.Lock()
 
@@ -32,6 +35,11 @@ RC_NAMES = {0: 0, -1: "einval", -2: "enomem", -3: "wouldwait", -4: "ebudget",
             -5: "erange", -8: "estate"}
 COUNTERS = ("entries", "unique", "tail", "opt", "hot", "host", "scan_max",
             "evicted")
+
+
+def source_path() -> str:
+    """The oracle source this module builds and loads."""
+    return _SRC
 
 
 def build(force: bool = False) -> str:
@@ -46,49 +54,54 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Set the argument and result types of the oracle's entry points on a
+    loaded copy of the library."""
+    i32, i64, u32, vp = (ctypes.c_int32, ctypes.c_int64,
+                         ctypes.c_uint32, ctypes.c_void_p)
+    L.orc_pool_new.restype = vp
+    L.orc_pool_new.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, i64]
+    L.orc_pool_free.restype = None
+    L.orc_pool_free.argtypes = [vp]
+    L.orc_pool_used.restype = i64
+    L.orc_pool_used.argtypes = [vp]
+    L.orc_admit.restype = ctypes.c_int
+    L.orc_admit.argtypes = [vp, i32, i32, vp, i64, vp, vp]
+    L.orc_reclaim.restype = ctypes.c_int
+    L.orc_reclaim.argtypes = [vp, vp, i32, i64, vp]
+    L.orc_release.restype = ctypes.c_int
+    L.orc_release.argtypes = [vp, i32]
+    L.orc_append.restype = ctypes.c_int
+    L.orc_append.argtypes = [vp, i32, i32, i32, vp]
+    L.orc_resolve.restype = ctypes.c_int
+    L.orc_resolve.argtypes = [vp, u32, i32, i32, i32, i32, vp, vp, vp]
+    L.orc_admit_device.restype = ctypes.c_int
+    L.orc_admit_device.argtypes = [vp, i32, i32, vp, i64, vp, vp]
+    L.orc_backup.restype = ctypes.c_int
+    L.orc_backup.argtypes = [vp, i64, vp]
+    L.orc_refill.restype = ctypes.c_int
+    L.orc_refill.argtypes = [vp, i64, vp]
+    L.orc_pending_backup.restype = i64
+    L.orc_pending_backup.argtypes = [vp]
+    L.orc_resolve_union.restype = ctypes.c_int
+    L.orc_resolve_union.argtypes = [vp, u32, i32, i32, i32, i32, vp, vp, vp, vp]
+    L.orc_gather.restype = ctypes.c_int
+    L.orc_gather.argtypes = [vp, vp, i64, vp]
+    L.orc_read_state.restype = ctypes.c_int
+    L.orc_read_state.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+    L.orc_read_rows.restype = ctypes.c_int
+    L.orc_read_rows.argtypes = [vp, i32, i32, ctypes.c_int, i64, i64, vp]
+    L.orc_check.restype = ctypes.c_int
+    L.orc_check.argtypes = [vp, i32, i32]
+    return L
+
+
 def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
             build()
-            L = ctypes.CDLL(_LIB_PATH)
-            i32, i64, u32, vp = (ctypes.c_int32, ctypes.c_int64,
-                                 ctypes.c_uint32, ctypes.c_void_p)
-            L.orc_pool_new.restype = vp
-            L.orc_pool_new.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, i64]
-            L.orc_pool_free.restype = None
-            L.orc_pool_free.argtypes = [vp]
-            L.orc_pool_used.restype = i64
-            L.orc_pool_used.argtypes = [vp]
-            L.orc_admit.restype = ctypes.c_int
-            L.orc_admit.argtypes = [vp, i32, i32, vp, i64, vp, vp]
-            L.orc_reclaim.restype = ctypes.c_int
-            L.orc_reclaim.argtypes = [vp, vp, i32, i64, vp]
-            L.orc_release.restype = ctypes.c_int
-            L.orc_release.argtypes = [vp, i32]
-            L.orc_append.restype = ctypes.c_int
-            L.orc_append.argtypes = [vp, i32, i32, i32, vp]
-            L.orc_resolve.restype = ctypes.c_int
-            L.orc_resolve.argtypes = [vp, u32, i32, i32, i32, i32, vp, vp, vp]
-            L.orc_admit_device.restype = ctypes.c_int
-            L.orc_admit_device.argtypes = [vp, i32, i32, vp, i64, vp, vp]
-            L.orc_backup.restype = ctypes.c_int
-            L.orc_backup.argtypes = [vp, i64, vp]
-            L.orc_refill.restype = ctypes.c_int
-            L.orc_refill.argtypes = [vp, i64, vp]
-            L.orc_pending_backup.restype = i64
-            L.orc_pending_backup.argtypes = [vp]
-            L.orc_resolve_union.restype = ctypes.c_int
-            L.orc_resolve_union.argtypes = [vp, u32, i32, i32, i32, i32, vp, vp, vp, vp]
-            L.orc_gather.restype = ctypes.c_int
-            L.orc_gather.argtypes = [vp, vp, i64, vp]
-            L.orc_read_state.restype = ctypes.c_int
-            L.orc_read_state.argtypes = [vp, i32, i32, vp, vp, vp, vp]
-            L.orc_read_rows.restype = ctypes.c_int
-            L.orc_read_rows.argtypes = [vp, i32, i32, ctypes.c_int, i64, i64, vp]
-            L.orc_check.restype = ctypes.c_int
-            L.orc_check.argtypes = [vp, i32, i32]
-            _lib = L
+            _lib = declare(ctypes.CDLL(_LIB_PATH))
     return _lib
 
 
