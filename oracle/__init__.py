@@ -93,6 +93,8 @@ def declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.orc_read_rows.argtypes = [vp, i32, i32, ctypes.c_int, i64, i64, vp]
     L.orc_check.restype = ctypes.c_int
     L.orc_check.argtypes = [vp, i32, i32]
+    L.orc_admit_window.restype = ctypes.c_int
+    L.orc_admit_window.argtypes = [vp, i32, i32, vp, i64]
     return L
 
 
@@ -156,6 +158,14 @@ class OraclePool:
             assert rows.size >= N * self.E
         rc = lib().orc_admit_device(self._h, r, s, _p(rows), N, _p(mask), ctypes.byref(d))
         return RC_NAMES[rc], d.value
+
+    def admit_window(self, r, s, N, rows=None):
+        """Admit a window source: the tail ring is its only storage; `rows`
+        are the window's rows [N - min(N, T), N)."""
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.uint16)
+            assert rows.size >= min(N, self.T) * self.E
+        return RC_NAMES[lib().orc_admit_window(self._h, r, s, _p(rows), N)]
 
     def backup(self, max_pages):
         n = ctypes.c_int64(0)

@@ -20,7 +20,9 @@
  *     found -- (1) the tail and the ready optional-history map, (2) a scan of
  *     the hot cache bounded by B with LRU replacement, (3) a copy from pinned
  *     host memory into the hot cache.
- *   - Speculative state: verification queries share missing-row retrieval.
+ *   - Speculative state: verification queries share missing-row retrieval;
+ *     the drafter keeps only its visible window, in a ring buffer (a window
+ *     source: the tail ring is its only storage).
  *   - Model-specific reuse: Reuse layers inherit the prior location vector
  *     (here: a gather of an existing location vector, no resolution).
  *   - Limits: rows generated during decoding always follow hot-cache rules.
@@ -70,6 +72,7 @@
 typedef struct {
   int admitted;
   int tracked;        /* holds row bytes (else metadata only) */
+  int window;         /* a window source: the tail ring is its only storage */
   int64_t N;          /* imported rows */
   int64_t L;          /* current length */
   int32_t *page_slot; /* [pages_max]: optional-pool slot, -1 = not ready */
@@ -103,7 +106,7 @@ static void reset_source_state(const orc_pool *p, orc_source *s) {
     s->backed[q] = 1;
     s->pend[q] = 0;
   }
-  s->admitted = 0; s->tracked = 0; s->N = 0; s->L = 0;
+  s->admitted = 0; s->tracked = 0; s->window = 0; s->N = 0; s->L = 0;
   free(s->host); free(s->tail); free(s->hot); free(s->imported);
   s->host = s->tail = s->hot = s->imported = NULL;
 }
@@ -413,12 +416,46 @@ int orc_release(orc_pool *p, int32_t r) {
   return ORC_OK;
 }
 
+/*
+ * Admit (r, s) as a window source ("Speculative state": the drafter keeps
+ * only its visible window, in a ring buffer).  The ring of T rows is all the
+ * source has: no host copy, no optional pages (it takes no capacity), and its
+ * rows never enter the hot cache.  A window of N rows holds rows
+ * [N - m, N), m = min(N, T), at ring slots row mod T; `rows` gives those m
+ * rows in order (NULL = metadata only).  L = N; N counts no imported pages.
+ */
+int orc_admit_window(orc_pool *p, int32_t r, int32_t s, const uint16_t *rows, int64_t N) {
+  orc_source *src = get_src(p, r, s);
+  if (!src || N < 0 || N > p->max_rows) return ORC_EINVAL;
+  if (src->admitted) return ORC_ESTATE;
+  if (rows) {
+    size_t E = (size_t)p->E;
+    src->tail = (uint16_t *)calloc((size_t)p->T * E, 2);
+    src->hot = (uint16_t *)calloc((size_t)p->B * E, 2);
+    if (!src->tail || !src->hot) {
+      free(src->tail); free(src->hot);
+      src->tail = src->hot = NULL;
+      return ORC_ENOMEM;
+    }
+    int64_t m = N < p->T ? N : p->T;
+    for (int64_t j = 0; j < m; ++j) {
+      int64_t row = N - m + j;
+      memcpy(src->tail + (size_t)(row % p->T) * E, rows + (size_t)j * E, E * 2);
+    }
+    src->tracked = 1;
+  }
+  src->window = 1;
+  src->N = 0; src->L = N; src->admitted = 1;
+  return ORC_OK;
+}
+
 /* ------------------------------------------------------------ append */
 
 /*
  * Append `count` decode rows to (r, s): row L+j goes to tail slot
  * (L+j) mod T and is written through to the host copy, so every row keeps
- * a host copy once it leaves the tail.  count <= T.
+ * a host copy once it leaves the tail.  A window source has no host copy:
+ * the row it overwrites leaves the window for good.  count <= T.
  */
 int orc_append(orc_pool *p, int32_t r, int32_t s, int32_t count,
                const uint16_t *rows) {
@@ -432,7 +469,7 @@ int orc_append(orc_pool *p, int32_t r, int32_t s, int32_t count,
     for (int32_t j = 0; j < count; ++j) {
       int64_t row = src->L + j;
       memcpy(src->tail + (size_t)(row % p->T) * E, rows + (size_t)j * E, E * 2);
-      memcpy(src->host + (size_t)row * E, rows + (size_t)j * E, E * 2);
+      if (!src->window) memcpy(src->host + (size_t)row * E, rows + (size_t)j * E, E * 2);
     }
   }
   src->L += count;
@@ -476,7 +513,9 @@ static uint32_t step1_location(const orc_pool *p, const orc_source *src,
 
 /*
  * Resolve the Q x k selection `sel` of (r, s) at `step` (>= 1) into `loc`
- * (Q*k) and `counters` (8).  On ORC_ERANGE (a row outside [0, L)) or
+ * (Q*k) and `counters` (8).  A window source holds only rows [L-T, L): any
+ * other row is out of its range.  On ORC_ERANGE (a row outside [0, L), or
+ * outside a window source's window) or
  * ORC_EBUDGET (more misses than unprotected hot slots) nothing changes and
  * every counter is 0; step 1 reads no state that resolution changes, so the
  * entries it resolves keep their locations and every other entry is
@@ -492,8 +531,10 @@ int orc_resolve(orc_pool *p, uint32_t step, int32_t r, int32_t s, int32_t Q,
   const int64_t pair = (int64_t)r * p->S + s;
   const int64_t L = src->L, B = p->B;
   for (int c = 0; c < 8; ++c) counters[c] = 0;
+  /* lowest row the source can serve: a window source only has its ring */
+  const int64_t lo = src->window && L > p->T ? L - p->T : 0;
   for (int64_t e = 0; e < n; ++e)
-    if (sel[e] < 0 || (int64_t)sel[e] >= L) {
+    if ((int64_t)sel[e] < lo || (int64_t)sel[e] >= L) {
       for (int64_t f = 0; f < n; ++f) loc[f] = step1_location(p, src, pair, sel[f]);
       return ORC_ERANGE;
     }
@@ -693,6 +734,7 @@ int orc_read_rows(const orc_pool *p, int32_t r, int32_t s, int which,
   int64_t lim = which == 0 ? p->max_rows : which == 1 ? p->T : p->B;
   if (row0 + n > lim) return ORC_EINVAL;
   const uint16_t *base = which == 0 ? src->host : which == 1 ? src->tail : src->hot;
+  if (!base) return ORC_EINVAL; /* a window source has no host copy */
   memcpy(out, base + (size_t)row0 * p->E, (size_t)n * p->E * 2);
   return ORC_OK;
 }

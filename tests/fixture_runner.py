@@ -1,7 +1,7 @@
 """Parser and runner for the hand-worked traces under tests/golden.
 
-A trace is a list of commands (pool, admit, admitdev, backup, refill,
-pending, hostok, reclaim, release, used, pages, append, resolve) each
+A trace is a list of commands (pool, admit, admitdev, admitwin, backup,
+refill, pending, hostok, reclaim, release, used, pages, append, resolve) each
 followed by the values worked out by hand.  The runner
 drives any implementation through a small adapter (the oracle, or the CUDA
 library through its C ABI) and checks every expected value, plus byte truth:
@@ -54,6 +54,7 @@ def run_trace(name: str, api, elems: int | None = None):
         op = tok[0]
         if op == "pool":
             R, S, T, B, E0, PR, max_rows, cap, reserve = map(int, tok[1:10])
+            tail_rows = T
             E = elems or E0
             api.new_pool(R, S, T, B, E, PR, max_rows, cap, reserve)
         elif op == "admit":
@@ -76,6 +77,15 @@ def run_trace(name: str, api, elems: int | None = None):
             assert tok[5] == "->"
             assert rc == _rc(tok[6]), f"{where}: rc {rc} != {tok[6]}"
             assert deficit == int(tok[7]), f"{where}: deficit {deficit} != {tok[7]}"
+            if rc == 0:
+                lengths[(r, s)] = N
+        elif op == "admitwin":
+            r, s, N = map(int, tok[1:4])
+            m = min(N, tail_rows)
+            rows = dhs_workload.payload_rows(PAYLOAD_TAG, s, r, N - m, m, E)
+            rc = api.admit_window(r, s, N, rows)
+            assert tok[4] == "->"
+            assert rc == _rc(tok[5]), f"{where}: rc {rc} != {tok[5]}"
             if rc == 0:
                 lengths[(r, s)] = N
         elif op in ("backup", "refill"):
@@ -160,6 +170,9 @@ class OracleAdapter:
 
     def admit_device(self, r, s, N, mask, rows):
         return self.p.admit_device(r, s, N, mask, rows)
+
+    def admit_window(self, r, s, N, rows):
+        return self.p.admit_window(r, s, N, rows)
 
     def backup(self, n):
         return self.p.backup(n)

@@ -12,7 +12,8 @@ why).  The pins themselves live in the other test_oracle_*.py files.
 Passages the mutants break: "Adaptive DHiSparse", How it works -- Memory
 split (complete pages, capacity rule, lowest free slot), Resolution (tail
 before the optional map, B-bounded scan, LRU victims, host copy), Speculative
-state (one union per verify block), Resident-first admission and
+state (one union per verify block; the drafter's ring-buffer window),
+Resident-first admission and
 Reclamation and refill (backup order, backup before free, bounded
 round-robin refill), Limits (decode rows written through to the host).
 """
@@ -56,7 +57,7 @@ MUTANTS = [
      "    for (int64_t e = 0; e < n; ++e) loc[e] = step1_location(p, src, pair, sel[e]);",
      "    for (int64_t e = 0; e < n; ++e) loc[e] = ORC_NO_LOC;", None),
     ("no_host_write_through",
-     "      memcpy(src->host + (size_t)row * E, rows + (size_t)j * E, E * 2);",
+     "      if (!src->window) memcpy(src->host + (size_t)row * E, rows + (size_t)j * E, E * 2);",
      "      (void)0;", None),
     ("allocator_highest_slot", "for (int64_t i = p->first_free; i < p->capacity; ++i)",
      "for (int64_t i = p->capacity - 1; i >= 0; --i)", None),
@@ -79,6 +80,14 @@ MUTANTS = [
      "      from = o->host + (size_t)row * E;", None),
     ("union_per_query_layout", "      loc[u] = per_entry[e];", "      loc[e] = per_entry[e];",
      None),
+    ("window_lower_bound_off_by_one",
+     "const int64_t lo = src->window && L > p->T ? L - p->T : 0;",
+     "const int64_t lo = src->window && L > p->T ? L - p->T - 1 : 0;", None),
+    ("window_admission_ring_slot", "      int64_t row = N - m + j;",
+     "      int64_t row = N - m + j + 1;", None),
+    ("window_serves_whole_history",
+     "const int64_t lo = src->window && L > p->T ? L - p->T : 0;",
+     "const int64_t lo = 0;", None),
 ] + [
     # each invariant check of orc_check taken out in turn
     (f"check_{k}_removed", f"return {k};", ";", "int orc_check(") for k in range(1, 10)

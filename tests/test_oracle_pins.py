@@ -28,7 +28,7 @@ from oracle import OraclePool, decode
 from oracle.run import OracleRun
 
 TRACES = ["resolve_micro_b2.txt", "resolve_micro_b3_pairs.txt",
-          "admission_micro.txt", "backup_refill_micro.txt"]
+          "admission_micro.txt", "backup_refill_micro.txt", "window_micro.txt"]
 
 
 @pytest.mark.parametrize("trace", TRACES)
@@ -250,3 +250,58 @@ def test_workload_byte_truth_and_invariants(oracle_lib, gen_lib, cfg):
             got = run.pool.rows(r, s, 0, 0, L)
             want = dhs_workload.payload_rows(cfg.tag, s, r, 0, L, cfg.row_elems)
             assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------ window sources
+
+@pytest.mark.parametrize("T", [1, 5, 16])
+def test_window_source_closed_form(oracle_lib, gen_lib, T):
+    """A window source ("Speculative state": the drafter keeps only its
+    visible window, in a ring buffer) beside an ordinary one, under random
+    appends and selections.  Closed form: a selection inside [L-T, L)
+    resolves entirely from the ring -- entry e at tail index pair*T +
+    sel[e] mod T, counters (Q*k, distinct, distinct, 0, 0, 0, 0, 0) -- and
+    gathers the payload of its rows; a selection with any row outside it is
+    ERANGE, its in-window entries keeping their ring locations and the rest
+    none.  The hot cache is never touched and no capacity is taken."""
+    rng = np.random.default_rng(T)
+    E, tag = 8, 96
+    p = OraclePool(2, 2, T, 4, E, 4, 400, 16)
+    assert p.admit(0, 0, 40, None, dhs_workload.payload_rows(tag, 0, 0, 0, 40, E))[0] == 0
+    used = p.used()
+    N = int(rng.integers(0, 60))
+    m = min(N, T)
+    assert p.admit_window(1, 1, N, dhs_workload.payload_rows(tag, 1, 1, N - m, m, E)) == 0
+    assert p.used() == used
+    pair, L = 1 * 2 + 1, N
+    for step in range(1, 60):
+        a = int(rng.integers(0, T + 1))
+        if a and L + a <= 400:
+            assert p.append(1, 1, a, dhs_workload.payload_rows(tag, 1, 1, L, a, E)) == 0
+            L += a
+        lo = max(0, L - T)
+        Q, k = int(rng.integers(1, 4)), int(rng.integers(1, 9))
+        if L == 0 or rng.random() < 0.3:  # some rows outside the window
+            sel = rng.integers(-2, L + 3, size=(Q, k))
+        else:
+            sel = rng.integers(lo, L, size=(Q, k))
+        rc, loc, cnt = p.resolve(step, 1, 1, sel)
+        inside = (sel >= lo) & (sel < L)
+        want_loc = np.where(inside, pair * T + np.mod(sel, T), 0xFFFFFFFF).astype(np.uint32)
+        assert np.array_equal(loc, want_loc), (step, sel, loc)
+        if inside.all():
+            u = np.unique(sel).size
+            assert rc == 0 and list(cnt) == [Q * k, u, u, 0, 0, 0, 0, 0]
+            rcg, st = p.gather(loc)
+            assert rcg == 0
+            for q in range(Q):
+                for i in range(k):
+                    want = dhs_workload.payload_row(tag, 1, 1, int(sel[q, i]), E)
+                    assert np.array_equal(st[q, i], want), (step, q, i)
+        else:
+            assert rc == "erange" and not cnt.any()
+        tags, stamps, pages, lens = p.state(1, 1)
+        assert (tags == -1).all() and (stamps == 0).all() and (pages == -1).all()
+        assert lens == (0, L, 1)
+        assert p.check(1, 1) == 0
+    p.close()
