@@ -6,7 +6,9 @@
 // ready on the GPU or has a host copy); Limits: rows generated during
 // decoding always follow hot-cache rules, so once a decode row leaves the
 // tail it is found only through the hot cache or the host copy.  Row L+j of
-// a pair goes to tail slot (L+j) mod T and to host row L+j.
+// a pair goes to tail slot (L+j) mod T and to host row L+j.  A window source
+// ("Speculative state": a drafter retains only the rows its window covers,
+// stored as a ring) has no host copy: its rows go to the ring only.
 #include "dhs_internal.h"
 
 namespace dhs {
@@ -33,7 +35,7 @@ __global__ void __launch_bounds__(kAppendThreads)
     const uint4 v = *reinterpret_cast<const uint4*>(it.rows + (size_t)j * rb + p * 16);
     uint8_t* t = c.tail + ((size_t)it.pair * c.T + (size_t)(row % c.T)) * rb + p * 16;
     *reinterpret_cast<uint4*>(t) = v;
-    *reinterpret_cast<uint4*>(it.host + (size_t)row * rb + p * 16) = v;
+    if (it.host) *reinterpret_cast<uint4*>(it.host + (size_t)row * rb + p * 16) = v;
   }
 }
 

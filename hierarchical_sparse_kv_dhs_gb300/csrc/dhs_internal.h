@@ -21,6 +21,10 @@ constexpr uint32_t kStatusEtimeout = 8u;
 constexpr int32_t kErrRange = -5, kErrBudget = -4;  // DHS_ERANGE, DHS_EBUDGET
 constexpr int kMaxHotRows = 16384;
 
+// Polls for a published loc_ready / copy_ready mark before falling back to
+// waiting for the grids (DHS_OPT_MARK_POLLS default).
+constexpr uint32_t kMarkPolls = 1u << 20;
+
 // Sequence numbers of resolve launches as published in loc_ready / copy_ready
 // marks (never 0, which is what a zeroed mark holds).
 constexpr uint32_t kSeqMask = 0x1FFFFFFFu;
@@ -80,12 +84,14 @@ struct ResolveItem {
   // decode rows appended by this launch (dhs_decode_step), else count 0
   const uint8_t* app_rows;  // [app_count][row_bytes] device
   uint8_t* app_host;        // device-visible pointer of the pair's host rows
+                            // (null: a window source, no host copy)
   int64_t app_L0;           // length before the append
   int32_t app_count;
   int16_t stage;       // list, per miss, the entries that selected it (host
                        // copy writes them into staging)
   int16_t loc_shared;  // a gather-only item of the launch reads `loc` too
   int32_t* index;  // union staging: [n] union rank of each entry; null = per-query
+  int64_t lo;      // lowest row the source serves: 0, or L - T for a window source
 };
 
 struct ResolveCommon {
@@ -167,6 +173,8 @@ struct CopyCommon {
   int32_t ent_cap;
   const int32_t* miss_off;    // [pairs][Mcap + 1] (items with staging)
   const int32_t* miss_ent;    // [pairs][ent_cap]
+  uint32_t mark_polls;        // polls of a copy_ready mark before waiting for the grid;
+                              // 0: never read the marks
 };
 
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,
@@ -233,6 +241,7 @@ struct GatherCommon {
   int32_t tpc;                // TMA gather: consecutive tiles per CTA (>= 1)
   int32_t read_once;          // no row of the launch is read twice (one query per item,
                               // no gather-only item): bulk loads hint L2 evict-first
+  uint32_t mark_polls;        // polls of a loc_ready mark before waiting for the grids
 };
 
 // Each kernel file sets its kernels' shared-memory carveout to the maximum,
@@ -260,7 +269,8 @@ constexpr int kAppendItemsMax = 256;
 
 struct AppendItem {
   const uint8_t* rows;  // [count][row_bytes] device
-  uint8_t* host;        // device-visible pointer of the pair's host rows
+  uint8_t* host;        // device-visible pointer of the pair's host rows (null: a
+                        // window source, whose rows go to the tail ring only)
   int64_t L0;           // length before the append
   int32_t pair;
   int32_t count;

@@ -61,13 +61,12 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 }
 
 // Bounded wait (whole warp) until the resolve kernel has published the
-// item's locations; false if they did not come out in time -- the caller
-// then waits for the resolve / host-copy grids instead, so giving up costs
-// time, never correctness.  Every lane takes its own acquire.
-constexpr uint32_t kLocPolls = 1u << 20;
+// item's locations; false if they did not come out within c.mark_polls polls
+// -- the caller then waits for the resolve / host-copy grids instead, so
+// giving up costs time, never correctness.  Every lane takes its own acquire.
 __device__ __forceinline__ bool wait_loc_ready(const GatherCommon& c, const GatherItem& it) {
   const uint32_t want = it.seq & kSeqMask;
-  for (uint32_t i = 0; i < kLocPolls; ++i) {
+  for (uint32_t i = 0; i < c.mark_polls; ++i) {
     const bool r = ld_acquire(&c.loc_ready[it.pair]) == want;
     if (__all_sync(0xFFFFFFFFu, r)) return true;
     __nanosleep(200);

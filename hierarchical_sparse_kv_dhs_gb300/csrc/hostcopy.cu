@@ -30,8 +30,6 @@ __device__ __forceinline__ uint4 ld_sys(const uint8_t* p) {
 constexpr int kRowsPerWarp = 4;
 constexpr int kChunksPerLane = 3;  // rows up to 96 x 16 = 1536 bytes
 
-constexpr uint32_t kReadyPolls = 1u << 20;
-
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -45,8 +43,9 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 // CTA does not wait for the whole resolve grid: it
 // takes, in order, every owned item whose mark is out as one batch (waiting,
 // bounded, only when none is), and its warps copy the batch's rows as one
-// flat list, four rows per warp in flight.  A poll that runs out falls back
-// to waiting for the resolve grid.
+// flat list, four rows per warp in flight.  A poll that runs out (after
+// c.mark_polls polls; with 0 the marks are never read) falls back to waiting
+// for the resolve grid.
 constexpr int kBatchMax = 64;
 
 template <int MAXI, bool kSmallRow>
@@ -72,9 +71,10 @@ __global__ void __launch_bounds__(kCopyThreads)
       uint32_t acc = 0;
       while (j < c.n_items && n < kBatchMax) {
         const uint32_t* mark = c.ready + P.items[j].pair;
-        uint32_t v = waited ? 0u : ld_acquire_u32(mark);
-        bool ok = waited || (v & kSeqMask) == want;
-        for (uint32_t i = 0; !ok && n == 0 && i < kReadyPolls; ++i) {
+        const bool read = !waited && c.mark_polls != 0;
+        uint32_t v = read ? ld_acquire_u32(mark) : 0u;
+        bool ok = waited || (read && (v & kSeqMask) == want);
+        for (uint32_t i = 0; !ok && n == 0 && i < c.mark_polls; ++i) {
           __nanosleep(256);
           v = ld_acquire_u32(mark);
           ok = (v & kSeqMask) == want;

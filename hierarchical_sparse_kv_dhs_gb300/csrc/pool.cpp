@@ -130,6 +130,7 @@ int validate_geometry(const dhs_pool_config* c) {
 
 struct PairState {
   bool admitted = false;
+  bool window = false;          // window source: the tail ring is its only storage
   int64_t N = 0, L = 0;
   uint8_t* host = nullptr;      // caller's pinned host rows
   uint8_t* host_dev = nullptr;  // device-visible address of the same rows
@@ -187,6 +188,7 @@ struct dhs_pool {
   int32_t* miss_ent = nullptr;  // [pairs][ent_cap]
   int64_t ent_cap = 0;
   int stage_misses = 1;         // DHS_OPT_STAGE_MISSES
+  uint32_t mark_polls = dhs::kMarkPolls;  // DHS_OPT_MARK_POLLS
   std::vector<uint8_t> staged_pair;  // the host copy stages this pair's misses this step
   std::vector<uint8_t> staged_item;  // per item of the step: a gather-only item whose
                                      // staging the host copy writes too
@@ -612,6 +614,11 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     pool->gather_tpc = (int)value;
     return DHS_OK;
   }
+  if (key == DHS_OPT_MARK_POLLS) {
+    if (value < -1 || value > (int64_t)dhs::kMarkPolls) return DHS_EINVAL;
+    pool->mark_polls = value < 0 ? dhs::kMarkPolls : (uint32_t)value;
+    return DHS_OK;
+  }
   return DHS_EINVAL;
 }
 
@@ -637,6 +644,7 @@ int dhs_get_option(dhs_pool* pool, int32_t key, int64_t* value) {
     case DHS_OPT_FRESH_LIST: *value = use_fresh_list(pool) ? 1 : 0; return DHS_OK;
     case DHS_OPT_GATHER_TPC: *value = pool->gather_tpc; return DHS_OK;
     case DHS_OPT_STAGE_MISSES: *value = pool->stage_misses; return DHS_OK;
+    case DHS_OPT_MARK_POLLS: *value = pool->mark_polls; return DHS_OK;
     default: return DHS_EINVAL;
   }
 }
@@ -808,6 +816,37 @@ int dhs_backup(dhs_pool* p, int64_t max_pages, int64_t* done) {
   }
   if ((rc = run_moves(p))) return rc;
   if (done) *done = n;
+  return DHS_OK;
+}
+
+int dhs_admit_window(dhs_pool* p, int32_t req, int32_t src, const void* dev_rows,
+                     int64_t n_rows) {
+  if (!p || req < 0 || req >= p->cfg.max_requests || src < 0 || src >= p->cfg.sources)
+    return DHS_EINVAL;
+  const dhs_pool_config& c = p->cfg;
+  if (n_rows < 0 || n_rows > c.max_rows_per_request) return DHS_EINVAL;
+  if (n_rows > 0 && (!dev_rows || (uintptr_t)dev_rows % 16)) return DHS_EINVAL;
+  const int64_t pair = (int64_t)req * c.sources + src;
+  PairState& s = p->ps[pair];
+  if (s.admitted) return DHS_ESTATE;
+  int rc = enter(p);
+  if (rc) return rc;
+  // the window's rows [N - m, N) into ring slots row mod T (at most two runs)
+  const int64_t T = c.tail_rows, rb = c.row_bytes;
+  const int64_t m = std::min<int64_t>(n_rows, T);
+  for (int64_t row = n_rows - m; row < n_rows;) {
+    const int64_t slot = row % T;
+    const int64_t run = std::min(n_rows - row, T - slot);
+    cudaError_t e = cudaMemcpyAsync((uint8_t*)c.tail_dev + ((size_t)pair * T + slot) * rb,
+                                    (const uint8_t*)dev_rows + (size_t)(row - (n_rows - m)) * rb,
+                                    run * rb, cudaMemcpyDeviceToDevice, p->stream);
+    if (e != cudaSuccess) return DHS_ECUDA;
+    row += run;
+  }
+  s.admitted = true;
+  s.window = true;
+  s.N = 0;  // no imported pages: nothing for the optional map, refill or reclaim
+  s.L = n_rows;
   return DHS_OK;
 }
 
@@ -1016,6 +1055,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     r.index = (it.flags & DHS_ITEM_UNION) ? it.index_dev : nullptr;
     r.L = s.L;
     r.N = s.N;
+    r.lo = s.window ? std::max<int64_t>(0, s.L - c.tail_rows) : 0;
     r.pair = (int32_t)pair;
     r.n = it.queries * it.topk;
     // fused steps: the host copy writes the misses into the item's staging,
@@ -1094,6 +1134,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   ccm.Mcap = (int32_t)p->mcap;
   ccm.row_bytes = c.row_bytes;
   ccm.trace = p->trace;
+  ccm.mark_polls = p->mark_polls;
   const size_t nr = p->ritems.size();
   for (size_t b = 0; b < nr; b += dhs::kResolveItemsLarge) {
     const int n = (int)std::min<size_t>(dhs::kResolveItemsLarge, nr - b);
@@ -1193,6 +1234,7 @@ static int launch_gathers(dhs_pool* p, const dhs_step* st, bool fused) {
   g.later_cap = (uint32_t)std::min<int64_t>(p->later_cap, UINT32_MAX);
   g.gen = p->gen;
   g.tpc = p->gather_tpc;
+  g.mark_polls = p->mark_polls;
   // the step's resolved items publish their locations; gathers of them (and
   // Reuse items handed the same location vector) may go before the grids end
   const bool lr = fused && p->early && p->fused_resolved && tma_gather(p);
@@ -1499,7 +1541,9 @@ extern "C" int dhs_resolve_noalloc(dhs_pool* p, const dhs_step* st) {
   if (rc) return rc;
   if (p->pairs > dhs::kNoallocPairs || p->pairs * p->mcap > dhs::kNoallocMissCap)
     return DHS_EINVAL;  // the pool's miss lists do not fit the fixed scratch
-  if ((rc = enter(p))) return rc;
+  // as dhs_resolve: an outstanding dhs_prefetch is joined only when the step
+  // touches its pairs (its miss lists are the pool's, not the fixed array)
+  if ((rc = enter_step(p, st))) return rc;
   dhs::NoallocScratch scr{};
   if (dhs::noalloc_scratch(&scr) != cudaSuccess) return DHS_ECUDA;
   if ((rc = flush(p))) return rc;

@@ -25,6 +25,9 @@
 //     miss in ascending row order picks;
 //   * the misses' (row, slot) pairs go to a global miss list read by the
 //     host-copy kernel; locations and counters are written last.
+// A window source ("Speculative state": a drafter retains only the rows its
+// window covers, stored as a ring) serves only rows [L-T, L): the range check starts
+// at the item's `lo`, and every row that passes it is a tail row.
 // State (tags, stamps) is written only after the budget check passes, so a
 // failing item changes nothing.
 #include "dhs_internal.h"
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
       const uint4 v = *reinterpret_cast<const uint4*>(it.app_rows + (size_t)j * rb + p * 16);
       *reinterpret_cast<uint4*>(c.tail + ((size_t)pair * T + (size_t)(row % T)) * rb +
                                 p * 16) = v;
-      *reinterpret_cast<uint4*>(it.app_host + (size_t)row * rb + p * 16) = v;
+      if (it.app_host) *reinterpret_cast<uint4*>(it.app_host + (size_t)row * rb + p * 16) = v;
     }
   }
 
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
     int cur = -1;
     for (int j = 0; j < 4 && b + j < n; ++j) {
       const int32_t row = it.sel[b + j];
-      if (row < 0 || (int64_t)row >= L) {
+      if ((int64_t)row < it.lo || (int64_t)row >= L) {
         s_bad = 1;
         continue;
       }

@@ -45,6 +45,7 @@ DHS_OPT_EARLY = 4
 DHS_OPT_FRESH_LIST = 5
 DHS_OPT_GATHER_TPC = 6
 DHS_OPT_STAGE_MISSES = 7
+DHS_OPT_MARK_POLLS = 8
 DHS_BUF_HOT, DHS_BUF_TAIL, DHS_BUF_OPT, DHS_BUF_META = range(4)
 
 _i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
@@ -100,6 +101,7 @@ def _load():
         "dhs_decode_step_host_async": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _i32, _vp,
                                                       _vp, _i32, _vp]),
         "dhs_admit_device": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _i64, _vp, P(_i64)]),
+        "dhs_admit_window": (ctypes.c_int, [_vp, _i32, _i32, _vp, _i64]),
         "dhs_backup": (ctypes.c_int, [_vp, _i64, P(_i64)]),
         "dhs_pending_backup": (_i64, [_vp]),
         "dhs_refill": (ctypes.c_int, [_vp, _i64, P(_i64)]),
@@ -186,6 +188,10 @@ def dhs_admit_device(h, req, src, dev_ptr, host_ptr, n_rows, mask=None):
         m = mask.ctypes.data
     rc = lib.dhs_admit_device(h, req, src, dev_ptr, host_ptr, n_rows, m, ctypes.byref(d))
     return rc, d.value
+
+
+def dhs_admit_window(h, req, src, dev_ptr, n_rows):
+    return lib.dhs_admit_window(h, req, src, dev_ptr, n_rows)
 
 
 def dhs_backup(h, max_pages):
@@ -375,6 +381,9 @@ class Pool:
 
     def admit_device(self, req, src, dev_ptr, host_ptr, n_rows, mask=None):
         return dhs_admit_device(self.h, req, src, dev_ptr, host_ptr, n_rows, mask)
+
+    def admit_window(self, req, src, dev_ptr, n_rows):
+        return dhs_admit_window(self.h, req, src, dev_ptr, n_rows)
 
     def backup(self, max_pages):
         return dhs_backup(self.h, max_pages)

@@ -124,7 +124,10 @@ enum { DHS_BUF_HOT = 0, DHS_BUF_TAIL, DHS_BUF_OPT, DHS_BUF_META, DHS_NUM_BUFS };
 /*
  * Bytes of the four device buffers the caller must allocate for `cfg`
  * (pointer and stream fields are ignored), written to out[DHS_NUM_BUFS].
- * Every buffer must be 256-byte aligned.  Pure host arithmetic.
+ * Every buffer must be 256-byte aligned.  Pure host arithmetic.  The pages
+ * have no passage for this call: it exists because the caller, not the
+ * library, owns device memory (their "Memory split" fixes what the buffers
+ * hold, not how they are sized).
  * Errors: DHS_EINVAL for an invalid geometry.
  */
 int dhs_pool_bytes(const dhs_pool_config *cfg, size_t out[DHS_NUM_BUFS]);
@@ -202,6 +205,31 @@ int dhs_release(dhs_pool *pool, int32_t req);
 int dhs_admit_device(dhs_pool *pool, int32_t req, int32_t src, const void *dev_rows,
                      void *host_rows, int64_t n_rows, const uint8_t *resident_page_mask,
                      int64_t *deficit_pages);
+
+/*
+ * Admit (req, src) as a window source ("Speculative state": a drafter
+ * retains only the rows its window covers, stored as a ring).  The source's tail ring
+ * of tail_rows rows is its only storage: it has no host copy, no optional
+ * pages (it takes no pool capacity) and its rows never enter the hot cache.
+ * A window of n_rows rows holds rows [n_rows - m, n_rows), m = min(n_rows,
+ * tail_rows), at ring slots row mod tail_rows.
+ *   dev_rows  device memory, 16-byte aligned: those m rows in order, row j
+ *             at dev_rows + j * row_bytes; read only by copies this call
+ *             enqueues on the pool's stream (reuse it after the stream has
+ *             passed them).  May be NULL when n_rows is 0.
+ * Afterwards: dhs_append writes a window source's rows into the ring only
+ * (each overwrites the row tail_rows before it, which leaves the window for
+ * good); a resolve gives every selected row in [L - tail_rows, L) its tail
+ * location (counters: entries, unique, tail = unique, the rest 0), and a
+ * selection holding any other row is DHS_ERANGE (device-side, as for rows
+ * outside [0, L): the item keeps only its in-window locations).  Gathers,
+ * release and the status calls treat it like any source.  The layout of the
+ * location vector is unchanged (tier DHS_TIER_TAIL).
+ * Errors: DHS_EINVAL (arguments, alignment, n_rows > max_rows_per_request),
+ * DHS_ESTATE (already admitted), DHS_ECUDA.
+ */
+int dhs_admit_window(dhs_pool *pool, int32_t req, int32_t src, const void *dev_rows,
+                     int64_t n_rows);
 
 /*
  * Deferred host backup: enqueue the device-to-host copies of at most
@@ -347,7 +375,10 @@ int dhs_resolve(dhs_pool *pool, const dhs_step *step);
 int dhs_prefetch(dhs_pool *pool, const dhs_step *step, void *side_stream);
 
 /*
- * Gather: staging_dev[q][i] = the row at loc_dev[q][i] for every item
+ * Gather ("Memory split": verification staging holds the selected rows that
+ * sparse attention reads; "Speculative state": each verify query's rows are
+ * staged; "Model-specific reuse": Reuse layers gather an inherited location
+ * vector).  staging_dev[q][i] = the row at loc_dev[q][i] for every item
  * (resolved or gather-only); DHS_NO_LOC rows become zeros and DHS_END_LOC
  * entries are skipped (staging untouched).  staging_dev must
  * be 16-byte aligned.  Stream-ordered after any earlier dhs_resolve.
@@ -375,8 +406,13 @@ int dhs_gather(dhs_pool *pool, const dhs_step *step);
  *     (other streams, other pools) race on it: issue them in one stream
  *     order.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first
- *     call before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current and keeps it for the
+ *     life of the process; make that first call before any stream capture.
+ *     A cudaDeviceReset unloads the array with the library's device code,
+ *     so the kept address is stale afterwards: do not use this entry point
+ *     on a device after resetting it.
+ *   - An outstanding dhs_prefetch is waited for only when the step names
+ *     one of its (request, source) pairs, as in dhs_resolve.
  * Errors: as dhs_resolve, plus DHS_EINVAL for pools beyond the limit.
  */
 int dhs_resolve_noalloc(dhs_pool *pool, const dhs_step *step);
@@ -459,6 +495,8 @@ int dhs_decode_step_host_async(dhs_pool *pool, const dhs_copy *in, int32_t n_in,
 
 /*
  * Synchronise the pool's stream, read and clear the sticky device status.
+ * The pages have no passage for this call: device-side errors cannot be
+ * returned by the asynchronous call that caused them, so they are read here.
  * *flags (may be NULL) receives DHS_STATUS_* bits.  Returns DHS_OK when no
  * flag was set, else DHS_ERANGE (ERANGE or ELOC), DHS_EBUDGET or
  * DHS_ETIMEDOUT, or DHS_ECUDA if the stream reported an error.
@@ -476,7 +514,12 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
                    uint32_t *stamps, int32_t *page_slot, int64_t *info);
 
 /* Tunables (performance only; results do not depend on them). */
-#define DHS_OPT_COPY_CTAS 1 /* host-copy CTAs; 0 = 32 */
+/* Host-copy CTAs; 0 = 32.  The pages scale the copy kernel from 4 to 32
+ * thread blocks with batch size; on GB300 fewer than about 16 blocks leave
+ * the host link idle (miss-heavy workload: 4 blocks 78 GB/s, 16 188, 32 198
+ * of a 211 GB/s pinned copy), so the default is the upper end at every
+ * batch size. */
+#define DHS_OPT_COPY_CTAS 1
 #define DHS_OPT_GATHER_IMPL 2 /* 1 = TMA bulk copy, 16-row tiles of two
                                      warps (default); 0 = 16-byte vector copy,
                                      256 threads per 32-row tile (the only one
@@ -507,6 +550,13 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
  * entry of the resolved item that selected it, and the gather leaves those
  * rows out; 0 = the gather copies them from the hot cache after the copy. */
 #define DHS_OPT_STAGE_MISSES 7
+/* Fused steps: how many times a gather tile polls for its item's published
+ * locations, and a host-copy block for an item's published miss list,
+ * before it gives up and waits for the whole resolve (and host-copy) grids
+ * instead -- the slower path, with the same results.  -1 (default) = 2^20
+ * polls; 0 .. 2^20.  0 sends every such tile and block down that path at
+ * once (for tests of it). */
+#define DHS_OPT_MARK_POLLS 8
 int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
 /* The value in effect (DHS_OPT_FRESH_LIST: 0 or 1, the auto rule resolved
  * for the pool's current admissions).  DHS_EINVAL for an unknown key. */

@@ -21,8 +21,8 @@
  *     the hot cache bounded by B with LRU replacement, (3) a copy from pinned
  *     host memory into the hot cache.
  *   - Speculative state: verification queries share missing-row retrieval;
- *     the drafter keeps only its visible window, in a ring buffer (a window
- *     source: the tail ring is its only storage).
+ *     a drafter retains only the rows its window covers, stored as a ring (a
+ *     window source: the tail ring is its only storage).
  *   - Model-specific reuse: Reuse layers inherit the prior location vector
  *     (here: a gather of an existing location vector, no resolution).
  *   - Limits: rows generated during decoding always follow hot-cache rules.
@@ -417,8 +417,8 @@ int orc_release(orc_pool *p, int32_t r) {
 }
 
 /*
- * Admit (r, s) as a window source ("Speculative state": the drafter keeps
- * only its visible window, in a ring buffer).  The ring of T rows is all the
+ * Admit (r, s) as a window source ("Speculative state": a drafter retains
+ * only the rows its window covers, stored as a ring).  The ring of T rows is all the
  * source has: no host copy, no optional pages (it takes no capacity), and its
  * rows never enter the hot cache.  A window of N rows holds rows
  * [N - m, N), m = min(N, T), at ring slots row mod T; `rows` gives those m

@@ -46,6 +46,15 @@ class GpuAdapter:
             self.lengths[(r, s)] = N
         return dhs.RC_NAMES[rc], d
 
+    def admit_window(self, r, s, N, rows):
+        m = min(N, self.T)
+        dev = torch.from_numpy(np.ascontiguousarray(rows[:m]).view(np.int16).copy()).cuda()
+        rc = self.pool.admit_window(r, s, dev.data_ptr() if m else None, N)
+        torch.cuda.synchronize()  # dev is read by the copies just enqueued
+        if rc == 0:
+            self.lengths[(r, s)] = N
+        return dhs.RC_NAMES[rc]
+
     def backup(self, n):
         rc, k = self.pool.backup(n)
         torch.cuda.synchronize()

@@ -37,7 +37,7 @@ def _as_u32(t):
 
 def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
                 gather_impl=0, patch=None, early=1, union=False, fresh=None, tpc=None,
-                stage=None):
+                stage=None, polls=None):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
@@ -56,6 +56,8 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
         gpu.pool.set_option(dhs.DHS_OPT_GATHER_TPC, tpc)
     if stage is not None:
         gpu.pool.set_option(dhs.DHS_OPT_STAGE_MISSES, stage)
+    if polls is not None:
+        gpu.pool.set_option(dhs.DHS_OPT_MARK_POLLS, polls)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
     orc = OracleRun(cfg, wl, requests=sampled, union=union)
     try:
@@ -272,6 +274,34 @@ def test_location_mark_of_step1_only_items_read_by_reuse_items():
         run.close()
 
 
+@pytest.mark.parametrize("cfg", SMALL + [UNION[3], REUSE5, RESIDENT_REUSE],
+                         ids=[c.name for c in SMALL] + ["v8", "reuse5", "resident_reuse"])
+def test_mark_poll_fallbacks(cfg):
+    """Poll limit 0: no gather tile reads an item's published locations and
+    no host-copy block reads an item's published miss list; every one of
+    them takes the fallback of waiting for the whole resolve (and host-copy)
+    grids.  The results stay bit-exact, per query and union layout, with the
+    fresh-row list on and off."""
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    compare_run(cfg, gather_impl=1, polls=0)
+    compare_run(cfg, gather_impl=1, polls=0, fresh=0)
+    compare_run(cfg, gather_impl=1, polls=0, union=True)
+    # the option's range and its value in effect
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    run = GpuRun(TINY, Workload(TINY))
+    try:
+        h, key = run.pool.h, dhs.DHS_OPT_MARK_POLLS
+        assert run.pool.get_option(key) == 1 << 20
+        assert dhs.dhs_set_option(h, key, 0) == dhs.DHS_OK
+        assert run.pool.get_option(key) == 0
+        assert dhs.dhs_set_option(h, key, (1 << 20) + 1) == dhs.DHS_EINVAL
+        assert dhs.dhs_set_option(h, key, -2) == dhs.DHS_EINVAL
+        assert dhs.dhs_set_option(h, key, -1) == dhs.DHS_OK
+        assert run.pool.get_option(key) == 1 << 20
+    finally:
+        run.close()
+
+
 @pytest.mark.parametrize("tpc", [2, 5])
 @pytest.mark.parametrize("cfg", [SMALL[1], SMALL[2], SMALL[4]], ids=["v3", "reuse", "evict"])
 def test_gather_tiles_per_cta(cfg, tpc):
@@ -407,11 +437,11 @@ def test_c8_full_size_sampled(impl, early):
 
 
 def test_c64_full_size_sampled():
-    compare_run(C64, sampled=[0, 63], check_all_bytes=False)
+    compare_run(C64, sampled=[0, 63])
 
 
 def test_c64_union_full_size_sampled():
-    compare_run(C64, sampled=[0, 63], check_all_bytes=False, union=True)
+    compare_run(C64, sampled=[0, 63], union=True)
 
 
 def test_decode_step_fallback_matches_split_calls():
@@ -459,7 +489,7 @@ def test_c128_full_size_sampled():
 
 
 def test_long_full_size_sampled():
-    compare_run(LONG, sampled=[0, 31], check_all_bytes=False)
+    compare_run(LONG, sampled=[0, 31])
 
 
 def test_admission_rejects_misaligned_host_rows():

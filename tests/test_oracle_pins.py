@@ -256,8 +256,8 @@ def test_workload_byte_truth_and_invariants(oracle_lib, gen_lib, cfg):
 
 @pytest.mark.parametrize("T", [1, 5, 16])
 def test_window_source_closed_form(oracle_lib, gen_lib, T):
-    """A window source ("Speculative state": the drafter keeps only its
-    visible window, in a ring buffer) beside an ordinary one, under random
+    """A window source ("Speculative state": a drafter retains only the rows
+    its window covers, stored as a ring) beside an ordinary one, under random
     appends and selections.  Closed form: a selection inside [L-T, L)
     resolves entirely from the ring -- entry e at tail index pair*T +
     sel[e] mod T, counters (Q*k, distinct, distinct, 0, 0, 0, 0, 0) -- and

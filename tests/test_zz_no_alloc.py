@@ -36,39 +36,63 @@ def lib():
     return dhs
 
 
+def _same_results(cfg, ref, new):
+    torch.cuda.synchronize()
+    assert ref.status() == (0, 0) and new.status() == (0, 0)
+    assert torch.equal(ref.loc, new.loc)
+    assert torch.equal(ref.counters, new.counters)
+    assert torch.equal(ref.staging.view(torch.int16), new.staging.view(torch.int16))
+    for r in range(cfg.requests):
+        for s in range(cfg.sources):
+            a, b = ref.pool.read_state(r, s), new.pool.read_state(r, s)
+            assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert ref.counters[..., 5].sum().item() > 0, "the workload must fetch rows from host"
+
+
+def _resolve_noalloc(dhs, run, step):
+    st, _ = run._steps[step - 1]
+    assert dhs.lib.dhs_resolve_noalloc(run.pool.h, ctypes.byref(st)) == dhs.DHS_OK
+
+
 def test_noalloc_resolve_matches_resolve_two_calls(lib):
+    """Two identical pools, two decode steps, one pool resolved through each
+    entry point.  Between the two steps another pool, with more (request,
+    source) pairs and longer miss lists (so the fixed array is laid out
+    differently), resolves through the no-allocation entry point on the same
+    stream: it overwrites the shared array, and the first pool's second step
+    must still match, since every entry a call reads it wrote itself."""
     dhs = lib
     from dhs_workload.configs import TINY, Workload
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
 
     cfg = TINY.scaled(name="noalloc", tag=71, requests=3, sources=2, residency=0.1,
                       hot=300, steps=2)
-    wl = Workload(cfg)
-    ref = GpuRun(cfg, wl)
-    new = GpuRun(cfg, wl)
+    other_cfg = TINY.scaled(name="noalloc_other", tag=72, requests=5, sources=2,
+                            residency=0.0, hot=500, topk=400, steps=1)
+    wl, other_wl = Workload(cfg), Workload(other_cfg)
+    ref, new = GpuRun(cfg, wl), GpuRun(cfg, wl)
+    other_ref, other = GpuRun(other_cfg, other_wl), GpuRun(other_cfg, other_wl)
+    assert new.pool.stream.cuda_stream == other.pool.stream.cuda_stream
     try:
         for step in (1, 2):
             ref.append(step)
             new.append(step)
             ref.resolve(step)
-            st, _ = new._steps[step - 1]
-            assert dhs.lib.dhs_resolve_noalloc(new.pool.h, ctypes.byref(st)) == dhs.DHS_OK
+            _resolve_noalloc(dhs, new, step)
             ref.gather(step)
             new.gather(step)
-            torch.cuda.synchronize()
-            assert ref.status() == (0, 0) and new.status() == (0, 0)
-            assert torch.equal(ref.loc, new.loc), step
-            assert torch.equal(ref.counters, new.counters), step
-            assert torch.equal(ref.staging.view(torch.int16), new.staging.view(torch.int16)), step
-            for r in range(cfg.requests):
-                for s in range(cfg.sources):
-                    a, b = ref.pool.read_state(r, s), new.pool.read_state(r, s)
-                    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
-            host = ref.counters[..., 5].sum().item()
-            assert host > 0, "the workload must fetch rows from host memory"
+            _same_results(cfg, ref, new)
+            if step == 1:
+                other_ref.append(1)
+                other.append(1)
+                other_ref.resolve(1)
+                _resolve_noalloc(dhs, other, 1)
+                other_ref.gather(1)
+                other.gather(1)
+                _same_results(other_cfg, other_ref, other)
     finally:
-        ref.close()
-        new.close()
+        for run in (ref, new, other_ref, other):
+            run.close()
 
 
 def test_noalloc_rejects_pools_beyond_the_limit(lib):
