@@ -3,25 +3,30 @@
 One step = append every source's decode rows, resolve every request's
 selections through tail / optional map / hot cache / pinned host, and
 gather every layer into staging, over one batch of a synthetic workload
-(default: the C8 decode workload -- 8 requests x 4 layers x 32K-row
-histories of 576 bf16, top-k 2048, B 4096, all imported history
-optional-resident).
+(default: the C64 speculative-verify workload -- 64 requests x 4 layers x
+32K-row histories of 576 bf16, 8 verify queries of top-k 2048 each, B 4096,
+40 % of complete pages optional-resident, misses fetched from pinned host
+memory; the largest per-step work of the single-GPU workloads).
 
 The bench cycles through the workload's decode steps; after the last one
 the pool is reset (every request released and admitted again, untimed) and
 the sequence starts over, so any number of genuine decode steps can be
-timed.  A workload's own warm-up steps (C128: 16) always run untimed.
+timed.  A workload's own warm-up steps (C128: 16) and the first step after
+every reset (hot caches empty) always run untimed.
 
 Prints one JSON line.  value = selected rows resolved + gathered per second
 with every input resident in HBM: device time from CUDA events on the
-launching stream, L2 flushed (a 256 MB write, then a 256 MB read of another
-buffer) before every timed step.  A second pass times the same steps through dhs_resolve and
-dhs_gather separately, so the gather kernel's own duration gives the roofline.
-e2e = the same metric through the C ABI with each step's selections and
-decode rows copied from pinned host memory and its locations + counters
-read back, copies inside the timed region.
+launching stream.  L2: a workload whose step moves less than four times the
+L2 size (C8, Tiny) is timed with L2 flushed before every step (a 256 MB
+write, then a 256 MB read of another buffer); the others have inputs far
+larger than L2 and are timed as consecutive steps (--l2 overrides).  The
+line carries the other method's figure too.  A second pass times the same
+steps through dhs_resolve and dhs_gather separately, so the gather kernel's
+own duration gives the roofline.  e2e = the same metric through the C ABI
+with each step's selections and decode rows copied from pinned host memory
+and its locations + counters read back, copies inside the timed region.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c8]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c64]
   python bench.py --impl reference ...   (the CPU oracle as the reference arm)
 """
 from __future__ import annotations
@@ -42,6 +47,7 @@ sys.path.insert(0, ROOT)
 METRIC = ("selected KV rows resolved+gathered/sec and GB/s vs HBM & host-link "
           "roofline")
 UNIT = "rows/s"
+L2_BYTES = 129 << 20  # GB300 L2, about 129 MB
 GATHER_WRITE_BYTES_PER_ENTRY = 1152 + 4  # staging row write + location read
 # host-buffer pipeline depth: output sets a serving loop cycles through (the
 # host reads step s-3's outputs after enqueuing step s).  C8, µs a step with
@@ -49,40 +55,72 @@ GATHER_WRITE_BYTES_PER_ENTRY = 1152 + 4  # staging row write + location read
 E2E_SETS = 4
 
 
+_ALG_CACHE = {}
+
+
 def gather_alg_bytes(cfg, wl, step, union=False):
+    key = (cfg, step, union)
+    if key not in _ALG_CACHE:
+        _ALG_CACHE[key] = _gather_alg_bytes(cfg, wl, step, union)
+    return _ALG_CACHE[key]
+
+
+def _gather_alg_bytes(cfg, wl, step, union=False):
     """Algorithmic HBM bytes of one step's gather launch: every unique
     selected row of a resolved (request, source) read once (verify queries
     and reuse layers read the same rows again), and every gathered entry
     written to staging with its location read.  Union staging writes each
     layer's distinct rows once and still reads every entry's location."""
     import numpy as np
-    reads = writes = 0
-    for r in range(cfg.requests):
-        u = [int(np.unique(wl.sel(step, r, s)).size) for s in range(cfg.sources)]
-        reads += sum(u)
-        if union:
-            writes += sum(u) + cfg.reuse_layers * u[0]
+    sel = wl.selections()[step - 1]  # [R][sel_sources][Q][k]
+    flat = np.sort(sel.reshape(sel.shape[0], sel.shape[1], -1), axis=-1)
+    # distinct rows of each (request, selection source)
+    u = 1 + np.count_nonzero(np.diff(flat, axis=-1), axis=-1)
+    if u.shape[1] != cfg.sources:  # one selection shared by every source
+        u = np.repeat(u, cfg.sources, axis=1)
+    reads = int(u.sum())
+    writes = int(u.sum() + cfg.reuse_layers * u[:, 0].sum()) if union else 0
     if not union:
         return reads * cfg.row_bytes + cfg.entries_per_step * GATHER_WRITE_BYTES_PER_ENTRY
     return (reads + writes) * cfg.row_bytes + cfg.entries_per_step * 4
 
 
+def l2_flushed(args, cfg, wl) -> bool:
+    """Whether timed steps start from a flushed L2: --l2, or (auto) when the
+    gather's algorithmic bytes per step, averaged over the cycle, are below
+    four times the L2 size -- otherwise every step's inputs are far larger
+    than L2 and steps are timed back to back.  Both arms take the same
+    decision, so their configurations match."""
+    if args.l2 != "auto":
+        return args.l2 == "flush"
+    probe = Cycle(cfg, None)
+    steps = [s for s in range(1, cfg.total_steps + 1) if probe.timed(s)]
+    mean = sum(gather_alg_bytes(cfg, wl, s, args.union) for s in steps) / len(steps)
+    return mean < 4 * L2_BYTES
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 3000 on c8/tiny, 320 otherwise)")
     ap.add_argument("--warmup", type=int, default=8)
-    ap.add_argument("--config", default="c8")
+    ap.add_argument("--config", default="c64")
+    ap.add_argument("--l2", default="auto", choices=["auto", "flush", "none"],
+                    help="L2 between timed steps: flushed, or consecutive steps; auto = "
+                         "flush when a step moves less than 4x the L2 size")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--copy-ctas", type=int, default=0)
     ap.add_argument("--gather-impl", type=int, default=1)
+    ap.add_argument("--early", type=int, default=1,
+                    help="DHS_OPT_EARLY: 1 = fused gathers copy rows before the grids end")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=5.0)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--kernel-steps", type=int, default=500)
     ap.add_argument("--trace-steps", type=int, default=100)
     ap.add_argument("--b2b-steps", type=int, default=200,
-                    help="consecutive fused steps timed without L2 flushes (breakdown)")
+                    help="steps timed with the other L2 method (step_hbm), 0 = none")
     ap.add_argument("--no-hugepages", action="store_true")
     ap.add_argument("--gemm", type=int, default=4096,
                     help="--experiment prefetch: per-layer compute, an n x n x n bf16 GEMM")
@@ -93,7 +131,7 @@ def parse():
     return ap.parse_args()
 
 
-def workload_desc(cfg, union=False):
+def workload_desc(cfg, union=False, flushed=True):
     return {
         "staging": ("union: each distinct row of a verify block staged once, plus "
                     "per-query index lists") if union else "per query [Q][k] rows",
@@ -107,7 +145,11 @@ def workload_desc(cfg, union=False):
         "residency": cfg.residency if cfg.residency is not None else
         f"admission-driven, pool {cfg.capacity_frac:.0%} of pages",
         "entries_per_step": cfg.entries_per_step,
-        "l2": "flushed before every timed step (256 MB write, then a read of another 256 MB)",
+        "l2": ("flushed before every timed step (256 MB write, then a read of another 256 MB)"
+               if flushed else
+               "not flushed: consecutive steps, each moving far more than the L2 size "
+               "(inputs larger than L2)"),
+        "cold_steps": "the first step after each pool reset runs untimed (hot caches empty)",
     }
 
 
@@ -131,10 +173,14 @@ def reduce_max(x: float, device) -> float:
 
 
 class Cycle:
-    """Next decode step of a workload, resetting after its last step."""
+    """Next decode step of a workload, resetting after its last step.  A
+    workload's own warm-up steps, and at least the first step after a reset
+    (every hot cache empty, which a serving pool meets only for newly
+    admitted requests), are not timed."""
 
-    def __init__(self, cfg, reset):
+    def __init__(self, cfg, reset, cold=1):
         self.cfg, self.reset, self.s = cfg, reset, 0
+        self.untimed = max(cfg.warmup_steps, min(cold, cfg.total_steps - 1))
 
     def next(self):
         if self.s == self.cfg.total_steps:
@@ -144,7 +190,7 @@ class Cycle:
         return self.s
 
     def timed(self, s):
-        return s > self.cfg.warmup_steps
+        return s > self.untimed
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -210,6 +256,7 @@ def run_reference(args, cfg):
         return
     from dhs_workload.configs import Workload
     wl = Workload(cfg)
+    flushed = l2_flushed(args, cfg, wl)
     ot = OracleTimer(cfg, wl, union=args.union)
     for _ in range(args.warmup):
         ot.step()
@@ -222,7 +269,7 @@ def run_reference(args, cfg):
         "n_gpus": args.gpus, "steps": K, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": workload_desc(cfg, args.union),
+        "config": workload_desc(cfg, args.union, flushed),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": ot.threads,
                          "kind": "oracle",
                          "sample": f"{K} decode steps of the workload, requests 0-{ot.sampled - 1} "
@@ -325,16 +372,17 @@ def h2d_peak_gbs(dev, nbytes=1 << 30, reps=5):
     return best
 
 
-def traced_pass(run, cycle, steps, dev, flush_l2):
-    """Kernel timeline of `steps` fused steps (DHS_OPT_TRACE, synchronised per
-    step -- not the headline): per-kernel durations, and the host-copy
-    kernel's bytes and time for the host-link roofline."""
+def traced_pass(run, cycle, steps, dev, flush_l2, trace):
+    """Kernel timeline of `steps` fused steps (DHS_OPT_TRACE into `trace`,
+    int64[8] allocated beforehand; synchronised per step -- not the
+    headline): per-kernel durations, and the host-copy kernel's bytes and
+    time for the host-link roofline (aggregate, and the median step's)."""
     import torch
     from hierarchical_sparse_kv_dhs_gb300 import dhs
     cfg = run.cfg
-    trace = torch.zeros(8, dtype=torch.int64, device=dev)
     run.pool.set_option(dhs.DHS_OPT_TRACE, trace.data_ptr())
     res, cp, ga, lt, span, host_b, copy_s = [], [], [], [], [], 0, 0.0
+    rates = []
     for _ in range(steps):
         s = cycle.next()
         while not cycle.timed(s):
@@ -359,44 +407,17 @@ def traced_pass(run, cycle, steps, dev, flush_l2):
             if hb:
                 host_b += hb
                 copy_s += (t[3] - t[2]) / 1e9
+                rates.append(hb / (t[3] - t[2]))
     run.pool.set_option(dhs.DHS_OPT_TRACE, 0)
     med = statistics.median
     return {"resolve_us": med(res), "gather_us": med(ga),
             "copy_us": med(cp) if cp else None,
+            "copy_us_max": max(cp) if cp else None,
             "fresh_list_us": med(lt) if lt else None,
             "step_span_us": med(span),
             "host_bytes_per_step": host_b / steps,
-            "copy_gbs": (host_b / copy_s / 1e9) if copy_s else None}
-
-
-def back_to_back(run, cycle, steps, dev, stream):
-    """Device time per step of consecutive fused steps with no L2 flush
-    between them (not the headline): CUDA events around each run of
-    consecutive steps of a cycle.  Each step's gather then also writes back
-    the previous step's staging lines still dirty in L2, which the flushed
-    timing moves into the flush, and each step's first kernel starts only
-    after the previous step's gather has drained."""
-    import torch
-    T = run.cfg.total_steps
-    total_ms, n = 0.0, 0
-    while n < steps:
-        s = cycle.next()
-        while not cycle.timed(s):
-            run.step(s)
-            s = cycle.next()
-        seg = [s]
-        while len(seg) < steps - n and seg[-1] < T:
-            seg.append(cycle.next())
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for s in seg:
-            run.step(s)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        total_ms += e0.elapsed_time(e1)
-        n += len(seg)
-    return total_ms * 1e3 / n
+            "copy_gbs": (host_b / copy_s / 1e9) if copy_s else None,
+            "copy_gbs_median_step": med(rates) if rates else None}
 
 
 def measure_e2e(run, cycle, steps, dev, stream):
@@ -447,6 +468,10 @@ def measure_e2e(run, cycle, steps, dev, stream):
             s = cycle.next()
         return s
 
+    # the allocations above changed the page tables: untimed steps re-warm
+    # the host copy's translations before anything is timed
+    for _ in range(3):
+        run.step(next_timed())
     # blocking calls
     torch.cuda.synchronize(dev)
     sync_dt = 0.0
@@ -635,6 +660,8 @@ def main():
         return
     from dhs_workload.configs import CONFIGS
     cfg = CONFIGS[args.config]
+    if args.steps is None:
+        args.steps = 3000 if cfg.name in ("c8", "tiny") else 320
     if args.impl == "reference":
         run_reference(args, cfg)
         return
@@ -656,24 +683,19 @@ def main():
     if args.copy_ctas:
         run.pool.set_option(dhs.DHS_OPT_COPY_CTAS, args.copy_ctas)
     run.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, args.gather_impl)
+    run.pool.set_option(dhs.DHS_OPT_EARLY, args.early)
     stream = torch.cuda.current_stream(dev)
+    # Every device buffer the bench uses is allocated here, before any step
+    # is timed: a new device allocation changes the GPU's page tables, and
+    # the host copy after it re-walks the translations of the pinned host
+    # region (a cold copy, like the first one after admission).
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    cycle = Cycle(cfg, run.reset)
-
-    def next_timed():
-        s = cycle.next()
-        while not cycle.timed(s):
-            run.step(s)
-            s = cycle.next()
-        return s
-
-    for _ in range(W):
-        run.step(next_timed())
-    rc, flags = run.status()
-    if rc != 0:
-        raise RuntimeError(f"device status {rc} flags {flags} during warm-up")
-
     clean64 = torch.zeros(32 << 20, dtype=torch.int64, device=dev)  # 256 MB
+    trace = torch.zeros(8, dtype=torch.int64, device=dev)
+    ctx_src = torch.empty(cfg.entries_per_step * cfg.row_bytes, dtype=torch.uint8, device=dev)
+    ctx_dst = torch.empty_like(ctx_src)
+    tiny = torch.zeros(1, dtype=torch.int32, device=dev)
+    h2d = h2d_peak_gbs(dev)
 
     def flush_l2():
         # write 256 MB (evicts the previous step's lines and writes back its
@@ -682,20 +704,80 @@ def main():
         flush.zero_()
         clean64.sum()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    # One calibration cycle from the admitted state (every cycle after a
+    # reset repeats it exactly): the host fetches of each step, for the
+    # step's algorithmic bytes.  It also warms the kernels up.
+    T = cfg.total_steps
+    host_rows_of = {}
+    for s in range(1, T + 1):
+        run.step(s)
+        torch.cuda.synchronize(dev)
+        host_rows_of[s] = int(run.counters[..., 5].sum().item())
+    rc, flags = run.status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} flags {flags} during calibration")
+    run.reset()
+    cycle = Cycle(cfg, run.reset)
+    timed_of = [s for s in range(1, T + 1) if cycle.timed(s)]
+    gather_alg = {s: gather_alg_bytes(cfg, wl, s, args.union) for s in timed_of}
+    # the whole step: the gather's bytes, every resolved entry's selection
+    # read, and each host fetch's write into its hot slot
+    step_alg = {s: gather_alg[s] + cfg.resolved_per_step * 4 + host_rows_of[s] * cfg.row_bytes
+                for s in timed_of}
+    flushed = l2_flushed(args, cfg, wl)
+
+    def next_timed():
+        s = cycle.next()
+        while not cycle.timed(s):
+            run.step(s)
+            s = cycle.next()
+        return s
+
+    def time_steps(n, with_flush):
+        """Device ms of each of n further timed steps and the steps run.
+        with_flush: L2 flushed before every step, events around each step;
+        else runs of consecutive steps (to the end of the cycle), an event
+        after each step."""
+        ms, steps = [], []
+        while len(steps) < n:
+            if with_flush:
+                s = next_timed()
+                flush_l2()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                run.step(s)  # dhs_decode_step: append + resolve + gather
+                e1.record(stream)
+                ms.append((e0, e1))
+                steps.append(s)
+                continue
+            seg = [next_timed()]
+            while len(seg) < n - len(steps) and seg[-1] < T:
+                seg.append(next_timed())
+            torch.cuda.synchronize(dev)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(seg) + 1)]
+            evs[0].record(stream)
+            for j, s in enumerate(seg):
+                run.step(s)
+                evs[j + 1].record(stream)
+            torch.cuda.synchronize(dev)
+            ms += list(zip(evs[:-1], evs[1:]))
+            steps += seg
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ms], steps
+
+    for _ in range(W):
+        run.step(next_timed())
+    rc, flags = run.status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} flags {flags} during warm-up")
+
     clocks = ClockSampler(local)
     clocks.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     t_wall0 = time.perf_counter()
-    for i in range(K):
-        s = next_timed()
-        flush_l2()
-        ev[i][0].record(stream)
-        run.step(s)  # dhs_decode_step: append + resolve + gather
-        ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+    step_ms, steps_run = time_steps(K, flushed)
     t_wall1 = time.perf_counter()
     if world > 1:
         torch.distributed.barrier()
@@ -703,10 +785,43 @@ def main():
     rc, flags = run.status()
     if rc != 0:
         raise RuntimeError(f"device status {rc} flags {flags} in the timed region")
-    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     total_s = reduce_max(sum(step_ms) / 1e3, dev)
     entries = cfg.entries_per_step
     value = world * entries * K / total_s
+
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "of measured" if peak else "of fallback"
+    peak = peak or 6800.0
+
+    def step_level(ms, steps):
+        """The whole step's algorithmic HBM bytes over its device time."""
+        gbs = sum(step_alg[s] for s in steps) / (sum(ms) / 1e3) / 1e9
+        srt = sorted(ms)
+        return {"us_per_step_mean": sum(ms) * 1e3 / len(ms),
+                "us_per_step_median": statistics.median(ms) * 1e3,
+                "us_per_step_p90": srt[min(len(srt) - 1, int(0.9 * len(srt)))] * 1e3,
+                "us_per_step_max": srt[-1] * 1e3,
+                "rows_per_s": entries * len(ms) / (sum(ms) / 1e3),
+                "alg_GBps": gbs, "hbm_frac": gbs / peak, "steps": len(ms)}
+
+    # The other L2 method, for comparison (breakdown)
+    other_ms, other_steps = (time_steps(min(K, args.b2b_steps), not flushed)
+                             if args.b2b_steps else (None, None))
+    step_hbm = {("flushed" if flushed else "back_to_back"): step_level(step_ms, steps_run)}
+    if other_ms:
+        step_hbm["back_to_back" if flushed else "flushed"] = step_level(other_ms, other_steps)
+    step_hbm["bytes"] = ("per step: the gather's algorithmic bytes (each distinct selected "
+                         "row read once, every entry's staging row written and location "
+                         "read), every resolved entry's 4-byte selection read, and 1152 B "
+                         "per host fetch written into its hot slot")
+    step_hbm["peak"] = f"{peak} GB/s hbm_gbs {peak_src}"
+    maybe_flush = flush_l2 if flushed else (lambda: None)
 
     # Kernel timing pass (not the headline): the same steps through
     # dhs_resolve then dhs_gather, events around each, so the gather kernel
@@ -717,7 +832,7 @@ def main():
     for i in range(K2):
         s = next_timed()
         k_steps.append(s)
-        flush_l2()
+        maybe_flush()
         ev2[i][0].record(stream)
         run.append(s)
         run.resolve(s)
@@ -727,14 +842,11 @@ def main():
     torch.cuda.synchronize(dev)
     gather_ms = [e[1].elapsed_time(e[2]) for e in ev2]
     resolve_ms = [e[0].elapsed_time(e[1]) for e in ev2]
-    b2b_us = back_to_back(run, cycle, args.b2b_steps, dev, stream) if args.b2b_steps else None
 
     # Context for the gather's roofline, timed the same way (flush, events):
     # a contiguous device copy of the staging bytes, and one trivial launch
     ctx_n = min(K2, 100)
-    src_b = torch.empty(cfg.entries_per_step * cfg.row_bytes, dtype=torch.uint8, device=dev)
-    dst_b = torch.empty_like(src_b)
-    tiny = torch.zeros(1, dtype=torch.int32, device=dev)
+    src_b, dst_b = ctx_src, ctx_dst
     ctx = {}
     for name, fn in (("contiguous_copy_us", lambda: dst_b.copy_(src_b)),
                      ("empty_launch_us", lambda: tiny.fill_(0))):
@@ -750,10 +862,10 @@ def main():
     ctx["what"] = (f"cudaMemcpyAsync device-to-device of {src_b.numel()} contiguous bytes "
                    "(the step's staging bytes) and a 1-element fill, medians of "
                    f"{ctx_n}, L2 flushed before each")
-    del src_b, dst_b
-
-    trace_info = traced_pass(run, cycle, min(K, args.trace_steps), dev, flush_l2)
-    h2d = h2d_peak_gbs(dev)
+    # two untimed steps re-warm whatever the copy context left cold
+    for _ in range(2):
+        run.step(next_timed())
+    trace_info = traced_pass(run, cycle, min(K, args.trace_steps), dev, maybe_flush, trace)
     link = None
     if trace_info["copy_gbs"]:
         link = {"bound": "host link (NVLink-C2C)", "kernel": "hostcopy",
@@ -761,7 +873,12 @@ def main():
                 "frac": trace_info["copy_gbs"] / h2d,
                 "peak_source": "measured in this run: pinned H2D cudaMemcpyAsync, 1 GiB",
                 "bytes_per_step": trace_info["host_bytes_per_step"],
-                "copy_us": trace_info["copy_us"]}
+                "copy_us": trace_info["copy_us"],
+                "achieved_median_step": trace_info["copy_gbs_median_step"],
+                "timed": (f"{min(K, args.trace_steps)} traced fused steps "
+                          f"({'L2 flushed before each' if flushed else 'no flush'}): "
+                          "host bytes fetched / span of the copy kernel's copying "
+                          "(%globaltimer)")}
 
     cnt = run.counters.cpu().numpy().reshape(-1, 8).astype("int64")
     tiers = {"unique": int(cnt[:, 1].sum()), "tail": int(cnt[:, 2].sum()),
@@ -797,18 +914,8 @@ def main():
         cpu["single_thread_value"] = n1 * ot1.rows_per_step / dt1
         cpu["single_thread_sample"] = f"{n1} decode steps, {dt1:.1f} s timed, 1 thread"
 
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except OSError:
-        pass
-    peak = peaks.get("hbm_gbs")
-    peak_src = "of measured" if peak else "of fallback"
-    peak = peak or 6800.0
     gather_avg = sum(gather_ms) / K2 / 1e3
-    alg_of = {s: gather_alg_bytes(cfg, wl, s, args.union) for s in set(k_steps)}
-    alg_bytes = sum(alg_of[s] for s in k_steps) / K2  # per launch, averaged
+    alg_bytes = sum(gather_alg[s] for s in k_steps) / K2  # per launch, averaged
     achieved = alg_bytes / gather_avg / 1e9
     gather_src = "gather.cu"
     traffic = traffic_from_profile(
@@ -822,13 +929,13 @@ def main():
     # append folded into resolve; resolve + host copy per chunk, the gathers,
     # and the fresh-row list copy when it is on
     launches = K * (2 * n_resolve + n_gather + fresh)
-    step_bytes = alg_bytes + cfg.resolved_per_step * 4
     impl = ["vector", "tma"][args.gather_impl]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": sum(step_ms) / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u8", "data": "synthetic", "config": workload_desc(cfg, args.union),
+        "dtype": "u8", "data": "synthetic",
+        "config": workload_desc(cfg, args.union, flushed),
         "roofline": {"bound": "hbm", "kernel": f"gather_{impl}", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"hbm_gbs {peak_src} (copy, read+write bytes)",
@@ -838,9 +945,11 @@ def main():
                                      "launch ends are written back after it, by the next "
                                      "step's traffic or the flush",
                      "timed": f"{K2} launches, CUDA events around dhs_gather "
-                              "(L2 flushed before each step)",
+                              + ("(L2 flushed before each step)" if flushed else
+                                 "(consecutive steps, no flush)"),
                      "context": ctx},
         "host_link": link,
+        "step_hbm": step_hbm,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -850,13 +959,10 @@ def main():
                     f"and gather PDL-overlapped{', fresh-row list copy' if fresh else ''}), "
                     f"gather {impl}",
             "step_ms_median": statistics.median(step_ms),
-            "step_GBps_alg": step_bytes / (sum(step_ms) / K / 1e3) / 1e9,
             "traced_kernel_us": trace_info,
             "h2d_peak_gbs": h2d,
             "split_append_resolve_hostcopy_ms": sum(resolve_ms) / K2,
             "split_gather_ms": sum(gather_ms) / K2,
-            "back_to_back_us_per_step": b2b_us,
-            "back_to_back_rows_per_s": entries / (b2b_us * 1e-6) if b2b_us else None,
             "wall_s_timed_region": t_wall1 - t_wall0,
             "last_step_unique_rows": tiers,
             "last_step_host_bytes": host_rows * cfg.row_bytes,

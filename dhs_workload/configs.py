@@ -131,7 +131,14 @@ LONG = Config("long", 5, requests=32, sources=3, history=512000, tail=256,
 MISS = Config("miss", 6, requests=16, sources=2, history=32768, tail=256, hot=4096,
               topk=2048, steps=16, residency=0.0)
 
-CONFIGS = {c.name: c for c in (TINY, C8, C64, C128, LONG, MISS)}
+# the same miss-heavy shape over a pinned region past the host link's
+# translation reach: 32 requests x 2 sources x 768K-row histories (58 GB of
+# pinned rows) with about 0.25 GB on the device; the host copy reads rows
+# scattered over the whole region every step
+WIDE = Config("wide", 7, requests=32, sources=2, history=786432, tail=256, hot=4096,
+              topk=2048, steps=16, residency=0.0)
+
+CONFIGS = {c.name: c for c in (TINY, C8, C64, C128, LONG, MISS, WIDE)}
 
 
 class Workload:
