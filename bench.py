@@ -112,6 +112,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--copy-ctas", type=int, default=0)
     ap.add_argument("--gather-impl", type=int, default=1)
+    ap.add_argument("--stage-misses", type=int, default=1,
+                    help="DHS_OPT_STAGE_MISSES: 1 = the host copy writes fetched rows into staging")
     ap.add_argument("--early", type=int, default=1,
                     help="DHS_OPT_EARLY: 1 = fused gathers copy rows before the grids end")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -372,11 +374,13 @@ def h2d_peak_gbs(dev, nbytes=1 << 30, reps=5):
     return best
 
 
-def traced_pass(run, cycle, steps, dev, flush_l2, trace):
+def traced_pass(run, cycle, steps, dev, flush_l2, trace, alone=False):
     """Kernel timeline of `steps` fused steps (DHS_OPT_TRACE into `trace`,
     int64[8] allocated beforehand; synchronised per step -- not the
     headline): per-kernel durations, and the host-copy kernel's bytes and
-    time for the host-link roofline (aggregate, and the median step's)."""
+    time for the host-link roofline (aggregate, and the median step's).
+    alone: each step's append + resolve + host copy only, no gather (the
+    copy without the gather's traffic beside it)."""
     import torch
     from hierarchical_sparse_kv_dhs_gb300 import dhs
     cfg = run.cfg
@@ -391,12 +395,17 @@ def traced_pass(run, cycle, steps, dev, flush_l2, trace):
         flush_l2()
         trace[0::2] = (1 << 63) - 1
         trace[1::2] = 0
-        run.step(s)
+        if alone:
+            run.append(s)
+            run.resolve(s)
+        else:
+            run.step(s)
         torch.cuda.synchronize(dev)
         t = trace.cpu().tolist()
         hb = int(run.counters[..., 5].sum().item()) * cfg.row_bytes
         res.append((t[1] - t[0]) / 1e3)
-        ga.append((t[5] - t[4]) / 1e3)
+        if t[5] > t[4] > 0:
+            ga.append((t[5] - t[4]) / 1e3)
         end = max(t[1], t[3], t[5])
         if t[7] > t[6] > 0:  # fresh-row list copy
             lt.append((t[7] - t[6]) / 1e3)
@@ -410,7 +419,7 @@ def traced_pass(run, cycle, steps, dev, flush_l2, trace):
                 rates.append(hb / (t[3] - t[2]))
     run.pool.set_option(dhs.DHS_OPT_TRACE, 0)
     med = statistics.median
-    return {"resolve_us": med(res), "gather_us": med(ga),
+    return {"resolve_us": med(res), "gather_us": med(ga) if ga else None,
             "copy_us": med(cp) if cp else None,
             "copy_us_max": max(cp) if cp else None,
             "fresh_list_us": med(lt) if lt else None,
@@ -684,6 +693,7 @@ def main():
         run.pool.set_option(dhs.DHS_OPT_COPY_CTAS, args.copy_ctas)
     run.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, args.gather_impl)
     run.pool.set_option(dhs.DHS_OPT_EARLY, args.early)
+    run.pool.set_option(dhs.DHS_OPT_STAGE_MISSES, args.stage_misses)
     stream = torch.cuda.current_stream(dev)
     # Every device buffer the bench uses is allocated here, before any step
     # is timed: a new device allocation changes the GPU's page tables, and
@@ -866,6 +876,8 @@ def main():
     for _ in range(2):
         run.step(next_timed())
     trace_info = traced_pass(run, cycle, min(K, args.trace_steps), dev, maybe_flush, trace)
+    alone_info = traced_pass(run, cycle, min(K, args.trace_steps), dev, maybe_flush, trace,
+                             alone=True)
     link = None
     if trace_info["copy_gbs"]:
         link = {"bound": "host link (NVLink-C2C)", "kernel": "hostcopy",
@@ -875,6 +887,11 @@ def main():
                 "bytes_per_step": trace_info["host_bytes_per_step"],
                 "copy_us": trace_info["copy_us"],
                 "achieved_median_step": trace_info["copy_gbs_median_step"],
+                "alone": {"achieved": alone_info["copy_gbs"],
+                          "frac": (alone_info["copy_gbs"] or 0.0) / h2d,
+                          "copy_us": alone_info["copy_us"],
+                          "what": "the same steps' append + resolve + host copy without the "
+                                  "gather running beside the copy"},
                 "timed": (f"{min(K, args.trace_steps)} traced fused steps "
                           f"({'L2 flushed before each' if flushed else 'no flush'}): "
                           "host bytes fetched / span of the copy kernel's copying "
