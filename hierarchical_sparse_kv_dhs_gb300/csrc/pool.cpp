@@ -189,6 +189,7 @@ struct dhs_pool {
   int64_t ent_cap = 0;
   int stage_misses = 1;         // DHS_OPT_STAGE_MISSES
   uint32_t mark_polls = dhs::kMarkPolls;  // DHS_OPT_MARK_POLLS
+  int copy_pdl = -1;            // DHS_OPT_COPY_PDL: -1 auto, 0 off, 1 on
   std::vector<uint8_t> staged_pair;  // the host copy stages this pair's misses this step
   std::vector<uint8_t> staged_item;  // per item of the step: a gather-only item whose
                                      // staging the host copy writes too
@@ -242,14 +243,48 @@ namespace {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? DHS_OK : DHS_ECUDA; }
 
-// Host-copy grid: the upper end of the pages' 4-to-32-block scaling.  On
+// Host-copy launch policy.
+//
+// Grid: at least the upper end of the pages' 4-to-32-block scaling.  On
 // GB300 the host link needs about 1024 rows in flight (16 blocks x 16 warps x
 // 4 rows); below that the copy is latency-bound (miss-heavy workload: 4
 // blocks 78 GB/s, 8 130, 16 188, 32 198 of the 211 GB/s pinned peak), and in
 // same-box runs 32 blocks were as fast as or faster than 16 on every
-// workload with misses (warm steps: C64 1969 vs 2066 us, C128 640 vs 627,
-// miss-heavy 147 vs 152), so the grid does not shrink with the batch.
-int default_copy_ctas(int64_t /*requests*/) { return 32; }
+// workload with misses, so the grid never shrinks below 32.
+//
+// Address translation of the pinned rows: a block copies the items b, b + G,
+// ... of a launch, so its host footprint is the sum of those items' pinned
+// regions.  Measured with the copy alone on GB300: while a block's footprint
+// stays within about 1 GiB and each block lands on the same SM step after
+// step, the copy runs at the link's rate even over a 58 GB pinned region
+// (wide workload, 64 items of 0.9 GB: 64 blocks 199 GB/s); at 1.8 GiB per
+// block it falls to 40-52 GB/s (32 blocks).  So the grid grows until every
+// block's share of the items fits 1 GiB, up to one block per item and one per
+// SM.
+int copy_ctas(const dhs_pool* p, int64_t n_items) {
+  if (p->copy_ctas > 0) return p->copy_ctas;
+  const int64_t item_span = p->cfg.max_rows_per_request * (int64_t)p->cfg.row_bytes;
+  const int64_t per_block = std::max<int64_t>(1, (int64_t(1) << 30) / std::max<int64_t>(1, item_span));
+  const int64_t want = (n_items + per_block - 1) / per_block;
+  const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(n_items, std::max(1, p->sm_count)));
+  return (int)std::max<int64_t>(32, std::min(want, cap));
+}
+
+// Programmatic dependent launch of the host copy (its blocks start while the
+// resolve grid still runs and copy each item once its miss list is out) pays
+// while the launch's pinned regions are small enough for the GPU's
+// translation caches to hold them whatever SMs the blocks land on (C64: 9.7
+// GB, 205 GB/s).  Past that, blocks placed on whichever SMs the resolve grid
+// frees land on different SMs from step to step and re-walk their
+// translations: the copy then launches after the resolve grid, onto an idle
+// GPU, so block b lands on the same SM every step (copy alone, pinned span
+// 57 GB with 96 blocks: 44-53 GB/s with the early start, 149 without it; 30
+// GB with 32 blocks: 58-84 against 182).
+bool copy_pdl(const dhs_pool* p, int64_t n_items) {
+  if (p->copy_pdl >= 0) return p->copy_pdl == 1;
+  const int64_t item_span = p->cfg.max_rows_per_request * (int64_t)p->cfg.row_bytes;
+  return n_items * item_span <= (int64_t(16) << 30);
+}
 
 // Pages small enough for the page-move kernel's 32-bit chunk arithmetic.
 bool small_pages(const dhs_pool* p) {
@@ -614,6 +649,11 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     pool->gather_tpc = (int)value;
     return DHS_OK;
   }
+  if (key == DHS_OPT_COPY_PDL) {
+    if (value < -1 || value > 1) return DHS_EINVAL;
+    pool->copy_pdl = (int)value;
+    return DHS_OK;
+  }
   if (key == DHS_OPT_MARK_POLLS) {
     if (value < -1 || value > (int64_t)dhs::kMarkPolls) return DHS_EINVAL;
     pool->mark_polls = value < 0 ? dhs::kMarkPolls : (uint32_t)value;
@@ -645,6 +685,7 @@ int dhs_get_option(dhs_pool* pool, int32_t key, int64_t* value) {
     case DHS_OPT_GATHER_TPC: *value = pool->gather_tpc; return DHS_OK;
     case DHS_OPT_STAGE_MISSES: *value = pool->stage_misses; return DHS_OK;
     case DHS_OPT_MARK_POLLS: *value = pool->mark_polls; return DHS_OK;
+    case DHS_OPT_COPY_PDL: *value = pool->copy_pdl; return DHS_OK;
     default: return DHS_EINVAL;
   }
 }
@@ -1138,16 +1179,13 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   const size_t nr = p->ritems.size();
   for (size_t b = 0; b < nr; b += dhs::kResolveItemsLarge) {
     const int n = (int)std::min<size_t>(dhs::kResolveItemsLarge, nr - b);
-    int64_t wmax = 0, qmax = 0, requests = 0, last_req = -1;
+    int64_t wmax = 0, qmax = 0;
     bool uni = false;
     for (int i = 0; i < n; ++i) {
       const dhs::ResolveItem& r = p->ritems[b + i];
       uni |= r.index != nullptr;
       wmax = std::max<int64_t>(wmax, (r.L + 63) / 64);
       qmax = std::max<int64_t>(qmax, std::min<int64_t>(r.n, r.L));
-      const int64_t req = r.pair / c.sources;
-      if (req != last_req) ++requests;
-      last_req = req;
     }
     rcm.w64cap = (int32_t)wmax;
     rcm.qkcap = (int32_t)qmax;
@@ -1160,10 +1198,8 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni);
     if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, smem, p->stream) != cudaSuccess)
       return DHS_ECUDA;
-    int ctas = p->copy_ctas;
-    if (ctas <= 0) ctas = default_copy_ctas(requests);
-    if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, ctas, true, p->stream) !=
-        cudaSuccess)
+    if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, copy_ctas(p, n), copy_pdl(p, n),
+                             p->stream) != cudaSuccess)
       return DHS_ECUDA;
   }
   return DHS_OK;

@@ -514,11 +514,14 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
                    uint32_t *stamps, int32_t *page_slot, int64_t *info);
 
 /* Tunables (performance only; results do not depend on them). */
-/* Host-copy CTAs; 0 = 32.  The pages scale the copy kernel from 4 to 32
- * thread blocks with batch size; on GB300 fewer than about 16 blocks leave
- * the host link idle (miss-heavy workload: 4 blocks 78 GB/s, 16 188, 32 198
- * of a 211 GB/s pinned copy), so the default is the upper end at every
- * batch size. */
+/* Host-copy CTAs; 0 = automatic.  The pages scale the copy kernel from 4 to
+ * 32 thread blocks with batch size; on GB300 fewer than about 16 blocks
+ * leave the host link idle (miss-heavy workload: 4 blocks 78 GB/s, 16 188,
+ * 32 198 of a 211 GB/s pinned copy), so the automatic grid is never below
+ * 32.  It grows past 32 until each block's items span at most 1 GiB of
+ * pinned rows (max_rows_per_request * row_bytes per item), up to one block
+ * per item and per SM: a block whose rows lie in a larger region re-walks
+ * address translations and copies at a fraction of the link's rate. */
 #define DHS_OPT_COPY_CTAS 1
 #define DHS_OPT_GATHER_IMPL 2 /* 1 = TMA bulk copy, 16-row tiles of two
                                      warps (default); 0 = 16-byte vector copy,
@@ -557,6 +560,12 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
  * polls; 0 .. 2^20.  0 sends every such tile and block down that path at
  * once (for tests of it). */
 #define DHS_OPT_MARK_POLLS 8
+/* The host copy starts while the resolve kernel runs (programmatic dependent
+ * launch: 1) or after it (0).  -1 (default) = 1 while a launch's items span
+ * at most 16 GiB of pinned rows, else 0: past that the copy's blocks must land
+ * on the same SMs step after step, which only a launch onto an idle GPU
+ * gives, for the GPU to keep their address translations. */
+#define DHS_OPT_COPY_PDL 9
 int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
 /* The value in effect (DHS_OPT_FRESH_LIST: 0 or 1, the auto rule resolved
  * for the pool's current admissions).  DHS_EINVAL for an unknown key. */

@@ -37,7 +37,7 @@ def _as_u32(t):
 
 def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
                 gather_impl=0, patch=None, early=1, union=False, fresh=None, tpc=None,
-                stage=None, polls=None):
+                stage=None, polls=None, copy_pdl=None, copy_ctas=None):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
@@ -58,6 +58,10 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
         gpu.pool.set_option(dhs.DHS_OPT_STAGE_MISSES, stage)
     if polls is not None:
         gpu.pool.set_option(dhs.DHS_OPT_MARK_POLLS, polls)
+    if copy_pdl is not None:
+        gpu.pool.set_option(dhs.DHS_OPT_COPY_PDL, copy_pdl)
+    if copy_ctas is not None:
+        gpu.pool.set_option(dhs.DHS_OPT_COPY_CTAS, copy_ctas)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
     orc = OracleRun(cfg, wl, requests=sampled, union=union)
     try:
@@ -300,6 +304,21 @@ def test_mark_poll_fallbacks(cfg):
         assert run.pool.get_option(key) == 1 << 20
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("cfg", SMALL + [UNION[3], REUSE5],
+                         ids=[c.name for c in SMALL] + ["v8", "reuse5"])
+def test_host_copy_launched_after_the_resolve_grid(cfg):
+    """The host copy launched after the resolve grid instead of overlapping it
+    (DHS_OPT_COPY_PDL 0, what pools with large pinned regions do), with one
+    block per item and with more blocks than items: bit-exact, fused and
+    split, both staging layouts."""
+    items = cfg.requests * cfg.sources
+    for ctas in (0, max(1, items), 3 * items + 5):
+        compare_run(cfg, gather_impl=1, copy_pdl=0, copy_ctas=ctas or None)
+    compare_run(cfg, gather_impl=1, copy_pdl=0, fused=False)
+    compare_run(cfg, gather_impl=1, copy_pdl=0, union=True)
+    compare_run(cfg, gather_impl=0, copy_pdl=0)
 
 
 @pytest.mark.parametrize("tpc", [2, 5])
