@@ -123,10 +123,13 @@ struct ResolveCommon {
   int32_t* miss_off;     // [pairs][Mcap + 1] per miss: first entry in miss_ent
   int32_t* miss_ent;     // [pairs][ent_cap] staging entries of the misses
   int32_t ent_cap;
-  int32_t pad3;
+  int32_t selcap;        // selection entries staged in shared memory (0 = none)
 };
 
-size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni);
+// Shared-memory plan of one resolve CTA: bitmaps of w64cap words, qkcap
+// candidate rows (at most B: more fail the budget before they are listed), B
+// slots, and selcap staged selection entries.
+size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni, int selcap);
 cudaError_t resolve_set_smem_limit(size_t bytes);
 cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,
                            int n_items, size_t smem, cudaStream_t stream);

@@ -103,9 +103,10 @@ int log2i(int64_t x) {
 // Shared-memory plan of the resolve kernel at the pool's largest sizes.
 size_t max_resolve_smem(const dhs_pool_config& c, bool uni) {
   const int64_t w64 = (c.max_rows_per_request + 63) / 64;
-  const int64_t qk = std::min<int64_t>((int64_t)c.max_queries * c.max_topk,
-                                       c.max_rows_per_request);
-  return dhs::resolve_smem_bytes((int)w64, (int)qk, c.hot_rows, uni);
+  const int64_t qk = std::min<int64_t>(
+      std::min<int64_t>((int64_t)c.max_queries * c.max_topk, c.max_rows_per_request),
+      c.hot_rows);
+  return dhs::resolve_smem_bytes((int)w64, (int)qk, c.hot_rows, uni, 0);
 }
 
 int validate_geometry(const dhs_pool_config* c) {
@@ -184,6 +185,7 @@ struct dhs_pool {
   std::set<std::pair<uint64_t, int64_t>> backup_order;  // (order, pair * pmax + page)
   int32_t rr = 0;               // refill cursor: the next request visited
   int sm_count = 0;
+  int smem_optin = 0;           // opt-in shared memory per block
   int32_t* miss_off = nullptr;  // [pairs][Mcap + 1] staging entries of each miss
   int32_t* miss_ent = nullptr;  // [pairs][ent_cap]
   int64_t ent_cap = 0;
@@ -536,6 +538,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->union_ok = union_ok;
     p->gather_impl = dhs::kGatherTma;
     p->sm_count = sms;
+    p->smem_optin = optin;
     p->stream = (cudaStream_t)cfg->stream;
     p->device = dev;
     p->pairs = (int64_t)cfg->max_requests * cfg->sources;
@@ -1179,13 +1182,14 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   const size_t nr = p->ritems.size();
   for (size_t b = 0; b < nr; b += dhs::kResolveItemsLarge) {
     const int n = (int)std::min<size_t>(dhs::kResolveItemsLarge, nr - b);
-    int64_t wmax = 0, qmax = 0;
+    int64_t wmax = 0, qmax = 0, nmax = 0;
     bool uni = false;
     for (int i = 0; i < n; ++i) {
       const dhs::ResolveItem& r = p->ritems[b + i];
       uni |= r.index != nullptr;
       wmax = std::max<int64_t>(wmax, (r.L + 63) / 64);
-      qmax = std::max<int64_t>(qmax, std::min<int64_t>(r.n, r.L));
+      qmax = std::max<int64_t>(qmax, std::min<int64_t>(std::min<int64_t>(r.n, r.L), c.hot_rows));
+      nmax = std::max<int64_t>(nmax, r.n);
     }
     rcm.w64cap = (int32_t)wmax;
     rcm.qkcap = (int32_t)qmax;
@@ -1195,7 +1199,17 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     ccm.seq = rcm.seq;
     for (int i = 0; i < n; ++i) p->seq_of_pair[p->ritems[b + i].pair] = rcm.seq;
     rcm.uni = uni ? 1 : 0;
-    const size_t smem = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni);
+    // stage the selections in shared memory when the plan leaves room for them
+    const size_t base = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni, 0);
+    const size_t staged =
+        dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni, (int)nmax);
+    rcm.selcap = 0;
+    if (nmax >= 8 * dhs::resolve_threads(n <= dhs::kResolveItemsSmall ? dhs::kResolveItemsSmall
+                                                                       : dhs::kResolveItemsLarge) &&
+        staged + 1024 <= (size_t)p->smem_optin &&
+        dhs::resolve_set_smem_limit(staged) == cudaSuccess)
+      rcm.selcap = (int32_t)nmax;
+    const size_t smem = rcm.selcap ? staged : base;
     if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, smem, p->stream) != cudaSuccess)
       return DHS_ECUDA;
     if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, copy_ctas(p, n), copy_pdl(p, n),

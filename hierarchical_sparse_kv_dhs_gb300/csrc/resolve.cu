@@ -45,12 +45,13 @@ struct Smem {
   uint16_t* sort_b;   // [B]
   uint64_t* ubm;      // [w64cap] union bitmap (union staging launches only)
   uint32_t* upre;     // [w64cap] exclusive prefix of its popcounts
+  int32_t* sel;       // [selcap] the item's selection, staged (null: read from global)
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-__host__ __device__ inline size_t carve(int w64cap, int qkcap, int B, bool uni, Smem* s,
-                                        unsigned char* base) {
+__host__ __device__ inline size_t carve(int w64cap, int qkcap, int B, bool uni, int selcap,
+                                        Smem* s, unsigned char* base) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -66,6 +67,7 @@ __host__ __device__ inline size_t carve(int w64cap, int qkcap, int B, bool uni, 
   unsigned char* p6 = take(sizeof(uint16_t) * (size_t)B);
   unsigned char* p7 = uni ? take(sizeof(uint64_t) * (size_t)w64cap) : nullptr;
   unsigned char* p8 = uni ? take(sizeof(uint32_t) * (size_t)w64cap) : nullptr;
+  unsigned char* p9 = selcap > 0 ? take(sizeof(int32_t) * (size_t)selcap) : nullptr;
   if (s) {
     s->bm = (uint64_t*)p0;
     s->wpre = (uint32_t*)p1;
@@ -76,6 +78,7 @@ __host__ __device__ inline size_t carve(int w64cap, int qkcap, int B, bool uni, 
     s->sort_b = (uint16_t*)p6;
     s->ubm = (uint64_t*)p7;
     s->upre = (uint32_t*)p8;
+    s->sel = (int32_t*)p9;
   }
   return off;
 }
@@ -108,6 +111,37 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch, uint32_t* tot
   }
   __syncthreads();
   uint32_t r = scratch[warp] + inc - v;
+  *total = scratch[32];
+  __syncthreads();
+  return r;
+}
+
+// Exclusive prefix of a 64-bit v over the block (four 16-bit counters
+// packed in one word scan at once); *total = block sum.  scratch: 33 words.
+__device__ uint64_t block_excl_scan64(uint64_t v, uint64_t* scratch, uint64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  uint64_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const uint64_t w = lane < nw ? scratch[lane] : 0ull;
+    uint64_t wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    if (lane < nw) scratch[lane] = wi - w;
+    if (lane == 31) scratch[32] = wi;
+  }
+  __syncthreads();
+  const uint64_t r = scratch[warp] + inc - v;
   *total = scratch[32];
   __syncthreads();
   return r;
@@ -295,6 +329,7 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
     resolve_kernel(const __grid_constant__ ResolveParams<MAXI> P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint32_t scratch[4 * 33];
+  __shared__ uint64_t scratch64[33];
   __shared__ int s_bad;
 
   // Dependent launches (the host copy, then the gather) may start now: they
@@ -326,7 +361,42 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
   if (c.later_count && blockIdx.x == 0 && tid == 0) c.later_count[(c.gen & 1u) ^ 1u] = 0u;
 
   Smem s;
-  carve(c.w64cap, c.qkcap, B, c.uni != 0, &s, smem_raw);
+  carve(c.w64cap, c.qkcap, B, c.uni != 0, c.selcap, &s, smem_raw);
+  // The selection is read by several passes.  A large one (at least eight
+  // entries per thread: verify blocks) is staged in shared memory once, with
+  // coalesced loads, eight in flight per thread, when the launch's plan has
+  // room; a small one is read from global memory by each pass (staging it
+  // costs one more round of load latency than it saves).
+  const bool staged = s.sel != nullptr && it.n <= c.selcap && it.n >= 8 * nt;
+  if (staged) {
+    for (int e0 = tid; e0 < it.n; e0 += 8 * nt) {
+      int32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = e0 + u * nt < it.n ? it.sel[e0 + u * nt] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (e0 + u * nt < it.n) s.sel[e0 + u * nt] = v[u];
+    }
+    __syncthreads();
+  }
+  const int32_t* sel = staged ? s.sel : it.sel;
+  // f(entry, row) over every entry of the selection, each thread issuing the
+  // loads of four entries before using them
+  auto for_entries = [&](auto&& f) {
+    for (int e0 = tid; e0 < it.n; e0 += 4 * nt) {
+      int32_t r4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * nt;
+        r4[u] = e < it.n ? sel[e] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * nt;
+        if (e < it.n) f(e, r4[u]);
+      }
+    }
+  };
   const bool uni = it.index != nullptr;  // union staging (launch has c.uni)
 
   // ---- decode rows appended by this launch (dhs_decode_step): row L0+j to
@@ -349,26 +419,37 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
   for (int w = tid; w < W; w += nt) s.bm[w] = 0ull;
   if (tid == 0) s_bad = 0;
   __syncthreads();
-  // Each thread ORs the bits of four consecutive entries into a register and
-  // updates shared memory once per 64-row word they touch.  Selections
-  // cluster (a recency window, sorted top-k lists), so this is usually one
-  // atomic per four entries instead of one per entry, many on the same word.
-  for (int b = tid * 4; b < n; b += nt * 4) {
+  // Each thread takes a run of consecutive entries (at least four: one run
+  // per thread when the selection is large), ORs the bits that fall in one
+  // 64-row word into a register and updates shared memory once per word it
+  // touches.  Selections cluster (a recency window, sorted top-k lists; a
+  // verify block repeats the same window in every query), so this is about
+  // one atomic per run instead of one per entry, many on the same word.
+  const int run = max(4, (((n + nt - 1) / nt) + 3) & ~3);
+  for (int b = tid * run; b < n; b += nt * run) {
     uint64_t acc = 0ull;
     int cur = -1;
-    for (int j = 0; j < 4 && b + j < n; ++j) {
-      const int32_t row = it.sel[b + j];
-      if ((int64_t)row < it.lo || (int64_t)row >= L) {
-        s_bad = 1;
-        continue;
+    const int end = min(n, b + run);
+    for (int j0 = b; j0 < end; j0 += 4) {
+      int32_t r4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) r4[u] = j0 + u < end ? sel[j0 + u] : 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (j0 + u >= end) break;
+        const int32_t row = r4[u];
+        if ((int64_t)row < it.lo || (int64_t)row >= L) {
+          s_bad = 1;
+          continue;
+        }
+        const int w = row >> 6;
+        if (w != cur) {
+          if (cur >= 0) atomicOr((unsigned long long*)&s.bm[cur], (unsigned long long)acc);
+          cur = w;
+          acc = 0ull;
+        }
+        acc |= 1ull << (row & 63);
       }
-      const int w = row >> 6;
-      if (w != cur) {
-        if (cur >= 0) atomicOr((unsigned long long*)&s.bm[cur], (unsigned long long)acc);
-        cur = w;
-        acc = 0ull;
-      }
-      acc |= 1ull << (row & 63);
     }
     if (cur >= 0) atomicOr((unsigned long long*)&s.bm[cur], (unsigned long long)acc);
   }
@@ -405,6 +486,14 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
   const uint32_t C = cnt[3];  // rows left for the hot cache (block-uniform)
   if (uni) block_scan_array(s.upre, W, scratch);  // union ranks
 
+  // More rows left for the hot cache than it has slots: whatever the scan
+  // finds, the misses (C - hits) outnumber the unprotected slots (at most
+  // B - hits), so the item fails the budget now -- and the candidate arrays,
+  // sized for B rows, are never filled past their end.
+  if (C > (uint32_t)B) {
+    fail_item(c, it, kErrBudget, kStatusEbudget);
+    return;
+  }
   uint32_t hits = 0u, m_miss = 0u, scan_max = 0u, evicted = 0u;
   if (C) {
     block_scan_array(s.wpre, W, scratch);  // candidate ranks
@@ -485,16 +574,26 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
       const int U = (int)unprot;
       const int per = (U + nt - 1) / nt;
       const int b = tid * per, e = min(U, b + per);
-      for (int bit = 0; bit < nbits; ++bit) {  // stable LSD split per bit
-        uint32_t z = 0;
-        for (int i = b; i < e; ++i) z += !(((s.st[src[i]] - kmin) >> bit) & 1u);
-        uint32_t ztot;
-        uint32_t zpos = block_excl_scan(z, scratch, &ztot);
-        uint32_t opos = ztot + (uint32_t)b - zpos;
+      // stable LSD radix sort, two bits per pass: each thread counts the four
+      // digits of its contiguous range in 16-bit fields of one word (U <=
+      // 16384 fits), one block scan gives every thread its place in each
+      // digit's bucket, and each range is written out in order
+      for (int sh = 0; sh < nbits; sh += 2) {
+        uint64_t cnt = 0ull;
+        for (int i = b; i < e; ++i)
+          cnt += 1ull << (16u * (((s.st[src[i]] - kmin) >> sh) & 3u));
+        uint64_t tot;
+        const uint64_t pre = block_excl_scan64(cnt, scratch64, &tot);
+        // bucket d starts after every smaller digit's total; this thread's
+        // place in it is its prefix field (positions packed like the counts)
+        const uint64_t t0 = tot & 0xFFFFull, t1 = (tot >> 16) & 0xFFFFull,
+                       t2 = (tot >> 32) & 0xFFFFull;
+        uint64_t pos = pre + ((t0 << 16) | ((t0 + t1) << 32) | ((t0 + t1 + t2) << 48));
         for (int i = b; i < e; ++i) {
           const uint16_t v = src[i];
-          if (((s.st[v] - kmin) >> bit) & 1u) dst[opos++] = v;
-          else dst[zpos++] = v;
+          const uint32_t sh16 = 16u * (((s.st[v] - kmin) >> sh) & 3u);
+          dst[(uint32_t)(pos >> sh16) & 0xFFFFu] = v;
+          pos += 1ull << sh16;
         }
         __syncthreads();
         uint16_t* t = src;
@@ -553,10 +652,10 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
     for (uint32_t j = tid; j < m_miss; j += nt) s.st[j] = 0u;
     __syncthreads();
     if (!uni) {
-      for (int e = tid; e < n; e += nt) {
-        const int32_t mi = miss_of(it.sel[e]);
+      for_entries([&](int, int32_t row) {
+        const int32_t mi = miss_of(row);
         if (mi >= 0) atomicAdd(&s.st[mi], 1u);
-      }
+      });
     } else {  // one staging row per distinct row
       for (int w = tid; w < W; w += nt)
         for (uint64_t m = s.ubm[w]; m; m &= m - 1) {
@@ -570,10 +669,10 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
     if (tid == 0) off[m_miss] = (int32_t)total;
     __syncthreads();
     if (!uni) {
-      for (int e = tid; e < n; e += nt) {
-        const int32_t mi = miss_of(it.sel[e]);
+      for_entries([&](int e, int32_t row) {
+        const int32_t mi = miss_of(row);
         if (mi >= 0) ent[atomicAdd(&s.st[mi], 1u)] = e;
-      }
+      });
     } else {
       for (int w = tid; w < W; w += nt) {
         uint32_t u = s.upre[w];
@@ -608,12 +707,27 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
     return (kTierOpt << 30) | (uint32_t)(((int64_t)slot << ps) + (row & pmask));
   };
   if (!uni) {
-    for (int e = tid; e < n; e += nt) it.loc[e] = loc_of(it.sel[e]);
+    // four locations computed (their page-map loads in flight together)
+    // before they are stored
+    for (int e0 = tid; e0 < n; e0 += 4 * nt) {
+      int32_t r4[4];
+      uint32_t l4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * nt;
+        r4[u] = e < n ? sel[e] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) l4[u] = e0 + u * nt < n ? loc_of(r4[u]) : 0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (e0 + u * nt < n) it.loc[e0 + u * nt] = l4[u];
+    }
   } else {
     // union staging: each entry's rank among the distinct rows, the distinct
     // rows' locations in ascending row order, then the end marker
     for (int e = tid; e < n; e += nt) {
-      const int32_t row = it.sel[e];
+      const int32_t row = sel[e];
       const uint64_t bit = 1ull << (row & 63);
       it.index[e] = (int32_t)(s.upre[row >> 6] +
                               (uint32_t)__popcll(s.ubm[row >> 6] & (bit - 1ull)));
@@ -673,8 +787,8 @@ cudaError_t launch_t(const ResolveCommon& c, const ResolveItem* items, int n,
 
 }  // namespace
 
-size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni) {
-  return carve(w64cap, qkcap, B, uni, nullptr, nullptr);
+size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni, int selcap) {
+  return carve(w64cap, qkcap, B, uni, selcap, nullptr, nullptr);
 }
 
 cudaError_t resolve_set_smem_limit(size_t bytes) {

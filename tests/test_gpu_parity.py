@@ -130,7 +130,8 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
 # ------------------------------------------------------------ golden traces
 
 @pytest.mark.parametrize("trace", ["resolve_micro_b2.txt", "resolve_micro_b3_pairs.txt",
-                                   "admission_micro.txt", "backup_refill_micro.txt"])
+                                   "admission_micro.txt", "backup_refill_micro.txt",
+                                   "resolve_micro_same_step.txt"])
 def test_golden_trace_gpu(trace):
     from gpu_adapter import GpuAdapter
     run_trace(trace, GpuAdapter(), elems=8)  # 16-byte rows

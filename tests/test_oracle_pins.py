@@ -28,7 +28,8 @@ from oracle import OraclePool, decode
 from oracle.run import OracleRun
 
 TRACES = ["resolve_micro_b2.txt", "resolve_micro_b3_pairs.txt",
-          "admission_micro.txt", "backup_refill_micro.txt", "window_micro.txt"]
+          "admission_micro.txt", "backup_refill_micro.txt", "window_micro.txt",
+          "resolve_micro_same_step.txt"]
 
 
 @pytest.mark.parametrize("trace", TRACES)
