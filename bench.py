@@ -816,7 +816,15 @@ def main():
         """The whole step's algorithmic HBM bytes over its device time."""
         gbs = sum(step_alg[s] for s in steps) / (sum(ms) / 1e3) / 1e9
         srt = sorted(ms)
-        return {"us_per_step_mean": sum(ms) * 1e3 / len(ms),
+        # position in the workload's cycle: the early steps after each pool
+        # reset fill the hot caches again (and the host copy's translations)
+        early = [m for m, s in zip(ms, steps) if s <= T // 2]
+        late = [m for m, s in zip(ms, steps) if s > T // 2]
+        halves = {"us_median_first_half_of_cycle":
+                  statistics.median(early) * 1e3 if early else None,
+                  "us_median_second_half_of_cycle":
+                  statistics.median(late) * 1e3 if late else None}
+        return {**halves, "us_per_step_mean": sum(ms) * 1e3 / len(ms),
                 "us_per_step_median": statistics.median(ms) * 1e3,
                 "us_per_step_p90": srt[min(len(srt) - 1, int(0.9 * len(srt)))] * 1e3,
                 "us_per_step_max": srt[-1] * 1e3,
