@@ -11,6 +11,8 @@ in-window entries keep their locations.  Locations, counters, status flags,
 hot-cache state and every staged byte must match the oracle exactly, fused
 and split, with either gather, early copies on and off.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -41,7 +43,10 @@ def payload(r, s, row0, n):
     return dhs_workload.payload_rows(TAG, s, r, row0, n, E)
 
 
-def run_window_pool(T, mode, steps=12, seed=0):
+def run_window_pool(T, mode, steps=12, seed=0, union=False, how="plain"):
+    """how: "plain" (dhs_decode_step when fused, else append + resolve +
+    gather), "prefetch" (resolves by dhs_prefetch on a side stream, then the
+    gather) or "noalloc" (resolves by dhs_resolve_noalloc)."""
     from hierarchical_sparse_kv_dhs_gb300 import dhs
     from oracle import OraclePool
     rng = np.random.default_rng(seed)
@@ -77,6 +82,7 @@ def run_window_pool(T, mode, steps=12, seed=0):
     sel_d = torch.zeros((R, S, Q, K), dtype=torch.int32, device="cuda")
     loc_d = torch.zeros((R, S, Q, K), dtype=torch.int32, device="cuda")
     cnt_d = torch.zeros((R, S, 8), dtype=torch.int32, device="cuda")
+    idx_d = torch.zeros((R, S, Q, K), dtype=torch.int32, device="cuda")
     stg_d = torch.zeros((R, S, Q, K, E), dtype=torch.int16, device="cuda")
     items = []
     for r in range(R):
@@ -87,6 +93,9 @@ def run_window_pool(T, mode, steps=12, seed=0):
             it.loc_dev = loc_d[r, s].data_ptr()
             it.counters_dev = cnt_d[r, s].data_ptr()
             it.staging_dev = stg_d[r, s].data_ptr()
+            if union:
+                it.flags = dhs.DHS_ITEM_UNION
+                it.index_dev = idx_d[r, s].data_ptr()
             items.append(it)
     erange_steps = 0
     try:
@@ -121,7 +130,19 @@ def run_window_pool(T, mode, steps=12, seed=0):
                     sel[r, 1, 1, 5] = lo - 1 if lo > 0 else hi
             sel_d.copy_(torch.from_numpy(sel))
             st, arr = dhs.make_step(step, items)
-            if fused:
+            if how == "prefetch":
+                if apps:
+                    assert dhs.dhs_append(pool.h, apps) == 0
+                side = torch.cuda.Stream()
+                assert dhs.lib.dhs_prefetch(pool.h, ctypes.byref(st),
+                                            ctypes.c_void_p(side.cuda_stream)) == 0
+                assert dhs.dhs_gather(pool.h, st) == 0
+            elif how == "noalloc":
+                if apps:
+                    assert dhs.dhs_append(pool.h, apps) == 0
+                assert dhs.lib.dhs_resolve_noalloc(pool.h, ctypes.byref(st)) == 0
+                assert dhs.dhs_gather(pool.h, st) == 0
+            elif fused:
                 assert dhs.dhs_decode_step(pool.h, apps, st) == 0
             else:
                 if apps:
@@ -133,18 +154,31 @@ def run_window_pool(T, mode, steps=12, seed=0):
             want_flags = 0
             loc = loc_d.cpu().numpy().view(np.uint32)
             cnt = cnt_d.cpu().numpy().view(np.uint32)
+            idx = idx_d.cpu().numpy()
             stg = stg_d.cpu().numpy().view(np.uint16)
             for r in range(R):
                 for s in range(S):
-                    orc_rc, oloc, ocnt = orc.resolve(step, r, s, sel[r, s])
+                    if union:
+                        orc_rc, oloc, oidx, ocnt = orc.resolve_union(step, r, s, sel[r, s])
+                        assert np.array_equal(idx[r, s], oidx), (mode, step, r, s)
+                        oloc = oloc.reshape(Q, K)
+                    else:
+                        orc_rc, oloc, ocnt = orc.resolve(step, r, s, sel[r, s])
                     if orc_rc == "erange":
                         want_flags |= 1
                         erange_steps += s == 1
                     assert np.array_equal(loc[r, s], oloc), (mode, step, r, s)
                     assert np.array_equal(cnt[r, s], ocnt), (mode, step, r, s, cnt[r, s], ocnt)
-                    grc, ostg = orc.gather(oloc)
-                    assert grc == 0
-                    assert np.array_equal(stg[r, s], ostg), (mode, step, r, s)
+                    if union:  # the distinct rows staged once, in row order
+                        u = int(ocnt[1])
+                        grc, ostg = orc.gather(oloc.ravel()[:u])
+                        assert grc == 0
+                        got = stg[r, s].reshape(Q * K, E)[:u]
+                        assert np.array_equal(got, ostg), (mode, step, r, s)
+                    else:
+                        grc, ostg = orc.gather(oloc)
+                        assert grc == 0
+                        assert np.array_equal(stg[r, s], ostg), (mode, step, r, s)
                     tags, stamps, pages, info = pool.read_state(r, s)
                     ot, os_, op, ln = orc.state(r, s)
                     assert np.array_equal(tags, ot) and np.array_equal(stamps, os_)
@@ -171,6 +205,16 @@ MODES = {"fused-tma": (True, 1, 1), "fused-vec": (True, 0, 1), "fused-tma-late":
 @pytest.mark.parametrize("mode", list(MODES))
 def test_window_sources_match_oracle(T, mode):
     run_window_pool(T, MODES[mode], seed=T)
+
+
+@pytest.mark.parametrize("how", ["union-fused", "union-split", "prefetch", "noalloc"])
+def test_window_sources_other_entry_points(how):
+    """Window sources under union staging (fused and split), resolved by
+    dhs_prefetch on a side stream, and by dhs_resolve_noalloc."""
+    if how.startswith("union"):
+        run_window_pool(16, (how == "union-fused", 1, 1), seed=7, union=True)
+    else:
+        run_window_pool(16, (False, 1, 1), seed=8, how=how)
 
 
 def test_window_golden_trace_gpu():
