@@ -111,6 +111,9 @@ def parse():
                          "flush when a step moves less than 4x the L2 size")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--copy-ctas", type=int, default=0)
+    ap.add_argument("--resolve-paired", type=int, default=-1,
+                    help="DHS_OPT_RESOLVE_PAIRED: -1 auto, 0 one 1024-thread CTA per SM, 1 "
+                         "512-thread CTAs two per SM whenever they fit")
     ap.add_argument("--copy-pdl", type=int, default=-1,
                     help="DHS_OPT_COPY_PDL: -1 auto, 0 copy after the resolve grid, 1 overlapped")
     ap.add_argument("--gather-impl", type=int, default=1)
@@ -694,6 +697,7 @@ def main():
     if args.copy_ctas:
         run.pool.set_option(dhs.DHS_OPT_COPY_CTAS, args.copy_ctas)
     run.pool.set_option(dhs.DHS_OPT_COPY_PDL, args.copy_pdl)
+    run.pool.set_option(dhs.DHS_OPT_RESOLVE_PAIRED, args.resolve_paired)
     run.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, args.gather_impl)
     run.pool.set_option(dhs.DHS_OPT_EARLY, args.early)
     run.pool.set_option(dhs.DHS_OPT_STAGE_MISSES, args.stage_misses)

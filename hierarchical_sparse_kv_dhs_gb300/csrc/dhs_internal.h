@@ -72,6 +72,10 @@ constexpr int kResolveItemsLarge = 256, kResolveItemsSmall = 32;
 constexpr int resolve_threads(int max_items) {
   return max_items <= kResolveItemsSmall ? 512 : 1024;
 }
+// A large launch whose shared-memory plan lets two CTAs share an SM can run
+// 512-thread CTAs two per SM instead: more items than SMs then resolve in one
+// wave instead of two.
+constexpr int kResolvePairThreads = 512;
 
 struct ResolveItem {
   const int32_t* sel;   // [n] selected rows (Q*k, verify queries back to back)
@@ -131,8 +135,10 @@ struct ResolveCommon {
 // slots, and selcap staged selection entries.
 size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni, int selcap);
 cudaError_t resolve_set_smem_limit(size_t bytes);
+// paired: a launch of more than kResolveItemsSmall items as 512-thread CTAs
+// two per SM (the caller checks that two plans fit one SM).
 cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,
-                           int n_items, size_t smem, cudaStream_t stream);
+                           int n_items, size_t smem, bool paired, cudaStream_t stream);
 
 // ------------------------------------------------------------ page moves
 // Whole optional pages between the optional arena and the pinned host copy

@@ -192,6 +192,8 @@ struct dhs_pool {
   int stage_misses = 1;         // DHS_OPT_STAGE_MISSES
   uint32_t mark_polls = dhs::kMarkPolls;  // DHS_OPT_MARK_POLLS
   int copy_pdl = -1;            // DHS_OPT_COPY_PDL: -1 auto, 0 off, 1 on
+  int resolve_paired = -1;      // DHS_OPT_RESOLVE_PAIRED: -1 auto, 0 off, 1 whenever it fits
+  int smem_per_sm = 0;          // shared memory per SM
   std::vector<uint8_t> staged_pair;  // the host copy stages this pair's misses this step
   std::vector<uint8_t> staged_item;  // per item of the step: a gather-only item whose
                                      // staging the host copy writes too
@@ -270,6 +272,20 @@ int copy_ctas(const dhs_pool* p, int64_t n_items) {
   const int64_t want = (n_items + per_block - 1) / per_block;
   const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(n_items, std::max(1, p->sm_count)));
   return (int)std::max<int64_t>(32, std::min(want, cap));
+}
+
+// Resolve launches of more items than SMs take two waves of 1024-thread CTAs,
+// one per SM.  When the host copy waits for the whole resolve grid anyway
+// (copy_pdl false) and two CTAs' shared-memory plans fit one SM, 512-thread
+// CTAs two per SM resolve every item in one wave instead, and the copy and
+// the gather behind it start that much earlier.  With the copy overlapped
+// (C64) the two waves stay: the first wave's items reach the host link sooner.
+bool copy_pdl(const dhs_pool* p, int64_t n_items);
+bool resolve_paired(const dhs_pool* p, int64_t n_items, size_t plan) {
+  if (p->resolve_paired == 0 || n_items <= dhs::kResolveItemsSmall) return false;
+  const bool fits = 2 * (plan + 1024) <= (size_t)p->smem_per_sm;
+  if (p->resolve_paired == 1) return fits;
+  return fits && n_items > p->sm_count && !copy_pdl(p, n_items);
 }
 
 // Programmatic dependent launch of the host copy (its blocks start while the
@@ -522,8 +538,10 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
       cudaSuccess)
     return DHS_ECUDA;
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+  int sms = 0, smem_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+          cudaSuccess)
     return DHS_ECUDA;
   const size_t smem = max_resolve_smem(*cfg, false);
   if (smem + 1024 > (size_t)optin) return DHS_EINVAL;
@@ -539,6 +557,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->gather_impl = dhs::kGatherTma;
     p->sm_count = sms;
     p->smem_optin = optin;
+    p->smem_per_sm = smem_sm;
     p->stream = (cudaStream_t)cfg->stream;
     p->device = dev;
     p->pairs = (int64_t)cfg->max_requests * cfg->sources;
@@ -652,6 +671,11 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     pool->gather_tpc = (int)value;
     return DHS_OK;
   }
+  if (key == DHS_OPT_RESOLVE_PAIRED) {
+    if (value < -1 || value > 1) return DHS_EINVAL;
+    pool->resolve_paired = (int)value;
+    return DHS_OK;
+  }
   if (key == DHS_OPT_COPY_PDL) {
     if (value < -1 || value > 1) return DHS_EINVAL;
     pool->copy_pdl = (int)value;
@@ -689,6 +713,7 @@ int dhs_get_option(dhs_pool* pool, int32_t key, int64_t* value) {
     case DHS_OPT_STAGE_MISSES: *value = pool->stage_misses; return DHS_OK;
     case DHS_OPT_MARK_POLLS: *value = pool->mark_polls; return DHS_OK;
     case DHS_OPT_COPY_PDL: *value = pool->copy_pdl; return DHS_OK;
+    case DHS_OPT_RESOLVE_PAIRED: *value = pool->resolve_paired; return DHS_OK;
     default: return DHS_EINVAL;
   }
 }
@@ -1203,14 +1228,18 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     const size_t base = dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni, 0);
     const size_t staged =
         dhs::resolve_smem_bytes(rcm.w64cap, rcm.qkcap, c.hot_rows, uni, (int)nmax);
+    const bool paired = resolve_paired(p, n, base);
+    const int threads = n <= dhs::kResolveItemsSmall
+                            ? dhs::resolve_threads(dhs::kResolveItemsSmall)
+                            : (paired ? dhs::kResolvePairThreads
+                                      : dhs::resolve_threads(dhs::kResolveItemsLarge));
     rcm.selcap = 0;
-    if (nmax >= 8 * dhs::resolve_threads(n <= dhs::kResolveItemsSmall ? dhs::kResolveItemsSmall
-                                                                       : dhs::kResolveItemsLarge) &&
-        staged + 1024 <= (size_t)p->smem_optin &&
+    if (!paired && nmax >= 8 * threads && staged + 1024 <= (size_t)p->smem_optin &&
         dhs::resolve_set_smem_limit(staged) == cudaSuccess)
       rcm.selcap = (int32_t)nmax;
     const size_t smem = rcm.selcap ? staged : base;
-    if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, smem, p->stream) != cudaSuccess)
+    if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, smem, paired, p->stream) !=
+        cudaSuccess)
       return DHS_ECUDA;
     if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, copy_ctas(p, n), copy_pdl(p, n),
                              p->stream) != cudaSuccess)

@@ -324,8 +324,8 @@ struct ResolveParams {
 // kernel parameter space holds at most 32764 bytes
 static_assert(sizeof(ResolveParams<kResolveItemsLarge>) <= 32764, "resolve item table too large");
 
-template <int MAXI>
-__global__ void __launch_bounds__(resolve_threads(MAXI), 1)
+template <int MAXI, int THREADS, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB)
     resolve_kernel(const __grid_constant__ ResolveParams<MAXI> P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint32_t scratch[4 * 33];
@@ -774,16 +774,21 @@ __global__ void __launch_bounds__(resolve_threads(MAXI), 1)
   }
 }
 
-template <int MAXI>
+template <int MAXI, int THREADS, int MINB>
 cudaError_t launch_t(const ResolveCommon& c, const ResolveItem* items, int n,
                      size_t smem, cudaStream_t stream) {
   ResolveParams<MAXI> P;
   P.c = c;
   P.c.n_items = n;
   for (int i = 0; i < n; ++i) P.items[i] = items[i];
-  resolve_kernel<MAXI><<<n, resolve_threads(MAXI), smem, stream>>>(P);
+  resolve_kernel<MAXI, THREADS, MINB><<<n, THREADS, smem, stream>>>(P);
   return cudaGetLastError();
 }
+
+// the three instances: small launches, large launches, large launches two per SM
+#define DHS_RESOLVE_SMALL kResolveItemsSmall, resolve_threads(kResolveItemsSmall), 1
+#define DHS_RESOLVE_LARGE kResolveItemsLarge, resolve_threads(kResolveItemsLarge), 1
+#define DHS_RESOLVE_PAIRED kResolveItemsLarge, kResolvePairThreads, 2
 
 }  // namespace
 
@@ -802,26 +807,33 @@ cudaError_t resolve_set_smem_limit(size_t bytes) {
     if ((int)bytes <= device_limit[dev]) return cudaSuccess;
     device_limit[dev] = (int)bytes;
   }
-  e = cudaFuncSetAttribute(resolve_kernel<kResolveItemsSmall>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)bytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(resolve_kernel<kResolveItemsLarge>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  for (const void* k : {(const void*)resolve_kernel<DHS_RESOLVE_SMALL>,
+                        (const void*)resolve_kernel<DHS_RESOLVE_LARGE>,
+                        (const void*)resolve_kernel<DHS_RESOLVE_PAIRED>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t resolve_set_carveout() {
-  cudaError_t e = cudaFuncSetAttribute(resolve_kernel<kResolveItemsSmall>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(resolve_kernel<kResolveItemsLarge>, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  for (const void* k : {(const void*)resolve_kernel<DHS_RESOLVE_SMALL>,
+                        (const void*)resolve_kernel<DHS_RESOLVE_LARGE>,
+                        (const void*)resolve_kernel<DHS_RESOLVE_PAIRED>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,
-                           int n_items, size_t smem, cudaStream_t stream) {
+                           int n_items, size_t smem, bool paired, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
   if (n_items <= kResolveItemsSmall)
-    return launch_t<kResolveItemsSmall>(c, items, n_items, smem, stream);
-  return launch_t<kResolveItemsLarge>(c, items, n_items, smem, stream);
+    return launch_t<DHS_RESOLVE_SMALL>(c, items, n_items, smem, stream);
+  if (paired) return launch_t<DHS_RESOLVE_PAIRED>(c, items, n_items, smem, stream);
+  return launch_t<DHS_RESOLVE_LARGE>(c, items, n_items, smem, stream);
 }
 
 }  // namespace dhs

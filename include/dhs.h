@@ -566,6 +566,11 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
  * on the same SMs step after step, which only a launch onto an idle GPU
  * gives, for the GPU to keep their address translations. */
 #define DHS_OPT_COPY_PDL 9
+/* Resolve launches of more than 32 items: -1 (default) = 512-thread CTAs two
+ * per SM (one wave for more items than SMs) when the host copy launches after
+ * the resolve grid and two CTAs' shared memory fits an SM, else 1024-thread
+ * CTAs one per SM; 0 = always the latter; 1 = the former whenever it fits. */
+#define DHS_OPT_RESOLVE_PAIRED 10
 int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
 /* The value in effect (DHS_OPT_FRESH_LIST: 0 or 1, the auto rule resolved
  * for the pool's current admissions).  DHS_EINVAL for an unknown key. */

@@ -37,7 +37,7 @@ def _as_u32(t):
 
 def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
                 gather_impl=0, patch=None, early=1, union=False, fresh=None, tpc=None,
-                stage=None, polls=None, copy_pdl=None, copy_ctas=None):
+                stage=None, polls=None, copy_pdl=None, copy_ctas=None, resolve_paired=None):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
@@ -62,6 +62,8 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
         gpu.pool.set_option(dhs.DHS_OPT_COPY_PDL, copy_pdl)
     if copy_ctas is not None:
         gpu.pool.set_option(dhs.DHS_OPT_COPY_CTAS, copy_ctas)
+    if resolve_paired is not None:
+        gpu.pool.set_option(dhs.DHS_OPT_RESOLVE_PAIRED, resolve_paired)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
     orc = OracleRun(cfg, wl, requests=sampled, union=union)
     try:
@@ -703,6 +705,17 @@ MANY = TINY.scaled(name="many", tag=57, requests=200, sources=2, history=512, ta
 def test_steps_of_several_launches_per_kernel(mode):
     compare_run(MANY, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
                 union=mode.endswith("union"))
+
+
+@pytest.mark.parametrize("mode", ["fused-tma", "split-vec", "fused-tma-union", "fused-tma-late-copy"])
+def test_resolve_two_ctas_per_sm(mode):
+    """Resolve launches of more than 32 items as 512-thread CTAs two per SM
+    (what the pool picks when the host copy waits for the resolve grid):
+    bit-exact on steps of 400 pairs, fused and split, both layouts, with the
+    copy overlapped and launched after the resolve grid."""
+    compare_run(MANY, fused=mode.startswith("fused"), gather_impl=IMPLS[mode.split("-")[1]],
+                union=mode.endswith("union"), resolve_paired=1,
+                copy_pdl=0 if mode.endswith("late-copy") else None)
 
 
 MAXHOT = TINY.scaled(name="maxhot", tag=53, requests=1, sources=1, hot=16384, history=65536,
