@@ -4,10 +4,14 @@
 // Reads the missing rows straight out of mapped pinned host memory over
 // NVLink-C2C into their victim hot-cache slots.  The pages note that the
 // copy kernel scales from 4 to 32 thread blocks with batch size; on GB300
-// fewer than about 16 blocks leave the host link idle, so the grid is the
-// upper end, 32 blocks, whatever the batch (overridable for sweeps).  Each
-// warp keeps up to four 1152-byte rows in flight (12 x 16-byte loads per
-// lane) so the link sees enough outstanding requests to cover its latency.
+// fewer than about 16 blocks leave the host link idle, so the grid is at
+// least the upper end, 32 blocks, whatever the batch.  The pool grows it
+// further when the items' pinned regions are large (each block's share
+// kept within about 1 GiB, so that the translations of its rows stay cached
+// near its SM), and launches it after the resolve grid past 16 GiB of pinned
+// rows so that block b lands on the same SM every step.  Each warp keeps up
+// to four 1152-byte rows in flight (12 x 16-byte loads per lane) so the link
+// sees enough outstanding requests to cover its latency.
 #include <algorithm>
 
 #include "dhs_internal.h"
