@@ -220,6 +220,15 @@ __device__ uint32_t block_scan_array(uint32_t* a, int n, uint32_t* scratch) {
   return total;
 }
 
+// OR a 64-bit mask into a shared bitmap word as two 32-bit atomics (only
+// the halves that have bits): 32-bit shared-memory atomics are native.
+__device__ __forceinline__ void or_word(uint64_t* word, uint64_t bits) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(word);
+  const uint32_t lo = (uint32_t)bits, hi = (uint32_t)(bits >> 32);
+  if (lo) atomicOr(w, lo);
+  if (hi) atomicOr(w + 1, hi);
+}
+
 // ---------------------------------------------------------------- masks
 
 // Rows of word w (rows 64w .. 64w+63) that lie in the tail [t0, ...).
@@ -444,14 +453,14 @@ __global__ void __launch_bounds__(THREADS, MINB)
         }
         const int w = row >> 6;
         if (w != cur) {
-          if (cur >= 0) atomicOr((unsigned long long*)&s.bm[cur], (unsigned long long)acc);
+          if (cur >= 0) or_word(&s.bm[cur], acc);
           cur = w;
           acc = 0ull;
         }
         acc |= 1ull << (row & 63);
       }
     }
-    if (cur >= 0) atomicOr((unsigned long long*)&s.bm[cur], (unsigned long long)acc);
+    if (cur >= 0) or_word(&s.bm[cur], acc);
   }
   __syncthreads();
   if (s_bad) {
