@@ -80,3 +80,48 @@ def test_union_error_leaves_empty_list(oracle_lib):
     rc, loc, idx, cnt = p2.resolve_union(2, 0, 0, np.array([[9, 7], [7, 9]], np.int32))
     assert rc == 0 and cnt[1] == 2 and idx.tolist() == [[1, 0], [0, 1]]
     assert loc[2:].tolist() == [oracle.END_LOC] * 2
+
+
+def test_verify_block_fetches_each_missing_row_once(oracle_lib):
+    """Verification queries share missing-row retrieval ("Adaptive
+    DHiSparse", How it works / Speculative state).  From the pool's state
+    before each step (tail window, ready pages, hot tags), the rows no tier
+    holds are the block's distinct selected rows minus those: the host
+    fetches must equal their count -- once per row however many queries
+    select it -- which is at most the sum of each query's own missing rows."""
+    rng = np.random.default_rng(5)
+    R, S, T, B, E, PR, N = 1, 1, 8, 48, 4, 16, 512
+    p = OraclePool(R, S, T, B, E, PR, N + 64, 40)
+    mask = (rng.random(N // PR) < 0.4).astype(np.uint8)
+    assert p.admit(0, 0, N, mask, None)[0] == 0
+    L, shared = N, 0
+    for step in range(1, 25):
+        assert p.append(0, 0, 1) == 0
+        L += 1
+        core = rng.choice(L, size=12, replace=False)
+        sel = np.stack([np.concatenate([core, rng.choice(L, size=4, replace=False)])
+                        for _ in range(3)]).astype(np.int32)
+        tags, _, page_slot, _ = p.state(0, 0)
+        held = set(tags[tags >= 0].tolist())
+
+        def missing(rows):
+            out = set()
+            for row in np.unique(rows).tolist():
+                if row >= L - T:
+                    continue  # tail
+                if (row // PR + 1) * PR <= N and page_slot[row // PR] >= 0:
+                    continue  # ready optional page
+                if row not in held:
+                    out.add(row)
+            return out
+
+        want = missing(sel)
+        per_query = sum(len(missing(q)) for q in sel)
+        rc, loc, cnt = p.resolve(step, 0, 0, sel)
+        if rc != 0:
+            continue
+        assert int(cnt[5]) == len(want), (step, cnt, len(want))
+        assert int(cnt[5]) <= per_query
+        shared += per_query - int(cnt[5])
+    assert shared > 0, "some missing rows must be selected by several queries"
+    p.close()
