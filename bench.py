@@ -574,6 +574,18 @@ def run_loadstep(args):
     print(json.dumps(out), flush=True)
 
 
+def set_pool_options(run, args):
+    """The pool options that the command line sets (library defaults otherwise)."""
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    if args.copy_ctas:
+        run.pool.set_option(dhs.DHS_OPT_COPY_CTAS, args.copy_ctas)
+    run.pool.set_option(dhs.DHS_OPT_COPY_PDL, args.copy_pdl)
+    run.pool.set_option(dhs.DHS_OPT_RESOLVE_PAIRED, args.resolve_paired)
+    run.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, args.gather_impl)
+    run.pool.set_option(dhs.DHS_OPT_EARLY, args.early)
+    run.pool.set_option(dhs.DHS_OPT_STAGE_MISSES, args.stage_misses)
+
+
 def run_prefetch(args, cfg):
     """Per-layer decode with the caller's compute between layers (a bf16
     GEMM standing in for each layer's attention + MLP), two schedules over
@@ -590,6 +602,7 @@ def run_prefetch(args, cfg):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     wl = Workload(cfg)
     run = GpuRun(cfg, wl)
+    set_pool_options(run, args)
     n = args.gemm
     A = torch.randn(n, n, device="cuda", dtype=torch.bfloat16)
     B = torch.randn(n, n, device="cuda", dtype=torch.bfloat16)
@@ -694,13 +707,7 @@ def main():
 
     wl = Workload(cfg)
     run = GpuRun(cfg, wl, device=dev, hugepages=not args.no_hugepages, union=args.union)
-    if args.copy_ctas:
-        run.pool.set_option(dhs.DHS_OPT_COPY_CTAS, args.copy_ctas)
-    run.pool.set_option(dhs.DHS_OPT_COPY_PDL, args.copy_pdl)
-    run.pool.set_option(dhs.DHS_OPT_RESOLVE_PAIRED, args.resolve_paired)
-    run.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, args.gather_impl)
-    run.pool.set_option(dhs.DHS_OPT_EARLY, args.early)
-    run.pool.set_option(dhs.DHS_OPT_STAGE_MISSES, args.stage_misses)
+    set_pool_options(run, args)
     stream = torch.cuda.current_stream(dev)
     # Every device buffer the bench uses is allocated here, before any step
     # is timed: a new device allocation changes the GPU's page tables, and
