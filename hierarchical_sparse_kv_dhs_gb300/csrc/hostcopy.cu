@@ -8,8 +8,9 @@
 // least the upper end, 32 blocks, whatever the batch.  The pool grows it
 // further when the items' pinned regions are large (each block's share
 // kept within about 1 GiB, so that the translations of its rows stay cached
-// near its SM), and launches it after the resolve grid past 16 GiB of pinned
-// rows so that block b lands on the same SM every step.  Each warp keeps up
+// near its SM).  Past 16 GiB of pinned rows it launches the copy after the
+// resolve grid, so that block b lands on the same SM every step, unless every
+// copy block finds an SM that the resolve grid leaves free.  Each warp keeps up
 // to four 1152-byte rows in flight (12 x 16-byte loads per lane) so the link
 // sees enough outstanding requests to cover its latency.
 #include <algorithm>

@@ -292,16 +292,25 @@ bool resolve_paired(const dhs_pool* p, int64_t n_items, size_t plan) {
 // resolve grid still runs and copy each item once its miss list is out) pays
 // while the launch's pinned regions are small enough for the GPU's
 // translation caches to hold them whatever SMs the blocks land on (C64: 9.7
-// GB, 205 GB/s).  Past that, blocks placed on whichever SMs the resolve grid
-// frees land on different SMs from step to step and re-walk their
-// translations: the copy then launches after the resolve grid, onto an idle
-// GPU, so block b lands on the same SM every step (copy alone, pinned span
-// 57 GB with 96 blocks: 44-53 GB/s with the early start, 149 without it; 30
-// GB with 32 blocks: 58-84 against 182).
+// GB, 205 GB/s).  Past that it still pays when every copy block finds an SM
+// that the resolve grid leaves free (a copy block holds a whole SM's
+// registers, so it never shares an SM with a resolve CTA): the blocks are
+// then all placed at launch, on the same SMs every step.  Otherwise blocks placed on
+// whichever SMs the resolve grid frees land on different SMs from step to
+// step and re-walk their translations, so the copy launches after the
+// resolve grid, onto an idle GPU, where block b lands on the same SM every
+// step (copy alone, pinned span 57 GB, 96 items and 96 blocks: 44-53 GB/s
+// with the early start, 149 without it; 30 GB, 256 items and 32 blocks:
+// 58-84 against 182).  One layer of the same 57 GB pool, 32 items beside 32
+// blocks, runs faster overlapped, and much faster when other streams keep
+// the GPU busy, since no launch then finds it idle (per-layer decode with
+// side-stream prefetch and gathers on a second stream: 0.97-1.07 ms a step
+// against 2.02-2.16).
 bool copy_pdl(const dhs_pool* p, int64_t n_items) {
   if (p->copy_pdl >= 0) return p->copy_pdl == 1;
   const int64_t item_span = p->cfg.max_rows_per_request * (int64_t)p->cfg.row_bytes;
-  return n_items * item_span <= (int64_t(16) << 30);
+  if (n_items * item_span <= (int64_t(16) << 30)) return true;
+  return n_items + copy_ctas(p, n_items) <= (int64_t)p->sm_count;
 }
 
 // Pages small enough for the page-move kernel's 32-bit chunk arithmetic.

@@ -562,9 +562,11 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
 #define DHS_OPT_MARK_POLLS 8
 /* The host copy starts while the resolve kernel runs (programmatic dependent
  * launch: 1) or after it (0).  -1 (default) = 1 while a launch's items span
- * at most 16 GiB of pinned rows, else 0: past that the copy's blocks must land
- * on the same SMs step after step, which only a launch onto an idle GPU
- * gives, for the GPU to keep their address translations. */
+ * at most 16 GiB of pinned rows, or when the launch's items plus its copy
+ * blocks number at most the GPU's SMs (every copy block then finds an SM the
+ * resolve grid leaves free); else 0.  Past 16 GiB the copy's blocks must land
+ * on the same SMs step after step for the GPU to keep their address
+ * translations, which a launch onto an idle GPU, or onto SMs left free, gives. */
 #define DHS_OPT_COPY_PDL 9
 /* Resolve launches of more than 32 items: -1 (default) = 512-thread CTAs two
  * per SM (one wave for more items than SMs) when the host copy launches after
