@@ -257,6 +257,45 @@ __device__ __forceinline__ uint64_t opt_mask(int w, int64_t N, const int32_t* ma
   return m;
 }
 
+// Rank of a row among the set bits of a bitmap over [0, L), given the
+// exclusive prefix of the words' bit counts.
+__device__ __forceinline__ uint32_t union_rank(const uint64_t* bm, const uint32_t* pre,
+                                               int32_t row) {
+  const uint64_t bit = 1ull << (row & 63);
+  return pre[row >> 6] + (uint32_t)__popcll(bm[row >> 6] & (bit - 1ull));
+}
+
+// Position of the k-th set bit (from 0) of a word holding more than k bits,
+// by halving: count the low half's bits, step into the half that holds it.
+__device__ __forceinline__ int nth_set_bit(uint64_t m, uint32_t k) {
+  int pos = 0;
+#pragma unroll
+  for (int w = 32; w >= 1; w >>= 1) {
+    const uint64_t low = m & ((1ull << w) - 1ull);
+    const uint32_t c = (uint32_t)__popcll(low);
+    if (k >= c) {
+      k -= c;
+      pos += w;
+      m >>= w;
+    } else {
+      m = low;
+    }
+  }
+  return pos;
+}
+
+// The row of union rank u (u below the union's size): the last word whose
+// prefix is at most u holds it (empty words share the next word's prefix).
+__device__ __forceinline__ int32_t union_row(const uint64_t* bm, const uint32_t* pre, int W,
+                                             uint32_t u) {
+  int lo = 0, hi = W - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return (lo << 6) + nth_set_bit(bm[lo], u - pre[lo]);
+}
+
 // Publish that an item's locations (and the decode rows it appended) are
 // written (thread 0 only, after a block barrier).
 __device__ __forceinline__ void publish_loc(const ResolveCommon& c, int pair) {
@@ -645,7 +684,20 @@ __global__ void __launch_bounds__(THREADS, MINB)
   // ---- staging entries of each miss (the host copy writes them): entries
   // grouped by miss index, CSR in miss_off / miss_ent.  After the stamp
   // commit the working stamps serve as per-miss counters, then cursors.
-  if (it.stage && m_miss) {
+  if (it.stage && m_miss && uni) {
+    // one staging row per distinct row: a miss's only staging entry is its
+    // row's rank in the union, so miss i takes entry i
+    int32_t* off = c.miss_off + (size_t)pair * (c.Mcap + 1);
+    int32_t* ent = c.miss_ent + (size_t)pair * c.ent_cap;
+    const int32_t* mrows = c.miss_rows + (size_t)pair * c.Mcap;
+    __syncthreads();
+    for (uint32_t j = tid; j < m_miss; j += nt) {
+      const int32_t row = mrows[j];
+      off[j] = (int32_t)j;
+      ent[j] = (int32_t)union_rank(s.ubm, s.upre, row);
+    }
+    if (tid == 0) off[m_miss] = (int32_t)m_miss;
+  } else if (it.stage && m_miss) {
     int32_t* off = c.miss_off + (size_t)pair * (c.Mcap + 1);
     int32_t* ent = c.miss_ent + (size_t)pair * c.ent_cap;
     // miss index of the entry's row, or -1 when the row is not a miss
@@ -660,37 +712,19 @@ __global__ void __launch_bounds__(THREADS, MINB)
     __syncthreads();
     for (uint32_t j = tid; j < m_miss; j += nt) s.st[j] = 0u;
     __syncthreads();
-    if (!uni) {
-      for_entries([&](int, int32_t row) {
-        const int32_t mi = miss_of(row);
-        if (mi >= 0) atomicAdd(&s.st[mi], 1u);
-      });
-    } else {  // one staging row per distinct row
-      for (int w = tid; w < W; w += nt)
-        for (uint64_t m = s.ubm[w]; m; m &= m - 1) {
-          const int32_t mi = miss_of((w << 6) + __ffsll((long long)m) - 1);
-          if (mi >= 0) atomicAdd(&s.st[mi], 1u);
-        }
-    }
+    for_entries([&](int, int32_t row) {
+      const int32_t mi = miss_of(row);
+      if (mi >= 0) atomicAdd(&s.st[mi], 1u);
+    });
     __syncthreads();
     const uint32_t total = block_scan_array(s.st, (int)m_miss, scratch);
     for (uint32_t j = tid; j < m_miss; j += nt) off[j] = (int32_t)s.st[j];
     if (tid == 0) off[m_miss] = (int32_t)total;
     __syncthreads();
-    if (!uni) {
-      for_entries([&](int e, int32_t row) {
-        const int32_t mi = miss_of(row);
-        if (mi >= 0) ent[atomicAdd(&s.st[mi], 1u)] = e;
-      });
-    } else {
-      for (int w = tid; w < W; w += nt) {
-        uint32_t u = s.upre[w];
-        for (uint64_t m = s.ubm[w]; m; m &= m - 1, ++u) {
-          const int32_t mi = miss_of((w << 6) + __ffsll((long long)m) - 1);
-          if (mi >= 0) ent[atomicAdd(&s.st[mi], 1u)] = (int32_t)u;
-        }
-      }
-    }
+    for_entries([&](int e, int32_t row) {
+      const int32_t mi = miss_of(row);
+      if (mi >= 0) ent[atomicAdd(&s.st[mi], 1u)] = e;
+    });
   }
   __syncthreads();
   if (tid == 0) {
@@ -735,20 +769,23 @@ __global__ void __launch_bounds__(THREADS, MINB)
   } else {
     // union staging: each entry's rank among the distinct rows, the distinct
     // rows' locations in ascending row order, then the end marker
-    for (int e = tid; e < n; e += nt) {
-      const int32_t row = sel[e];
-      const uint64_t bit = 1ull << (row & 63);
-      it.index[e] = (int32_t)(s.upre[row >> 6] +
-                              (uint32_t)__popcll(s.ubm[row >> 6] & (bit - 1ull)));
-    }
-    for (int w = tid; w < W; w += nt) {
-      uint64_t m = s.ubm[w];
-      uint32_t u = s.upre[w];
-      while (m) {
-        const int b = __ffsll((long long)m) - 1;
-        m &= m - 1;
-        it.loc[u++] = loc_of((w << 6) + b);
+    for (int e = tid; e < n; e += nt) it.index[e] = (int32_t)union_rank(s.ubm, s.upre, sel[e]);
+    // rank u's row: the word whose rank range holds u (binary search of the
+    // word prefix), then the matching set bit; four ranks a thread in flight,
+    // stores coalesced
+    for (int u0 = tid; u0 < (int)n_unique; u0 += 4 * nt) {
+      int32_t r4[4];
+      uint32_t l4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int u = u0 + q * nt;
+        r4[q] = u < (int)n_unique ? union_row(s.ubm, s.upre, W, (uint32_t)u) : 0;
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) l4[q] = u0 + q * nt < (int)n_unique ? loc_of(r4[q]) : 0u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (u0 + q * nt < (int)n_unique) it.loc[u0 + q * nt] = l4[q];
     }
     for (int u = (int)n_unique + tid; u < n; u += nt) it.loc[u] = kEndLoc;
   }
