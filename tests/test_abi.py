@@ -108,3 +108,24 @@ def test_null_arguments(dhs):
     assert dhs.lib.dhs_set_option(None, dhs.DHS_OPT_EARLY, 1) == E
     assert dhs.lib.dhs_get_option(None, dhs.DHS_OPT_EARLY, ctypes.byref(n64)) == E
     assert dhs.lib.dhs_read_state(None, 0, 0, None, None, None, None) == E
+
+
+def test_binding_constants_match_the_header():
+    """Every integer constant include/dhs.h defines has the same value in the
+    Python binding (options, item flags, error codes, status flags)."""
+    import re
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    with open(os.path.join(ROOT, "include", "dhs.h")) as f:
+        text = f.read()
+    defs = dict(re.findall(r"^#define\s+(DHS_[A-Z0-9_]+)\s+\(?(-?(?:0x)?[0-9A-Fa-f]+)u?\)?\s*(?:/\*.*)?$",
+                           text, flags=re.M))
+    assert len(defs) > 20
+    missing, wrong = [], []
+    for name, v in defs.items():
+        want = int(v, 0)
+        if not hasattr(dhs, name):
+            missing.append(name)
+        elif getattr(dhs, name) != want:
+            wrong.append((name, getattr(dhs, name), want))
+    assert not wrong, wrong
+    assert not missing, missing
