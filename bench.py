@@ -116,6 +116,9 @@ def parse():
                          "512-thread CTAs two per SM whenever they fit")
     ap.add_argument("--copy-pdl", type=int, default=-1,
                     help="DHS_OPT_COPY_PDL: -1 auto, 0 copy after the resolve grid, 1 overlapped")
+    ap.add_argument("--copy-steal", type=int, default=-1,
+                    help="DHS_OPT_COPY_STEAL: -1 auto, 0 each copy block keeps to its own items, "
+                         "1 rows claimed through per-item cursors")
     ap.add_argument("--gather-impl", type=int, default=1)
     ap.add_argument("--stage-misses", type=int, default=1,
                     help="DHS_OPT_STAGE_MISSES: 1 = the host copy writes fetched rows into staging")
@@ -580,6 +583,7 @@ def set_pool_options(run, args):
     if args.copy_ctas:
         run.pool.set_option(dhs.DHS_OPT_COPY_CTAS, args.copy_ctas)
     run.pool.set_option(dhs.DHS_OPT_COPY_PDL, args.copy_pdl)
+    run.pool.set_option(dhs.DHS_OPT_COPY_STEAL, args.copy_steal)
     run.pool.set_option(dhs.DHS_OPT_RESOLVE_PAIRED, args.resolve_paired)
     run.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, args.gather_impl)
     run.pool.set_option(dhs.DHS_OPT_EARLY, args.early)

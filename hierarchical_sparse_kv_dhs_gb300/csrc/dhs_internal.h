@@ -105,6 +105,7 @@ struct ResolveCommon {
   int32_t* miss_rows;    // [pairs][Mcap]
   int32_t* miss_slots;   // [pairs][Mcap]
   uint32_t* miss_count;  // [pairs]
+  uint32_t* copy_cursor; // [pairs] miss rows the host copy has claimed (zeroed here)
   int32_t* pair_status;  // [pairs]
   uint32_t* status;      // sticky flags
   int32_t T, B, Pmax, Mcap;
@@ -175,6 +176,7 @@ struct CopyCommon {
   const int32_t* miss_rows;
   const int32_t* miss_slots;
   const uint32_t* miss_count;
+  uint32_t* cursor;           // [pairs] miss rows claimed so far (the resolve launch zeroes it)
   int32_t B, Mcap, row_bytes, n_items;
   unsigned long long* trace;  // null = off
   const uint32_t* ready;      // [pairs] the resolve launch's copy_ready marks, null = none
@@ -184,10 +186,16 @@ struct CopyCommon {
   const int32_t* miss_ent;    // [pairs][ent_cap]
   uint32_t mark_polls;        // polls of a copy_ready mark before waiting for the grid;
                               // 0: never read the marks
+  int32_t steal;              // 1: rows claimed through the cursors, and blocks done with
+                              // their own items take other items' unclaimed rows
 };
 
+// hold_smem: dynamic shared memory each block reserves (and leaves unused)
+// so that no other CTA shares its SM; at most the limit set by
+// hostcopy_set_carveout.
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,
-                            int n_items, int ctas, bool pdl, cudaStream_t stream);
+                            int n_items, int ctas, bool pdl, size_t hold_smem,
+                            cudaStream_t stream);
 
 // ------------------------------------------------------------ gather (e)
 constexpr int kGatherThreads = 256;
@@ -257,7 +265,7 @@ struct GatherCommon {
 // so consecutive kernels of a step never make an SM reconfigure its L1 /
 // shared split.
 cudaError_t resolve_set_carveout();
-cudaError_t hostcopy_set_carveout();
+cudaError_t hostcopy_set_carveout(size_t hold_smem);
 cudaError_t gather_set_carveout();
 cudaError_t append_set_carveout();
 

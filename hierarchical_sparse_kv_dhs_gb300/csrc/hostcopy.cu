@@ -41,34 +41,147 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   return v;
 }
 
-// Copy the miss rows of the launch's items.  CTA b owns items b, b + gridDim,
-// ...  An item's miss list (rows ascending, victim slots, staging entries)
-// is complete once the resolve kernel has published its copy_ready mark
-// (== seq, after a fence; before the item's locations are written), so the
-// CTA does not wait for the whole resolve grid: it
-// takes, in order, every owned item whose mark is out as one batch (waiting,
-// bounded, only when none is), and its warps copy the batch's rows as one
-// flat list, four rows per warp in flight.  A poll that runs out (after
-// c.mark_polls polls; with 0 the marks are never read) falls back to waiting
-// for the resolve grid.
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Copy up to kRowsPerWarp miss rows, row r being miss mi[r] of the launch's
+// item itm[r] (itm[r] < 0: none): one warp of the claiming copy.  Each row goes to its victim hot
+// slot and, for items whose host copy stages, to its staging entries
+// (miss_off / miss_ent) in the item's staging and in that of the gather-only
+// items sharing its locations.
+template <bool kSmallRow, int MAXI>
+__device__ __forceinline__ void copy_rows(const CopyParams<MAXI>& P,
+                                          const int (&itm)[kRowsPerWarp],
+                                          const uint32_t (&mi)[kRowsPerWarp], int lane) {
+  const CopyCommon& c = P.c;
+  const int rb = c.row_bytes, cpr = rb >> 4;
+  const uint8_t* src[kRowsPerWarp];
+  uint8_t* dst[kRowsPerWarp];
+  const int32_t* ents[kRowsPerWarp];
+  int32_t e0[kRowsPerWarp], e1[kRowsPerWarp];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    src[r] = nullptr;
+    dst[r] = nullptr;
+    ents[r] = nullptr;
+    e0[r] = e1[r] = 0;
+    if (itm[r] >= 0) {
+      const CopyItem& it = P.items[itm[r]];
+      const size_t off = (size_t)it.pair * c.Mcap + mi[r];
+      const int32_t row = c.miss_rows[off];
+      const int32_t slot = c.miss_slots[off];
+      src[r] = it.host + (size_t)row * rb;
+      dst[r] = c.hot + ((size_t)it.pair * c.B + slot) * rb;
+      if (it.staging) {
+        const int32_t* mo = c.miss_off + (size_t)it.pair * (c.Mcap + 1);
+        ents[r] = c.miss_ent + (size_t)it.pair * c.ent_cap;
+        e0[r] = mo[mi[r]];
+        e1[r] = mo[mi[r] + 1];
+      }
+    }
+  }
+  if (kSmallRow) {
+    uint4 v[kRowsPerWarp][kChunksPerLane];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+      for (int q = 0; q < kChunksPerLane; ++q) {
+        const int ch = lane + 32 * q;
+        if (src[r] && ch < cpr) v[r][q] = ld_sys(src[r] + ch * 16);
+      }
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+#pragma unroll
+      for (int q = 0; q < kChunksPerLane; ++q) {
+        const int ch = lane + 32 * q;
+        if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
+      }
+      if (e0[r] == e1[r]) continue;
+      const CopyItem& it = P.items[itm[r]];
+      for (int k = e0[r]; k < e1[r]; ++k) {
+        const size_t eo = (size_t)ents[r][k] * rb;
+        for (int j = -1; j < it.nshare; ++j) {
+          uint8_t* to = (j < 0 ? it.staging : it.share[j]) + eo;
+#pragma unroll
+          for (int q = 0; q < kChunksPerLane; ++q) {
+            const int ch = lane + 32 * q;
+            if (ch < cpr) *reinterpret_cast<uint4*>(to + ch * 16) = v[r][q];
+          }
+        }
+      }
+    }
+  } else {
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      if (!src[r]) continue;
+      const CopyItem& it = P.items[itm[r]];
+      for (int ch = lane; ch < cpr; ch += 32) {
+        const uint4 v = ld_sys(src[r] + ch * 16);
+        *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v;
+        for (int k = e0[r]; k < e1[r]; ++k) {
+          const size_t eo = (size_t)ents[r][k] * rb + ch * 16;
+          *reinterpret_cast<uint4*>(it.staging + eo) = v;
+          for (int j = 0; j < it.nshare; ++j) *reinterpret_cast<uint4*>(it.share[j] + eo) = v;
+        }
+      }
+    }
+  }
+}
+
+// Copy the miss rows of the launch's items.  An item's miss list (rows
+// ascending, victim slots, staging entries) is complete once the resolve
+// kernel has published its copy_ready mark (== seq, after a fence; before
+// the item's locations are written), so the copy does not wait for the whole
+// resolve grid.  CTA b owns items b, b + gridDim, ...: it takes, in order,
+// every owned item whose mark is out as one batch (waiting, bounded, only
+// when none is).  How its warps split the batch depends on c.steal:
+//   - 0: the batch's rows form one flat list, four consecutive rows per warp
+//     in turn (pinned regions past the GPU's translation reach, where a block
+//     must keep to its own items' rows);
+//   - 1: the warps claim each item's rows four at a time from the item's
+//     claim cursor (zeroed by the resolve launch), the next claim in flight
+//     while they copy, and a CTA whose own items are done then claims the
+//     rows no CTA has claimed yet in the other items whose marks are out,
+//     the next CTA's items first.  The copy blocks' speeds differ by SM and
+//     the step waits for the last row.
+// A poll that runs out (after c.mark_polls polls; with 0 the marks are never
+// read) falls back to waiting for the resolve grid.
 constexpr int kBatchMax = 64;
 
-template <int MAXI, bool kSmallRow>
+template <int MAXI, bool kSmallRow, bool kSteal>
 __global__ void __launch_bounds__(kCopyThreads)
     hostcopy_kernel(const __grid_constant__ CopyParams<MAXI> P) {
   __shared__ int s_n, s_next, s_wait;
   __shared__ int s_item[kBatchMax];
-  __shared__ uint32_t s_pre[kBatchMax + 1];
+  __shared__ uint32_t s_pre[kBatchMax + 1];  // flat list: rows before each batch item
   const CopyCommon& c = P.c;
   const int tid = threadIdx.x, lane = tid & 31;
   // the gather may be launched now
   asm volatile("griddepcontrol.launch_dependents;");
-  const int rb = c.row_bytes;
-  const int cpr = rb >> 4;
   const uint32_t warp = (uint32_t)tid >> 5, nwarps = blockDim.x >> 5;
   const uint32_t want = c.seq & kSeqMask;
   bool waited = c.ready == nullptr, traced = false;
   if (waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // every unclaimed row of item j (cnt rows), kRowsPerWarp per claim: lane
+  // 0's atomic, its result taken only after the current rows are copied
+  auto drain = [&](int j, uint32_t cnt) {
+    uint32_t* cur_p = c.cursor + P.items[j].pair;
+    uint32_t cur = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(cur_p, (uint32_t)kRowsPerWarp) : 0u, 0);
+    while (cur < cnt) {
+      const uint32_t pend = lane == 0 ? atomicAdd(cur_p, (uint32_t)kRowsPerWarp) : 0u;
+      int itm[kRowsPerWarp];
+      uint32_t mi[kRowsPerWarp];
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        mi[r] = cur + r;
+        itm[r] = cur + r < cnt ? j : -1;
+      }
+      copy_rows<kSmallRow>(P, itm, mi, lane);
+      cur = __shfl_sync(0xffffffffu, pend, 0);
+    }
+  };
   int next = blockIdx.x;
   for (;;) {
     if (tid == 0) {  // the next batch: owned items whose miss lists are out
@@ -115,90 +228,98 @@ __global__ void __launch_bounds__(kCopyThreads)
       trace_mark(c.trace, kTraceCopy, false);  // copying starts
       traced = true;
     }
-    const uint32_t total = s_pre[n];
-    for (uint32_t base = warp * kRowsPerWarp; base < total; base += nwarps * kRowsPerWarp) {
-      const uint8_t* src[kRowsPerWarp];
-      uint8_t* dst[kRowsPerWarp];
-      // staging entries of the row (items whose host copy stages): the
-      // entries e0 .. e1 of the item's miss_ent list, written at stg + e * rb
-      uint8_t* stg[kRowsPerWarp];
-      const int32_t* ents[kRowsPerWarp];
-      int32_t e0[kRowsPerWarp], e1[kRowsPerWarp], itm[kRowsPerWarp];
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-        const uint32_t i = base + r;
-        src[r] = nullptr;
-        dst[r] = nullptr;
-        stg[r] = nullptr;
-        ents[r] = nullptr;
-        e0[r] = e1[r] = 0;
-        itm[r] = 0;
-        if (i < total) {
-          int lo = 0, hi = n - 1;  // last batch entry with s_pre <= i
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_pre[mid] <= i) lo = mid; else hi = mid - 1;
-          }
-          itm[r] = s_item[lo];
-          const CopyItem& it = P.items[itm[r]];
-          const uint32_t mi = i - s_pre[lo];
-          const size_t off = (size_t)it.pair * c.Mcap + mi;
-          const int32_t row = c.miss_rows[off];
-          const int32_t slot = c.miss_slots[off];
-          src[r] = it.host + (size_t)row * rb;
-          dst[r] = c.hot + ((size_t)it.pair * c.B + slot) * rb;
-          if (it.staging) {
-            const int32_t* mo = c.miss_off + (size_t)it.pair * (c.Mcap + 1);
-            stg[r] = it.staging;
-            ents[r] = c.miss_ent + (size_t)it.pair * c.ent_cap;
-            e0[r] = mo[mi];
-            e1[r] = mo[mi + 1];
-          }
-        }
+    if constexpr (kSteal) {
+      for (int b = 0; b < n; ++b) {
+        const uint32_t cnt = s_pre[b + 1] - s_pre[b];
+        if (cnt) drain(s_item[b], cnt);
       }
-      if (kSmallRow) {
-        uint4 v[kRowsPerWarp][kChunksPerLane];
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-          for (int q = 0; q < kChunksPerLane; ++q) {
-            const int ch = lane + 32 * q;
-            if (src[r] && ch < cpr) v[r][q] = ld_sys(src[r] + ch * 16);
-          }
-#pragma unroll
+    } else {
+      const int rb = c.row_bytes, cpr = rb >> 4;
+      const uint32_t total = s_pre[n];
+      for (uint32_t base = warp * kRowsPerWarp; base < total; base += nwarps * kRowsPerWarp) {
+        const uint8_t* src[kRowsPerWarp];
+        uint8_t* dst[kRowsPerWarp];
+        // staging entries of the row (items whose host copy stages): the
+        // entries e0 .. e1 of the item's miss_ent list, written at stg + e * rb
+        uint8_t* stg[kRowsPerWarp];
+        const int32_t* ents[kRowsPerWarp];
+        int32_t e0[kRowsPerWarp], e1[kRowsPerWarp], itm[kRowsPerWarp];
+  #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) {
-#pragma unroll
-          for (int q = 0; q < kChunksPerLane; ++q) {
-            const int ch = lane + 32 * q;
-            if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
-          }
-          // the same bytes to its staging entries, in the item's staging and
-          // in that of the gather-only items sharing its locations
-          const int ns = stg[r] ? P.items[itm[r]].nshare : 0;
-          for (int k = e0[r]; k < e1[r]; ++k) {
-            const size_t eo = (size_t)ents[r][k] * rb;
-            for (int j = -1; j < ns; ++j) {
-              uint8_t* to = (j < 0 ? stg[r] : P.items[itm[r]].share[j]) + eo;
-#pragma unroll
-              for (int q = 0; q < kChunksPerLane; ++q) {
-                const int ch = lane + 32 * q;
-                if (ch < cpr) *reinterpret_cast<uint4*>(to + ch * 16) = v[r][q];
-              }
+          const uint32_t i = base + r;
+          src[r] = nullptr;
+          dst[r] = nullptr;
+          stg[r] = nullptr;
+          ents[r] = nullptr;
+          e0[r] = e1[r] = 0;
+          itm[r] = 0;
+          if (i < total) {
+            int lo = 0, hi = n - 1;  // last batch entry with s_pre <= i
+            while (lo < hi) {
+              const int mid = (lo + hi + 1) >> 1;
+              if (s_pre[mid] <= i) lo = mid; else hi = mid - 1;
+            }
+            itm[r] = s_item[lo];
+            const CopyItem& it = P.items[itm[r]];
+            const uint32_t mi = i - s_pre[lo];
+            const size_t off = (size_t)it.pair * c.Mcap + mi;
+            const int32_t row = c.miss_rows[off];
+            const int32_t slot = c.miss_slots[off];
+            src[r] = it.host + (size_t)row * rb;
+            dst[r] = c.hot + ((size_t)it.pair * c.B + slot) * rb;
+            if (it.staging) {
+              const int32_t* mo = c.miss_off + (size_t)it.pair * (c.Mcap + 1);
+              stg[r] = it.staging;
+              ents[r] = c.miss_ent + (size_t)it.pair * c.ent_cap;
+              e0[r] = mo[mi];
+              e1[r] = mo[mi + 1];
             }
           }
         }
-      } else {
-        for (int r = 0; r < kRowsPerWarp; ++r) {
-          if (!src[r]) continue;
-          const int ns = stg[r] ? P.items[itm[r]].nshare : 0;
-          for (int ch = lane; ch < cpr; ch += 32) {
-            const uint4 v = ld_sys(src[r] + ch * 16);
-            *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v;
+        if (kSmallRow) {
+          uint4 v[kRowsPerWarp][kChunksPerLane];
+  #pragma unroll
+          for (int r = 0; r < kRowsPerWarp; ++r)
+  #pragma unroll
+            for (int q = 0; q < kChunksPerLane; ++q) {
+              const int ch = lane + 32 * q;
+              if (src[r] && ch < cpr) v[r][q] = ld_sys(src[r] + ch * 16);
+            }
+  #pragma unroll
+          for (int r = 0; r < kRowsPerWarp; ++r) {
+  #pragma unroll
+            for (int q = 0; q < kChunksPerLane; ++q) {
+              const int ch = lane + 32 * q;
+              if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
+            }
+            // the same bytes to its staging entries, in the item's staging and
+            // in that of the gather-only items sharing its locations
+            const int ns = stg[r] ? P.items[itm[r]].nshare : 0;
             for (int k = e0[r]; k < e1[r]; ++k) {
-              const size_t eo = (size_t)ents[r][k] * rb + ch * 16;
-              *reinterpret_cast<uint4*>(stg[r] + eo) = v;
-              for (int j = 0; j < ns; ++j)
-                *reinterpret_cast<uint4*>(P.items[itm[r]].share[j] + eo) = v;
+              const size_t eo = (size_t)ents[r][k] * rb;
+              for (int j = -1; j < ns; ++j) {
+                uint8_t* to = (j < 0 ? stg[r] : P.items[itm[r]].share[j]) + eo;
+  #pragma unroll
+                for (int q = 0; q < kChunksPerLane; ++q) {
+                  const int ch = lane + 32 * q;
+                  if (ch < cpr) *reinterpret_cast<uint4*>(to + ch * 16) = v[r][q];
+                }
+              }
+            }
+          }
+        } else {
+          for (int r = 0; r < kRowsPerWarp; ++r) {
+            if (!src[r]) continue;
+            const int ns = stg[r] ? P.items[itm[r]].nshare : 0;
+            for (int ch = lane; ch < cpr; ch += 32) {
+              const uint4 v = ld_sys(src[r] + ch * 16);
+              *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v;
+              for (int k = e0[r]; k < e1[r]; ++k) {
+                const size_t eo = (size_t)ents[r][k] * rb + ch * 16;
+                *reinterpret_cast<uint4*>(stg[r] + eo) = v;
+                for (int j = 0; j < ns; ++j)
+                  *reinterpret_cast<uint4*>(P.items[itm[r]].share[j] + eo) = v;
+              }
             }
           }
         }
@@ -207,9 +328,30 @@ __global__ void __launch_bounds__(kCopyThreads)
     __syncthreads();  // the batch tables are rebuilt
     next = nxt;
   }
+  // c.steal: the other items' unclaimed rows, the next CTA's items first: the
+  // lanes test 32 items at a time with relaxed reads (a hint), then the warp
+  // acquires each candidate's mark (every lane its own acquire) and drains it
+  for (int base = 1; kSteal && base < c.n_items; base += 32) {
+    const int k = base + lane;
+    int j = 0;
+    bool cand = false;
+    if (k < c.n_items) {
+      j = (blockIdx.x + k) % c.n_items;
+      const int pair = P.items[j].pair;
+      const uint32_t v = waited ? want : ld_relaxed_u32(c.ready + pair);
+      if ((v & kSeqMask) == want && !(v & kMarkNoMiss))
+        cand = ld_relaxed_u32(c.cursor + pair) < ld_relaxed_u32(c.miss_count + pair);
+    }
+    for (uint32_t m = __ballot_sync(0xffffffffu, cand); m; m &= m - 1) {
+      const int jj = __shfl_sync(0xffffffffu, j, __ffs(m) - 1);
+      const int pair = P.items[jj].pair;
+      if (!waited) (void)ld_acquire_u32(c.ready + pair);
+      drain(jj, c.miss_count[pair]);
+    }
+  }
   // this grid completes only after the resolve grid (the gather and the
   // fresh-row copy rely on that): its last block waits for it.  The others
-  // leave once their items are copied; each holds a whole SM's registers
+  // leave once no row is left to copy; each holds a whole SM's registers
   // (512 threads x 128), which the gather can use as soon as it is gone.
   if (!waited && blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
@@ -218,7 +360,7 @@ __global__ void __launch_bounds__(kCopyThreads)
 
 template <int MAXI>
 cudaError_t launch_t(const CopyCommon& c, const CopyItem* items, int n, int ctas,
-                     bool pdl, cudaStream_t stream) {
+                     bool pdl, size_t hold_smem, cudaStream_t stream) {
   CopyParams<MAXI> P;
   P.c = c;
   P.c.n_items = n;
@@ -227,6 +369,7 @@ cudaError_t launch_t(const CopyCommon& c, const CopyItem* items, int n, int ctas
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kCopyThreads);
+  cfg.dynamicSmemBytes = hold_smem;  // unused by the kernel: keeps other CTAs off its SM
   cfg.stream = stream;
   if (pdl) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -234,9 +377,12 @@ cudaError_t launch_t(const CopyCommon& c, const CopyItem* items, int n, int ctas
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  if ((c.row_bytes >> 4) <= 32 * kChunksPerLane)
-    return cudaLaunchKernelEx(&cfg, hostcopy_kernel<MAXI, true>, P);
-  return cudaLaunchKernelEx(&cfg, hostcopy_kernel<MAXI, false>, P);
+  const bool small = (c.row_bytes >> 4) <= 32 * kChunksPerLane;
+  if (c.steal)
+    return small ? cudaLaunchKernelEx(&cfg, hostcopy_kernel<MAXI, true, true>, P)
+                 : cudaLaunchKernelEx(&cfg, hostcopy_kernel<MAXI, false, true>, P);
+  return small ? cudaLaunchKernelEx(&cfg, hostcopy_kernel<MAXI, true, false>, P)
+               : cudaLaunchKernelEx(&cfg, hostcopy_kernel<MAXI, false, false>, P);
 }
 
 // ---------------------------------------------------------------- page moves
@@ -298,26 +444,32 @@ cudaError_t launch_page_moves(const PageMove* moves, int n, int page_bytes, int 
   return cudaSuccess;
 }
 
-cudaError_t hostcopy_set_carveout() {
-  for (const void* k : {(const void*)hostcopy_kernel<kCopyItemsMax, true>,
-                        (const void*)hostcopy_kernel<kCopyItemsMax, false>,
-                        (const void*)hostcopy_kernel<kCopyItemsSmall, true>,
-                        (const void*)hostcopy_kernel<kCopyItemsSmall, false>}) {
+cudaError_t hostcopy_set_carveout(size_t hold_smem) {
+  for (const void* k : {(const void*)hostcopy_kernel<kCopyItemsMax, true, false>,
+                        (const void*)hostcopy_kernel<kCopyItemsMax, false, false>,
+                        (const void*)hostcopy_kernel<kCopyItemsSmall, true, false>,
+                        (const void*)hostcopy_kernel<kCopyItemsSmall, false, false>,
+                        (const void*)hostcopy_kernel<kCopyItemsMax, true, true>,
+                        (const void*)hostcopy_kernel<kCopyItemsMax, false, true>,
+                        (const void*)hostcopy_kernel<kCopyItemsSmall, true, true>,
+                        (const void*)hostcopy_kernel<kCopyItemsSmall, false, true>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hold_smem);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items, int n_items,
-                            int ctas, bool pdl, cudaStream_t stream) {
+                            int ctas, bool pdl, size_t hold_smem, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
   if (n_items > kCopyItemsMax || n_items > kCopyThreads) return cudaErrorInvalidValue;
   // the whole table travels with every launch: a small one for small steps
   if (n_items <= kCopyItemsSmall)
-    return launch_t<kCopyItemsSmall>(c, items, n_items, ctas, pdl, stream);
-  return launch_t<kCopyItemsMax>(c, items, n_items, ctas, pdl, stream);
+    return launch_t<kCopyItemsSmall>(c, items, n_items, ctas, pdl, hold_smem, stream);
+  return launch_t<kCopyItemsMax>(c, items, n_items, ctas, pdl, hold_smem, stream);
 }
 
 }  // namespace dhs

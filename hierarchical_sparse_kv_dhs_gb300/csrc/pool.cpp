@@ -37,7 +37,7 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct MetaLayout {
-  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, pair_status;
+  size_t tags, stamps, map, miss_rows, miss_slots, miss_count, copy_cursor, pair_status;
   size_t loc_ready, copy_ready, fill, later_count, status, later, miss_off, miss_ent;
   size_t total;
 };
@@ -79,6 +79,7 @@ MetaLayout meta_layout(const dhs_pool_config& c) {
   m.miss_rows = take(pairs * (size_t)mcap_of(c) * 4);
   m.miss_slots = take(pairs * (size_t)mcap_of(c) * 4);
   m.miss_count = take(pairs * 4);
+  m.copy_cursor = take(pairs * 4);
   m.pair_status = take(pairs * 4);
   m.loc_ready = take(pairs * 4);
   m.copy_ready = take(pairs * 4);
@@ -155,6 +156,7 @@ struct dhs_pool {
   int32_t* miss_rows = nullptr;
   int32_t* miss_slots = nullptr;
   uint32_t* miss_count = nullptr;
+  uint32_t* copy_cursor = nullptr;
   int32_t* pair_status = nullptr;
   uint32_t* status = nullptr;
   std::vector<PairState> ps;
@@ -193,6 +195,7 @@ struct dhs_pool {
   uint32_t mark_polls = dhs::kMarkPolls;  // DHS_OPT_MARK_POLLS
   int copy_pdl = -1;            // DHS_OPT_COPY_PDL: -1 auto, 0 off, 1 on
   int resolve_paired = -1;      // DHS_OPT_RESOLVE_PAIRED: -1 auto, 0 off, 1 whenever it fits
+  int copy_steal = -1;          // DHS_OPT_COPY_STEAL: -1 auto, 0 off, 1 on
   int smem_per_sm = 0;          // shared memory per SM
   std::vector<uint8_t> staged_pair;  // the host copy stages this pair's misses this step
   std::vector<uint8_t> staged_item;  // per item of the step: a gather-only item whose
@@ -311,6 +314,30 @@ bool copy_pdl(const dhs_pool* p, int64_t n_items) {
   const int64_t item_span = p->cfg.max_rows_per_request * (int64_t)p->cfg.row_bytes;
   if (n_items * item_span <= (int64_t(16) << 30)) return true;
   return n_items + copy_ctas(p, n_items) <= (int64_t)p->sm_count;
+}
+
+// Claiming rows through per-item cursors (and blocks done with their own
+// items taking the rest of others') evens out the copy blocks' finishing
+// times while the launch's pinned regions stay within the GPU's translation
+// reach (C64, alternated on one box: 1738 us a step against 1762-1766).
+// Past that a block that takes another item's rows reads from a region whose
+// translations its SM does not hold, and the claims themselves cost an
+// atomic round trip per item and warp where items have few misses each
+// (C128: about 57 rows an item; its copy span 120 us against 94), so each block
+// keeps to its own items there.
+bool copy_steal(const dhs_pool* p, int64_t n_items) {
+  if (p->copy_steal >= 0) return p->copy_steal == 1;
+  const int64_t item_span = p->cfg.max_rows_per_request * (int64_t)p->cfg.row_bytes;
+  return n_items * item_span <= (int64_t(16) << 30);
+}
+
+// Where each block keeps to its own items (past the translation reach), it
+// also keeps its SM to itself: it reserves all but 2 KB of the shared memory
+// a block may take, so no gather CTA lands beside it and evicts its host
+// rows' translations from the SM's caches with its own device addresses.
+size_t copy_hold_limit(int smem_optin) { return (size_t)std::max(0, smem_optin - 2048); }
+size_t copy_hold_smem(const dhs_pool* p, int64_t n_items) {
+  return copy_steal(p, n_items) ? 0 : copy_hold_limit(p->smem_optin);
 }
 
 // Pages small enough for the page-move kernel's 32-bit chunk arithmetic.
@@ -581,6 +608,7 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     p->miss_rows = (int32_t*)(m + p->layout.miss_rows);
     p->miss_slots = (int32_t*)(m + p->layout.miss_slots);
     p->miss_count = (uint32_t*)(m + p->layout.miss_count);
+    p->copy_cursor = (uint32_t*)(m + p->layout.copy_cursor);
     p->pair_status = (int32_t*)(m + p->layout.pair_status);
     p->loc_ready = (uint32_t*)(m + p->layout.loc_ready);
     p->copy_ready = (uint32_t*)(m + p->layout.copy_ready);
@@ -608,7 +636,8 @@ int dhs_pool_create(const dhs_pool_config* cfg, dhs_pool** out) {
     delete p;
     return DHS_ENOMEM;
   }
-  if (dhs::resolve_set_carveout() != cudaSuccess || dhs::hostcopy_set_carveout() != cudaSuccess ||
+  if (dhs::resolve_set_carveout() != cudaSuccess ||
+      dhs::hostcopy_set_carveout(copy_hold_limit(optin)) != cudaSuccess ||
       dhs::gather_set_carveout() != cudaSuccess || dhs::append_set_carveout() != cudaSuccess) {
     delete p;
     return DHS_ECUDA;
@@ -690,6 +719,11 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     pool->copy_pdl = (int)value;
     return DHS_OK;
   }
+  if (key == DHS_OPT_COPY_STEAL) {
+    if (value < -1 || value > 1) return DHS_EINVAL;
+    pool->copy_steal = (int)value;
+    return DHS_OK;
+  }
   if (key == DHS_OPT_MARK_POLLS) {
     if (value < -1 || value > (int64_t)dhs::kMarkPolls) return DHS_EINVAL;
     pool->mark_polls = value < 0 ? dhs::kMarkPolls : (uint32_t)value;
@@ -723,6 +757,7 @@ int dhs_get_option(dhs_pool* pool, int32_t key, int64_t* value) {
     case DHS_OPT_MARK_POLLS: *value = pool->mark_polls; return DHS_OK;
     case DHS_OPT_COPY_PDL: *value = pool->copy_pdl; return DHS_OK;
     case DHS_OPT_RESOLVE_PAIRED: *value = pool->resolve_paired; return DHS_OK;
+    case DHS_OPT_COPY_STEAL: *value = pool->copy_steal; return DHS_OK;
     default: return DHS_EINVAL;
   }
 }
@@ -1178,6 +1213,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   rcm.miss_rows = scr ? scr->miss_rows : p->miss_rows;
   rcm.miss_slots = scr ? scr->miss_slots : p->miss_slots;
   rcm.miss_count = scr ? scr->miss_count : p->miss_count;
+  rcm.copy_cursor = p->copy_cursor;
   rcm.pair_status = p->pair_status;
   rcm.status = p->status;
   rcm.T = c.tail_rows;
@@ -1205,6 +1241,7 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
   ccm.miss_rows = rcm.miss_rows;
   ccm.miss_slots = rcm.miss_slots;
   ccm.miss_count = rcm.miss_count;
+  ccm.cursor = p->copy_cursor;
   ccm.miss_off = p->miss_off;
   ccm.miss_ent = p->miss_ent;
   ccm.ent_cap = (int32_t)p->ent_cap;
@@ -1250,8 +1287,9 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
     if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, smem, paired, p->stream) !=
         cudaSuccess)
       return DHS_ECUDA;
+    ccm.steal = copy_steal(p, n) ? 1 : 0;
     if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, copy_ctas(p, n), copy_pdl(p, n),
-                             p->stream) != cudaSuccess)
+                             copy_hold_smem(p, n), p->stream) != cudaSuccess)
       return DHS_ECUDA;
   }
   return DHS_OK;

@@ -354,6 +354,7 @@ __device__ void fail_item(const ResolveCommon& c, const ResolveItem& it, int32_t
   __syncthreads();
   if (threadIdx.x == 0) {
     c.miss_count[it.pair] = 0u;  // before the marks: the host copy reads it then
+    c.copy_cursor[it.pair] = 0u;
     c.pair_status[it.pair] = code;
     publish_copy(c, it.pair, true);
     publish_loc(c, it.pair);
@@ -731,6 +732,7 @@ __global__ void __launch_bounds__(THREADS, MINB)
     // the miss count, miss lists and staging entries are written: the host
     // copy of this item may start while its locations are being written
     c.miss_count[pair] = m_miss;
+    c.copy_cursor[pair] = 0u;  // the copy's blocks claim rows from here
     publish_copy(c, pair, m_miss == 0);
   }
 

@@ -573,6 +573,13 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
  * the resolve grid and two CTAs' shared memory fits an SM, else 1024-thread
  * CTAs one per SM; 0 = always the latter; 1 = the former whenever it fits. */
 #define DHS_OPT_RESOLVE_PAIRED 10
+/* How the host copy's blocks share a launch's miss rows.  1: every item's
+ * rows are claimed four at a time through a per-item cursor, and a block
+ * whose own items are done claims the rows left in the others; 0: each block
+ * copies its own items' rows.  -1 (default) = 1 while a launch's items span at
+ * most 16 GiB of pinned rows, else 0 (past that a block reading another
+ * item's rows walks translations its SM does not hold). */
+#define DHS_OPT_COPY_STEAL 11
 int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
 /* The value in effect (DHS_OPT_FRESH_LIST: 0 or 1, the auto rule resolved
  * for the pool's current admissions).  DHS_EINVAL for an unknown key. */

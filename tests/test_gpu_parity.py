@@ -37,7 +37,8 @@ def _as_u32(t):
 
 def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
                 gather_impl=0, patch=None, early=1, union=False, fresh=None, tpc=None,
-                stage=None, polls=None, copy_pdl=None, copy_ctas=None, resolve_paired=None):
+                stage=None, polls=None, copy_pdl=None, copy_ctas=None, resolve_paired=None,
+                steal=None):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
@@ -64,6 +65,8 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
         gpu.pool.set_option(dhs.DHS_OPT_COPY_CTAS, copy_ctas)
     if resolve_paired is not None:
         gpu.pool.set_option(dhs.DHS_OPT_RESOLVE_PAIRED, resolve_paired)
+    if steal is not None:
+        gpu.pool.set_option(dhs.DHS_OPT_COPY_STEAL, steal)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
     orc = OracleRun(cfg, wl, requests=sampled, union=union)
     try:
@@ -322,6 +325,42 @@ def test_host_copy_launched_after_the_resolve_grid(cfg):
     compare_run(cfg, gather_impl=1, copy_pdl=0, fused=False)
     compare_run(cfg, gather_impl=1, copy_pdl=0, union=True)
     compare_run(cfg, gather_impl=0, copy_pdl=0)
+
+
+@pytest.mark.parametrize("cfg", SMALL + [UNION[3], REUSE5],
+                         ids=[c.name for c in SMALL] + ["v8", "reuse5"])
+def test_host_copy_block_sharing(cfg):
+    """The host copy's blocks each copying only their own items' rows
+    (DHS_OPT_COPY_STEAL 0, what launches past the translation reach do), and
+    claiming rows through the per-item cursors with blocks done with their
+    own items taking the others' rows (1; also with more blocks than items,
+    and with the copy after the resolve grid): bit-exact, fused and split,
+    both staging layouts, both gathers."""
+    items = cfg.requests * cfg.sources
+    compare_run(cfg, gather_impl=1, steal=0)
+    compare_run(cfg, gather_impl=1, steal=0, copy_pdl=0, union=True)
+    compare_run(cfg, gather_impl=0, steal=0, fused=False)
+    compare_run(cfg, gather_impl=1, steal=1, copy_ctas=3 * items + 5)
+    compare_run(cfg, gather_impl=1, steal=1, copy_pdl=0, fused=False)
+    compare_run(cfg, gather_impl=0, steal=1, union=True)
+    compare_run(cfg, gather_impl=1, steal=1, polls=0)
+
+
+def test_copy_steal_option_bounds():
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    cfg = SMALL[0]
+    run = GpuRun(cfg, Workload(cfg))
+    try:
+        h, key = run.pool.h, dhs.DHS_OPT_COPY_STEAL
+        assert run.pool.get_option(key) == -1
+        for v in (0, 1, -1):
+            assert dhs.dhs_set_option(h, key, v) == dhs.DHS_OK
+            assert run.pool.get_option(key) == v
+        assert dhs.dhs_set_option(h, key, 2) == dhs.DHS_EINVAL
+        assert dhs.dhs_set_option(h, key, -2) == dhs.DHS_EINVAL
+    finally:
+        run.close()
 
 
 @pytest.mark.parametrize("tpc", [2, 5])
