@@ -137,9 +137,12 @@ struct ResolveCommon {
 size_t resolve_smem_bytes(int w64cap, int qkcap, int B, bool uni, int selcap);
 cudaError_t resolve_set_smem_limit(size_t bytes);
 // paired: a launch of more than kResolveItemsSmall items as 512-thread CTAs
-// two per SM (the caller checks that two plans fit one SM).
+// two per SM (the caller checks that two plans fit one SM).  ctas: CTAs of
+// the grid when below n_items (each then resolves several items in turn),
+// else one per item.
 cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,
-                           int n_items, size_t smem, bool paired, cudaStream_t stream);
+                           int n_items, int ctas, size_t smem, bool paired,
+                           cudaStream_t stream);
 
 // ------------------------------------------------------------ page moves
 // Whole optional pages between the optional arena and the pinned host copy

@@ -196,6 +196,7 @@ struct dhs_pool {
   int copy_pdl = -1;            // DHS_OPT_COPY_PDL: -1 auto, 0 off, 1 on
   int resolve_paired = -1;      // DHS_OPT_RESOLVE_PAIRED: -1 auto, 0 off, 1 whenever it fits
   int copy_steal = -1;          // DHS_OPT_COPY_STEAL: -1 auto, 0 off, 1 on
+  int resolve_ctas = 0;         // DHS_OPT_RESOLVE_CTAS: 0 auto, > 0 at most that many
   int smem_per_sm = 0;          // shared memory per SM
   std::vector<uint8_t> staged_pair;  // the host copy stages this pair's misses this step
   std::vector<uint8_t> staged_item;  // per item of the step: a gather-only item whose
@@ -335,6 +336,20 @@ bool copy_steal(const dhs_pool* p, int64_t n_items) {
 // also keeps its SM to itself: it reserves all but 2 KB of the shared memory
 // a block may take, so no gather CTA lands beside it and evicts its host
 // rows' translations from the SM's caches with its own device addresses.
+// Resolve grid.  A launch of more items than SMs whose host copy overlaps it
+// (within the translation reach) runs one CTA per SM it leaves to the copy:
+// sm_count - copy blocks CTAs resolve every item, a few each in turn, all of
+// them resident from the start.  The copy grid, a programmatic dependant,
+// launches only once every resolve CTA has started, so with one CTA per
+// item its blocks waited for the second wave's CTAs to be placed and took
+// their SMs only then (C64: copying began 52 us into the step); now they
+// are placed at once and start on each item as its miss list comes out.
+int resolve_ctas(const dhs_pool* p, int64_t n_items, bool paired) {
+  if (p->resolve_ctas > 0) return (int)std::min<int64_t>(n_items, p->resolve_ctas);
+  if (paired || n_items <= p->sm_count || !copy_pdl(p, n_items)) return (int)n_items;
+  return std::max(1, p->sm_count - copy_ctas(p, n_items));
+}
+
 size_t copy_hold_limit(int smem_optin) { return (size_t)std::max(0, smem_optin - 2048); }
 size_t copy_hold_smem(const dhs_pool* p, int64_t n_items) {
   return copy_steal(p, n_items) ? 0 : copy_hold_limit(p->smem_optin);
@@ -724,6 +739,11 @@ int dhs_set_option(dhs_pool* pool, int32_t key, int64_t value) {
     pool->copy_steal = (int)value;
     return DHS_OK;
   }
+  if (key == DHS_OPT_RESOLVE_CTAS) {
+    if (value < 0 || value > (1 << 20)) return DHS_EINVAL;
+    pool->resolve_ctas = (int)value;
+    return DHS_OK;
+  }
   if (key == DHS_OPT_MARK_POLLS) {
     if (value < -1 || value > (int64_t)dhs::kMarkPolls) return DHS_EINVAL;
     pool->mark_polls = value < 0 ? dhs::kMarkPolls : (uint32_t)value;
@@ -758,6 +778,7 @@ int dhs_get_option(dhs_pool* pool, int32_t key, int64_t* value) {
     case DHS_OPT_COPY_PDL: *value = pool->copy_pdl; return DHS_OK;
     case DHS_OPT_RESOLVE_PAIRED: *value = pool->resolve_paired; return DHS_OK;
     case DHS_OPT_COPY_STEAL: *value = pool->copy_steal; return DHS_OK;
+    case DHS_OPT_RESOLVE_CTAS: *value = pool->resolve_ctas; return DHS_OK;
     default: return DHS_EINVAL;
   }
 }
@@ -1284,7 +1305,8 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
         dhs::resolve_set_smem_limit(staged) == cudaSuccess)
       rcm.selcap = (int32_t)nmax;
     const size_t smem = rcm.selcap ? staged : base;
-    if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, smem, paired, p->stream) !=
+    if (dhs::launch_resolve(rcm, p->ritems.data() + b, n, resolve_ctas(p, n, paired), smem,
+                            paired, p->stream) !=
         cudaSuccess)
       return DHS_ECUDA;
     ccm.steal = copy_steal(p, n) ? 1 : 0;

@@ -373,21 +373,14 @@ struct ResolveParams {
 // kernel parameter space holds at most 32764 bytes
 static_assert(sizeof(ResolveParams<kResolveItemsLarge>) <= 32764, "resolve item table too large");
 
-template <int MAXI, int THREADS, int MINB>
-__global__ void __launch_bounds__(THREADS, MINB)
-    resolve_kernel(const __grid_constant__ ResolveParams<MAXI> P) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ uint32_t scratch[4 * 33];
-  __shared__ uint64_t scratch64[33];
-  __shared__ int s_bad;
-
-  // Dependent launches (the host copy, then the gather) may start now: they
-  // wait for this grid's completion before reading anything it writes.
-  asm volatile("griddepcontrol.launch_dependents;");
-
+// Resolve launch item `item` with the whole CTA (every return is taken by
+// all its threads alike).
+template <int MAXI>
+__device__ __forceinline__ void resolve_one(const ResolveParams<MAXI>& P, const int item,
+                                            unsigned char* smem_raw, uint32_t* scratch,
+                                            uint64_t* scratch64, int& s_bad) {
   const ResolveCommon& c = P.c;
-  if (threadIdx.x == 0) trace_mark(c.trace, kTraceResolve, false);
-  const ResolveItem& it = P.items[blockIdx.x];
+  const ResolveItem& it = P.items[item];
   const int tid = threadIdx.x, nt = blockDim.x;
   const int B = c.B;
   const int64_t T = c.T;
@@ -407,7 +400,7 @@ __global__ void __launch_bounds__(THREADS, MINB)
   uint32_t* fill = c.fill ? c.fill + (size_t)pair * c.fill_words : nullptr;
   if (fill)
     for (int j = tid; j < c.fill_words; j += nt) fill[j] = 0u;
-  if (c.later_count && blockIdx.x == 0 && tid == 0) c.later_count[(c.gen & 1u) ^ 1u] = 0u;
+  if (c.later_count && item == 0 && tid == 0) c.later_count[(c.gen & 1u) ^ 1u] = 0u;
 
   Smem s;
   carve(c.w64cap, c.qkcap, B, c.uni != 0, c.selcap, &s, smem_raw);
@@ -822,14 +815,36 @@ __global__ void __launch_bounds__(THREADS, MINB)
   }
 }
 
+// CTA b resolves items b, b + gridDim, ... one after the other (one item per
+// CTA unless the launch asks for fewer CTAs than items).
 template <int MAXI, int THREADS, int MINB>
-cudaError_t launch_t(const ResolveCommon& c, const ResolveItem* items, int n,
+__global__ void __launch_bounds__(THREADS, MINB)
+    resolve_kernel(const __grid_constant__ ResolveParams<MAXI> P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ uint32_t scratch[4 * 33];
+  __shared__ uint64_t scratch64[33];
+  __shared__ int s_bad;
+
+  // Dependent launches (the host copy, then the gather) may start now: they
+  // wait for this grid's completion, or for an item's marks, before reading
+  // anything it writes.
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (threadIdx.x == 0) trace_mark(P.c.trace, kTraceResolve, false);
+  for (int item = blockIdx.x; item < P.c.n_items; item += gridDim.x) {
+    resolve_one(P, item, smem_raw, scratch, scratch64, s_bad);
+    __syncthreads();  // the next item reuses the shared-memory plan
+  }
+}
+
+template <int MAXI, int THREADS, int MINB>
+cudaError_t launch_t(const ResolveCommon& c, const ResolveItem* items, int n, int ctas,
                      size_t smem, cudaStream_t stream) {
   ResolveParams<MAXI> P;
   P.c = c;
   P.c.n_items = n;
   for (int i = 0; i < n; ++i) P.items[i] = items[i];
-  resolve_kernel<MAXI, THREADS, MINB><<<n, THREADS, smem, stream>>>(P);
+  const int grid = ctas > 0 && ctas < n ? ctas : n;
+  resolve_kernel<MAXI, THREADS, MINB><<<grid, THREADS, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
@@ -876,12 +891,13 @@ cudaError_t resolve_set_carveout() {
 }
 
 cudaError_t launch_resolve(const ResolveCommon& c, const ResolveItem* items,
-                           int n_items, size_t smem, bool paired, cudaStream_t stream) {
+                           int n_items, int ctas, size_t smem, bool paired,
+                           cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
   if (n_items <= kResolveItemsSmall)
-    return launch_t<DHS_RESOLVE_SMALL>(c, items, n_items, smem, stream);
-  if (paired) return launch_t<DHS_RESOLVE_PAIRED>(c, items, n_items, smem, stream);
-  return launch_t<DHS_RESOLVE_LARGE>(c, items, n_items, smem, stream);
+    return launch_t<DHS_RESOLVE_SMALL>(c, items, n_items, ctas, smem, stream);
+  if (paired) return launch_t<DHS_RESOLVE_PAIRED>(c, items, n_items, ctas, smem, stream);
+  return launch_t<DHS_RESOLVE_LARGE>(c, items, n_items, ctas, smem, stream);
 }
 
 }  // namespace dhs

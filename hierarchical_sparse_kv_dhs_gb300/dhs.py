@@ -49,6 +49,7 @@ DHS_OPT_MARK_POLLS = 8
 DHS_OPT_COPY_PDL = 9
 DHS_OPT_RESOLVE_PAIRED = 10
 DHS_OPT_COPY_STEAL = 11
+DHS_OPT_RESOLVE_CTAS = 12
 DHS_BUF_HOT, DHS_BUF_TAIL, DHS_BUF_OPT, DHS_BUF_META = range(4)
 
 _i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p

@@ -580,6 +580,12 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
  * most 16 GiB of pinned rows, else 0 (past that a block reading another
  * item's rows walks translations its SM does not hold). */
 #define DHS_OPT_COPY_STEAL 11
+/* Resolve grid: 0 (default) = automatic (one CTA per item, except that a
+ * launch of more items than SMs whose host copy overlaps the resolve kernel
+ * runs one CTA for each SM the copy's blocks leave free, each resolving
+ * several items in turn); n > 0 = at most n CTAs, each resolving items b,
+ * b + n, ... */
+#define DHS_OPT_RESOLVE_CTAS 12
 int dhs_set_option(dhs_pool *pool, int32_t key, int64_t value);
 /* The value in effect (DHS_OPT_FRESH_LIST: 0 or 1, the auto rule resolved
  * for the pool's current admissions).  DHS_EINVAL for an unknown key. */

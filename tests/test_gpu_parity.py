@@ -38,7 +38,7 @@ def _as_u32(t):
 def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
                 gather_impl=0, patch=None, early=1, union=False, fresh=None, tpc=None,
                 stage=None, polls=None, copy_pdl=None, copy_ctas=None, resolve_paired=None,
-                steal=None):
+                steal=None, resolve_ctas=None):
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     from oracle.run import OracleRun
     wl = Workload(cfg)
@@ -67,6 +67,8 @@ def compare_run(cfg: Config, sampled=None, check_all_bytes=True, fused=True,
         gpu.pool.set_option(dhs.DHS_OPT_RESOLVE_PAIRED, resolve_paired)
     if steal is not None:
         gpu.pool.set_option(dhs.DHS_OPT_COPY_STEAL, steal)
+    if resolve_ctas is not None:
+        gpu.pool.set_option(dhs.DHS_OPT_RESOLVE_CTAS, resolve_ctas)
     sampled = list(range(cfg.requests)) if sampled is None else sampled
     orc = OracleRun(cfg, wl, requests=sampled, union=union)
     try:
@@ -344,6 +346,50 @@ def test_host_copy_block_sharing(cfg):
     compare_run(cfg, gather_impl=1, steal=1, copy_pdl=0, fused=False)
     compare_run(cfg, gather_impl=0, steal=1, union=True)
     compare_run(cfg, gather_impl=1, steal=1, polls=0)
+
+
+@pytest.mark.parametrize("cfg", SMALL + [UNION[3], REUSE5],
+                         ids=[c.name for c in SMALL] + ["v8", "reuse5"])
+def test_resolve_ctas_several_items_each(cfg):
+    """Fewer resolve CTAs than items (DHS_OPT_RESOLVE_CTAS): CTA b resolves
+    items b, b + n, ... one after the other, publishing each item's marks as
+    it goes, while the host copy and the gather run beside it.  Bit-exact,
+    fused and split, both staging layouts, both copy modes."""
+    for ctas in (1, 3):
+        compare_run(cfg, gather_impl=1, resolve_ctas=ctas)
+    compare_run(cfg, gather_impl=1, resolve_ctas=2, union=True)
+    compare_run(cfg, gather_impl=0, resolve_ctas=2, fused=False)
+    compare_run(cfg, gather_impl=1, resolve_ctas=2, copy_pdl=0, steal=0)
+    compare_run(cfg, gather_impl=1, resolve_ctas=2, resolve_paired=1, polls=0)
+
+
+def test_resolve_ctas_with_failed_items():
+    """A CTA whose item fails (ERANGE, EBUDGET) goes on to its next item."""
+    cfg = TINY.scaled(name="range", tag=46, requests=2, sources=2, steps=4, residency=0.6)
+    compare_run(cfg, gather_impl=1, patch=_bad_row, resolve_ctas=1)
+    compare_run(cfg, gather_impl=1, patch=_bad_row, resolve_ctas=3, union=True)
+    cfg = TINY.scaled(name="budget", tag=47, requests=2, sources=1, hot=16, topk=64,
+                      residency=0.4, steps=4)
+    compare_run(cfg, gather_impl=1, resolve_ctas=1)
+    cfg = TINY.scaled(name="ubudget", tag=50, requests=2, sources=1, hot=16, topk=64,
+                      queries=2, verify_core=32, residency=0.0, steps=4)
+    compare_run(cfg, union=True, gather_impl=1, resolve_ctas=1)
+
+
+def test_resolve_ctas_option_bounds():
+    from hierarchical_sparse_kv_dhs_gb300 import dhs
+    from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
+    cfg = SMALL[0]
+    run = GpuRun(cfg, Workload(cfg))
+    try:
+        h, key = run.pool.h, dhs.DHS_OPT_RESOLVE_CTAS
+        assert run.pool.get_option(key) == 0
+        assert dhs.dhs_set_option(h, key, 5) == dhs.DHS_OK
+        assert run.pool.get_option(key) == 5
+        assert dhs.dhs_set_option(h, key, -1) == dhs.DHS_EINVAL
+        assert dhs.dhs_set_option(h, key, 0) == dhs.DHS_OK
+    finally:
+        run.close()
 
 
 def test_copy_steal_option_bounds():
