@@ -1,8 +1,9 @@
 """Load-step workload: admission pressure rising and draining.
 
-"Adaptive DHiSparse", Evidence (load-step on/off experiment): optional
-residency cuts host-fetched selections at low load, releases memory under
-pressure and repopulates as requests drain.  The pages give no schedule,
+"Adaptive DHiSparse", Evidence (load-step on/off experiment): with optional
+residency on, fewer selected rows come from the host while load is low; the
+optional pages give way when admissions need memory and come back once the
+extra requests have left.  The pages give no schedule,
 model or sizes for it; this recipe stands in with three phases over one
 pool whose optional capacity holds `low` requests' histories:
 

@@ -1,11 +1,11 @@
 // Append kernel: decode rows enter the mutable tail ring and are written
 // through to the pinned host copy.
 //
-// "Adaptive DHiSparse", How it works / Memory split (each request and KV
-// source has a mutable tail) and Reclamation and refill (every row is either
-// ready on the GPU or has a host copy); Limits: rows generated during
-// decoding always follow hot-cache rules, so once a decode row leaves the
-// tail it is found only through the hot cache or the host copy.  Row L+j of
+// "Adaptive DHiSparse", How it works / Memory split (a mutable tail per
+// request and KV source) and Reclamation and refill (no row is left without
+// a copy: it is ready on the GPU or backed on the host); Limits (decode rows
+// are served the hot-cache way), so once a decode row leaves the tail it is
+// found only through the hot cache or the host copy.  Row L+j of
 // a pair goes to tail slot (L+j) mod T and to host row L+j.  A window source
 // ("Speculative state": a drafter retains only the rows its window covers,
 // stored as a ring) has no host copy: its rows go to the ring only.

@@ -1,18 +1,23 @@
-// Host-copy kernel: step 3 of resolution ("a copy from pinned host memory
-// into the hot cache"; "Adaptive DHiSparse", How it works / Resolution).
+// Host-copy kernel: step 3 of resolution, the fetch of a row that neither
+// the tail, the resident optional pages nor the hot cache holds, from its
+// pinned host copy into a hot-cache slot ("Adaptive DHiSparse", How it
+// works / Resolution).
 //
 // Reads the missing rows straight out of mapped pinned host memory over
-// NVLink-C2C into their victim hot-cache slots.  The pages note that the
-// copy kernel scales from 4 to 32 thread blocks with batch size; on GB300
-// fewer than about 16 blocks leave the host link idle, so the grid is at
-// least the upper end, 32 blocks, whatever the batch.  The pool grows it
-// further when the items' pinned regions are large (each block's share
-// kept within about 1 GiB, so that the translations of its rows stay cached
-// near its SM).  Past 16 GiB of pinned rows it launches the copy after the
-// resolve grid, so that block b lands on the same SM every step, unless every
-// copy block finds an SM that the resolve grid leaves free.  Each warp keeps up
-// to four 1152-byte rows in flight (12 x 16-byte loads per lane) so the link
-// sees enough outstanding requests to cover its latency.
+// NVLink-C2C into their victim hot-cache slots.  The pages size the copy
+// kernel's grid between 4 and 32 blocks by batch size; on GB300 fewer than
+// about 16 blocks leave the host link idle, so the grid is at least the
+// upper end, 32 blocks, whatever the batch.  The pool grows it further when
+// the items' pinned regions are large (each block's share kept within about
+// 1 GiB, so that the translations of its rows stay cached near its SM).
+// Within 16 GiB of pinned rows the blocks claim rows through per-item
+// cursors and take each other's leftovers.  Past that each block keeps to
+// its own items and reserves its SM's shared memory, so that no gather CTA
+// lands beside it; the copy then launches after the resolve grid, so that
+// block b lands on the same SM every step, unless every copy block finds an
+// SM that the resolve grid leaves free.  Each warp keeps up to four
+// 1152-byte rows in flight (12 x 16-byte loads per lane) so the link sees
+// enough outstanding requests to cover its latency.
 #include <algorithm>
 
 #include "dhs_internal.h"

@@ -2,10 +2,11 @@
 //
 // "Adaptive DHiSparse: Speculative Decoding over a Load-Adaptive KV
 // Hierarchy", How it works:
-//   Memory split -- per (request, KV source) a fixed hot cache of B rows,
-//     a mutable tail and metadata (never lent); complete imported pages in
-//     reclaimable optional capacity under required + optional + admission
-//     reserve <= pool capacity.  Required memory is laid out per request
+//   Memory split -- every (request, KV source) pair owns B hot-cache rows, its
+//     tail ring and its metadata, none of which is lent out; whole pages of
+//     imported history may occupy optional capacity that can be taken back,
+//     as long as required, optional and the admission reserve together fit
+//     the pool.  Required memory is laid out per request
 //     slot up front, so the rule is checked on the optional arena.
 //   Resident-first admission -- resident pages take optional slots at
 //     admission (lowest free slot first, pages ascending).

@@ -1,11 +1,12 @@
 // Resolve kernel: one CTA per (request, KV source) item of a decode step.
 //
 // "Adaptive DHiSparse: Speculative Decoding over a Load-Adaptive KV
-// Hierarchy", How it works / Resolution: the resolver checks, in order,
-// (1) the tail and the ready optional-history map, (2) a scan of the hot
-// cache bounded by B with LRU replacement, (3) a copy from pinned host memory
-// into the hot cache, stopping once every selected row is found.
-// Speculative state: verification queries share missing-row retrieval.
+// Hierarchy", How it works / Resolution: a selected row is looked up first
+// in the tail ring and the map of GPU-resident optional pages, then among
+// the B hot-cache tags (least-recently-used slots give way), and only then
+// fetched from its pinned host copy into a hot-cache slot; each row stops at
+// the first place that holds it.  Speculative state: the queries of one
+// verify block fetch each missing row once between them.
 //
 // GB300 design.  Everything for one item lives in shared memory:
 //   * the union of the Q verify queries is a bitmap over [0, L) (64 rows per

@@ -4,11 +4,12 @@
  *
  * The operation is the per-decode-step path of "Adaptive DHiSparse:
  * Speculative Decoding over a Load-Adaptive KV Hierarchy" (How it works):
- * each request's top-k selected KV rows are resolved through three ordered
- * places -- (1) the mutable tail and the ready optional-history page map,
- * (2) a hot-cache tag scan bounded by B with LRU replacement, (3) a copy from
- * pinned host memory into the victim hot-cache slot -- and the selected rows
- * are gathered into a contiguous staging buffer for sparse attention.
+ * each request's top-k selected KV rows are located, each at the first of
+ * three places that holds it -- (1) the tail ring of recent rows or an
+ * imported page resident on the GPU, (2) one of the B hot-cache slots, found
+ * by their tags, least recently used slots making room, (3) otherwise its
+ * pinned host copy, fetched into a victim hot-cache slot -- and the selected
+ * rows are gathered into a contiguous staging buffer for sparse attention.
  *
  * Conventions for every call:
  *   - Return value: DHS_OK (0) or a negative DHS_E* code.  No call throws,
@@ -96,9 +97,9 @@ enum {
 typedef struct dhs_pool dhs_pool;
 
 /*
- * Pool geometry ("Memory split": every request and KV source has a fixed hot
- * cache of B rows, a mutable tail and metadata that are never lent; complete
- * pages of imported history may sit in reclaimable optional capacity).
+ * Pool geometry ("Memory split": every request/KV-source pair owns B hot-cache
+ * rows, its tail ring and its metadata, none of them lent out; whole pages of
+ * imported history may occupy optional capacity that can be taken back).
  */
 typedef struct {
   int32_t max_requests;          /* R: request slots 0..R-1 */
@@ -188,8 +189,8 @@ int dhs_release(dhs_pool *pool, int32_t req);
 
 /*
  * Resident-first admission of rows that are on the device ("Resident-first
- * admission": a new request keeps its imported history on device and defers
- * host backup while HBM is spare).  dev_rows: device memory, rows
+ * admission": while HBM has room, an arriving request's imported history
+ * stays on the GPU and its host backup is put off).  dev_rows: device memory, rows
  * [0, n_rows) of row_bytes each (e.g. the prefill's output), read only by
  * copies this call enqueues on the pool's stream (reuse it after the stream
  * has passed them).  host_rows: as for dhs_admit, but its imported rows need
@@ -235,9 +236,10 @@ int dhs_admit_window(dhs_pool *pool, int32_t req, int32_t src, const void *dev_r
  * Deferred host backup: enqueue the device-to-host copies of at most
  * max_pages pages in backup order; *done = pages backed up.  dhs_reclaim
  * backs up a reclaimed page that is still pending before freeing its slot
- * ("pages are freed only after host backup completes and earlier readers
- * finish"): the copy is ordered on the pool's stream after every earlier
- * reader and before any later copy into the slot.  Released requests' pages
+ * (Reclamation and refill: a page's slot is reused only once its host backup
+ * is done and its earlier readers have finished): the copy is ordered on
+ * the pool's stream after every earlier reader and before any later copy
+ * into the slot.  Released requests' pages
  * need no backup.  Errors: DHS_EINVAL, DHS_ECUDA.
  */
 int dhs_backup(dhs_pool *pool, int64_t max_pages, int64_t *done);
@@ -284,11 +286,11 @@ typedef struct {
 } dhs_append_item;
 
 /*
- * Append decode rows (Limits: rows generated during decoding always follow
- * hot-cache rules).  Row L+j of (req, src) goes to tail slot (L+j) mod T and
- * is written through to the pinned host copy, so every row that leaves the
- * tail keeps a host copy ("every row is either ready on the GPU or has a
- * host copy").  L grows by count.  (req, src) pairs must be distinct.
+ * Append decode rows (Limits: decode rows are served the hot-cache way).
+ * Row L+j of (req, src) goes to tail slot (L+j) mod T and is written through
+ * to the pinned host copy, so every row that leaves the tail keeps a host
+ * copy (Reclamation and refill: no row is without a copy on the GPU or on
+ * the host).  L grows by count.  (req, src) pairs must be distinct.
  * Errors: DHS_EINVAL (count > T, L + count > max_rows_per_request, null
  * rows), DHS_ESTATE, DHS_ECUDA.
  */
@@ -296,7 +298,7 @@ int dhs_append(dhs_pool *pool, const dhs_append_item *items, int32_t n_items);
 
 #define DHS_ITEM_GATHER_ONLY 1u /* skip resolution: gather loc_dev as given */
 /* Union verification staging ("Memory split": verification staging;
- * "Speculative state": verification queries share missing-row retrieval):
+ * "Speculative state": a verify block's queries fetch a missing row once):
  * each distinct row of the verify block is staged once.  Resolution writes
  *   loc_dev[u]   u < U: location of the u-th distinct selected row, in
  *                ascending row order; DHS_END_LOC for U <= u < Q*k;
@@ -320,8 +322,9 @@ int dhs_append(dhs_pool *pool, const dhs_append_item *items, int32_t n_items);
  *   staging_dev  [Q][k][row_bytes] device gather target (gather only)
  *   counters_dev uint32 [DHS_NUM_COUNTERS] device or NULL
  *   index_dev    int32 [Q][k] device (DHS_ITEM_UNION only, else ignored)
- * A DHS_ITEM_GATHER_ONLY item is a Reuse layer ("Model-specific reuse":
- * Reuse layers inherit the prior location vector): it is not resolved and
+ * A DHS_ITEM_GATHER_ONLY item is a Reuse layer ("Model-specific reuse": a
+ * Reuse layer takes over the location vector of the layer before it): it is
+ * not resolved and
  * gathers loc_dev as given (req/src unused).
  */
 typedef struct {
@@ -346,8 +349,8 @@ typedef struct {
 
 /*
  * "Resolution" for every item without DHS_ITEM_GATHER_ONLY.  Per item, over
- * the union of its Q verify queries ("Speculative state": verification
- * queries share missing-row retrieval): each distinct row resolves in the
+ * the union of its Q verify queries ("Speculative state": the queries of a
+ * verify block fetch each missing row once): each distinct row resolves in the
  * first place that holds it -- tail (rows >= L-T, checked first), the ready
  * optional map (complete imported pages), the hot cache (B tags; a hit
  * refreshes the slot's stamp to `step`) -- and the remaining rows, in
@@ -514,8 +517,8 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
                    uint32_t *stamps, int32_t *page_slot, int64_t *info);
 
 /* Tunables (performance only; results do not depend on them). */
-/* Host-copy CTAs; 0 = automatic.  The pages scale the copy kernel from 4 to
- * 32 thread blocks with batch size; on GB300 fewer than about 16 blocks
+/* Host-copy CTAs; 0 = automatic.  The pages size the copy kernel's grid
+ * between 4 and 32 blocks by batch size; on GB300 fewer than about 16 blocks
  * leave the host link idle (miss-heavy workload: 4 blocks 78 GB/s, 16 188,
  * 32 198 of a 211 GB/s pinned copy), so the automatic grid is never below
  * 32.  It grows past 32 until each block's items span at most 1 GiB of

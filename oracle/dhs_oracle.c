@@ -10,22 +10,25 @@
  * It is a plain, slow, literal statement of what "Adaptive DHiSparse:
  * Speculative Decoding over a Load-Adaptive KV Hierarchy" describes under
  * "How it works":
- *   - Memory split: per (request, KV source) a fixed hot cache of B rows, a
- *     mutable tail and metadata, never lent; complete pages of imported
- *     history may sit in reclaimable optional capacity, subject to
- *     required + optional + admission reserve <= pool capacity.
+ *   - Memory split: every (request, KV source) pair owns B hot-cache rows, its
+ *     tail ring and its metadata, none of them lent out; whole pages of
+ *     imported history may occupy optional capacity that can be taken back,
+ *     as long as required, optional and the admission reserve together fit
+ *     the pool.
  *   - Reclamation: whole requests' optional pages are taken in reclaim order
  *     until the deficit is covered, otherwise the admission waits.
- *   - Resolution: three ordered steps that stop once every selected row is
- *     found -- (1) the tail and the ready optional-history map, (2) a scan of
- *     the hot cache bounded by B with LRU replacement, (3) a copy from pinned
- *     host memory into the hot cache.
- *   - Speculative state: verification queries share missing-row retrieval;
- *     a drafter retains only the rows its window covers, stored as a ring (a
- *     window source: the tail ring is its only storage).
- *   - Model-specific reuse: Reuse layers inherit the prior location vector
- *     (here: a gather of an existing location vector, no resolution).
- *   - Limits: rows generated during decoding always follow hot-cache rules.
+ *   - Resolution: each selected row is looked for in three places in turn,
+ *     stopping at the first that holds it -- (1) the tail ring, then the map
+ *     of optional pages resident on the GPU; (2) the B hot-cache tags, the
+ *     least recently used slots giving way; (3) its pinned host copy,
+ *     fetched into the hot cache.
+ *   - Speculative state: the queries of a verify block fetch a missing row
+ *     once between them; a drafter retains only the rows its window covers,
+ *     stored as a ring (a window source: the tail ring is its only storage).
+ *   - Model-specific reuse: a Reuse layer takes over the location vector of
+ *     the layer before it (here: a gather of an existing location vector, no
+ *     resolution).
+ *   - Limits: decode rows are served the hot-cache way.
  *
  * Readings where the pages are silent (each restated beside the code):
  *   tail = the most recent T rows [L-T, L) held in a ring at row mod T,
@@ -236,8 +239,8 @@ int orc_release(orc_pool *p, int32_t r);
 
 /*
  * Resident-first admission of rows that are on the device ("Resident-first
- * admission": a new request keeps its imported history on device and
- * defers host backup while HBM is spare).  `rows` (N rows, NULL = metadata
+ * admission": while HBM has room, an arriving request's imported history
+ * stays on the GPU and its host backup is put off).  `rows` (N rows, NULL = metadata
  * only) are the imported rows as the device holds them.  Pages are chosen
  * and the capacity rule applied exactly as in orc_admit.  Every complete
  * page marked in `mask` becomes a ready optional page whose host backup is
@@ -566,7 +569,7 @@ int orc_resolve(orc_pool *p, uint32_t step, int32_t r, int32_t s, int32_t Q,
       if ((l1 >> 30) == ORC_TIER_TAIL) c_tail++; else c_opt++;
       continue;
     }
-    /* step 2: scan of the hot cache, bounded by B */
+    /* step 2: the B hot-cache tags, in slot order */
     int64_t j = 0;
     while (j < B && src->tags[j] != row) ++j;
     if (j < B) {
@@ -625,9 +628,9 @@ int orc_resolve(orc_pool *p, uint32_t step, int32_t r, int32_t s, int32_t Q,
 
 /*
  * Union verification staging ("Memory split": verification staging;
- * "Speculative state": verification queries share missing-row
- * retrieval).  The same resolution as orc_resolve, laid out so that each
- * distinct row of the verify block is staged once:
+ * "Speculative state": a verify block's queries fetch a missing row once).
+ * The same resolution as orc_resolve, laid out so that each distinct row of
+ * the verify block is staged once:
  *   loc[u]     u < U: location of the u-th distinct selected row, ascending
  *              row order; loc[u] = ORC_END_LOC for U <= u < Q*k;
  *   index[e]   position of sel[e] among those U rows.
@@ -764,7 +767,7 @@ int orc_check(const orc_pool *p, int32_t r, int32_t s) {
     if (sl >= p->capacity || p->slot_pair[sl] != pair || p->slot_page[sl] != q)
       return 6;
   }
-  /* every row is either ready on the GPU or has a host copy */
+  /* no row without a copy: each page is ready on the GPU or backed on the host */
   for (int64_t q = 0; q < p->pages_max; ++q) {
     if (src->page_slot[q] < 0 && !src->backed[q]) return 7;
     if (src->backed[q] && src->pend[q]) return 8;

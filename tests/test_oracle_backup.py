@@ -4,8 +4,9 @@ is freed, and bounded round-robin refill ("Adaptive DHiSparse", How it
 works / Resident-first admission; Reclamation and refill).
 
   * random sequences of every admission, decode and resolution call on tiny
-    pools: after each call the invariant "every row is either ready on the
-    GPU or has a host copy" and the pool's bookkeeping hold, and every
+    pools: after each call the invariant that no row is without a copy
+    (ready on the GPU or backed on the host) and the pool's bookkeeping
+    hold, and every
     gathered row is the generator's payload of its row (a page freed
     without its backup, or refilled from a missing host copy, breaks it);
   * refill never takes the admission reserve;

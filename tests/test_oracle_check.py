@@ -14,8 +14,8 @@ violation must be reported by exactly the check that covers it:
   8  a page both backed up and still pending backup
   9  a page counted as backed up whose host rows differ from the device's
 
-Checks 7 and 9 are the pages' invariant that every row is either ready on the
-GPU or has a host copy ("Adaptive DHiSparse", How it works / Reclamation and
+Checks 7 and 9 are the pages' invariant that no row is without a copy, on
+the GPU or on the host ("Adaptive DHiSparse", How it works / Reclamation and
 refill; Resident-first admission defers the host backup, so a page can be
 ready without one).  Checks 1-4 restate the hot cache of "Resolution" (B
 slots, LRU stamps, empty slots tag -1 stamp 0); 5-6 restate "Memory split"

@@ -1,7 +1,8 @@
 """The load-step experiment on the oracle: its shape ("Adaptive
-DHiSparse", Evidence: optional residency cuts host-fetched selections at
-low load, releases memory under pressure and repopulates as requests
-drain), and the machinery's invariants at every step."""
+DHiSparse", Evidence: with optional residency on, fewer selected rows come
+from the host while load is low; the optional pages give way under memory
+pressure and come back once the extra requests have left), and the
+machinery's invariants at every step."""
 import numpy as np
 
 from dhs_workload.loadstep import LOADSTEP_SMALL, phase_fractions, run

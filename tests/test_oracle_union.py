@@ -83,8 +83,8 @@ def test_union_error_leaves_empty_list(oracle_lib):
 
 
 def test_verify_block_fetches_each_missing_row_once(oracle_lib):
-    """Verification queries share missing-row retrieval ("Adaptive
-    DHiSparse", How it works / Speculative state).  From the pool's state
+    """A verify block's queries fetch each missing row once between them
+    ("Adaptive DHiSparse", How it works / Speculative state).  From the pool's state
     before each step (tail window, ready pages, hot tags), the rows no tier
     holds are the block's distinct selected rows minus those: the host
     fetches must equal their count -- once per row however many queries
