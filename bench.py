@@ -583,7 +583,8 @@ def set_pool_options(run, args):
     if args.copy_ctas:
         run.pool.set_option(dhs.DHS_OPT_COPY_CTAS, args.copy_ctas)
     run.pool.set_option(dhs.DHS_OPT_COPY_PDL, args.copy_pdl)
-    run.pool.set_option(dhs.DHS_OPT_COPY_STEAL, args.copy_steal)
+    if args.copy_steal != -1:
+        run.pool.set_option(dhs.DHS_OPT_COPY_STEAL, args.copy_steal)
     run.pool.set_option(dhs.DHS_OPT_RESOLVE_PAIRED, args.resolve_paired)
     run.pool.set_option(dhs.DHS_OPT_GATHER_IMPL, args.gather_impl)
     run.pool.set_option(dhs.DHS_OPT_EARLY, args.early)
