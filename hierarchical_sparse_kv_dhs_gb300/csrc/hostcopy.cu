@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(kCopyThreads)
     }
   };
   int next = blockIdx.x;
+  bool had_rows = false;  // block-uniform: some owned item had misses
   for (;;) {
     if (tid == 0) {  // the next batch: owned items whose miss lists are out
       int n = 0, j = next, need_wait = 0;
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(kCopyThreads)
       trace_mark(c.trace, kTraceCopy, false);  // copying starts
       traced = true;
     }
+    had_rows = had_rows || s_pre[n] != 0;
     if constexpr (kSteal) {
       for (int b = 0; b < n; ++b) {
         const uint32_t cnt = s_pre[b + 1] - s_pre[b];
@@ -335,8 +337,11 @@ __global__ void __launch_bounds__(kCopyThreads)
   }
   // c.steal: the other items' unclaimed rows, the next CTA's items first: the
   // lanes test 32 items at a time with relaxed reads (a hint), then the warp
-  // acquires each candidate's mark (every lane its own acquire) and drains it
-  for (int base = 1; kSteal && base < c.n_items; base += 32) {
+  // acquires each candidate's mark (every lane its own acquire) and drains it.
+  // A block whose own items had no misses leaves at once instead: in a launch
+  // with few or no misses (C8 has none) the gather wants its SM back, and the
+  // scan would hold it about a microsecond longer for nothing.
+  for (int base = 1; kSteal && had_rows && base < c.n_items; base += 32) {
     const int k = base + lane;
     int j = 0;
     bool cand = false;
