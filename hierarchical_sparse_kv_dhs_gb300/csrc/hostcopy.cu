@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(kCopyThreads)
   // 0's atomic, its result taken only after the current rows are copied
   auto drain = [&](int j, uint32_t cnt) {
     uint32_t* cur_p = c.cursor + P.items[j].pair;
-    uint32_t cur = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(cur_p, (uint32_t)kRowsPerWarp) : 0u, 0);
+    const uint32_t first = lane == 0 ? atomicAdd(cur_p, (uint32_t)kRowsPerWarp) : 0u;
+    uint32_t cur = __shfl_sync(0xffffffffu, first, 0);
     while (cur < cnt) {
       const uint32_t pend = lane == 0 ? atomicAdd(cur_p, (uint32_t)kRowsPerWarp) : 0u;
       int itm[kRowsPerWarp];

@@ -279,12 +279,14 @@ int copy_ctas(const dhs_pool* p, int64_t n_items) {
   return (int)std::max<int64_t>(32, std::min(want, cap));
 }
 
-// Resolve launches of more items than SMs take two waves of 1024-thread CTAs,
-// one per SM.  When the host copy waits for the whole resolve grid anyway
-// (copy_pdl false) and two CTAs' shared-memory plans fit one SM, 512-thread
-// CTAs two per SM resolve every item in one wave instead, and the copy and
-// the gather behind it start that much earlier.  With the copy overlapped
-// (C64) the two waves stay: the first wave's items reach the host link sooner.
+// Resolve launches of more items than SMs would take two waves of 1024-thread
+// CTAs, one per SM.  When the host copy waits for the whole resolve grid
+// anyway (copy_pdl false) and two CTAs' shared-memory plans fit one SM,
+// 512-thread CTAs two per SM resolve every item in one wave instead, and the
+// copy and the gather behind it start that much earlier.  With the copy
+// overlapped (C64) the grid is instead one 1024-thread CTA per SM the copy
+// leaves free (resolve_ctas): two CTAs per SM would spread over every SM and
+// leave the copy's blocks none.
 bool copy_pdl(const dhs_pool* p, int64_t n_items);
 bool resolve_paired(const dhs_pool* p, int64_t n_items, size_t plan) {
   if (p->resolve_paired == 0 || n_items <= dhs::kResolveItemsSmall) return false;
@@ -300,11 +302,11 @@ bool resolve_paired(const dhs_pool* p, int64_t n_items, size_t plan) {
 // GB, 205 GB/s).  Past that it still pays when every copy block finds an SM
 // that the resolve grid leaves free (a copy block holds a whole SM's
 // registers, so it never shares an SM with a resolve CTA): the blocks are
-// then all placed at launch, on the same SMs every step.  Otherwise blocks placed on
-// whichever SMs the resolve grid frees land on different SMs from step to
-// step and re-walk their translations, so the copy launches after the
-// resolve grid, onto an idle GPU, where block b lands on the same SM every
-// step (copy alone, pinned span 57 GB, 96 items and 96 blocks: 44-53 GB/s
+// then all placed at launch, on the same SMs every step.  Otherwise blocks
+// placed on whichever SMs the resolve grid frees land on different SMs from
+// step to step and re-walk their translations, so the copy launches after
+// the resolve grid, onto an idle GPU, where block b lands on the same SM
+// every step (copy alone, pinned span 57 GB, 96 items and 96 blocks: 44-53 GB/s
 // with the early start, 149 without it; 30 GB, 256 items and 32 blocks:
 // 58-84 against 182).  One layer of the same 57 GB pool, 32 items beside 32
 // blocks, runs faster overlapped, and much faster when other streams keep
@@ -325,18 +327,14 @@ bool copy_pdl(const dhs_pool* p, int64_t n_items) {
 // Past that a block that takes another item's rows reads from a region whose
 // translations its SM does not hold, and the claims themselves cost an
 // atomic round trip per item and warp where items have few misses each
-// (C128: about 57 rows an item; its copy span 120 us against 94), so each block
-// keeps to its own items there.
+// (C128: about 57 rows an item; its copy span 120 us against 94), so each
+// block keeps to its own items there.
 bool copy_steal(const dhs_pool* p, int64_t n_items) {
   if (p->copy_steal >= 0) return p->copy_steal == 1;
   const int64_t item_span = p->cfg.max_rows_per_request * (int64_t)p->cfg.row_bytes;
   return n_items * item_span <= (int64_t(16) << 30);
 }
 
-// Where each block keeps to its own items (past the translation reach), it
-// also keeps its SM to itself: it reserves all but 2 KB of the shared memory
-// a block may take, so no gather CTA lands beside it and evicts its host
-// rows' translations from the SM's caches with its own device addresses.
 // Resolve grid.  A launch of more items than SMs whose host copy overlaps it
 // (within the translation reach) runs one CTA per SM it leaves to the copy:
 // sm_count - copy blocks CTAs resolve every item, a few each in turn, all of
@@ -351,6 +349,10 @@ int resolve_ctas(const dhs_pool* p, int64_t n_items, bool paired) {
   return std::max(1, p->sm_count - copy_ctas(p, n_items));
 }
 
+// Where each block keeps to its own items (past the translation reach), it
+// also keeps its SM to itself: it reserves all but 2 KB of the shared memory
+// a block may take, so no gather CTA lands beside it and evicts its host
+// rows' translations from the SM's caches with its own device addresses.
 size_t copy_hold_limit(int smem_optin) { return (size_t)std::max(0, smem_optin - 2048); }
 size_t copy_hold_smem(const dhs_pool* p, int64_t n_items) {
   return copy_steal(p, n_items) ? 0 : copy_hold_limit(p->smem_optin);
