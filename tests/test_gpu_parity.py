@@ -336,8 +336,8 @@ def test_host_copy_block_sharing(cfg):
     (DHS_OPT_COPY_STEAL 0, what launches past the translation reach do), and
     claiming rows through the per-item cursors with blocks done with their
     own items taking the others' rows (1; also with more blocks than items,
-    and with the copy after the resolve grid): bit-exact, fused and split,
-    both staging layouts, both gathers."""
+    and with the copy after the resolve grid): bit-exact, fused, split and
+    side-stream prefetch, both staging layouts, both gathers."""
     items = cfg.requests * cfg.sources
     compare_run(cfg, gather_impl=1, steal=0)
     compare_run(cfg, gather_impl=1, steal=0, copy_pdl=0, union=True)
@@ -346,6 +346,8 @@ def test_host_copy_block_sharing(cfg):
     compare_run(cfg, gather_impl=1, steal=1, copy_pdl=0, fused=False)
     compare_run(cfg, gather_impl=0, steal=1, union=True)
     compare_run(cfg, gather_impl=1, steal=1, polls=0)
+    compare_run(cfg, fused="prefetch", gather_impl=1, steal=1)
+    compare_run(cfg, fused="prefetch", gather_impl=1, steal=0)
 
 
 @pytest.mark.parametrize("cfg", SMALL + [UNION[3], REUSE5],
@@ -354,13 +356,15 @@ def test_resolve_ctas_several_items_each(cfg):
     """Fewer resolve CTAs than items (DHS_OPT_RESOLVE_CTAS): CTA b resolves
     items b, b + n, ... one after the other, publishing each item's marks as
     it goes, while the host copy and the gather run beside it.  Bit-exact,
-    fused and split, both staging layouts, both copy modes."""
+    fused, split and side-stream prefetch, both staging layouts, both copy
+    modes."""
     for ctas in (1, 3):
         compare_run(cfg, gather_impl=1, resolve_ctas=ctas)
     compare_run(cfg, gather_impl=1, resolve_ctas=2, union=True)
     compare_run(cfg, gather_impl=0, resolve_ctas=2, fused=False)
     compare_run(cfg, gather_impl=1, resolve_ctas=2, copy_pdl=0, steal=0)
     compare_run(cfg, gather_impl=1, resolve_ctas=2, resolve_paired=1, polls=0)
+    compare_run(cfg, fused="prefetch", gather_impl=1, resolve_ctas=2)
 
 
 def test_resolve_ctas_with_failed_items():
