@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kCopyThreads)
         uint8_t* stg[kRowsPerWarp];
         const int32_t* ents[kRowsPerWarp];
         int32_t e0[kRowsPerWarp], e1[kRowsPerWarp], itm[kRowsPerWarp];
-  #pragma unroll
+#pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) {
           const uint32_t i = base + r;
           src[r] = nullptr;
@@ -286,16 +286,16 @@ __global__ void __launch_bounds__(kCopyThreads)
         }
         if (kSmallRow) {
           uint4 v[kRowsPerWarp][kChunksPerLane];
-  #pragma unroll
+#pragma unroll
           for (int r = 0; r < kRowsPerWarp; ++r)
-  #pragma unroll
+#pragma unroll
             for (int q = 0; q < kChunksPerLane; ++q) {
               const int ch = lane + 32 * q;
               if (src[r] && ch < cpr) v[r][q] = ld_sys(src[r] + ch * 16);
             }
-  #pragma unroll
+#pragma unroll
           for (int r = 0; r < kRowsPerWarp; ++r) {
-  #pragma unroll
+#pragma unroll
             for (int q = 0; q < kChunksPerLane; ++q) {
               const int ch = lane + 32 * q;
               if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kCopyThreads)
               const size_t eo = (size_t)ents[r][k] * rb;
               for (int j = -1; j < ns; ++j) {
                 uint8_t* to = (j < 0 ? stg[r] : P.items[itm[r]].share[j]) + eo;
-  #pragma unroll
+#pragma unroll
                 for (int q = 0; q < kChunksPerLane; ++q) {
                   const int ch = lane + 32 * q;
                   if (ch < cpr) *reinterpret_cast<uint4*>(to + ch * 16) = v[r][q];
