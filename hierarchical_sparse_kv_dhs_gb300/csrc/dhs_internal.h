@@ -30,6 +30,9 @@ constexpr uint32_t kMarkPolls = 1u << 20;
 constexpr uint32_t kSeqMask = 0x1FFFFFFFu;
 // copy_ready mark bit: the item has no misses, so its copy reads nothing of it
 constexpr uint32_t kMarkNoMiss = 0x20000000u;
+// copy_ready mark bit: the miss count and lists are written, the staging
+// entries not yet (a second store clears the bit once they are)
+constexpr uint32_t kMarkEntriesPending = 0x40000000u;
 
 // Optional timeline (DHS_OPT_TRACE): per kernel kind, the earliest CTA start
 // and the latest CTA end in %globaltimer nanoseconds.

@@ -52,42 +52,33 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
   return v;
 }
 
-// Copy up to kRowsPerWarp miss rows, row r being miss mi[r] of the launch's
-// item itm[r] (itm[r] < 0: none): one warp of the claiming copy.  Each row goes to its victim hot
-// slot and, for items whose host copy stages, to its staging entries
-// (miss_off / miss_ent) in the item's staging and in that of the gather-only
-// items sharing its locations.
-template <bool kSmallRow, int MAXI>
-__device__ __forceinline__ void copy_rows(const CopyParams<MAXI>& P,
-                                          const int (&itm)[kRowsPerWarp],
-                                          const uint32_t (&mi)[kRowsPerWarp], int lane) {
+// Copy misses [r0, r1) (at most kRowsPerWarp) of one item: one warp of the
+// claiming copy.  Each row goes to its victim hot slot and, for items whose
+// host copy stages, to its staging entries (miss_off / miss_ent) in the
+// item's staging and in that of the gather-only items sharing its
+// locations.  wait_entries() returns once those entries are written; the
+// rows' host reads and hot-slot writes go ahead of it.
+template <bool kSmallRow, int MAXI, typename WaitEntries>
+__device__ __forceinline__ void copy_rows(const CopyParams<MAXI>& P, const CopyItem& it,
+                                          uint32_t r0, uint32_t r1, int lane,
+                                          WaitEntries&& wait_entries) {
   const CopyCommon& c = P.c;
   const int rb = c.row_bytes, cpr = rb >> 4;
+  const size_t base = (size_t)it.pair * c.Mcap;
   const uint8_t* src[kRowsPerWarp];
   uint8_t* dst[kRowsPerWarp];
-  const int32_t* ents[kRowsPerWarp];
-  int32_t e0[kRowsPerWarp], e1[kRowsPerWarp];
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r) {
+    const uint32_t i = r0 + r;
     src[r] = nullptr;
     dst[r] = nullptr;
-    ents[r] = nullptr;
-    e0[r] = e1[r] = 0;
-    if (itm[r] >= 0) {
-      const CopyItem& it = P.items[itm[r]];
-      const size_t off = (size_t)it.pair * c.Mcap + mi[r];
-      const int32_t row = c.miss_rows[off];
-      const int32_t slot = c.miss_slots[off];
-      src[r] = it.host + (size_t)row * rb;
-      dst[r] = c.hot + ((size_t)it.pair * c.B + slot) * rb;
-      if (it.staging) {
-        const int32_t* mo = c.miss_off + (size_t)it.pair * (c.Mcap + 1);
-        ents[r] = c.miss_ent + (size_t)it.pair * c.ent_cap;
-        e0[r] = mo[mi[r]];
-        e1[r] = mo[mi[r] + 1];
-      }
+    if (i < r1) {
+      src[r] = it.host + (size_t)c.miss_rows[base + i] * rb;
+      dst[r] = c.hot + ((size_t)it.pair * c.B + c.miss_slots[base + i]) * rb;
     }
   }
+  const int32_t* mo = c.miss_off + (size_t)it.pair * (c.Mcap + 1);
+  const int32_t* ents = c.miss_ent + (size_t)it.pair * c.ent_cap;
   if (kSmallRow) {
     uint4 v[kRowsPerWarp][kChunksPerLane];
 #pragma unroll
@@ -98,16 +89,20 @@ __device__ __forceinline__ void copy_rows(const CopyParams<MAXI>& P,
         if (src[r] && ch < cpr) v[r][q] = ld_sys(src[r] + ch * 16);
       }
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
+    for (int r = 0; r < kRowsPerWarp; ++r)
 #pragma unroll
       for (int q = 0; q < kChunksPerLane; ++q) {
         const int ch = lane + 32 * q;
         if (dst[r] && ch < cpr) *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v[r][q];
       }
-      if (e0[r] == e1[r]) continue;
-      const CopyItem& it = P.items[itm[r]];
-      for (int k = e0[r]; k < e1[r]; ++k) {
-        const size_t eo = (size_t)ents[r][k] * rb;
+    if (!it.staging) return;
+    wait_entries();
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      if (!src[r]) continue;
+      const uint32_t i = r0 + r;
+      for (int k = mo[i]; k < mo[i + 1]; ++k) {
+        const size_t eo = (size_t)ents[k] * rb;
         for (int j = -1; j < it.nshare; ++j) {
           uint8_t* to = (j < 0 ? it.staging : it.share[j]) + eo;
 #pragma unroll
@@ -119,14 +114,16 @@ __device__ __forceinline__ void copy_rows(const CopyParams<MAXI>& P,
       }
     }
   } else {
+    if (it.staging) wait_entries();
     for (int r = 0; r < kRowsPerWarp; ++r) {
       if (!src[r]) continue;
-      const CopyItem& it = P.items[itm[r]];
+      const uint32_t i = r0 + r;
+      const int e0 = it.staging ? mo[i] : 0, e1 = it.staging ? mo[i + 1] : 0;
       for (int ch = lane; ch < cpr; ch += 32) {
         const uint4 v = ld_sys(src[r] + ch * 16);
         *reinterpret_cast<uint4*>(dst[r] + ch * 16) = v;
-        for (int k = e0[r]; k < e1[r]; ++k) {
-          const size_t eo = (size_t)ents[r][k] * rb + ch * 16;
+        for (int k = e0; k < e1; ++k) {
+          const size_t eo = (size_t)ents[k] * rb + ch * 16;
           *reinterpret_cast<uint4*>(it.staging + eo) = v;
           for (int j = 0; j < it.nshare; ++j) *reinterpret_cast<uint4*>(it.share[j] + eo) = v;
         }
@@ -170,21 +167,34 @@ __global__ void __launch_bounds__(kCopyThreads)
   bool waited = c.ready == nullptr, traced = false;
   if (waited) asm volatile("griddepcontrol.wait;" ::: "memory");
   // every unclaimed row of item j (cnt rows), kRowsPerWarp per claim: lane
-  // 0's atomic, its result taken only after the current rows are copied
+  // 0's atomic, its result taken only after the current rows are copied.
+  // The item's staging entries may still be pending when its rows are
+  // claimed: before its first staging write the warp polls the mark (every
+  // lane its own acquire, bounded) until the entries are out, or falls back
+  // to waiting for the resolve grid.
   auto drain = [&](int j, uint32_t cnt) {
-    uint32_t* cur_p = c.cursor + P.items[j].pair;
+    const CopyItem& it = P.items[j];
+    uint32_t* cur_p = c.cursor + it.pair;
+    bool entries = waited;
+    auto wait_entries = [&]() {
+      for (uint32_t i = 0; !entries; ++i) {
+        const uint32_t v = ld_acquire_u32(c.ready + it.pair);
+        if (!(v & kMarkEntriesPending)) {
+          entries = true;
+        } else if (i >= c.mark_polls) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          waited = entries = true;
+        } else {
+          __nanosleep(256);
+        }
+      }
+    };
     const uint32_t first = lane == 0 ? atomicAdd(cur_p, (uint32_t)kRowsPerWarp) : 0u;
     uint32_t cur = __shfl_sync(0xffffffffu, first, 0);
     while (cur < cnt) {
       const uint32_t pend = lane == 0 ? atomicAdd(cur_p, (uint32_t)kRowsPerWarp) : 0u;
-      int itm[kRowsPerWarp];
-      uint32_t mi[kRowsPerWarp];
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-        mi[r] = cur + r;
-        itm[r] = cur + r < cnt ? j : -1;
-      }
-      copy_rows<kSmallRow>(P, itm, mi, lane);
+      copy_rows<kSmallRow>(P, it, cur, min(cnt, cur + (uint32_t)kRowsPerWarp), lane,
+                           wait_entries);
       cur = __shfl_sync(0xffffffffu, pend, 0);
     }
   };
@@ -197,12 +207,17 @@ __global__ void __launch_bounds__(kCopyThreads)
       while (j < c.n_items && n < kBatchMax) {
         const uint32_t* mark = c.ready + P.items[j].pair;
         const bool read = !waited && c.mark_polls != 0;
+        // the claiming copy takes an item once its lists are out; the flat
+        // list also needs its staging entries
+        auto out = [&](uint32_t v) {
+          return (v & kSeqMask) == want && (kSteal || !(v & kMarkEntriesPending));
+        };
         uint32_t v = read ? ld_acquire_u32(mark) : 0u;
-        bool ok = waited || (read && (v & kSeqMask) == want);
+        bool ok = waited || (read && out(v));
         for (uint32_t i = 0; !ok && n == 0 && i < c.mark_polls; ++i) {
           __nanosleep(256);
           v = ld_acquire_u32(mark);
-          ok = (v & kSeqMask) == want;
+          ok = out(v);
         }
         if (!ok) {
           need_wait = n == 0;

@@ -306,17 +306,20 @@ __device__ __forceinline__ void publish_loc(const ResolveCommon& c, int pair) {
                "r"(c.seq & kSeqMask) : "memory");
 }
 
-// Publish that an item's miss count, miss lists and staging entries are
-// written (thread 0 only, after a block barrier): its host copy may start.
-// An item without misses says so in the mark itself; the copy then reads
-// nothing the item wrote, so the mark needs no fence (a fence waits for the
-// block's earlier writes, microseconds while the gather fills the memory
-// system).
-__device__ __forceinline__ void publish_copy(const ResolveCommon& c, int pair, bool none) {
+// Publish that an item's miss count and miss lists are written, and its
+// staging entries too unless `pending` (thread 0 only, after a block
+// barrier): its host copy may start.  A pending mark is followed by a second
+// one without the bit once the entries are written.  An item without misses
+// says so in the mark itself; the copy then reads nothing the item wrote, so
+// the mark needs no fence (a fence waits for the block's earlier writes,
+// microseconds while the gather fills the memory system).
+__device__ __forceinline__ void publish_copy(const ResolveCommon& c, int pair, bool none,
+                                             bool pending = false) {
   if (!c.copy_ready) return;
   if (!none) __threadfence();
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(c.copy_ready + pair),
-               "r"((c.seq & kSeqMask) | (none ? kMarkNoMiss : 0u)) : "memory");
+               "r"((c.seq & kSeqMask) | (none ? kMarkNoMiss : 0u) |
+                   (pending ? kMarkEntriesPending : 0u)) : "memory");
 }
 
 // Write the failure result of one item: no state change, zero counters.
@@ -676,6 +679,21 @@ __device__ __forceinline__ void resolve_one(const ResolveParams<MAXI>& P, const 
       if (s.st[j] == step) stamps[j] = step;
   }
 
+  // A per-query item's staging entries take two passes over its selection
+  // (about 11 us of a C64 CTA's 38): its miss lists go out first, marked
+  // with the entries pending, so that its host copy can read the rows and
+  // fill their hot slots meanwhile, and writes staging once the second mark
+  // is out.
+  const bool entries_later = it.stage && m_miss && !uni;
+  if (entries_later) {
+    __syncthreads();  // every thread's miss-list writes are done
+    if (tid == 0) {
+      c.miss_count[pair] = m_miss;
+      c.copy_cursor[pair] = 0u;  // the copy's blocks claim rows from here
+      publish_copy(c, pair, false, true);
+    }
+  }
+
   // ---- staging entries of each miss (the host copy writes them): entries
   // grouped by miss index, CSR in miss_off / miss_ent.  After the stamp
   // commit the working stamps serve as per-miss counters, then cursors.
@@ -724,9 +742,12 @@ __device__ __forceinline__ void resolve_one(const ResolveParams<MAXI>& P, const 
   __syncthreads();
   if (tid == 0) {
     // the miss count, miss lists and staging entries are written: the host
-    // copy of this item may start while its locations are being written
-    c.miss_count[pair] = m_miss;
-    c.copy_cursor[pair] = 0u;  // the copy's blocks claim rows from here
+    // copy of this item may start (or write staging) while its locations
+    // are being written
+    if (!entries_later) {
+      c.miss_count[pair] = m_miss;
+      c.copy_cursor[pair] = 0u;  // the copy's blocks claim rows from here
+    }
     publish_copy(c, pair, m_miss == 0);
   }
 

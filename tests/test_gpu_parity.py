@@ -298,6 +298,11 @@ def test_mark_poll_fallbacks(cfg):
     compare_run(cfg, gather_impl=1, polls=0)
     compare_run(cfg, gather_impl=1, polls=0, fresh=0)
     compare_run(cfg, gather_impl=1, polls=0, union=True)
+    # a poll or two: marks that come late send single tiles, blocks or warps
+    # (a copy warp waiting for an item's staging entries) down the fallback
+    # while the others use the marks
+    compare_run(cfg, gather_impl=1, polls=1)
+    compare_run(cfg, gather_impl=0, polls=2, fused=False)
     # the option's range and its value in effect
     from hierarchical_sparse_kv_dhs_gb300.runner import GpuRun
     run = GpuRun(TINY, Workload(TINY))
