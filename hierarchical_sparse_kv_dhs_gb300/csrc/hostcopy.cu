@@ -141,13 +141,15 @@ __device__ __forceinline__ void copy_rows(const CopyParams<MAXI>& P, const CopyI
 // when none is).  How its warps split the batch depends on c.steal:
 //   - 0: the batch's rows form one flat list, four consecutive rows per warp
 //     in turn (pinned regions past the GPU's translation reach, where a block
-//     must keep to its own items' rows);
+//     must keep to its own items' rows); an item joins a batch once its
+//     staging entries are out too;
 //   - 1: the warps claim each item's rows four at a time from the item's
 //     claim cursor (zeroed by the resolve launch), the next claim in flight
 //     while they copy, and a CTA whose own items are done then claims the
 //     rows no CTA has claimed yet in the other items whose marks are out,
 //     the next CTA's items first.  The copy blocks' speeds differ by SM and
-//     the step waits for the last row.
+//     the step waits for the last row.  An item is taken as soon as its
+//     miss lists are out, its staging entries possibly still pending.
 // A poll that runs out (after c.mark_polls polls; with 0 the marks are never
 // read) falls back to waiting for the resolve grid.
 constexpr int kBatchMax = 64;
