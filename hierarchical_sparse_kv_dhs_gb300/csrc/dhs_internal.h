@@ -196,11 +196,11 @@ struct CopyCommon {
                               // their own items take other items' unclaimed rows
 };
 
-// hold_smem: dynamic shared memory each block reserves (and leaves unused)
-// so that no other CTA shares its SM; at most the limit set by
-// hostcopy_set_carveout.
+// threads: per block, a multiple of 32 up to kCopyThreads.  hold_smem:
+// dynamic shared memory each block reserves (and leaves unused) so that no
+// other CTA shares its SM; at most the limit set by hostcopy_set_carveout.
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items,
-                            int n_items, int ctas, bool pdl, size_t hold_smem,
+                            int n_items, int ctas, int threads, bool pdl, size_t hold_smem,
                             cudaStream_t stream);
 
 // ------------------------------------------------------------ gather (e)

@@ -137,10 +137,18 @@ __device__ __forceinline__ const uint8_t* step1_ptr(const GatherCommon& c,
 // / host-copy grids it overlaps (stream order for whatever follows), so its
 // last block waits for them; every other CTA leaves as soon as its rows are
 // written.
+// DHS_OPT_TRACE marks of the gather: one CTA in 64, and the last.  C64's
+// 262,144 CTAs all marking two shared words slowed the traced steps' host
+// copy by a fifth; the sampled first start and last end are within a CTA's
+// lifetime of the true ones.
+__device__ __forceinline__ bool trace_sampled() {
+  return (blockIdx.x & 63u) == 0 || blockIdx.x == gridDim.x - 1;
+}
+
 __device__ __forceinline__ void end_grid(const GatherCommon& c) {
   if (blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (c.trace) __syncthreads();  // the CTA's end is its last warp's end
-  if (threadIdx.x == 0) trace_mark(c.trace, kTraceGather, true);
+  if (threadIdx.x == 0 && trace_sampled()) trace_mark(c.trace, kTraceGather, true);
 }
 
 // ---------------------------------------------------------------- vector variant
@@ -201,7 +209,7 @@ __global__ void __launch_bounds__(kGatherThreads)
   uint8_t* dst = it.staging + (size_t)e0 * c.row_bytes;
   const bool early = c.early && it.sel != nullptr;
   asm volatile("griddepcontrol.launch_dependents;");
-  if (tid == 0) trace_mark(c.trace, kTraceGather, false);
+  if (tid == 0 && trace_sampled()) trace_mark(c.trace, kTraceGather, false);
 
   // phase 0: rows resolved in step 1 (fused launch only)
   int deferred = 0;
@@ -300,7 +308,7 @@ __global__ void __launch_bounds__(kTmaThreads)
   // lanes past the warp's rows hold none (their entries never exist)
   uint8_t* my_row = s_rows + (size_t)(warp * kTmaWarpRows + min(lane, kTmaWarpRows - 1)) * rb;
   asm volatile("griddepcontrol.launch_dependents;");
-  if (threadIdx.x == 0) trace_mark(c.trace, kTraceGather, false);
+  if (threadIdx.x == 0 && trace_sampled()) trace_mark(c.trace, kTraceGather, false);
   if (lane == 0) mbar_init(&s_bar, 1);
   __syncwarp();
   uint32_t parity = 0;

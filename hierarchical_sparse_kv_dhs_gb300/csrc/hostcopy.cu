@@ -359,7 +359,8 @@ __global__ void __launch_bounds__(kCopyThreads)
   // A block whose own items had no misses leaves at once instead: in a launch
   // with few or no misses (C8 has none) the gather wants its SM back, and the
   // scan would hold it about a microsecond longer for nothing.
-  for (int base = 1; kSteal && had_rows && base < c.n_items; base += 32) {
+  for (int base = 1; kSteal && (had_rows || (int)blockIdx.x >= c.n_items) && base < c.n_items;
+       base += 32) {
     const int k = base + lane;
     int j = 0;
     bool cand = false;
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(kCopyThreads)
 }
 
 template <int MAXI>
-cudaError_t launch_t(const CopyCommon& c, const CopyItem* items, int n, int ctas,
+cudaError_t launch_t(const CopyCommon& c, const CopyItem* items, int n, int ctas, int threads,
                      bool pdl, size_t hold_smem, cudaStream_t stream) {
   CopyParams<MAXI> P;
   P.c = c;
@@ -396,7 +397,7 @@ cudaError_t launch_t(const CopyCommon& c, const CopyItem* items, int n, int ctas
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3((unsigned)ctas);
-  cfg.blockDim = dim3(kCopyThreads);
+  cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = hold_smem;  // unused by the kernel: keeps other CTAs off its SM
   cfg.stream = stream;
   if (pdl) {
@@ -491,13 +492,15 @@ cudaError_t hostcopy_set_carveout(size_t hold_smem) {
 }
 
 cudaError_t launch_hostcopy(const CopyCommon& c, const CopyItem* items, int n_items,
-                            int ctas, bool pdl, size_t hold_smem, cudaStream_t stream) {
+                            int ctas, int threads, bool pdl, size_t hold_smem,
+                            cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
   if (n_items > kCopyItemsMax || n_items > kCopyThreads) return cudaErrorInvalidValue;
+  if (threads < 32 || threads > kCopyThreads || threads % 32) return cudaErrorInvalidValue;
   // the whole table travels with every launch: a small one for small steps
   if (n_items <= kCopyItemsSmall)
-    return launch_t<kCopyItemsSmall>(c, items, n_items, ctas, pdl, hold_smem, stream);
-  return launch_t<kCopyItemsMax>(c, items, n_items, ctas, pdl, hold_smem, stream);
+    return launch_t<kCopyItemsSmall>(c, items, n_items, ctas, threads, pdl, hold_smem, stream);
+  return launch_t<kCopyItemsMax>(c, items, n_items, ctas, threads, pdl, hold_smem, stream);
 }
 
 }  // namespace dhs

@@ -270,8 +270,11 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? DHS_OK : DHS_ECUDA; }
 // block it falls to 40-52 GB/s (32 blocks).  So the grid grows until every
 // block's share of the items fits 1 GiB, up to one block per item and one per
 // SM.
+bool copy_steal(const dhs_pool* p, int64_t n_items);
+bool copy_halves(const dhs_pool* p, int64_t n_items);
 int copy_ctas(const dhs_pool* p, int64_t n_items) {
   if (p->copy_ctas > 0) return p->copy_ctas;
+  if (copy_halves(p, n_items)) return std::min(64, std::max(1, p->sm_count));
   const int64_t item_span = p->cfg.max_rows_per_request * (int64_t)p->cfg.row_bytes;
   const int64_t per_block = std::max<int64_t>(1, (int64_t(1) << 30) / std::max<int64_t>(1, item_span));
   const int64_t want = (n_items + per_block - 1) / per_block;
@@ -347,6 +350,21 @@ int resolve_ctas(const dhs_pool* p, int64_t n_items, bool paired) {
   if (p->resolve_ctas > 0) return (int)std::min<int64_t>(n_items, p->resolve_ctas);
   if (paired || n_items <= p->sm_count || !copy_pdl(p, n_items)) return (int)n_items;
   return std::max(1, p->sm_count - copy_ctas(p, n_items));
+}
+
+// Block size.  A claiming launch of more items than SMs (C64: 256 items,
+// its resolve grid one CTA per SM the copy leaves free) runs the copy as 64
+// blocks of 256 threads instead of 32 of 512: as many rows in flight, over
+// twice the SMs, each with room left for gather CTAs beside its block
+// (C64, alternated on one box: 1715-1716 us median against 1723-1724).
+// Smaller launches keep 32 blocks of 512: C8 and the miss-heavy workload
+// were slower with the halved blocks (24.82-24.85 us against 24.66-24.68,
+// 137 against 133).
+bool copy_halves(const dhs_pool* p, int64_t n_items) {
+  return p->copy_ctas <= 0 && n_items > p->sm_count && copy_steal(p, n_items);
+}
+int copy_threads(const dhs_pool* p, int64_t n_items) {
+  return copy_halves(p, n_items) ? dhs::kCopyThreads / 2 : dhs::kCopyThreads;
 }
 
 // Where each block keeps to its own items (past the translation reach), it
@@ -1313,8 +1331,8 @@ static int resolve_impl(dhs_pool* p, const dhs_step* st, const dhs_append_item* 
         cudaSuccess)
       return DHS_ECUDA;
     ccm.steal = copy_steal(p, n) ? 1 : 0;
-    if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, copy_ctas(p, n), copy_pdl(p, n),
-                             copy_hold_smem(p, n), p->stream) != cudaSuccess)
+    if (dhs::launch_hostcopy(ccm, p->citems.data() + b, n, copy_ctas(p, n), copy_threads(p, n),
+                             copy_pdl(p, n), copy_hold_smem(p, n), p->stream) != cudaSuccess)
       return DHS_ECUDA;
   }
   return DHS_OK;

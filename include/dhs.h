@@ -524,7 +524,10 @@ int dhs_read_state(dhs_pool *pool, int32_t req, int32_t src, int32_t *tags,
  * 32.  It grows past 32 until each block's items span at most 1 GiB of
  * pinned rows (max_rows_per_request * row_bytes per item), up to one block
  * per item and per SM: a block whose rows lie in a larger region re-walks
- * address translations and copies at a fraction of the link's rate. */
+ * address translations and copies at a fraction of the link's rate.  A
+ * launch of more items than SMs whose copy blocks claim rows
+ * (DHS_OPT_COPY_STEAL) runs 64 blocks of 256 threads instead of 32 of 512.
+ * A value set here keeps 512 threads a block. */
 #define DHS_OPT_COPY_CTAS 1
 #define DHS_OPT_GATHER_IMPL 2 /* 1 = TMA bulk copy, 16-row tiles of two
                                      warps (default); 0 = 16-byte vector copy,
