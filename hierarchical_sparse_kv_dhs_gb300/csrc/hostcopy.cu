@@ -7,7 +7,9 @@
 // NVLink-C2C into their victim hot-cache slots.  The pages size the copy
 // kernel's grid between 4 and 32 blocks by batch size; on GB300 fewer than
 // about 16 blocks leave the host link idle, so the grid is at least the
-// upper end, 32 blocks, whatever the batch.  The pool grows it further when
+// upper end, 32 blocks of 512 threads, whatever the batch (a claiming launch
+// of more items than SMs runs the same warps as 64 blocks of 256, leaving
+// room beside each for gather CTAs).  The pool grows it further when
 // the items' pinned regions are large (each block's share kept within about
 // 1 GiB, so that the translations of its rows stay cached near its SM).
 // Within 16 GiB of pinned rows the blocks claim rows through per-item
