@@ -2,12 +2,12 @@
 //
 // "Adaptive DHiSparse: Speculative Decoding over a Load-Adaptive KV
 // Hierarchy", How it works:
-//   Memory split -- every (request, KV source) pair owns B hot-cache rows, its
-//     tail ring and its metadata, none of which is lent out; whole pages of
-//     imported history may occupy optional capacity that can be taken back,
-//     as long as required, optional and the admission reserve together fit
-//     the pool.  Required memory is laid out per request
-//     slot up front, so the rule is checked on the optional arena.
+//   Memory split -- every (request, KV source) pair owns B hot-cache rows,
+//     its tail ring and its metadata, none of which is lent out; whole pages
+//     of imported history may occupy optional capacity that can be taken
+//     back, as long as required, optional and the admission reserve
+//     together fit the pool.  Required memory is laid out per request slot
+//     up front, so the rule is checked on the optional arena.
 //   Resident-first admission -- resident pages take optional slots at
 //     admission (lowest free slot first, pages ascending).
 //   Reclamation and refill -- whole requests' pages are taken in reclaim
@@ -303,9 +303,10 @@ bool resolve_paired(const dhs_pool* p, int64_t n_items, size_t plan) {
 // while the launch's pinned regions are small enough for the GPU's
 // translation caches to hold them whatever SMs the blocks land on (C64: 9.7
 // GB, 205 GB/s).  Past that it still pays when every copy block finds an SM
-// that the resolve grid leaves free (a copy block holds a whole SM's
-// registers, so it never shares an SM with a resolve CTA): the blocks are
-// then all placed at launch, on the same SMs every step.  Otherwise blocks
+// that the resolve grid leaves free (a 1024-thread resolve CTA and a
+// flat-list copy block each hold a whole SM's registers, so they never share
+// an SM): the blocks are then all placed at launch, on the same SMs every
+// step.  Otherwise blocks
 // placed on whichever SMs the resolve grid frees land on different SMs from
 // step to step and re-walk their translations, so the copy launches after
 // the resolve grid, onto an idle GPU, where block b lands on the same SM
