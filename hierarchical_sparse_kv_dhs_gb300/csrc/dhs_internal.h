@@ -67,7 +67,7 @@ __device__ __forceinline__ void trace_mark(unsigned long long* trace, int kind, 
 
 // ------------------------------------------------------------ resolve (a-c)
 constexpr int kResolveItemsLarge = 256, kResolveItemsSmall = 32;
-// Threads per resolve CTA (one CTA per item).  A launch of at most
+// Threads per resolve CTA (a whole CTA per item).  A launch of at most
 // kResolveItemsSmall items leaves most SMs to the gather that overlaps it,
 // and its CTAs share their SMs with that gather: 512 threads there.  Larger
 // launches fill the GPU, and each item's copy starts when it is resolved:

@@ -1,4 +1,5 @@
-// Resolve kernel: one CTA per (request, KV source) item of a decode step.
+// Resolve kernel: a whole CTA per (request, KV source) item of a decode step
+// (one CTA per item, or fewer CTAs taking several items each in turn).
 //
 // "Adaptive DHiSparse: Speculative Decoding over a Load-Adaptive KV
 // Hierarchy", How it works / Resolution: a selected row is looked up first
