@@ -135,10 +135,11 @@ __device__ __forceinline__ void copy_rows(const CopyParams<MAXI>& P, const CopyI
 }
 
 // Copy the miss rows of the launch's items.  An item's miss list (rows
-// ascending, victim slots, staging entries) is complete once the resolve
-// kernel has published its copy_ready mark (== seq, after a fence; before
-// the item's locations are written), so the copy does not wait for the whole
-// resolve grid.  CTA b owns items b, b + gridDim, ...: it takes, in order,
+// ascending, victim slots) is complete once the resolve kernel has published
+// its copy_ready mark (== seq, after a fence; before the item's locations
+// are written), and its staging entries once the mark carries no
+// entries-pending bit, so the copy does not wait for the whole resolve
+// grid.  CTA b owns items b, b + gridDim, ...: it takes, in order,
 // every owned item whose mark is out as one batch (waiting, bounded, only
 // when none is).  How its warps split the batch depends on c.steal:
 //   - 0: the batch's rows form one flat list, four consecutive rows per warp
